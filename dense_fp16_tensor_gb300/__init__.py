@@ -1,0 +1,18 @@
+"""dense_fp16_tensor_gb300 -- fp16 TN GEMM for one GB300 (sm_103a).
+
+    D(m,n) = C(m,n) + sum_k A(m,k) B(n,k)
+
+A C-ABI library (include/gemm_tn.h, csrc/) with a ctypes binding of the same
+names (``binding``) and a torch-tensor front end (``gemm``).  Build with
+``build()``; there is no CPU or library fallback.
+"""
+from ._build import build  # noqa: F401
+from .binding import (ACC_F16, ACC_F32, MAJOR_K, MAJOR_MN, PATH_AUTO, PATH_LARGE,  # noqa: F401
+                      PATH_SKINNY, GemmTnError, gemm_tn, gemm_tn_check_device_error,
+                      gemm_tn_ex, gemm_tn_last_launch_count, gemm_tn_plan_path,
+                      gemm_tn_status_string, library_path, make_options)
+
+
+def gemm(*args, **kwargs):
+    from .tensor_api import gemm as _gemm
+    return _gemm(*args, **kwargs)

@@ -1,0 +1,118 @@
+"""Thin ctypes binding of libgemm_tn.so (include/gemm_tn.h).
+
+The functions keep the C names and arguments; this module only marshals
+arguments.  Every step of the computation runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+MAJOR_K, MAJOR_MN = 0, 1
+ACC_F32, ACC_F16 = 0, 1
+PATH_AUTO, PATH_LARGE, PATH_SKINNY = 0, 1, 2
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_ALIGNMENT = 2
+ERR_UNSUPPORTED = 3
+ERR_CUDA = 4
+ERR_DEVICE_TIMEOUT = 5
+ERR_NO_MEMORY = 6
+
+# Every symbol declared in include/gemm_tn.h.
+EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
+            "gemm_tn_last_launch_count", "gemm_tn_status_string")
+
+
+class GemmTnOptions(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("sync_check", ctypes.c_int), ("timeout_ns", ctypes.c_uint64),
+                ("test_stall", ctypes.c_int)]
+
+
+class GemmTnError(RuntimeError):
+    def __init__(self, status: int, what: str = "gemm_tn"):
+        self.status = status
+        super().__init__(f"{what} failed: {gemm_tn_status_string(status)} ({status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: run dense_fp16_tensor_gb300.build() "
+                               "(nvcc, sm_103a) first; there is no fallback path")
+        L = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        gemm_args = [i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, i64, i32, vp]
+        L.gemm_tn.restype = i32
+        L.gemm_tn.argtypes = gemm_args
+        L.gemm_tn_ex.restype = i32
+        L.gemm_tn_ex.argtypes = gemm_args + [ctypes.POINTER(GemmTnOptions)]
+        L.gemm_tn_check_device_error.restype = i32
+        L.gemm_tn_check_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.gemm_tn_plan_path.restype = i32
+        L.gemm_tn_plan_path.argtypes = [i64, i64, i64, i32, i32]
+        L.gemm_tn_last_launch_count.restype = i32
+        L.gemm_tn_last_launch_count.argtypes = []
+        L.gemm_tn_status_string.restype = ctypes.c_char_p
+        L.gemm_tn_status_string.argtypes = [i32]
+        _lib = L
+        return L
+
+
+def gemm_tn(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream) -> int:
+    """C ``gemm_tn``: pointers and the stream are integers (device addresses,
+    cudaStream_t).  Returns the gemm_tn_status."""
+    return lib().gemm_tn(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype,
+                         stream)
+
+
+def make_options(path=0, split_k=0, tile_n=0, sync_check=0, timeout_ns=0, test_stall=0):
+    return GemmTnOptions(path, split_k, tile_n, sync_check, timeout_ns, test_stall)
+
+
+def gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream,
+               opts=None) -> int:
+    """C ``gemm_tn_ex``; ``opts`` is a GemmTnOptions, a dict of its fields, or None."""
+    if isinstance(opts, dict):
+        opts = make_options(**opts)
+    p = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype,
+                            stream, p)
+
+
+def gemm_tn_check_device_error(stream) -> tuple[int, int]:
+    d = ctypes.c_uint32(0)
+    s = lib().gemm_tn_check_device_error(stream, ctypes.byref(d))
+    return s, d.value
+
+
+def gemm_tn_plan_path(M, N, K, a_major, b_major) -> int:
+    return lib().gemm_tn_plan_path(M, N, K, a_major, b_major)
+
+
+def gemm_tn_last_launch_count() -> int:
+    return lib().gemm_tn_last_launch_count()
+
+
+def gemm_tn_status_string(status: int) -> str:
+    return lib().gemm_tn_status_string(status).decode()

@@ -1,0 +1,297 @@
+// gemm_skinny.cuh -- HBM-streaming path for skinny M (M <= 64), sm_103a.
+//
+// With M this small the work is one pass over B (N x K fp16), so the kernel
+// is bound by HBM, not by the tensor cores.  The roles of the operands are
+// swapped so that B fills the 128-row side of tcgen05.mma:
+//
+//     D^T(n,m) = sum_k B(n,k) * A(m,k)      (MMA M = 128 rows of B,
+//                                            MMA N = M rounded up to 16)
+//
+// which is the same TN product read with A and B exchanged ("Reading CuTe's
+// make_tiled_mma", section "Fix the matrices and directions first": D is
+// symmetric in the roles of A and B up to a transpose).
+//
+// N/128 output tiles are far fewer than the SMs, so the K loop is split.
+// The (tile, K-block) units are laid out tile-major and cut into gridDim.x
+// equal contiguous ranges, one per CTA (persistent, one CTA per SM).  A range
+// covers whole or partial K loops of one or more tiles; each maximal piece
+// inside one tile is a segment whose fp32 partial sum (128 x MP) goes to the
+// workspace.  A second kernel adds, for every output, the partials of the
+// CTAs that touched its tile in increasing CTA order and then C, exactly
+// once, and rounds to fp16 -- the rule for K split across workers in the
+// same page's section "Thread groups along K, and the loop along K": the
+// partial sums must be reduced and the initial C added only once.  The fixed
+// order makes the result deterministic.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace gemm_tn_dev {
+
+constexpr int kSkinnyBN = 128;  // rows of B per tile (the MMA's M)
+constexpr int kSkinnyBK = 64;
+constexpr int kSkinnyThreads = 192;
+
+struct SkinnyArgs {
+  int M, N, K;
+  int mp;            // M rounded up to 16 (the MMA's N)
+  int tiles, k_blocks;
+  int64_t units;     // tiles * k_blocks
+  int max_segs;      // segments one CTA can produce
+  int grid;          // CTAs of the split kernel
+  float* ws;         // [gridDim.x * max_segs][128][mp] fp32 partials
+  uint64_t timeout_ns;
+  int test_stall;
+};
+
+template <int STAGES, int MP>
+struct SkinnySmem {
+  static constexpr uint32_t kBBytes = kSkinnyBN * kSkinnyBK * 2;  // 16 KiB
+  static constexpr uint32_t kABytes = MP * kSkinnyBK * 2;         // MP rows of 128 B
+  static constexpr uint32_t kStageBytes = kBBytes + kABytes;
+  static constexpr uint32_t kBarOffset = STAGES * kStageBytes;
+  static constexpr uint32_t kNumBars = 2 * STAGES + 5;
+  static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
+  static constexpr uint32_t kBytes = kCtlOffset + 16;
+  static constexpr uint32_t kDynamicBytes = kBytes + 1024;
+  static constexpr uint32_t kTmemCols = MP <= 16 ? 32 : (MP <= 32 ? 64 : 128);
+};
+
+__device__ __forceinline__ int64_t unit_begin(int64_t units, int cta, int grid) {
+  return units * cta / grid;
+}
+
+// Segments of CTA `cta`: consecutive pieces of [begin, end) that stay inside
+// one tile.  seg j covers [max(begin, (first_tile + j) * kb), min(end, ...)).
+struct SegIter {
+  int64_t begin, end;
+  int kb;
+  __device__ SegIter(int64_t units, int cta, int grid, int k_blocks)
+      : begin(unit_begin(units, cta, grid)), end(unit_begin(units, cta + 1, grid)),
+        kb(k_blocks) {}
+  __device__ int first_tile() const { return static_cast<int>(begin / kb); }
+  __device__ int count() const {
+    if (end <= begin) return 0;
+    return static_cast<int>((end - 1) / kb) - first_tile() + 1;
+  }
+  __device__ void seg(int j, int& tile, int& kb0, int& kb1) const {
+    tile = first_tile() + j;
+    const int64_t lo = max(begin, static_cast<int64_t>(tile) * kb);
+    const int64_t hi = min(end, static_cast<int64_t>(tile + 1) * kb);
+    kb0 = static_cast<int>(lo - static_cast<int64_t>(tile) * kb);
+    kb1 = static_cast<int>(hi - static_cast<int64_t>(tile) * kb);
+  }
+};
+
+template <int STAGES, int MP>
+__global__ void __launch_bounds__(kSkinnyThreads, 1)
+    gemm_tn_skinny_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const SkinnyArgs p) {
+  using L = SkinnySmem<STAGES, MP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  // stage s: B box at s*kStageBytes (16 KiB, 1024-aligned), A box right after
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kCtlOffset);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOffset + 4);
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + STAGES);
+  const uint32_t tfull0 = smem_u32(bars + 2 * STAGES);
+  const uint32_t tempty0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const SegIter segs(p.units, blockIdx.x, gridDim.x, p.k_blocks);
+  const int nseg = segs.count();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();   // A: re-read by every CTA
+      const uint64_t stream = l2_policy_evict_first();  // B: read once
+      uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nseg; ++j) {
+        int tile, kb0, kb1;
+        segs.seg(j, tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
+                            timeout_code(kRoleProducer, stage))) {
+            ok = false;
+            break;
+          }
+          if (!(p.test_stall && j == 0 && kb == kb0)) {
+            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t b_dst = smem_u32(smem + stage * L::kStageBytes);
+            const uint32_t a_dst = b_dst + L::kBBytes;
+            mbar_arrive_expect_tx(fb, L::kStageBytes);
+            tma_load_2d_hint(b_dst, &tmB, fb, kb * kSkinnyBK, tile * kSkinnyBN, stream);
+            tma_load_2d_hint(a_dst, &tmA, fb, kb * kSkinnyBK, 0, keep);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_mask >> s & 1u)
+            wait_bounded(full0 + 8 * s, issued_parity >> s & 1u, abort_flag, p.timeout_ns,
+                         timeout_code(kRoleProducer, 0x100 + s), false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_f16(kSkinnyBN, MP, true, 0, 0);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nseg; ++j) {
+        int tile, kb0, kb1;
+        segs.seg(j, tile, kb0, kb1);
+        if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
+                          timeout_code(kRoleMma, 0x200 + acc))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * MP;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
+                            timeout_code(kRoleMma, stage))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_base = smem_u32(smem + stage * L::kStageBytes);
+          const uint32_t a_base = b_base + L::kBBytes;
+#pragma unroll
+          for (int k = 0; k < kSkinnyBK / 16; ++k) {
+            // MMA A operand = tile of B (128 x 16), MMA B operand = A (MP x 16)
+            const uint64_t bd = make_sw128_desc(b_base + k * 32, 16, 1024);
+            const uint64_t ad = make_sw128_desc(a_base + k * 32, 16, 1024);
+            mma_f16(d_tmem, bd, ad, idesc, (kb != kb0) || (k != 0));
+          }
+          mma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok || *abort_flag) {
+        mma_commit(drain);
+        wait_bounded(drain, 0, abort_flag, p.timeout_ns, timeout_code(kRoleMma, 0x300), false);
+      }
+    }
+  } else {
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const int row = static_cast<int>(quad * 32 + lane);  // row of the B tile = n offset
+    uint32_t acc = 0, acc_phase = 0;
+    for (int j = 0; j < nseg; ++j) {
+      if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
+                        timeout_code(kRoleEpilogue, acc)))
+        break;
+      tc_fence_after();
+      const int64_t slot = static_cast<int64_t>(blockIdx.x) * p.max_segs + j;
+      float* dst = p.ws + (slot * kSkinnyBN + row) * MP;
+      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * MP;
+#pragma unroll
+      for (int c = 0; c < MP / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(t_row + c * 16, r);
+        tmem_wait_ld();
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          d4[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+// CTA whose unit range holds unit u (ranges from unit_begin are monotone).
+__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t units, int grid) {
+  int c = static_cast<int>(u * grid / units);
+  while (c + 1 < grid && unit_begin(units, c + 1, grid) <= u) ++c;
+  while (c > 0 && unit_begin(units, c, grid) > u) --c;
+  return c;
+}
+
+// D(m,n) = fp16( sum over the CTAs that touched tile n/128, in CTA order, of
+// their partial (n%128, m)  +  C(m,n) ).  One thread per output element, n
+// fastest so that C and D accesses are coalesced.
+__global__ void __launch_bounds__(256)
+    gemm_tn_splitk_reduce_kernel(const SkinnyArgs p, __half* CD, int64_t ldC) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(p.M) * p.N) return;
+  const int m = static_cast<int>(idx / p.N);
+  const int n = static_cast<int>(idx - static_cast<int64_t>(m) * p.N);
+  const int tile = n / kSkinnyBN, r = n % kSkinnyBN;
+  const int grid = p.grid;
+  const int64_t u0 = static_cast<int64_t>(tile) * p.k_blocks;
+  const int c_first = cta_of_unit(u0, p.units, grid);
+  const int c_last = cta_of_unit(u0 + p.k_blocks - 1, p.units, grid);
+  float s = 0.f;
+  for (int c = c_first; c <= c_last; ++c) {
+    const int64_t b = unit_begin(p.units, c, grid);
+    if (unit_begin(p.units, c + 1, grid) <= b) continue;  // empty range
+    const int j = tile - static_cast<int>(b / p.k_blocks);
+    const int64_t slot = static_cast<int64_t>(c) * p.max_segs + j;
+    s += p.ws[(slot * kSkinnyBN + r) * p.mp + m];
+  }
+  __half* d = CD + static_cast<int64_t>(m) * ldC + n;
+  *d = __float2half_rn(s + __half2float(*d));
+}
+
+}  // namespace gemm_tn_dev

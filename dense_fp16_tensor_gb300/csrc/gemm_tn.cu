@@ -1,0 +1,367 @@
+// gemm_tn.cu -- host side of the C ABI in include/gemm_tn.h: argument
+// checks, path choice, TMA descriptor construction and kernel launches.
+//
+// The operation, the operand views and the status codes are specified in the
+// header.  This file owns:
+//   * validation (sizes, leading dimensions, alignment, aliasing) before any
+//     work is enqueued;
+//   * tensor maps for A and B (128-byte swizzle, zero fill out of range),
+//     built with cuTensorMapEncodeTiled from the driver entry point;
+//   * the choice between the persistent tile kernel and the skinny split-K
+//     kernel, and their grid sizes (one CTA per SM);
+//   * the lazily grown per-device workspace of the skinny path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_tn.h"
+#include "gemm_large.cuh"
+#include "gemm_skinny.cuh"
+
+namespace {
+
+using namespace gemm_tn_dev;
+
+constexpr int kMaxDevices = 64;
+constexpr int kSkinnyMaxM = 64;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per wait
+
+thread_local int t_last_launches = 0;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int num_sms = 0;
+  bool attrs_set = false;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int resolve_encoder() {
+  if (g_encode) return GEMM_TN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return GEMM_TN_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return GEMM_TN_OK;
+}
+
+template <int STAGES, int MP>
+cudaError_t set_skinny_attr() {
+  return cudaFuncSetAttribute(gemm_tn_skinny_kernel<STAGES, MP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SkinnySmem<STAGES, MP>::kDynamicBytes);
+}
+
+constexpr int kSkinnyStages = 8;
+
+// Per-device set-up (under g_mu): capability check, SM count, kernel
+// attributes.  Returns a status.
+int device_setup(int dev, DeviceState*& st) {
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_TN_ERR_UNSUPPORTED;
+  st = &g_dev[dev];
+  if (!st->probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GEMM_TN_ERR_CUDA;
+    st->probed = true;
+    st->supported = (major == 10 && minor == 3);
+    st->num_sms = sms;
+  }
+  if (!st->supported) return GEMM_TN_ERR_UNSUPPORTED;
+  if (!st->attrs_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tn_large_kernel<256>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         LargeSmem<256>::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_large_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               LargeSmem<128>::kDynamicBytes);
+    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 16>();
+    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 32>();
+    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 48>();
+    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 64>();
+    if (e != cudaSuccess) return GEMM_TN_ERR_CUDA;
+    st->attrs_set = true;
+  }
+  if (resolve_encoder() != GEMM_TN_OK) return GEMM_TN_ERR_CUDA;
+  return GEMM_TN_OK;
+}
+
+// Tensor map over a (rows, K) operand.  K-major: dims {K, rows}, box
+// {64, box_rows}.  MN-major: dims {rows, K}, box {64, 64}.  128-byte
+// swizzle; out-of-range elements read as zero.
+int encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld,
+                   int mn_major, uint32_t box_rows) {
+  cuuint64_t dims[2], strides[1];
+  cuuint32_t box[2], estr[2] = {1, 1};
+  if (!mn_major) {
+    dims[0] = static_cast<cuuint64_t>(K);
+    dims[1] = static_cast<cuuint64_t>(rows);
+    box[0] = 64;
+    box[1] = box_rows;
+  } else {
+    dims[0] = static_cast<cuuint64_t>(rows);
+    dims[1] = static_cast<cuuint64_t>(K);
+    box[0] = 64;
+    box[1] = 64;
+  }
+  strides[0] = static_cast<cuuint64_t>(ld) * 2;
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
+}
+
+// Byte range [lo, hi) touched by a (rows, cols) view with the given major.
+void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, int mn_major, uintptr_t& lo,
+            uintptr_t& hi) {
+  const int64_t inner = mn_major ? rows : cols;
+  const int64_t outer = mn_major ? cols : rows;
+  lo = reinterpret_cast<uintptr_t>(p);
+  hi = lo + static_cast<uintptr_t>(((outer - 1) * ld + inner) * 2);
+}
+
+int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
+             const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum) {
+  const int64_t kMax = 0x7FFFFFFF;
+  if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM_TN_ERR_INVALID_ARG;
+  if ((a_major != GEMM_TN_MAJOR_K && a_major != GEMM_TN_MAJOR_MN) ||
+      (b_major != GEMM_TN_MAJOR_K && b_major != GEMM_TN_MAJOR_MN))
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (accum != GEMM_TN_ACC_F32 && accum != GEMM_TN_ACC_F16) return GEMM_TN_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_TN_OK;
+  if (CD == nullptr || ldC < N || ldC > kMax) return GEMM_TN_ERR_INVALID_ARG;
+  if (K > 0) {
+    if (A == nullptr || B == nullptr) return GEMM_TN_ERR_INVALID_ARG;
+    if (ldA < (a_major ? M : K) || ldB < (b_major ? N : K) || ldA > kMax || ldB > kMax)
+      return GEMM_TN_ERR_INVALID_ARG;
+    uintptr_t a0, a1, b0, b1, c0, c1;
+    extent(A, M, K, ldA, a_major, a0, a1);
+    extent(B, N, K, ldB, b_major, b0, b1);
+    extent(CD, M, N, ldC, 0, c0, c1);
+    if ((c0 < a1 && a0 < c1) || (c0 < b1 && b0 < c1)) return GEMM_TN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
+      return GEMM_TN_ERR_ALIGNMENT;
+    if ((ldA | ldB) & 7) return GEMM_TN_ERR_ALIGNMENT;
+  }
+  if ((reinterpret_cast<uintptr_t>(CD) & 15u) || (ldC & 7)) return GEMM_TN_ERR_ALIGNMENT;
+  return GEMM_TN_OK;
+}
+
+int plan(int64_t M, int a_major, int b_major, int accum, int requested) {
+  const bool skinny_ok = M <= kSkinnyMaxM && a_major == GEMM_TN_MAJOR_K &&
+                         b_major == GEMM_TN_MAJOR_K && accum == GEMM_TN_ACC_F32;
+  if (requested == GEMM_TN_PATH_SKINNY) return skinny_ok ? GEMM_TN_PATH_SKINNY : -1;
+  if (requested == GEMM_TN_PATH_LARGE) return GEMM_TN_PATH_LARGE;
+  return skinny_ok ? GEMM_TN_PATH_SKINNY : GEMM_TN_PATH_LARGE;
+}
+
+int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
+                 const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum,
+                 cudaStream_t stream, const gemm_tn_options& o, const DeviceState& st) {
+  const int bn = (o.tile_n == 128) ? 128 : 256;
+  CUtensorMap tmA, tmB;
+  int s = encode_operand(&tmA, A, M, K, ldA, a_major, kLargeBM);
+  if (s == GEMM_TN_OK) s = encode_operand(&tmB, B, N, K, ldB, b_major, static_cast<uint32_t>(bn));
+  if (s != GEMM_TN_OK) return s;
+  LargeArgs p;
+  std::memset(&p, 0, sizeof p);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.CD = static_cast<__half*>(CD);
+  p.ldC = ldC;
+  p.acc_f16 = accum == GEMM_TN_ACC_F16;
+  p.a_mn = a_major;
+  p.b_mn = b_major;
+  p.tiles_m = static_cast<int>((M + kLargeBM - 1) / kLargeBM);
+  p.tiles_n = static_cast<int>((N + bn - 1) / bn);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.k_blocks = static_cast<int>((K + kLargeBK - 1) / kLargeBK);
+  p.group_m = 16;
+  p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
+  p.test_stall = o.test_stall;
+  const int grid = std::min(p.num_tiles, st.num_sms);
+  if (bn == 256) {
+    gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
+        tmA, tmB, p);
+  } else {
+    gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
+        tmA, tmB, p);
+  }
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  t_last_launches = 1;
+  return GEMM_TN_OK;
+}
+
+template <int MP>
+void launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                      const SkinnyArgs& p, cudaStream_t stream) {
+  gemm_tn_skinny_kernel<kSkinnyStages, MP>
+      <<<grid, kSkinnyThreads, SkinnySmem<kSkinnyStages, MP>::kDynamicBytes, stream>>>(tmA, tmB,
+                                                                                      p);
+}
+
+int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, const void* B,
+                  int64_t ldB, void* CD, int64_t ldC, cudaStream_t stream,
+                  const gemm_tn_options& o, DeviceState& st) {
+  SkinnyArgs p;
+  std::memset(&p, 0, sizeof p);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.mp = static_cast<int>((M + 15) / 16 * 16);
+  p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
+  p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
+  p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
+  int grid = o.split_k > 0 ? o.split_k : st.num_sms;
+  grid = static_cast<int>(std::min<int64_t>(grid, p.units));
+  p.grid = grid;
+  // A range of ceil(units/grid) units spans at most that many / k_blocks + 2 tiles.
+  const int64_t per = (p.units + grid - 1) / grid;
+  p.max_segs = static_cast<int>(per / p.k_blocks + 2);
+  p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
+  p.test_stall = o.test_stall;
+
+  const size_t need = static_cast<size_t>(grid) * p.max_segs * kSkinnyBN * p.mp * sizeof(float);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (st.ws_bytes < need) {
+      if (st.ws) cudaFree(st.ws);
+      st.ws = nullptr;
+      st.ws_bytes = 0;
+      void* w = nullptr;
+      if (cudaMalloc(&w, need) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_TN_ERR_NO_MEMORY;
+      }
+      st.ws = static_cast<float*>(w);
+      st.ws_bytes = need;
+    }
+    p.ws = st.ws;
+  }
+
+  CUtensorMap tmA, tmB;
+  int s = encode_operand(&tmA, A, M, K, ldA, 0, static_cast<uint32_t>(p.mp));
+  if (s == GEMM_TN_OK) s = encode_operand(&tmB, B, N, K, ldB, 0, kSkinnyBN);
+  if (s != GEMM_TN_OK) return s;
+
+  switch (p.mp) {
+    case 16: launch_skinny_mp<16>(grid, tmA, tmB, p, stream); break;
+    case 32: launch_skinny_mp<32>(grid, tmA, tmB, p, stream); break;
+    case 48: launch_skinny_mp<48>(grid, tmA, tmB, p, stream); break;
+    default: launch_skinny_mp<64>(grid, tmA, tmB, p, stream); break;
+  }
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  const int64_t outs = M * N;
+  const int rblocks = static_cast<int>((outs + 255) / 256);
+  gemm_tn_splitk_reduce_kernel<<<rblocks, 256, 0, stream>>>(p, static_cast<__half*>(CD), ldC);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  t_last_launches = 2;
+  return GEMM_TN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  uint32_t word = 0, zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&word, gemm_tn_dev::g_error_word, sizeof word, 0,
+                                cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GEMM_TN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  if (word != 0u) {
+    if (cudaMemcpyToSymbolAsync(gemm_tn_dev::g_error_word, &zero, sizeof zero, 0,
+                                cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return GEMM_TN_ERR_CUDA;
+  }
+  if (detail) *detail = word;
+  return word ? GEMM_TN_ERR_DEVICE_TIMEOUT : GEMM_TN_OK;
+}
+
+GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA,
+                           int a_major, const void* B, int64_t ldB, int b_major, void* CD,
+                           int64_t ldC, int accum_dtype, void* stream,
+                           const gemm_tn_options* opts) {
+  t_last_launches = 0;
+  gemm_tn_options o;
+  std::memset(&o, 0, sizeof o);
+  if (opts) o = *opts;
+  if (o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
+      (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256))
+    return GEMM_TN_ERR_INVALID_ARG;
+  int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
+  if (s != GEMM_TN_OK) return s;
+  if (M == 0 || N == 0 || K == 0) return GEMM_TN_OK;  // D = C: nothing to do
+
+  const int path = plan(M, a_major, b_major, accum_dtype, o.path);
+  if (path < 0) return GEMM_TN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  DeviceState* st = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    s = device_setup(dev, st);
+  }
+  if (s != GEMM_TN_OK) return s;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (path == GEMM_TN_PATH_SKINNY)
+    s = launch_skinny(M, N, K, A, ldA, B, ldB, CD, ldC, cs, o, *st);
+  else
+    s = launch_large(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, cs, o, *st);
+  if (s != GEMM_TN_OK) return s;
+  if (o.sync_check) return gemm_tn_check_device_error(stream, nullptr);
+  return GEMM_TN_OK;
+}
+
+GEMM_TN_API int gemm_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA,
+                        int a_major, const void* B, int64_t ldB, int b_major, void* CD,
+                        int64_t ldC, int accum_dtype, void* stream) {
+  return gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream,
+                    nullptr);
+}
+
+GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major, int b_major) {
+  (void)N;
+  (void)K;
+  return plan(M, a_major, b_major, GEMM_TN_ACC_F32, GEMM_TN_PATH_AUTO);
+}
+
+GEMM_TN_API int gemm_tn_last_launch_count(void) { return t_last_launches; }
+
+GEMM_TN_API const char* gemm_tn_status_string(int status) {
+  switch (status) {
+    case GEMM_TN_OK: return "GEMM_TN_OK";
+    case GEMM_TN_ERR_INVALID_ARG: return "GEMM_TN_ERR_INVALID_ARG";
+    case GEMM_TN_ERR_ALIGNMENT: return "GEMM_TN_ERR_ALIGNMENT";
+    case GEMM_TN_ERR_UNSUPPORTED: return "GEMM_TN_ERR_UNSUPPORTED";
+    case GEMM_TN_ERR_CUDA: return "GEMM_TN_ERR_CUDA";
+    case GEMM_TN_ERR_DEVICE_TIMEOUT: return "GEMM_TN_ERR_DEVICE_TIMEOUT";
+    case GEMM_TN_ERR_NO_MEMORY: return "GEMM_TN_ERR_NO_MEMORY";
+    default: return "GEMM_TN_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+/*
+ * gemm_tn.h -- C ABI of the GB300 (sm_103a) fp16 TN GEMM library.
+ *
+ * Operation (page "Reading CuTe's make_tiled_mma: how one MMA tiles into a
+ * matrix", section "Fix the matrices and directions first"):
+ *
+ *     D(m,n) = C(m,n) + sum_{k<K} A(m,k) * B(n,k)
+ *
+ * with A of logical shape (M,K), B of logical shape (N,K) -- B(n,k) is the
+ * usual right-hand matrix read as B_math(k,n) -- and C/D of shape (M,N).
+ * "TN" names the operand form of the tensor-core instruction, not a memory
+ * order; memory order is given separately per operand.
+ *
+ * Operand views (page "CuTe Layout to Tensor Core", sections 1 "the outermost
+ * level: a matrix is a Shape + Stride layout" and 2 "Tensor = Pointer +
+ * Layout"): an operand is a pointer plus a two-mode shape:stride layout in
+ * which one mode is stride-1.
+ *   A, a_major == GEMM_TN_MAJOR_K : (M,K):(ldA,1), ldA >= K
+ *   A, a_major == GEMM_TN_MAJOR_MN: (M,K):(1,ldA), ldA >= M
+ *   B, b_major == GEMM_TN_MAJOR_K : (N,K):(ldB,1), ldB >= K
+ *   B, b_major == GEMM_TN_MAJOR_MN: (N,K):(1,ldB), ldB >= N
+ *   C/D                           : (M,N):(ldC,1), ldC >= N
+ * All elements are IEEE binary16.
+ *
+ * C and D share one buffer: each element of C is read before the element of
+ * D at the same position is written ("compute C = A*B + C in the original
+ * accumulator", page "Reading CuTe's retile_D", section "How the two
+ * fragments are handed to the MMA").  There is no alpha/beta; to compute
+ * D = A.B^T, zero the buffer first.
+ *
+ * Accumulation (same page, section "From CuTe's name to the instruction";
+ * make_tiled_mma page, section "Fix the matrices and directions first"):
+ *   GEMM_TN_ACC_F32: the products are summed in fp32, C is converted to fp32
+ *                    and added, and the sum is rounded once to fp16
+ *                    (round-to-nearest-even): the F32F16F16F32 form.
+ *   GEMM_TN_ACC_F16: the products are summed in an fp16 accumulator and C is
+ *                    added in fp16: the F16F16F16F16 form.
+ *
+ * Ownership: the caller owns A, B and CD (device memory); the library never
+ * frees or retains caller memory.  The library owns a per-device workspace
+ * for the split-K partial sums of the skinny path, created on first use with
+ * cudaMalloc and grown when a larger one is needed; it lives until process
+ * exit.  A call that needs to create or grow it must not be made during
+ * stream capture.
+ *
+ * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream).  It returns once the kernels are enqueued; D is
+ * valid after the stream has been synchronised.  Calls on one stream are
+ * ordered; calls that may overlap on different streams must not share the
+ * CD buffer.  All pointers are device pointers of the current device.
+ *
+ * Errors: every function returns a gemm_tn_status and never aborts or throws.
+ * Argument checks run before anything is enqueued, so an error return from
+ * them leaves the stream untouched.
+ */
+#ifndef GEMM_TN_H_
+#define GEMM_TN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GEMM_TN_API __attribute__((visibility("default")))
+#else
+#define GEMM_TN_API
+#endif
+
+typedef enum {
+  GEMM_TN_MAJOR_K = 0,  /* the K mode is stride-1 */
+  GEMM_TN_MAJOR_MN = 1  /* the M (for A) or N (for B) mode is stride-1 */
+} gemm_tn_major;
+
+typedef enum {
+  GEMM_TN_ACC_F32 = 0,
+  GEMM_TN_ACC_F16 = 1
+} gemm_tn_accum;
+
+typedef enum {
+  GEMM_TN_OK = 0,
+  GEMM_TN_ERR_INVALID_ARG = 1,     /* negative or too large size, ld too small,
+                                      NULL pointer with a nonzero extent, bad
+                                      enum, CD overlapping A or B */
+  GEMM_TN_ERR_ALIGNMENT = 2,       /* a pointer not 16-byte aligned or an ld
+                                      that is not a multiple of 8 elements */
+  GEMM_TN_ERR_UNSUPPORTED = 3,     /* no device of compute capability 10.3 */
+  GEMM_TN_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
+  GEMM_TN_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel expired;
+                                      that launch's D is not valid */
+  GEMM_TN_ERR_NO_MEMORY = 6        /* the workspace could not be allocated */
+} gemm_tn_status;
+
+typedef enum {
+  GEMM_TN_PATH_AUTO = 0,    /* skinny path for M <= 64 with K-major A and B,
+                               persistent tile path otherwise */
+  GEMM_TN_PATH_LARGE = 1,   /* persistent 128xBN tile kernel */
+  GEMM_TN_PATH_SKINNY = 2   /* swapped-operand split-K kernel + reduction;
+                               needs M <= 64 and K-major A and B */
+} gemm_tn_path;
+
+/* Extra controls for gemm_tn_ex.  Zero-initialise and set what you need;
+ * every zero field means "the library's default". */
+typedef struct {
+  int path;             /* gemm_tn_path */
+  int split_k;          /* skinny path: number of CTAs sharing the K loop of
+                           the output tiles (0 = one per SM) */
+  int tile_n;           /* large path: output tile width, 0 (= 256), 128 or 256 */
+  int sync_check;       /* nonzero: synchronise `stream` after the launch and
+                           return GEMM_TN_ERR_DEVICE_TIMEOUT if a kernel gave
+                           up waiting (the sticky device error word is read
+                           and cleared) */
+  uint64_t timeout_ns;  /* limit of every in-kernel wait (0 = 1 s) */
+  int test_stall;       /* TEST ONLY: nonzero makes the producer of the first
+                           tile withhold one pipeline stage, so that the
+                           consumer's bounded wait expires and the kernel
+                           reports GEMM_TN_ERR_DEVICE_TIMEOUT instead of
+                           hanging */
+} gemm_tn_options;
+
+/*
+ * D = C + A.B^T in place in CD, as described at the top of this file.
+ *
+ *   M, N, K      sizes, each in [0, 2^31 - 1].  M == 0 or N == 0 is a no-op;
+ *                K == 0 leaves CD unchanged (D = C) without a launch.
+ *   A, ldA       (M,K) operand storage and its leading dimension in elements
+ *   a_major      gemm_tn_major of A
+ *   B, ldB       (N,K) operand storage and its leading dimension
+ *   b_major      gemm_tn_major of B
+ *   CD, ldC      (M,N) row-major storage of C on entry and D on return
+ *   accum_dtype  gemm_tn_accum
+ *   stream       cudaStream_t the work is enqueued on
+ *
+ * Alignment: A, B, CD 16-byte aligned; ldA, ldB, ldC multiples of 8 (the
+ * tensor-memory-access unit moves 16-byte rows).
+ */
+GEMM_TN_API int gemm_tn(int64_t M, int64_t N, int64_t K,
+                        const void* A, int64_t ldA, int a_major,
+                        const void* B, int64_t ldB, int b_major,
+                        void* CD, int64_t ldC,
+                        int accum_dtype, void* stream);
+
+/* gemm_tn with explicit controls; opts may be NULL (same as gemm_tn). */
+GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
+                           const void* A, int64_t ldA, int a_major,
+                           const void* B, int64_t ldB, int b_major,
+                           void* CD, int64_t ldC,
+                           int accum_dtype, void* stream,
+                           const gemm_tn_options* opts);
+
+/* Synchronise `stream`, then read and clear the device error word that a
+ * kernel sets when one of its bounded waits expires.  Returns GEMM_TN_OK,
+ * GEMM_TN_ERR_DEVICE_TIMEOUT (and, if detail != NULL, the raw word: bits
+ * 16-23 the role that gave up -- 1 producer, 2 MMA issuer, 3 epilogue -- and
+ * bits 0-15 the pipeline stage), or GEMM_TN_ERR_CUDA. */
+GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail);
+
+/* Which path gemm_tn would take for these sizes and majors (gemm_tn_path). */
+GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major,
+                                  int b_major);
+
+/* Number of kernel launches the last successful gemm_tn / gemm_tn_ex call on
+ * this host thread enqueued (0 for the no-op cases). */
+GEMM_TN_API int gemm_tn_last_launch_count(void);
+
+/* Static, NUL-terminated name of a gemm_tn_status value. */
+GEMM_TN_API const char* gemm_tn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TN_H_ */

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds for
+sm_103a, loads, exports every function include/gemm_tn.h declares, and
+rejects bad arguments before it touches the device (the pointers below are
+never dereferenced: validation returns first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp16_tensor_gb300 as g
+from dense_fp16_tensor_gb300 import binding as gb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    g.build()
+    return gb.lib()
+
+
+def header_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"GEMM_TN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert set(gb.EXPORTED) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n  # ctypes resolves it with dlsym
+
+
+def test_status_strings(lib):
+    for s, name in [(0, "GEMM_TN_OK"), (1, "GEMM_TN_ERR_INVALID_ARG"),
+                    (2, "GEMM_TN_ERR_ALIGNMENT"), (5, "GEMM_TN_ERR_DEVICE_TIMEOUT"),
+                    (99, "GEMM_TN_ERR_UNKNOWN")]:
+        assert gb.gemm_tn_status_string(s) == name
+
+
+def test_plan_path(lib):
+    assert gb.gemm_tn_plan_path(16, 16384, 16384, 0, 0) == gb.PATH_SKINNY
+    assert gb.gemm_tn_plan_path(64, 100, 100, 0, 0) == gb.PATH_SKINNY
+    assert gb.gemm_tn_plan_path(65, 100, 100, 0, 0) == gb.PATH_LARGE
+    assert gb.gemm_tn_plan_path(16, 100, 100, 1, 0) == gb.PATH_LARGE
+    assert gb.gemm_tn_plan_path(8192, 8192, 8192, 0, 0) == gb.PATH_LARGE
+
+
+P = 0x7F0000000000  # a 16-byte aligned fake device address, never dereferenced
+
+
+def call(M=64, N=64, K=64, A=P, ldA=64, am=0, B=P + (1 << 20), ldB=64, bm=0,
+         CD=P + (2 << 20), ldC=64, acc=0, opts=None):
+    return gb.gemm_tn_ex(M, N, K, A, ldA, am, B, ldB, bm, CD, ldC, acc, None, opts)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), gb.ERR_INVALID_ARG),
+    (dict(K=1 << 31), gb.ERR_INVALID_ARG),
+    (dict(ldA=63), gb.ERR_INVALID_ARG),                  # K-major A needs ldA >= K
+    (dict(am=1, ldA=32), gb.ERR_INVALID_ARG),            # M-major A needs ldA >= M
+    (dict(ldB=8), gb.ERR_INVALID_ARG),
+    (dict(ldC=56), gb.ERR_INVALID_ARG),
+    (dict(am=2), gb.ERR_INVALID_ARG),
+    (dict(acc=3), gb.ERR_INVALID_ARG),
+    (dict(A=0), gb.ERR_INVALID_ARG),
+    (dict(CD=0), gb.ERR_INVALID_ARG),
+    (dict(CD=P), gb.ERR_INVALID_ARG),                    # CD overlaps A
+    (dict(CD=P + (1 << 20) + 128), gb.ERR_INVALID_ARG),  # CD overlaps B
+    (dict(A=P + 8), gb.ERR_ALIGNMENT),
+    (dict(CD=P + (2 << 20) + 2), gb.ERR_ALIGNMENT),
+    (dict(ldA=68), gb.ERR_ALIGNMENT),
+    (dict(ldC=68), gb.ERR_ALIGNMENT),
+    (dict(opts=gb.make_options(path=7)), gb.ERR_INVALID_ARG),
+    (dict(opts=gb.make_options(tile_n=96)), gb.ERR_INVALID_ARG),
+    (dict(M=100, opts=gb.make_options(path=2)), gb.ERR_INVALID_ARG),  # skinny needs M <= 64
+])
+def test_argument_errors_return_before_any_device_work(lib, kw, status):
+    assert call(**kw) == status
+    assert gb.gemm_tn_last_launch_count() == 0
+
+
+def test_noop_sizes_return_ok_without_a_device(lib):
+    assert call(M=0) == gb.OK
+    assert call(N=0) == gb.OK
+    assert call(K=0) == gb.OK  # D = C: nothing to launch
+    assert gb.gemm_tn_last_launch_count() == 0
+
+
+def test_null_operands_allowed_when_k_is_zero(lib):
+    assert call(K=0, A=0, B=0) == gb.OK
+
+
+def test_tensor_front_end_major_inference():
+    torch = pytest.importorskip("torch")
+    from dense_fp16_tensor_gb300.tensor_api import operand_view
+    a = torch.zeros(4, 16, dtype=torch.float16)
+    assert operand_view(a, "A") == (gb.MAJOR_K, 16)
+    assert operand_view(torch.zeros(16, 24, dtype=torch.float16).t(), "A") == (gb.MAJOR_MN, 24)
+    st = torch.zeros(40, 32, dtype=torch.float16)
+    assert operand_view(st[:, :20], "A") == (gb.MAJOR_K, 32)   # padded ld
+    with pytest.raises(ValueError):
+        operand_view(torch.zeros(8, 8, 2, dtype=torch.float16)[:, :, 0], "A")
