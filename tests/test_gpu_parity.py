@@ -132,14 +132,15 @@ def test_ragged_sweep(accum, a_major, b_major):
 @pytest.mark.parametrize("tile_n", [128, 256])
 def test_large_path_real_values_both_tiles(tile_n):
     M, N, K = 300, 520, 700
-    A_st = wl.operand(M, K, K + 8, 0, "u11", 11)
-    B_st = wl.operand(N, K, N + 8, 1, "u11", 12)  # B MN-major
+    ldA, ldB = K + 12, N + 8
+    A_st = wl.operand(M, K, ldA, 0, "u11", 11)
+    B_st = wl.operand(N, K, ldB, 1, "u11", 12)  # B MN-major
     C_st = wl.operand(M, N, N, 0, "u11", 13)
     for accum in (0, 1):
-        D_st, st = run_gpu(M, N, K, A_st, K + 8, 0, B_st, N + 8, 1, C_st, N, accum,
+        D_st, st = run_gpu(M, N, K, A_st, ldA, 0, B_st, ldB, 1, C_st, N, accum,
                            opts={"path": gb.PATH_LARGE, "tile_n": tile_n})
-        assert st == gb.OK
-        d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), K + 8, 0, np_bits(B_st), N + 8, 1,
+        assert st == gb.OK, gb.gemm_tn_status_string(st)
+        d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), ldA, 0, np_bits(B_st), ldB, 1,
                                   np_bits(C_st), N)
         check(result_view(D_st, M, N), d64, d16, K, accum, False, f"tile_n={tile_n}")
 
@@ -220,7 +221,7 @@ def test_bounded_wait_expires_and_reports_instead_of_hanging():
 def test_tensor_front_end_matches_oracle():
     import dense_fp16_tensor_gb300 as g
     dev = torch.device("cuda")
-    M, N, K = 136, 90, 200
+    M, N, K = 136, 96, 200
     A_st = wl.draw((K, M), "int2", 51)               # stored K rows of M: M-major
     B_st = wl.draw((N, K), "int2", 52)               # K-major
     C_st = wl.draw((M, N), "int4", 53)
