@@ -27,7 +27,10 @@ ERR_NO_MEMORY = 6
 
 # Every symbol declared in include/gemm_tn.h.
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
-            "gemm_tn_last_launch_count", "gemm_tn_status_string")
+            "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc")
+
+# Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class GemmTnOptions(ctypes.Structure):
@@ -75,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_tn_last_launch_count.argtypes = []
         L.gemm_tn_status_string.restype = ctypes.c_char_p
         L.gemm_tn_status_string.argtypes = [i32]
+        L.gemm_tn_skinny_noalloc.restype = i32
+        L.gemm_tn_skinny_noalloc.argtypes = gemm_args
         _lib = L
         return L
 
@@ -116,3 +121,17 @@ def gemm_tn_last_launch_count() -> int:
 
 def gemm_tn_status_string(status: int) -> str:
     return lib().gemm_tn_status_string(status).decode()
+
+
+def gemm_tn_skinny_noalloc(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype,
+                           stream) -> int:
+    """C ``gemm_tn_skinny_noalloc``: the skinny path (M <= 64, K-major A and B,
+    fp32 accumulation) for callers that cannot have device memory allocated on
+    their behalf -- latency-sensitive loops where cudaMalloc/cudaFree would
+    synchronise the device, or processes whose allocator already holds nearly
+    all device memory.  Its partial sums live in a fixed 16 MiB array inside
+    the library instead of a cudaMalloc'd workspace; larger problems are
+    rejected with GEMM_TN_ERR_INVALID_ARG.  Calls that overlap on the GPU share
+    that array and race.  Returns the gemm_tn_status."""
+    return lib().gemm_tn_skinny_noalloc(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC,
+                                        accum_dtype, stream)

@@ -365,3 +365,99 @@ GEMM_TN_API const char* gemm_tn_status_string(int status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_tn_skinny_noalloc: the skinny path with its partial sums in a fixed
+// array compiled into the library, so that callers that cannot have device
+// memory allocated for them (see the header) can still use it.  Nothing here
+// calls cudaMalloc, cudaFree or any other allocating routine.
+
+static __device__ __align__(256) float
+    g_noalloc_scratch[GEMM_TN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+// Device address of g_noalloc_scratch per device.  In host code the array's
+// name is only a host-side stand-in, so the address is looked up once per
+// device, with that device current, and passed to the kernels.
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(int dev, float** out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return GEMM_TN_OK;
+}
+
+}  // namespace
+
+extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K,
+                                                  const void* A, int64_t ldA, int a_major,
+                                                  const void* B, int64_t ldB, int b_major,
+                                                  void* CD, int64_t ldC, int accum_dtype,
+                                                  void* stream) {
+  t_last_launches = 0;
+  int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
+  if (s != GEMM_TN_OK) return s;
+  if (M > kSkinnyMaxM || a_major != GEMM_TN_MAJOR_K || b_major != GEMM_TN_MAJOR_K ||
+      accum_dtype != GEMM_TN_ACC_F32)
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (M == 0 || N == 0 || K == 0) return GEMM_TN_OK;  // D = C: nothing to do
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  DeviceState* st = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    s = device_setup(dev, st);
+  }
+  if (s != GEMM_TN_OK) return s;
+
+  // Same split as the skinny path of gemm_tn: one CTA per SM.
+  SkinnyArgs p;
+  std::memset(&p, 0, sizeof p);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.mp = static_cast<int>((M + 15) / 16 * 16);
+  p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
+  p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
+  p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
+  const int grid = static_cast<int>(std::min<int64_t>(st->num_sms, p.units));
+  p.grid = grid;
+  const int64_t per = (p.units + grid - 1) / grid;
+  p.max_segs = static_cast<int>(per / p.k_blocks + 2);
+  p.timeout_ns = kDefaultTimeoutNs;
+  const uint64_t need =
+      static_cast<uint64_t>(grid) * p.max_segs * kSkinnyBN * p.mp * sizeof(float);
+  if (need > GEMM_TN_NOALLOC_SCRATCH_BYTES) return GEMM_TN_ERR_INVALID_ARG;
+
+  s = noalloc_scratch(dev, &p.ws);
+  if (s != GEMM_TN_OK) return s;
+
+  CUtensorMap tmA, tmB;
+  s = encode_operand(&tmA, A, M, K, ldA, 0, static_cast<uint32_t>(p.mp));
+  if (s == GEMM_TN_OK) s = encode_operand(&tmB, B, N, K, ldB, 0, kSkinnyBN);
+  if (s != GEMM_TN_OK) return s;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  switch (p.mp) {
+    case 16: launch_skinny_mp<16>(grid, tmA, tmB, p, cs); break;
+    case 32: launch_skinny_mp<32>(grid, tmA, tmB, p, cs); break;
+    case 48: launch_skinny_mp<48>(grid, tmA, tmB, p, cs); break;
+    default: launch_skinny_mp<64>(grid, tmA, tmB, p, cs); break;
+  }
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  const int rblocks = static_cast<int>((M * N + 255) / 256);
+  gemm_tn_splitk_reduce_kernel<<<rblocks, 256, 0, cs>>>(p, static_cast<__half*>(CD), ldC);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  t_last_launches = 2;
+  return GEMM_TN_OK;
+}

@@ -167,6 +167,55 @@ GEMM_TN_API int gemm_tn_last_launch_count(void);
 /* Static, NUL-terminated name of a gemm_tn_status value. */
 GEMM_TN_API const char* gemm_tn_status_string(int status);
 
+/* Size of the fixed scratch array behind gemm_tn_skinny_noalloc: 16 MiB,
+ * held in device memory on every GPU that loads this library, until the
+ * process exits. */
+#define GEMM_TN_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * The skinny path (M <= 64, K-major A and B, GEMM_TN_ACC_F32) without any
+ * device allocation.  The source pages have no counterpart of this entry
+ * point; it exists for callers that cannot let a library allocate device
+ * memory behind their back:
+ *   - latency-sensitive loops, where cudaMalloc/cudaFree can synchronise the
+ *     device and stall every stream;
+ *   - processes whose framework allocator has already reserved nearly all
+ *     device memory, where a library's own cudaMalloc can fail at an
+ *     unpredictable moment;
+ *   - programs that must fix their device-memory footprint up front.
+ * gemm_tn's skinny path keeps its split-K partial sums in a workspace it
+ * creates with cudaMalloc on first use.  This entry point computes the same
+ * thing with the same kernels, but keeps the partial sums in one fixed
+ * array of GEMM_TN_NOALLOC_SCRATCH_BYTES compiled into the library, so no
+ * call ever allocates or frees device memory.
+ *
+ * Arguments, views and results are those of gemm_tn, restricted to
+ * M <= 64, a_major == b_major == GEMM_TN_MAJOR_K and
+ * accum_dtype == GEMM_TN_ACC_F32.  The caller still owns and passes A, B and
+ * CD.
+ *
+ * Limits and behaviour:
+ *   - returns GEMM_TN_ERR_INVALID_ARG, before enqueuing anything, when the
+ *     arguments are outside that restriction or when the problem needs more
+ *     partial-sum scratch than GEMM_TN_NOALLOC_SCRATCH_BYTES (the need is
+ *     (SMs) x (tiles one CTA touches) x 128 x round_up(M,16) x 4 bytes; the
+ *     M=16, N=K=16384 problem needs about 2.5 MiB);
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on that device;
+ *   - every call on a device shares the one array, and the array keeps
+ *     whatever the last call left in it.  Nothing in it needs to start at
+ *     zero (each partial sum is written before it is read within a call),
+ *     but calls that can overlap on the GPU -- for example on two streams
+ *     without ordering between them -- race on the array and produce wrong
+ *     results.  Order such calls on one stream or with events.
+ */
+GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t K,
+                                       const void* A, int64_t ldA, int a_major,
+                                       const void* B, int64_t ldB, int b_major,
+                                       void* CD, int64_t ldC,
+                                       int accum_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
