@@ -74,26 +74,35 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Source files that define each kernel (its device code and the PTX it uses).
+KERNEL_SOURCES = {
+    "gemm_tn_large_kernel": ["gemm_large.cuh", "common.cuh", "ptx.cuh"],
+    "gemm_tn_large2_kernel": ["gemm_large2.cuh", "gemm_large.cuh", "common.cuh", "ptx.cuh"],
+    "gemm_tn_skinny_kernel": ["gemm_skinny.cuh", "common.cuh", "ptx.cuh"],
+}
+
+
+def kernel_source_hash(kernel_key: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp16_tensor_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
+    for fn in KERNEL_SOURCES[kernel_key]:
+        p = os.path.join(csrc, fn)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
                 h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(kernel_key: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since those counters were taken."""
+    kernel's sources changed since those counters were taken."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel_key)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel_key):
         return None
     return e.get("dram_bytes_per_launch")
 
