@@ -27,7 +27,8 @@ ERR_NO_MEMORY = 6
 
 # Every symbol declared in include/gemm_tn.h.
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
-            "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc")
+            "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc",
+            "gemm_tn_last_kernels")
 
 # Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -36,7 +37,7 @@ NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 class GemmTnOptions(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_n", ctypes.c_int),
                 ("sync_check", ctypes.c_int), ("timeout_ns", ctypes.c_uint64),
-                ("test_stall", ctypes.c_int)]
+                ("test_stall", ctypes.c_int), ("cta_pair", ctypes.c_int)]
 
 
 class GemmTnError(RuntimeError):
@@ -78,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_tn_last_launch_count.argtypes = []
         L.gemm_tn_status_string.restype = ctypes.c_char_p
         L.gemm_tn_status_string.argtypes = [i32]
+        L.gemm_tn_last_kernels.restype = ctypes.c_char_p
+        L.gemm_tn_last_kernels.argtypes = []
         L.gemm_tn_skinny_noalloc.restype = i32
         L.gemm_tn_skinny_noalloc.argtypes = gemm_args
         _lib = L
@@ -91,8 +94,9 @@ def gemm_tn(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, str
                          stream)
 
 
-def make_options(path=0, split_k=0, tile_n=0, sync_check=0, timeout_ns=0, test_stall=0):
-    return GemmTnOptions(path, split_k, tile_n, sync_check, timeout_ns, test_stall)
+def make_options(path=0, split_k=0, tile_n=0, sync_check=0, timeout_ns=0, test_stall=0,
+                 cta_pair=0):
+    return GemmTnOptions(path, split_k, tile_n, sync_check, timeout_ns, test_stall, cta_pair)
 
 
 def gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream,
@@ -117,6 +121,10 @@ def gemm_tn_plan_path(M, N, K, a_major, b_major) -> int:
 
 def gemm_tn_last_launch_count() -> int:
     return lib().gemm_tn_last_launch_count()
+
+
+def gemm_tn_last_kernels() -> str:
+    return lib().gemm_tn_last_kernels().decode()
 
 
 def gemm_tn_status_string(status: int) -> str:

@@ -21,20 +21,28 @@ __device__ __forceinline__ uint32_t timeout_code(uint32_t role, uint32_t stage) 
 
 // Wait for the phase of `bar` with parity `parity`, giving up after
 // `limit_ns` of wall time.  On giving up, record `code` in the error word,
-// raise the CTA's abort flag and return false.  With honour_abort, also
-// return false (without recording) as soon as another role raised the flag.
+// raise the CTA's abort flag (and the peer CTA's, when peer_abort is a
+// shared::cluster address) and return false.  With honour_abort, also return
+// false (without recording) as soon as another role raised the flag.
+// kCluster selects cluster-scope acquire, for barriers other CTAs arrive on.
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile uint32_t* abort_flag, uint64_t limit_ns,
-                                             uint32_t code, bool honour_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                             uint32_t code, bool honour_abort = true,
+                                             uint32_t peer_abort = 0u) {
+  auto probe = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if ((i & 15u) == 0) {
       if (honour_abort && *abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         atomicCAS(&g_error_word, 0u, code);
         *abort_flag = 1u;
+        if (peer_abort) st_shared_cluster_u32(peer_abort, 1u);
         return false;
       }
     }

@@ -1,0 +1,260 @@
+// gemm_large2.cuh -- persistent tcgen05 TN GEMM on CTA pairs (cta_group::2).
+//
+// Same computation and tiling scheme as gemm_large.cuh, but two CTAs on two
+// SMs (a cluster of 2) compute one 256 x 256 output tile together:
+//
+//   * CTA r of the pair TMA-loads rows [128r, 128r+128) of the tile's A block
+//     and rows [128r, 128r+128) of its B block into its own 6-stage ring
+//     (32 KiB per 64-deep K block), so each SM pulls 64 B per clock of
+//     tensor work instead of 96 B with 128 x 256 single-CTA tiles.
+//   * One thread of the even CTA issues tcgen05.mma.cta_group::2 with
+//     M = 256, N = 256, K = 16: the instruction reads A from both CTAs'
+//     shared memory (split along M) and B from both (split along N), and
+//     writes rows [128r, 128r+128) of D into CTA r's tensor memory.
+//   * Stage completion: each CTA's copies signal its own `full` barrier, so
+//     each CTA can always drain its own copies.  One thread of the odd CTA
+//     forwards each completed stage to the even CTA's `full` barrier (which
+//     therefore expects two arrivals).  The MMA thread releases a stage in
+//     both CTAs with one multicast tcgen05.commit; accumulators are handed to
+//     both CTAs' epilogues the same way, and the eight epilogue warps of the
+//     pair return an accumulator by arriving on the even CTA's `tmem_empty`.
+//
+// Every wait is bounded; a CTA that gives up raises its own and its peer's
+// abort flag, both drain what they issued, free the pair's TMEM and return.
+#pragma once
+
+#include "gemm_large.cuh"
+
+namespace gemm_tn_dev {
+
+constexpr int kPairBM = 256;   // output rows per tile (128 per CTA)
+constexpr int kPairBN = 256;   // output columns per tile (B rows: 128 per CTA)
+constexpr int kPairBK = 64;
+constexpr int kPairStages = 6;
+constexpr int kPairThreads = 192;
+constexpr uint32_t kPairTmemCols = 512;  // two 256-column fp32 accumulators
+
+struct PairSmem {
+  static constexpr uint32_t kABytes = 128 * kPairBK * 2;  // 16 KiB
+  static constexpr uint32_t kBBytes = 128 * kPairBK * 2;  // 16 KiB
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kBarOffset = kPairStages * kStageBytes;
+  static constexpr uint32_t kNumBars = 2 * kPairStages + 5;
+  static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
+  static constexpr uint32_t kBytes = kCtlOffset + 16;
+  static constexpr uint32_t kDynamicBytes = kBytes + 1024;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    gemm_tn_large2_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB, const LargeArgs p) {
+  using L = PairSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  // stage s: A half at s*kStageBytes, B half right after (both 1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kCtlOffset);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOffset + 4);
+
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kPairStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kPairStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kPairStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kPairStages + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs, 1: peer
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full0 + 8 * s, leader ? 2 : 1);  // own copies (+ the peer's forward)
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 8);  // the pair's eight epilogue warps
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kPairTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t peer_abort = mapa_shared(smem_u32(smem + L::kCtlOffset), rank ^ 1u);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      int local = 0;
+      for (int t = pair; ok && t < p.num_tiles; t += num_pairs, ++local) {
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        const int a_row = tm * kPairBM + 128 * static_cast<int>(rank);
+        const int b_row = tn * kPairBN + 128 * static_cast<int>(rank);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
+                            timeout_code(kRoleProducer, stage), true, peer_abort)) {
+            ok = false;
+            break;
+          }
+          if (!(p.test_stall && local == 0 && kb == 0)) {
+            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
+            const uint32_t b_dst = a_dst + L::kABytes;
+            mbar_arrive_expect_tx(fb, L::kStageBytes);
+            const int k0 = kb * kPairBK;
+            if (!p.a_mn) {
+              tma_load_2d(a_dst, &tmA, fb, k0, a_row);
+            } else {
+              tma_load_2d(a_dst, &tmA, fb, a_row, k0);
+              tma_load_2d(a_dst + 8192, &tmA, fb, a_row + 64, k0);
+            }
+            if (!p.b_mn) {
+              tma_load_2d(b_dst, &tmB, fb, k0, b_row);
+            } else {
+              tma_load_2d(b_dst, &tmB, fb, b_row, k0);
+              tma_load_2d(b_dst + 8192, &tmB, fb, b_row + 64, k0);
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        for (int s = 0; s < kPairStages; ++s)
+          if (issued_mask >> s & 1u)
+            wait_bounded(full0 + 8 * s, issued_parity >> s & 1u, abort_flag, p.timeout_ns,
+                         timeout_code(kRoleProducer, 0x100 + s), false, peer_abort);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t idesc = make_idesc_f16(kPairBM, kPairBN, !p.acc_f16, p.a_mn, p.b_mn);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+        if (!wait_bounded<true>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
+                                timeout_code(kRoleMma, 0x200 + acc), true, peer_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kPairBN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded<true>(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
+                                  timeout_code(kRoleMma, stage), true, peer_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * L::kStageBytes);
+          const uint32_t b_base = a_base + L::kABytes;
+#pragma unroll
+          for (int k = 0; k < kPairBK / 16; ++k) {
+            const uint64_t ad = p.a_mn ? make_sw128_desc(a_base + k * 2048, 8192, 1024)
+                                       : make_sw128_desc(a_base + k * 32, 16, 1024);
+            const uint64_t bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
+                                       : make_sw128_desc(b_base + k * 32, 16, 1024);
+            mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // free the stage in both CTAs
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(tfull0 + 8 * acc, 0x3);  // accumulator ready in both CTAs
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok || *abort_flag) {
+        mma_commit_pair(drain);
+        wait_bounded(drain, 0, abort_flag, p.timeout_ns, timeout_code(kRoleMma, 0x300), false,
+                     peer_abort);
+      }
+    } else if (lane == 0) {
+      // ---------------------------------------------------------- forwarder
+      // Tell the even CTA when this CTA's half of a stage has landed.
+      const uint32_t leader_full0 = mapa_shared(full0, 0);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
+                            timeout_code(kRoleMma, 0x400 + stage), true, peer_abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(leader_full0 + 8 * stage);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const int row_in_tile = static_cast<int>(rank * 128 + quad * 32 + lane);
+    const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = pair; t < p.num_tiles; t += num_pairs) {
+      int tm, tn;
+      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
+                        timeout_code(kRoleEpilogue, acc), true, peer_abort))
+        break;
+      tc_fence_after();
+      const int m = tm * kPairBM + row_in_tile;
+      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN;
+#pragma unroll 1
+      for (int c = 0; c < kPairBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tmem_wait_ld();
+        store_chunk(p, m, tn * kPairBN + c * 32, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer's MMAs or arrivals may touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kPairTmemCols);
+  }
+}
+
+}  // namespace gemm_tn_dev

@@ -21,6 +21,7 @@
 
 #include "../../include/gemm_tn.h"
 #include "gemm_large.cuh"
+#include "gemm_large2.cuh"
 #include "gemm_skinny.cuh"
 
 namespace {
@@ -32,12 +33,14 @@ constexpr int kSkinnyMaxM = 64;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per wait
 
 thread_local int t_last_launches = 0;
+thread_local const char* t_last_kernels = "";
 
 struct DeviceState {
   bool probed = false;
   bool supported = false;
   int num_sms = 0;
   bool attrs_set = false;
+  int max_pairs = 0;  // CTA pairs of gemm_tn_large2_kernel that fit at once
   float* ws = nullptr;
   size_t ws_bytes = 0;
 };
@@ -91,6 +94,19 @@ int device_setup(int dev, DeviceState*& st) {
       e = cudaFuncSetAttribute(gemm_tn_large_kernel<128>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                LargeSmem<128>::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_large2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairSmem::kDynamicBytes);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg;
+      std::memset(&cfg, 0, sizeof cfg);
+      cfg.gridDim = dim3(2 * static_cast<unsigned>(st->num_sms / 2), 1, 1);
+      cfg.blockDim = dim3(kPairThreads, 1, 1);
+      cfg.dynamicSmemBytes = PairSmem::kDynamicBytes;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_large2_kernel, &cfg);
+      st->max_pairs = clusters;
+    }
     if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 16>();
     if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 32>();
     if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 48>();
@@ -175,10 +191,17 @@ int plan(int64_t M, int a_major, int b_major, int accum, int requested) {
 int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
                  const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum,
                  cudaStream_t stream, const gemm_tn_options& o, const DeviceState& st) {
-  const int bn = (o.tile_n == 128) ? 128 : 256;
+  // CTA pairs (256 x 256 tiles) unless the problem is too small to use them
+  // or the caller asked for single-CTA tiles.
+  const bool pair = o.cta_pair == 2 || (o.cta_pair == 0 && M > kLargeBM && N > 128 &&
+                                        st.max_pairs > 0);
+  if (pair && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
+  const int bn = pair ? kPairBN : ((o.tile_n == 128) ? 128 : 256);
+  const int bm = pair ? kPairBM : kLargeBM;
   CUtensorMap tmA, tmB;
   int s = encode_operand(&tmA, A, M, K, ldA, a_major, kLargeBM);
-  if (s == GEMM_TN_OK) s = encode_operand(&tmB, B, N, K, ldB, b_major, static_cast<uint32_t>(bn));
+  if (s == GEMM_TN_OK)
+    s = encode_operand(&tmB, B, N, K, ldB, b_major, static_cast<uint32_t>(pair ? 128 : bn));
   if (s != GEMM_TN_OK) return s;
   LargeArgs p;
   std::memset(&p, 0, sizeof p);
@@ -190,23 +213,31 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   p.acc_f16 = accum == GEMM_TN_ACC_F16;
   p.a_mn = a_major;
   p.b_mn = b_major;
-  p.tiles_m = static_cast<int>((M + kLargeBM - 1) / kLargeBM);
+  p.tiles_m = static_cast<int>((M + bm - 1) / bm);
   p.tiles_n = static_cast<int>((N + bn - 1) / bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.k_blocks = static_cast<int>((K + kLargeBK - 1) / kLargeBK);
-  p.group_m = 16;
+  p.group_m = pair ? 8 : 16;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
-  const int grid = std::min(p.num_tiles, st.num_sms);
-  if (bn == 256) {
-    gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
-        tmA, tmB, p);
+  if (pair) {
+    const int pairs = std::min(p.num_tiles, st.max_pairs);
+    gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(tmA, tmB,
+                                                                                     p);
   } else {
-    gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
-        tmA, tmB, p);
+    const int grid = std::min(p.num_tiles, st.num_sms);
+    if (bn == 256) {
+      gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
+          tmA, tmB, p);
+    } else {
+      gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
+          tmA, tmB, p);
+    }
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = 1;
+  t_last_kernels = pair ? "gemm_tn_large2_kernel"
+                        : (bn == 256 ? "gemm_tn_large_kernel<256>" : "gemm_tn_large_kernel<128>");
   return GEMM_TN_OK;
 }
 
@@ -274,6 +305,7 @@ int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, c
   gemm_tn_splitk_reduce_kernel<<<rblocks, 256, 0, stream>>>(p, static_cast<__half*>(CD), ldC);
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = 2;
+  t_last_kernels = "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel";
   return GEMM_TN_OK;
 }
 
@@ -304,11 +336,12 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64
                            int64_t ldC, int accum_dtype, void* stream,
                            const gemm_tn_options* opts) {
   t_last_launches = 0;
+  t_last_kernels = "";
   gemm_tn_options o;
   std::memset(&o, 0, sizeof o);
   if (opts) o = *opts;
   if (o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
-      (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256))
+      (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) || o.cta_pair < 0 || o.cta_pair > 2)
     return GEMM_TN_ERR_INVALID_ARG;
   int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
   if (s != GEMM_TN_OK) return s;
@@ -350,6 +383,8 @@ GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major, 
 }
 
 GEMM_TN_API int gemm_tn_last_launch_count(void) { return t_last_launches; }
+
+GEMM_TN_API const char* gemm_tn_last_kernels(void) { return t_last_kernels; }
 
 GEMM_TN_API const char* gemm_tn_status_string(int status) {
   switch (status) {
@@ -404,6 +439,7 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
                                                   void* CD, int64_t ldC, int accum_dtype,
                                                   void* stream) {
   t_last_launches = 0;
+  t_last_kernels = "";
   int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
   if (s != GEMM_TN_OK) return s;
   if (M > kSkinnyMaxM || a_major != GEMM_TN_MAJOR_K || b_major != GEMM_TN_MAJOR_K ||
@@ -459,5 +495,6 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   gemm_tn_splitk_reduce_kernel<<<rblocks, 256, 0, cs>>>(p, static_cast<__half*>(CD), ldC);
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = 2;
+  t_last_kernels = "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel";
   return GEMM_TN_OK;
 }

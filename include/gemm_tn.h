@@ -95,7 +95,8 @@ typedef enum {
 typedef enum {
   GEMM_TN_PATH_AUTO = 0,    /* skinny path for M <= 64 with K-major A and B,
                                persistent tile path otherwise */
-  GEMM_TN_PATH_LARGE = 1,   /* persistent 128xBN tile kernel */
+  GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernel: 256x256 tiles on CTA
+                               pairs, or 128xBN tiles on single CTAs */
   GEMM_TN_PATH_SKINNY = 2   /* swapped-operand split-K kernel + reduction;
                                needs M <= 64 and K-major A and B */
 } gemm_tn_path;
@@ -117,6 +118,9 @@ typedef struct {
                            consumer's bounded wait expires and the kernel
                            reports GEMM_TN_ERR_DEVICE_TIMEOUT instead of
                            hanging */
+  int cta_pair;         /* large path: 0 = choose, 1 = single-CTA 128 x tile_n
+                           tiles, 2 = CTA-pair 256 x 256 tiles (two SMs per
+                           tile, tcgen05 cta_group::2; tile_n is ignored) */
 } gemm_tn_options;
 
 /*
@@ -163,6 +167,11 @@ GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major,
 /* Number of kernel launches the last successful gemm_tn / gemm_tn_ex call on
  * this host thread enqueued (0 for the no-op cases). */
 GEMM_TN_API int gemm_tn_last_launch_count(void);
+
+/* Names of the kernels the last successful gemm_tn / gemm_tn_ex /
+ * gemm_tn_skinny_noalloc call on this host thread enqueued, '+'-separated
+ * ("" after a no-op call).  Static storage; never NULL. */
+GEMM_TN_API const char* gemm_tn_last_kernels(void);
 
 /* Static, NUL-terminated name of a gemm_tn_status value. */
 GEMM_TN_API const char* gemm_tn_status_string(int status);

@@ -83,6 +83,7 @@ def call(M=64, N=64, K=64, A=P, ldA=64, am=0, B=P + (1 << 20), ldB=64, bm=0,
 def test_argument_errors_return_before_any_device_work(lib, kw, status):
     assert call(**kw) == status
     assert gb.gemm_tn_last_launch_count() == 0
+    assert gb.gemm_tn_last_kernels() == ""
 
 
 def test_noop_sizes_return_ok_without_a_device(lib):
