@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--cta-pair", type=int, default=0,
+                    help="large path: 0 choose, 1 single-CTA tiles, 2 CTA-pair tiles")
     return ap.parse_args()
 
 
@@ -274,7 +276,8 @@ def run_ours(args):
     A, Bm, CD = A_st.to(dev), B_st.to(dev), C_st.to(dev)
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
-    opts = gb.make_options(tile_n=args.tile_n) if args.tile_n else None
+    opts = (gb.make_options(tile_n=args.tile_n, cta_pair=args.cta_pair)
+            if (args.tile_n or args.cta_pair) else None)
 
     def step(a_ptr=None, b_ptr=None, cd_ptr=None):
         st = gb.gemm_tn_ex(w.M, w.N, w.K, a_ptr or A.data_ptr(), w.ldA, w.a_major,
