@@ -23,10 +23,10 @@
  * All elements are IEEE binary16.
  *
  * C and D share one buffer: each element of C is read before the element of
- * D at the same position is written ("compute C = A*B + C in the original
- * accumulator", page "Reading CuTe's retile_D", section "How the two
- * fragments are handed to the MMA").  There is no alpha/beta; to compute
- * D = A.B^T, zero the buffer first.
+ * D at the same position is written.  (Page "Reading CuTe's retile_D",
+ * section "How the two fragments are handed to the MMA", accumulates the
+ * product onto C in place.)  There is no alpha/beta; to compute D = A.B^T,
+ * zero the buffer first.
  *
  * Accumulation (same page, section "From CuTe's name to the instruction";
  * make_tiled_mma page, section "Fix the matrices and directions first"):
