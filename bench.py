@@ -401,10 +401,14 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 in, f32 accumulate, f16 out",
         "data": "synthetic (seeded uniform [-1,1] fp16 operands, C = 0)",
-        "config": {"workload": f"{w.name}: M=N=K={w.M} TN, A,B K-major, fp32 accumulate, "
-                               "fp16 C/D in place",
+        "config": {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K} TN GEMM, "
+                               f"A {'K' if w.a_major == 0 else 'M'}-major ld {w.ldA}, "
+                               f"B {'K' if w.b_major == 0 else 'N'}-major ld {w.ldB}, "
+                               f"{'fp32' if w.accum == 0 else 'fp16'} accumulate, fp16 C/D in place",
                    "M": w.M, "N": w.N, "K": w.K, "parallelism": f"replicas x{ws}",
-                   "l2": "inputs larger than L2 (A+B+C/D = 384 MiB > 129 MB), no flush",
+                   "l2": (f"inputs larger than L2 (A+B+C/D = {w.min_bytes / 2**20:.0f} MiB "
+                          "> 129 MB), no flush" if w.min_bytes > 129e6 else
+                          "inputs smaller than L2, no flush"),
                    "path": "large" if path == gb.PATH_LARGE else "skinny"},
         "e2e": {"value": ws * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -269,29 +269,47 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t units, int grid) {
 }
 
 // D(m,n) = fp16( sum over the CTAs that touched tile n/128, in CTA order, of
-// their partial (n%128, m)  +  C(m,n) ).  One thread per output element, n
-// fastest so that C and D accesses are coalesced.
-__global__ void __launch_bounds__(256)
+// their partial (n%128, m)  +  C(m,n) ).  One block per tile and one thread
+// per output column n: the thread reads its MP partial sums of each
+// contributing CTA as contiguous 16-byte vectors and then walks m, so that
+// both the partial reads and the C/D accesses (consecutive n across a warp)
+// are coalesced.
+template <int MP>
+__global__ void __launch_bounds__(kSkinnyBN)
     gemm_tn_splitk_reduce_kernel(const SkinnyArgs p, __half* CD, int64_t ldC) {
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<int64_t>(p.M) * p.N) return;
-  const int m = static_cast<int>(idx / p.N);
-  const int n = static_cast<int>(idx - static_cast<int64_t>(m) * p.N);
-  const int tile = n / kSkinnyBN, r = n % kSkinnyBN;
+  const int tile = static_cast<int>(blockIdx.x);
+  const int r = static_cast<int>(threadIdx.x);
+  const int n = tile * kSkinnyBN + r;
+  if (n >= p.N) return;
   const int grid = p.grid;
   const int64_t u0 = static_cast<int64_t>(tile) * p.k_blocks;
   const int c_first = cta_of_unit(u0, p.units, grid);
   const int c_last = cta_of_unit(u0 + p.k_blocks - 1, p.units, grid);
-  float s = 0.f;
+  float acc[MP];
+#pragma unroll
+  for (int m = 0; m < MP; ++m) acc[m] = 0.f;
   for (int c = c_first; c <= c_last; ++c) {
     const int64_t b = unit_begin(p.units, c, grid);
     if (unit_begin(p.units, c + 1, grid) <= b) continue;  // empty range
     const int j = tile - static_cast<int>(b / p.k_blocks);
     const int64_t slot = static_cast<int64_t>(c) * p.max_segs + j;
-    s += p.ws[(slot * kSkinnyBN + r) * p.mp + m];
+    const float4* src = reinterpret_cast<const float4*>(p.ws + (slot * kSkinnyBN + r) * MP);
+#pragma unroll
+    for (int v = 0; v < MP / 4; ++v) {
+      const float4 x = src[v];
+      acc[4 * v] += x.x;
+      acc[4 * v + 1] += x.y;
+      acc[4 * v + 2] += x.z;
+      acc[4 * v + 3] += x.w;
+    }
   }
-  __half* d = CD + static_cast<int64_t>(m) * ldC + n;
-  *d = __float2half_rn(s + __half2float(*d));
+#pragma unroll
+  for (int m = 0; m < MP; ++m) {
+    if (m < p.M) {
+      __half* d = CD + static_cast<int64_t>(m) * ldC + n;
+      *d = __float2half_rn(acc[m] + __half2float(*d));
+    }
+  }
 }
 
 }  // namespace gemm_tn_dev

@@ -9,7 +9,7 @@
 //     built with cuTensorMapEncodeTiled from the driver entry point;
 //   * the choice between the persistent tile kernel and the skinny split-K
 //     kernel, and their grid sizes (one CTA per SM);
-//   * the lazily grown per-device workspace of the skinny path.
+//   * the skinny path's stream-ordered split-K workspace.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -41,8 +41,6 @@ struct DeviceState {
   int num_sms = 0;
   bool attrs_set = false;
   int max_pairs = 0;  // CTA pairs of gemm_tn_large2_kernel that fit at once
-  float* ws = nullptr;
-  size_t ws_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -241,17 +239,34 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   return GEMM_TN_OK;
 }
 
+// Split-K kernel and its reduction for one MMA width MP.
 template <int MP>
-void launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                      const SkinnyArgs& p, cudaStream_t stream) {
+cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const SkinnyArgs& p, __half* CD, int64_t ldC, cudaStream_t stream) {
   gemm_tn_skinny_kernel<kSkinnyStages, MP>
       <<<grid, kSkinnyThreads, SkinnySmem<kSkinnyStages, MP>::kDynamicBytes, stream>>>(tmA, tmB,
                                                                                       p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gemm_tn_splitk_reduce_kernel<MP><<<p.tiles, kSkinnyBN, 0, stream>>>(p, CD, ldC);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_skinny_kernels(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                  const SkinnyArgs& p, void* CD, int64_t ldC,
+                                  cudaStream_t stream) {
+  __half* cd = static_cast<__half*>(CD);
+  switch (p.mp) {
+    case 16: return launch_skinny_mp<16>(grid, tmA, tmB, p, cd, ldC, stream);
+    case 32: return launch_skinny_mp<32>(grid, tmA, tmB, p, cd, ldC, stream);
+    case 48: return launch_skinny_mp<48>(grid, tmA, tmB, p, cd, ldC, stream);
+    default: return launch_skinny_mp<64>(grid, tmA, tmB, p, cd, ldC, stream);
+  }
 }
 
 int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, const void* B,
                   int64_t ldB, void* CD, int64_t ldC, cudaStream_t stream,
-                  const gemm_tn_options& o, DeviceState& st) {
+                  const gemm_tn_options& o, const DeviceState& st) {
   SkinnyArgs p;
   std::memset(&p, 0, sizeof p);
   p.M = static_cast<int>(M);
@@ -271,39 +286,26 @@ int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, c
   p.test_stall = o.test_stall;
 
   const size_t need = static_cast<size_t>(grid) * p.max_segs * kSkinnyBN * p.mp * sizeof(float);
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (st.ws_bytes < need) {
-      if (st.ws) cudaFree(st.ws);
-      st.ws = nullptr;
-      st.ws_bytes = 0;
-      void* w = nullptr;
-      if (cudaMalloc(&w, need) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_TN_ERR_NO_MEMORY;
-      }
-      st.ws = static_cast<float*>(w);
-      st.ws_bytes = need;
-    }
-    p.ws = st.ws;
-  }
 
   CUtensorMap tmA, tmB;
   int s = encode_operand(&tmA, A, M, K, ldA, 0, static_cast<uint32_t>(p.mp));
   if (s == GEMM_TN_OK) s = encode_operand(&tmB, B, N, K, ldB, 0, kSkinnyBN);
   if (s != GEMM_TN_OK) return s;
 
-  switch (p.mp) {
-    case 16: launch_skinny_mp<16>(grid, tmA, tmB, p, stream); break;
-    case 32: launch_skinny_mp<32>(grid, tmA, tmB, p, stream); break;
-    case 48: launch_skinny_mp<48>(grid, tmA, tmB, p, stream); break;
-    default: launch_skinny_mp<64>(grid, tmA, tmB, p, stream); break;
+  // Stream-ordered workspace: concurrent calls on different streams never
+  // share it, and the pool keeps the memory for the next call.
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_NO_MEMORY;
   }
-  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
-  const int64_t outs = M * N;
-  const int rblocks = static_cast<int>((outs + 255) / 256);
-  gemm_tn_splitk_reduce_kernel<<<rblocks, 256, 0, stream>>>(p, static_cast<__half*>(CD), ldC);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  p.ws = static_cast<float*>(ws);
+  const cudaError_t e = launch_skinny_kernels(grid, tmA, tmB, p, CD, ldC, stream);
+  const cudaError_t f = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess || f != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_CUDA;
+  }
   t_last_launches = 2;
   t_last_kernels = "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel";
   return GEMM_TN_OK;
@@ -484,16 +486,10 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   if (s != GEMM_TN_OK) return s;
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  switch (p.mp) {
-    case 16: launch_skinny_mp<16>(grid, tmA, tmB, p, cs); break;
-    case 32: launch_skinny_mp<32>(grid, tmA, tmB, p, cs); break;
-    case 48: launch_skinny_mp<48>(grid, tmA, tmB, p, cs); break;
-    default: launch_skinny_mp<64>(grid, tmA, tmB, p, cs); break;
+  if (launch_skinny_kernels(grid, tmA, tmB, p, CD, ldC, cs) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
-  const int rblocks = static_cast<int>((M * N + 255) / 256);
-  gemm_tn_splitk_reduce_kernel<<<rblocks, 256, 0, cs>>>(p, static_cast<__half*>(CD), ldC);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = 2;
   t_last_kernels = "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel";
   return GEMM_TN_OK;

@@ -37,11 +37,11 @@
  *                    added in fp16: the F16F16F16F16 form.
  *
  * Ownership: the caller owns A, B and CD (device memory); the library never
- * frees or retains caller memory.  The library owns a per-device workspace
- * for the split-K partial sums of the skinny path, created on first use with
- * cudaMalloc and grown when a larger one is needed; it lives until process
- * exit.  A call that needs to create or grow it must not be made during
- * stream capture.
+ * frees or retains caller memory.  The skinny path's split-K partial sums
+ * live in a workspace taken from the current device's default memory pool
+ * with cudaMallocAsync on the call's stream and returned with cudaFreeAsync
+ * on the same stream, so calls on different streams never share it (see
+ * gemm_tn_skinny_noalloc for a variant that allocates nothing).
  *
  * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream).  It returns once the kernels are enqueued; D is
@@ -89,7 +89,8 @@ typedef enum {
   GEMM_TN_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
   GEMM_TN_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel expired;
                                       that launch's D is not valid */
-  GEMM_TN_ERR_NO_MEMORY = 6        /* the workspace could not be allocated */
+  GEMM_TN_ERR_NO_MEMORY = 6        /* the skinny path's workspace could not be
+                                      allocated */
 } gemm_tn_status;
 
 typedef enum {
@@ -192,8 +193,8 @@ GEMM_TN_API const char* gemm_tn_status_string(int status);
  *     device memory, where a library's own cudaMalloc can fail at an
  *     unpredictable moment;
  *   - programs that must fix their device-memory footprint up front.
- * gemm_tn's skinny path keeps its split-K partial sums in a workspace it
- * creates with cudaMalloc on first use.  This entry point computes the same
+ * gemm_tn's skinny path takes its split-K partial sums' workspace from the
+ * device memory pool on every call.  This entry point computes the same
  * thing with the same kernels, but keeps the partial sums in one fixed
  * array of GEMM_TN_NOALLOC_SCRATCH_BYTES compiled into the library, so no
  * call ever allocates or frees device memory.

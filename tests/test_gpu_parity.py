@@ -238,3 +238,33 @@ def test_tensor_front_end_matches_oracle():
     d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), M, 1, np_bits(B_st), K, 0,
                               np_bits(C_st), N)
     check(np_bits(D.cpu()), d64, d16, K, 0, True, "tensor front end")
+
+
+def test_skinny_calls_on_two_streams_do_not_share_scratch():
+    """Two skinny problems enqueued on two streams without ordering between
+    them: each must still match the oracle (each call has its own workspace)."""
+    dev = torch.device("cuda")
+    M, N, K = 16, 4096, 8192
+    probs = []
+    for seed in (71, 81):
+        A_st = wl.operand(M, K, K, 0, "int1", seed)
+        B_st = wl.operand(N, K, K, 0, "int1", seed + 1)
+        C_st = wl.operand(M, N, N, 0, "int4", seed + 2)
+        probs.append((A_st, B_st, C_st, A_st.to(dev), B_st.to(dev), C_st.to(dev)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        outs = []
+        for (A_st, B_st, C_st, A, Bm, C), s in zip(probs, streams):
+            CD = C.clone()
+            torch.cuda.synchronize()
+            outs.append(CD)
+        for (A_st, B_st, C_st, A, Bm, C), s, CD in zip(probs, streams, outs):
+            st = gb.gemm_tn(M, N, K, A.data_ptr(), K, 0, Bm.data_ptr(), K, 0, CD.data_ptr(), N, 0,
+                            s.cuda_stream)
+            assert st == gb.OK
+        torch.cuda.synchronize()
+        for (A_st, B_st, C_st, A, Bm, C), CD in zip(probs, outs):
+            d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), K, 0, np_bits(B_st), K, 0,
+                                      np_bits(C_st), N)
+            check(np_bits(CD.cpu()), d64, d16, K, 0, True, f"two streams rep {rep}")
