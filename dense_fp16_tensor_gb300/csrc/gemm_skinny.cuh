@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const SegIter segs(p.units, blockIdx.x, gridDim.x, p.k_blocks);
+  // The reduction kernel may be scheduled now; it waits for this grid's
+  // completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int nseg = segs.count();
 
   if (threadIdx.x == 0) {
@@ -269,45 +272,47 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t units, int grid) {
 }
 
 // D(m,n) = fp16( sum over the CTAs that touched tile n/128, in CTA order, of
-// their partial (n%128, m)  +  C(m,n) ).  One block per tile and one thread
-// per output column n: the thread reads its MP partial sums of each
-// contributing CTA as contiguous 16-byte vectors and then walks m, so that
-// both the partial reads and the C/D accesses (consecutive n across a warp)
-// are coalesced.
+// their partial (n%128, m)  +  C(m,n) ).  Block (tile, y) has 512 threads;
+// thread (g, r) owns column n = 128*tile + r and rows 4g..4g+3 with
+// g = 4y + threadIdx.x/128, reads one 16-byte vector of partials per
+// contributing CTA, and adds C once.  The kernel is
+// launched as a programmatic dependent of the split-K kernel: its blocks
+// become resident while the split-K kernel runs and wait for its completion
+// (and the visibility of its partial sums) in griddepcontrol.wait.
+constexpr int kReduceThreads = 4 * kSkinnyBN;  // four 4-row groups per block
+
 template <int MP>
-__global__ void __launch_bounds__(kSkinnyBN)
+__global__ void __launch_bounds__(kReduceThreads)
     gemm_tn_splitk_reduce_kernel(const SkinnyArgs p, __half* CD, int64_t ldC) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tile = static_cast<int>(blockIdx.x);
-  const int r = static_cast<int>(threadIdx.x);
+  const int r = static_cast<int>(threadIdx.x) % kSkinnyBN;
+  const int g = 4 * static_cast<int>(blockIdx.y) + static_cast<int>(threadIdx.x) / kSkinnyBN;
   const int n = tile * kSkinnyBN + r;
-  if (n >= p.N) return;
+  if (n >= p.N || 4 * g >= p.M) return;
   const int grid = p.grid;
   const int64_t u0 = static_cast<int64_t>(tile) * p.k_blocks;
   const int c_first = cta_of_unit(u0, p.units, grid);
   const int c_last = cta_of_unit(u0 + p.k_blocks - 1, p.units, grid);
-  float acc[MP];
-#pragma unroll
-  for (int m = 0; m < MP; ++m) acc[m] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c = c_first; c <= c_last; ++c) {
     const int64_t b = unit_begin(p.units, c, grid);
     if (unit_begin(p.units, c + 1, grid) <= b) continue;  // empty range
     const int j = tile - static_cast<int>(b / p.k_blocks);
     const int64_t slot = static_cast<int64_t>(c) * p.max_segs + j;
-    const float4* src = reinterpret_cast<const float4*>(p.ws + (slot * kSkinnyBN + r) * MP);
-#pragma unroll
-    for (int v = 0; v < MP / 4; ++v) {
-      const float4 x = src[v];
-      acc[4 * v] += x.x;
-      acc[4 * v + 1] += x.y;
-      acc[4 * v + 2] += x.z;
-      acc[4 * v + 3] += x.w;
-    }
+    const float4 x = *reinterpret_cast<const float4*>(p.ws + (slot * kSkinnyBN + r) * MP + 4 * g);
+    acc.x += x.x;
+    acc.y += x.y;
+    acc.z += x.z;
+    acc.w += x.w;
   }
+  const float v[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-  for (int m = 0; m < MP; ++m) {
+  for (int j = 0; j < 4; ++j) {
+    const int m = 4 * g + j;
     if (m < p.M) {
       __half* d = CD + static_cast<int64_t>(m) * ldC + n;
-      *d = __float2half_rn(acc[m] + __half2float(*d));
+      *d = __float2half_rn(v[j] + __half2float(*d));
     }
   }
 }

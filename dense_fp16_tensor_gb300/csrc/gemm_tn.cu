@@ -22,6 +22,7 @@
 #include "../../include/gemm_tn.h"
 #include "gemm_large.cuh"
 #include "gemm_large2.cuh"
+#include "gemm_wide.cuh"
 #include "gemm_skinny.cuh"
 
 namespace {
@@ -95,6 +96,9 @@ int device_setup(int dev, DeviceState*& st) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_tn_large2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                PairSmem::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               WideSmem::kDynamicBytes);
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg;
       std::memset(&cfg, 0, sizeof cfg);
@@ -139,6 +143,19 @@ int encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, i
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
+}
+
+// Tensor map over C/D (M,N):(ldC,1) for 32-row x 64-column epilogue boxes
+// with the 128-byte swizzle (the staging layout); out-of-range rows and
+// columns of a stored box are not written.
+int encode_cd(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int64_t ldC) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldC) * 2};
+  cuuint32_t box[2] = {64, 32}, estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
 }
 
@@ -189,15 +206,17 @@ int plan(int64_t M, int a_major, int b_major, int accum, int requested) {
 int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
                  const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum,
                  cudaStream_t stream, const gemm_tn_options& o, const DeviceState& st) {
-  // CTA pairs (256 x 256 tiles) unless the problem is too small to use them
-  // or the caller asked for single-CTA tiles.
-  const bool pair = o.cta_pair == 2 || (o.cta_pair == 0 && M > kLargeBM && N > 128 &&
-                                        st.max_pairs > 0);
-  if (pair && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
-  const int bn = pair ? kPairBN : ((o.tile_n == 128) ? 128 : 256);
-  const int bm = pair ? kPairBM : kLargeBM;
+  // Kernel choice: 256 x 256 single-CTA tiles (fewest operand bytes per
+  // flop per SM) unless the problem is too small to fill them or the caller
+  // asked for another tile kernel.
+  int kind = o.tile_kernel;
+  if (kind == 0) kind = (M > kLargeBM && N > 128) ? 3 : 1;
+  if (kind == 2 && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
+  const bool pair = kind == 2, wide = kind == 3;
+  const int bn = (pair || wide) ? 256 : ((o.tile_n == 128) ? 128 : 256);
+  const int bm = (pair || wide) ? 256 : kLargeBM;
   CUtensorMap tmA, tmB;
-  int s = encode_operand(&tmA, A, M, K, ldA, a_major, kLargeBM);
+  int s = encode_operand(&tmA, A, M, K, ldA, a_major, wide ? 256 : kLargeBM);
   if (s == GEMM_TN_OK)
     s = encode_operand(&tmB, B, N, K, ldB, b_major, static_cast<uint32_t>(pair ? 128 : bn));
   if (s != GEMM_TN_OK) return s;
@@ -215,10 +234,17 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   p.tiles_n = static_cast<int>((N + bn - 1) / bn);
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.k_blocks = static_cast<int>((K + kLargeBK - 1) / kLargeBK);
-  p.group_m = pair ? 8 : 16;
+  p.group_m = (pair || wide) ? 8 : 16;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
-  if (pair) {
+  if (wide) {
+    CUtensorMap tmD;
+    s = encode_cd(&tmD, CD, M, N, ldC);
+    if (s != GEMM_TN_OK) return s;
+    const int grid = std::min(p.num_tiles, st.num_sms);
+    gemm_tn_wide_kernel<<<grid, kWideThreads, WideSmem::kDynamicBytes, stream>>>(tmA, tmB, tmD,
+                                                                               p);
+  } else if (pair) {
     const int pairs = std::min(p.num_tiles, st.max_pairs);
     gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(tmA, tmB,
                                                                                      p);
@@ -234,7 +260,8 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = 1;
-  t_last_kernels = pair ? "gemm_tn_large2_kernel"
+  t_last_kernels = wide ? "gemm_tn_wide_kernel"
+                 : pair ? "gemm_tn_large2_kernel"
                         : (bn == 256 ? "gemm_tn_large_kernel<256>" : "gemm_tn_large_kernel<128>");
   return GEMM_TN_OK;
 }
@@ -248,7 +275,19 @@ cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap
                                                                                       p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  gemm_tn_splitk_reduce_kernel<MP><<<p.tiles, kSkinnyBN, 0, stream>>>(p, CD, ldC);
+  // programmatic dependent launch: resident early, waits in griddepcontrol.wait
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles), MP / 16, 1);
+  cfg.blockDim = dim3(kReduceThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_tn_splitk_reduce_kernel<MP>, p, CD, ldC);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -343,7 +382,8 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64
   std::memset(&o, 0, sizeof o);
   if (opts) o = *opts;
   if (o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
-      (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) || o.cta_pair < 0 || o.cta_pair > 2)
+      (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) || o.tile_kernel < 0 ||
+      o.tile_kernel > 3)
     return GEMM_TN_ERR_INVALID_ARG;
   int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
   if (s != GEMM_TN_OK) return s;

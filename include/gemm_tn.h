@@ -96,8 +96,8 @@ typedef enum {
 typedef enum {
   GEMM_TN_PATH_AUTO = 0,    /* skinny path for M <= 64 with K-major A and B,
                                persistent tile path otherwise */
-  GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernel: 256x256 tiles on CTA
-                               pairs, or 128xBN tiles on single CTAs */
+  GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernels: 256x256 tiles on one
+                               CTA or on a CTA pair, or 128xBN tiles */
   GEMM_TN_PATH_SKINNY = 2   /* swapped-operand split-K kernel + reduction;
                                needs M <= 64 and K-major A and B */
 } gemm_tn_path;
@@ -119,9 +119,11 @@ typedef struct {
                            consumer's bounded wait expires and the kernel
                            reports GEMM_TN_ERR_DEVICE_TIMEOUT instead of
                            hanging */
-  int cta_pair;         /* large path: 0 = choose, 1 = single-CTA 128 x tile_n
+  int tile_kernel;      /* large path: 0 = choose (3 when M and N exceed 128,
+                           else 1), 1 = single-CTA 128 x tile_n
                            tiles, 2 = CTA-pair 256 x 256 tiles (two SMs per
-                           tile, tcgen05 cta_group::2; tile_n is ignored) */
+                           tile, tcgen05 cta_group::2), 3 = single-CTA
+                           256 x 256 tiles (tile_n is ignored by 2 and 3) */
 } gemm_tn_options;
 
 /*

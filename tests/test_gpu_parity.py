@@ -105,12 +105,17 @@ def test_large_8192_sampled_and_full():
 SWEEP = [1, 15, 16, 17, 63, 127, 129, 200]
 
 
-@pytest.mark.parametrize("cta_pair", [1, 2])
+KERNEL_NAMES = {1: "gemm_tn_large_kernel<256>", 2: "gemm_tn_large2_kernel",
+                3: "gemm_tn_wide_kernel"}
+
+
+@pytest.mark.parametrize("tile_kernel", [1, 2, 3])
 @pytest.mark.parametrize("accum", [0, 1])
 @pytest.mark.parametrize("a_major,b_major", [(0, 0), (1, 0), (0, 1), (1, 1)])
-def test_ragged_sweep(accum, a_major, b_major, cta_pair):
-    """Tails in M, N and K across both majors and both tile kernels (single
-    CTA 128x256, CTA pair 256x256), integer values: bit-exact."""
+def test_ragged_sweep(accum, a_major, b_major, tile_kernel):
+    """Tails in M, N and K across both majors and every tile kernel (single
+    CTA 128x256, CTA pair 256x256, single CTA 256x256), integer values:
+    bit-exact."""
     rng = np.random.default_rng(100 + 10 * accum + 2 * a_major + b_major)
     cases = [(M, N, K) for M in (1, 17, 129, 200) for N in (1, 16, 129, 300)
              for K in (1, 15, 64, 129)]
@@ -123,18 +128,18 @@ def test_ragged_sweep(accum, a_major, b_major, cta_pair):
         B_st = wl.operand(N, K, ldB, b_major, "int2", int(rng.integers(1 << 30)))
         C_st = wl.operand(M, N, ldC, 0, "int4", int(rng.integers(1 << 30)), poison=False)
         D_st, st = run_gpu(M, N, K, A_st, ldA, a_major, B_st, ldB, b_major, C_st, ldC, accum,
-                           opts={"path": gb.PATH_LARGE, "cta_pair": cta_pair}, guard_rows=2)
+                           opts={"path": gb.PATH_LARGE, "tile_kernel": tile_kernel},
+                           guard_rows=2)
         assert st == gb.OK, (M, N, K, gb.gemm_tn_status_string(st))
-        assert gb.gemm_tn_last_kernels() == ("gemm_tn_large2_kernel" if cta_pair == 2
-                                             else "gemm_tn_large_kernel<256>")
+        assert gb.gemm_tn_last_kernels() == KERNEL_NAMES[tile_kernel]
         d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), ldA, a_major, np_bits(B_st), ldB,
                                   b_major, np_bits(C_st), ldC)
         check(result_view(D_st, M, N), d64, d16, K, accum, True, f"{M}x{N}x{K}")
         slack_untouched(D_st, C_st, N)
 
 
-@pytest.mark.parametrize("tile_n,cta_pair", [(128, 1), (256, 1), (256, 2)])
-def test_large_path_real_values_both_tiles(tile_n, cta_pair):
+@pytest.mark.parametrize("tile_n,tile_kernel", [(128, 1), (256, 1), (256, 2), (256, 3)])
+def test_large_path_real_values_every_tile_kernel(tile_n, tile_kernel):
     M, N, K = 300, 520, 700
     ldA, ldB = K + 12, N + 8
     A_st = wl.operand(M, K, ldA, 0, "u11", 11)
@@ -143,7 +148,7 @@ def test_large_path_real_values_both_tiles(tile_n, cta_pair):
     for accum in (0, 1):
         D_st, st = run_gpu(M, N, K, A_st, ldA, 0, B_st, ldB, 1, C_st, N, accum,
                            opts={"path": gb.PATH_LARGE, "tile_n": tile_n,
-                                 "cta_pair": cta_pair})
+                                 "tile_kernel": tile_kernel})
         assert st == gb.OK, gb.gemm_tn_status_string(st)
         d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), ldA, 0, np_bits(B_st), ldB, 1,
                                   np_bits(C_st), N)
@@ -210,14 +215,15 @@ def test_bounded_wait_expires_and_reports_instead_of_hanging():
     A_st = wl.operand(M, K, K, 0, "int1", 41)
     B_st = wl.operand(N, K, K, 0, "int1", 42)
     C_st = wl.operand(M, N, N, 0, "int4", 43)
-    for path, m, pair in ((gb.PATH_LARGE, M, 1), (gb.PATH_LARGE, M, 2), (gb.PATH_SKINNY, 16, 0)):
+    for path, m, pair in ((gb.PATH_LARGE, M, 1), (gb.PATH_LARGE, M, 2), (gb.PATH_LARGE, M, 3),
+                          (gb.PATH_SKINNY, 16, 0)):
         _, st = run_gpu(m, N, K, A_st, K, 0, B_st, K, 0, C_st, N, 0,
                         opts={"path": path, "test_stall": 1, "timeout_ns": 20_000_000,
-                              "sync_check": 1, "cta_pair": pair})
+                              "sync_check": 1, "tile_kernel": pair})
         assert st == gb.ERR_DEVICE_TIMEOUT, gb.gemm_tn_status_string(st)
         assert gb.gemm_tn_check_device_error(torch.cuda.current_stream().cuda_stream)[0] == gb.OK
         D_st, st = run_gpu(m, N, K, A_st, K, 0, B_st, K, 0, C_st, N, 0,
-                           opts={"path": path, "sync_check": 1, "cta_pair": pair})
+                           opts={"path": path, "sync_check": 1, "tile_kernel": pair})
         assert st == gb.OK
         d64, d16 = oracle.gemm_tn(m, N, K, np_bits(A_st), K, 0, np_bits(B_st), K, 0,
                                   np_bits(C_st), N)
