@@ -393,6 +393,7 @@ def run_ours(args):
     extra = {}
     if not args.no_extra and w.name != "skinny":
         extra["skinny_m16"] = bench_skinny(dev, stream)
+        extra["strided_4096"] = bench_strided(dev, stream)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -467,6 +468,45 @@ def bench_skinny(dev, stream, steps=200):
             "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": kind,
             "launches_per_call": 2, "calls": steps,
             "l2": "B (512 MiB) larger than L2, calls back to back"}
+
+
+def bench_strided(dev, stream, steps=20):
+    """General-stride path (gemm_tn_strided, copy producer) on M=N=K=4096 with
+    leading dimensions K+1 (not TMA-expressible), fp32 accumulation."""
+    import torch
+
+    from dense_fp16_tensor_gb300 import binding as gb
+    from dense_fp16_tensor_gb300 import workloads as wl
+    M = N = K = 4096
+    ld = K + 1
+    A = wl.draw((M * ld,), "u11", 7001).to(dev)
+    Bm = wl.draw((N * ld,), "u11", 7002).to(dev)
+    CD = torch.zeros(M * (N + 1), dtype=torch.float16, device=dev)
+    sp = stream.cuda_stream
+
+    def step():
+        st = gb.gemm_tn_strided(M, N, K, A.data_ptr(), ld, 1, Bm.data_ptr(), ld, 1,
+                                CD.data_ptr(), N + 1, 1, 0, sp)
+        if st != gb.OK:
+            raise gb.GemmTnError(st)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    peaks, kind = load_peaks()
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    return {"workload": "M=N=K=4096, ld = K+1 (A, B), ldC = N+1, fp32 accumulate",
+            "kernel": "gemm_tn_strided_kernel", "ms_per_call": ms, "TFLOP_per_s": tf,
+            "frac_of_peak": tf / float(peaks["bf16_tflops"]), "peak_kind": kind}
 
 
 def main():

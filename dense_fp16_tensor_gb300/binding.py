@@ -28,7 +28,7 @@ ERR_NO_MEMORY = 6
 # Every symbol declared in include/gemm_tn.h.
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
             "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc",
-            "gemm_tn_last_kernels")
+            "gemm_tn_last_kernels", "gemm_tn_strided")
 
 # Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_tn_last_launch_count.argtypes = []
         L.gemm_tn_status_string.restype = ctypes.c_char_p
         L.gemm_tn_status_string.argtypes = [i32]
+        L.gemm_tn_strided.restype = i32
+        L.gemm_tn_strided.argtypes = [i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
+                                      i32, vp]
         L.gemm_tn_last_kernels.restype = ctypes.c_char_p
         L.gemm_tn_last_kernels.argtypes = []
         L.gemm_tn_skinny_noalloc.restype = i32
@@ -124,6 +127,13 @@ def gemm_tn_plan_path(M, N, K, a_major, b_major) -> int:
 
 def gemm_tn_last_launch_count() -> int:
     return lib().gemm_tn_last_launch_count()
+
+
+def gemm_tn_strided(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype,
+                    stream) -> int:
+    """C ``gemm_tn_strided``: operands as pointers plus element strides."""
+    return lib().gemm_tn_strided(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype,
+                                 stream)
 
 
 def gemm_tn_last_kernels() -> str:

@@ -24,6 +24,7 @@
 #include "gemm_large2.cuh"
 #include "gemm_wide.cuh"
 #include "gemm_skinny.cuh"
+#include "gemm_strided.cuh"
 
 namespace {
 
@@ -99,6 +100,9 @@ int device_setup(int dev, DeviceState*& st) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_tn_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                WideSmem::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_strided_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               StridedSmem::kDynamicBytes);
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg;
       std::memset(&cfg, 0, sizeof cfg);
@@ -532,5 +536,93 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   }
   t_last_launches = 2;
   t_last_kernels = "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel";
+  return GEMM_TN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// General element strides (copy-producer kernel).
+
+namespace {
+
+// Byte range touched by a (rows, cols) view with element strides (s_r, s_c).
+void extent_strided(const void* p, int64_t rows, int64_t cols, int64_t s_r, int64_t s_c,
+                    uintptr_t& lo, uintptr_t& hi) {
+  lo = reinterpret_cast<uintptr_t>(p);
+  hi = lo + static_cast<uintptr_t>(((rows - 1) * s_r + (cols - 1) * s_c + 1) * 2);
+}
+
+// No two coordinates of the (rows, cols) view share an element.
+bool injective2(int64_t rows, int64_t cols, int64_t s_r, int64_t s_c) {
+  if (rows <= 1 && cols <= 1) return true;
+  if (rows <= 1) return s_c >= 1;
+  if (cols <= 1) return s_r >= 1;
+  if (s_r < 1 || s_c < 1) return false;
+  return s_r >= s_c * cols || s_c >= s_r * rows;
+}
+
+}  // namespace
+
+extern "C" GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K, const void* A,
+                                           int64_t sAm, int64_t sAk, const void* B, int64_t sBn,
+                                           int64_t sBk, void* CD, int64_t sCm, int64_t sCn,
+                                           int accum_dtype, void* stream) {
+  t_last_launches = 0;
+  t_last_kernels = "";
+  const int64_t kMax = 0x7FFFFFFF;
+  if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM_TN_ERR_INVALID_ARG;
+  if (sAm < 0 || sAk < 0 || sBn < 0 || sBk < 0 || sCm < 0 || sCn < 0)
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (accum_dtype != GEMM_TN_ACC_F32 && accum_dtype != GEMM_TN_ACC_F16)
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_TN_OK;
+  if (CD == nullptr || !injective2(M, N, sCm, sCn)) return GEMM_TN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(CD) & 1u) return GEMM_TN_ERR_ALIGNMENT;
+  if (K == 0) return GEMM_TN_OK;  // D = C
+  if (A == nullptr || B == nullptr) return GEMM_TN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u)
+    return GEMM_TN_ERR_ALIGNMENT;
+  uintptr_t a0, a1, b0, b1, c0, c1;
+  extent_strided(A, M, K, sAm, sAk, a0, a1);
+  extent_strided(B, N, K, sBn, sBk, b0, b1);
+  extent_strided(CD, M, N, sCm, sCn, c0, c1);
+  if ((c0 < a1 && a0 < c1) || (c0 < b1 && b0 < c1)) return GEMM_TN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  DeviceState* st = nullptr;
+  int s;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    s = device_setup(dev, st);
+  }
+  if (s != GEMM_TN_OK) return s;
+
+  StridedArgs p;
+  std::memset(&p, 0, sizeof p);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.A = static_cast<const __half*>(A);
+  p.sAm = sAm;
+  p.sAk = sAk;
+  p.B = static_cast<const __half*>(B);
+  p.sBn = sBn;
+  p.sBk = sBk;
+  p.CD = static_cast<__half*>(CD);
+  p.sCm = sCm;
+  p.sCn = sCn;
+  p.acc_f16 = accum_dtype == GEMM_TN_ACC_F16;
+  p.tiles_m = static_cast<int>((M + kStrBM - 1) / kStrBM);
+  p.tiles_n = static_cast<int>((N + kStrBN - 1) / kStrBN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.k_blocks = static_cast<int>((K + kStrBK - 1) / kStrBK);
+  p.group_m = 16;
+  p.timeout_ns = kDefaultTimeoutNs;
+  const int grid = std::min(p.num_tiles, st->num_sms);
+  gemm_tn_strided_kernel<<<grid, kStrThreads, StridedSmem::kDynamicBytes,
+                           static_cast<cudaStream_t>(stream)>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  t_last_launches = 1;
+  t_last_kernels = "gemm_tn_strided_kernel";
   return GEMM_TN_OK;
 }

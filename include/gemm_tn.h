@@ -156,6 +156,29 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
                            int accum_dtype, void* stream,
                            const gemm_tn_options* opts);
 
+/*
+ * D = C + A.B^T for operand views with arbitrary element strides (the layout
+ * page, sections 1-2: a matrix is any shape:stride view; neither mode needs
+ * to be stride-1):
+ *   A(m,k) = A[m*sAm + k*sAk],  B(n,k) = B[n*sBn + k*sBk],
+ *   C/D(m,n) = CD[m*sCm + n*sCn]     (strides in elements, all >= 0)
+ * The accumulation modes and in-place semantics are those of gemm_tn.
+ * Always runs the copy-producer kernel (threads gather 16-byte K chunks into
+ * shared memory instead of TMA), so it accepts layouts gemm_tn rejects:
+ * leading dimensions that are not multiples of 8, pointers that are only
+ * 2-byte aligned, and views with no stride-1 mode; gemm_tn is faster when
+ * its requirements hold.
+ * Errors: GEMM_TN_ERR_INVALID_ARG for negative sizes or strides, NULL with a
+ * nonzero extent, a C/D view in which two coordinates share an element, or
+ * C/D overlapping A or B; GEMM_TN_ERR_ALIGNMENT for a pointer that is not
+ * 2-byte aligned.  M == 0, N == 0 or K == 0 enqueue nothing.
+ */
+GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K,
+                                const void* A, int64_t sAm, int64_t sAk,
+                                const void* B, int64_t sBn, int64_t sBk,
+                                void* CD, int64_t sCm, int64_t sCn,
+                                int accum_dtype, void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word that a
  * kernel sets when one of its bounded waits expires.  Returns GEMM_TN_OK,
  * GEMM_TN_ERR_DEVICE_TIMEOUT (and, if detail != NULL, the raw word: bits

@@ -72,6 +72,9 @@ def _load():
         lib.oracle_gemm_tn.restype = i32
         lib.oracle_gemm_tn.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64, i32,
                                        vp, i64, vp, vp, i32]
+        lib.oracle_gemm_tn_strided.restype = i32
+        lib.oracle_gemm_tn_strided.argtypes = [i64, i64, i64, vp, i64, i64, vp, i64, i64,
+                                               vp, i64, i64, vp, vp, i32]
         lib.oracle_gemm_tn_sampled.restype = i32
         lib.oracle_gemm_tn_sampled.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64,
                                                i32, vp, i64, i64, vp, vp, vp, vp, i32]
@@ -195,6 +198,35 @@ def gemm_tn(M, N, K, A, ldA, a_major, B, ldB, b_major, C=None, ldC=None,
     lib.oracle_gemm_tn(M, N, K, _ptr(A), ldA, a_major, _ptr(B), ldB, b_major,
                        _ptr(C), ldC or 0, _ptr(d64), _ptr(d16),
                        nthreads or default_threads())
+    return d64, d16
+
+
+def _check_strided(rows, cols, X, s_r, s_c, name):
+    if rows == 0 or cols == 0:
+        return
+    if s_r < 0 or s_c < 0:
+        raise ValueError(f"{name}: negative strides are not supported")
+    need = (rows - 1) * s_r + (cols - 1) * s_c + 1
+    if X.size < need:
+        raise ValueError(f"{name}: storage holds {X.size} elements, view needs {need}")
+
+
+def gemm_tn_strided(M, N, K, A, sAm, sAk, B, sBn, sBk, C=None, sCm=0, sCn=1, want_f16=True,
+                    nthreads=None):
+    """Full D = C + A.B^T over arbitrary element strides:
+    A(m,k) = A[m*sAm + k*sAk], B(n,k) = B[n*sBn + k*sBk], C(m,n) = C[m*sCm + n*sCn].
+    Returns ``(d64, d16bits)`` like :func:`gemm_tn`."""
+    lib = _load()
+    A, B = _bits(A), _bits(B)
+    C = None if C is None else _bits(C)
+    _check_strided(M, K, A, sAm, sAk, "A")
+    _check_strided(N, K, B, sBn, sBk, "B")
+    if C is not None:
+        _check_strided(M, N, C, sCm, sCn, "C")
+    d64 = np.empty((M, N), np.float64)
+    d16 = np.empty((M, N), np.uint16) if want_f16 else None
+    lib.oracle_gemm_tn_strided(M, N, K, _ptr(A), sAm, sAk, _ptr(B), sBn, sBk, _ptr(C), sCm,
+                               sCn, _ptr(d64), _ptr(d16), nthreads or default_threads())
     return d64, d16
 
 

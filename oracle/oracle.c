@@ -256,12 +256,36 @@ static int run_threads(job_t* proto, int nthreads, int64_t total, int sampled) {
 }
 
 /*
- * Full oracle.  A, B, C are raw binary16 bit patterns.
- *   A(m,k): a_major 0 -> A[m*ldA + k], a_major 1 -> A[m + k*ldA]
- *   B(n,k): b_major 0 -> B[n*ldB + k], b_major 1 -> B[n + k*ldB]
- *   C(m,n): C[m*ldC + n]; C may be NULL (treated as zero).
+ * Full oracle over arbitrary element strides ("CuTe Layout to Tensor Core",
+ * sections 1-2: an operand is a pointer plus a shape:stride layout, and no
+ * mode has to be stride-1).  A, B, C are raw binary16 bit patterns:
+ *   A(m,k) = A[m*sAm + k*sAk],  B(n,k) = B[n*sBn + k*sBk],
+ *   C(m,n) = C[m*sCm + n*sCn]   (C may be NULL: treated as zero).
  * out_f64 / out_f16 are (M,N) row-major (either may be NULL).
  * Returns the number of threads used.
+ */
+ORACLE_EXPORT int oracle_gemm_tn_strided(int64_t M, int64_t N, int64_t K,
+                                         const uint16_t* A, int64_t sAm, int64_t sAk,
+                                         const uint16_t* B, int64_t sBn, int64_t sBk,
+                                         const uint16_t* C, int64_t sCm, int64_t sCn,
+                                         double* out_f64, uint16_t* out_f16, int nthreads) {
+  job_t j;
+  memset(&j, 0, sizeof j);
+  j.M = M; j.N = N; j.K = K;
+  j.A = A; j.B = B; j.C = C;
+  view2_t va = {M, K, sAm, sAk}, vb = {N, K, sBn, sBk}, vc = {M, N, sCm, sCn};
+  j.vA = va; j.vB = vb; j.vC = vc;
+  j.lut = half_lut();
+  j.out_f64 = out_f64;
+  j.out_f16 = out_f16;
+  return run_threads(&j, nthreads, M, 0);
+}
+
+/*
+ * Full oracle for (ptr, ld, major) operands -- the strided oracle with
+ *   A(m,k): a_major 0 -> A[m*ldA + k], a_major 1 -> A[m + k*ldA]
+ *   B(n,k): b_major 0 -> B[n*ldB + k], b_major 1 -> B[n + k*ldB]
+ *   C(m,n): C[m*ldC + n].
  */
 ORACLE_EXPORT int oracle_gemm_tn(int64_t M, int64_t N, int64_t K,
                                  const uint16_t* A, int64_t ldA, int a_major,
@@ -269,17 +293,9 @@ ORACLE_EXPORT int oracle_gemm_tn(int64_t M, int64_t N, int64_t K,
                                  const uint16_t* C, int64_t ldC,
                                  double* out_f64, uint16_t* out_f16,
                                  int nthreads) {
-  job_t j;
-  memset(&j, 0, sizeof j);
-  j.M = M; j.N = N; j.K = K;
-  j.A = A; j.B = B; j.C = C;
-  j.vA = make_view(M, K, ldA, a_major);
-  j.vB = make_view(N, K, ldB, b_major);
-  j.vC = make_view(M, N, ldC, 0);
-  j.lut = half_lut();
-  j.out_f64 = out_f64;
-  j.out_f16 = out_f16;
-  return run_threads(&j, nthreads, M, 0);
+  view2_t va = make_view(M, K, ldA, a_major), vb = make_view(N, K, ldB, b_major);
+  return oracle_gemm_tn_strided(M, N, K, A, va.s_row, va.s_col, B, vb.s_row, vb.s_col, C, ldC, 1,
+                                out_f64, out_f16, nthreads);
 }
 
 /* Sampled oracle: out[s] = D(sm[s], sn[s]) for s < count (same definition). */

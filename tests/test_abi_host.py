@@ -107,3 +107,31 @@ def test_tensor_front_end_major_inference():
     assert operand_view(st[:, :20], "A") == (gb.MAJOR_K, 32)   # padded ld
     with pytest.raises(ValueError):
         operand_view(torch.zeros(8, 8, 2, dtype=torch.float16)[:, :, 0], "A")
+
+
+def scall(M=64, N=64, K=64, A=P, sAm=64, sAk=1, B=P + (1 << 20), sBn=64, sBk=1,
+          CD=P + (2 << 20), sCm=64, sCn=1, acc=0):
+    return gb.gemm_tn_strided(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, acc, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), gb.ERR_INVALID_ARG),
+    (dict(sAk=-1), gb.ERR_INVALID_ARG),
+    (dict(sCm=0), gb.ERR_INVALID_ARG),               # two rows of D on the same elements
+    (dict(sCm=32, sCn=1), gb.ERR_INVALID_ARG),       # rows of 64 overlap with stride 32
+    (dict(sCm=1, sCn=1), gb.ERR_INVALID_ARG),
+    (dict(CD=P), gb.ERR_INVALID_ARG),                # overlaps A
+    (dict(A=0), gb.ERR_INVALID_ARG),
+    (dict(acc=2), gb.ERR_INVALID_ARG),
+    (dict(A=P + 1), gb.ERR_ALIGNMENT),               # fp16 needs 2-byte alignment
+    (dict(CD=P + (2 << 20) + 3), gb.ERR_ALIGNMENT),
+])
+def test_strided_argument_errors(lib, kw, status):
+    assert scall(**kw) == status
+    assert gb.gemm_tn_last_launch_count() == 0
+
+
+def test_strided_noop_sizes(lib):
+    assert scall(M=0) == gb.OK
+    assert scall(K=0, A=0, B=0) == gb.OK
+    assert scall(M=1, sCm=0, K=0) == gb.OK  # one row: a zero row stride is fine

@@ -229,3 +229,64 @@ def test_degenerate_sizes():
     d, _ = oracle.gemm_tn(0, 4, 5, np.zeros(0, np.float16), 5, K_MAJOR,
                           rnd((4, 5), 51).reshape(-1), 5, K_MAJOR, None, 4)
     assert d.shape == (0, 4)
+
+
+# ----------------------------------------------------------------------------
+# general element strides ("CuTe Layout to Tensor Core", sections 1-2)
+
+def test_strided_matches_gathered_copy_with_no_unit_stride():
+    """A view with neither mode stride-1 equals the product of its gathered
+    (numpy fancy-indexed) contiguous copy: a library gather, not the loop."""
+    rng = np.random.default_rng(60)
+    M, N, K = 21, 13, 37
+    sAm, sAk, sBn, sBk, sCm, sCn = 3 * 2 * K + 5, 3, 2, 2 * N + 7, 1, M + 9
+    XA = h(rng.uniform(-1, 1, (M - 1) * sAm + (K - 1) * sAk + 1))
+    XB = h(rng.uniform(-1, 1, (N - 1) * sBn + (K - 1) * sBk + 1))
+    XC = h(rng.uniform(-1, 1, (M - 1) * sCm + (N - 1) * sCn + 1))
+    d, d16 = oracle.gemm_tn_strided(M, N, K, XA, sAm, sAk, XB, sBn, sBk, XC, sCm, sCn)
+    a = XA[np.arange(M)[:, None] * sAm + np.arange(K)[None, :] * sAk]
+    b = XB[np.arange(N)[:, None] * sBn + np.arange(K)[None, :] * sBk]
+    c = XC[np.arange(M)[:, None] * sCm + np.arange(N)[None, :] * sCn]
+    d_ref, _ = run(a, b, c)
+    assert np.array_equal(d, d_ref)
+    assert np.allclose(d, a.astype(np.float64) @ b.astype(np.float64).T + c.astype(np.float64),
+                       rtol=1e-12, atol=1e-12)
+
+
+def test_strided_equals_ld_major_form():
+    rng = np.random.default_rng(61)
+    M, N, K = 19, 23, 41
+    A = h(rng.uniform(-1, 1, (M, K)))
+    B = h(rng.uniform(-1, 1, (N, K)))
+    C = h(rng.uniform(-1, 1, (M, N)))
+    sa = storage(A, MN_MAJOR, M + 3)
+    sb = storage(B, K_MAJOR, K + 5)
+    d1, _ = oracle.gemm_tn(M, N, K, sa, M + 3, MN_MAJOR, sb, K + 5, K_MAJOR, C.reshape(-1), N)
+    d2, _ = oracle.gemm_tn_strided(M, N, K, sa, 1, M + 3, sb, K + 5, 1, C.reshape(-1), N, 1)
+    assert np.array_equal(d1, d2)
+
+
+def test_broadcast_rows_closed_form():
+    """Stride 0 along M repeats one row of A: every row of D is C's row plus
+    the same vector B.a (computed here by BLAS)."""
+    rng = np.random.default_rng(62)
+    M, N, K = 7, 11, 29
+    a_row = h(rng.uniform(-1, 1, K))
+    B = h(rng.uniform(-1, 1, (N, K)))
+    C = h(rng.uniform(-1, 1, (M, N)))
+    d, _ = oracle.gemm_tn_strided(M, N, K, a_row, 0, 1, B.reshape(-1), K, 1, C.reshape(-1), N, 1)
+    v = B.astype(np.float64) @ a_row.astype(np.float64)
+    assert np.allclose(d, C.astype(np.float64) + v[None, :], rtol=1e-12, atol=1e-12)
+
+
+def test_column_major_d_is_the_transpose_layout():
+    rng = np.random.default_rng(63)
+    M, N, K = 9, 6, 17
+    A = h(rng.integers(-2, 3, (M, K)))
+    B = h(rng.integers(-2, 3, (N, K)))
+    C = h(rng.integers(-4, 5, (M, N)))
+    CT = np.ascontiguousarray(C.T)  # C/D stored column-major: C(m,n) at n*M + m
+    d, _ = oracle.gemm_tn_strided(M, N, K, A.reshape(-1), K, 1, B.reshape(-1), K, 1,
+                                  CT.reshape(-1), 1, M)
+    want = _brute(A, B, C)
+    assert all(Fraction(d[i, j]) == want[i, j] for i in range(M) for j in range(N))
