@@ -505,7 +505,7 @@ def bench_strided(dev, stream, steps=20):
     peaks, kind = load_peaks()
     tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     return {"workload": "M=N=K=4096, ld = K+1 (A, B), ldC = N+1, fp32 accumulate",
-            "kernel": "gemm_tn_strided_kernel", "ms_per_call": ms, "TFLOP_per_s": tf,
+            "kernels": gb.gemm_tn_last_kernels(), "ms_per_call": ms, "TFLOP_per_s": tf,
             "frac_of_peak": tf / float(peaks["bf16_tflops"]), "peak_kind": kind}
 
 

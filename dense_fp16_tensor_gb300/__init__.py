@@ -10,7 +10,7 @@ from ._build import build  # noqa: F401
 from .binding import (ACC_F16, ACC_F32, MAJOR_K, MAJOR_MN, PATH_AUTO, PATH_LARGE,  # noqa: F401
                       PATH_SKINNY, GemmTnError, gemm_tn, gemm_tn_check_device_error,
                       gemm_tn_ex, gemm_tn_last_kernels, gemm_tn_last_launch_count, gemm_tn_plan_path,
-                      gemm_tn_status_string, gemm_tn_strided, library_path,
+                      gemm_tn_status_string, gemm_tn_strided, gemm_tn_strided_ex, library_path,
                       make_options)
 
 

@@ -16,6 +16,7 @@ from . import _build
 MAJOR_K, MAJOR_MN = 0, 1
 ACC_F32, ACC_F16 = 0, 1
 PATH_AUTO, PATH_LARGE, PATH_SKINNY = 0, 1, 2
+PATH_STRIDED_COPY, PATH_STRIDED_REPACK = 3, 4
 
 OK = 0
 ERR_INVALID_ARG = 1
@@ -28,7 +29,7 @@ ERR_NO_MEMORY = 6
 # Every symbol declared in include/gemm_tn.h.
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
             "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc",
-            "gemm_tn_last_kernels", "gemm_tn_strided")
+            "gemm_tn_last_kernels", "gemm_tn_strided", "gemm_tn_strided_ex")
 
 # Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -82,6 +83,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_tn_strided.restype = i32
         L.gemm_tn_strided.argtypes = [i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
                                       i32, vp]
+        L.gemm_tn_strided_ex.restype = i32
+        L.gemm_tn_strided_ex.argtypes = [i64, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64,
+                                         i64, i32, vp, ctypes.POINTER(GemmTnOptions)]
         L.gemm_tn_last_kernels.restype = ctypes.c_char_p
         L.gemm_tn_last_kernels.argtypes = []
         L.gemm_tn_skinny_noalloc.restype = i32
@@ -134,6 +138,16 @@ def gemm_tn_strided(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype
     """C ``gemm_tn_strided``: operands as pointers plus element strides."""
     return lib().gemm_tn_strided(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype,
                                  stream)
+
+
+def gemm_tn_strided_ex(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype,
+                       stream, opts=None) -> int:
+    """C ``gemm_tn_strided_ex``; ``opts`` as for :func:`gemm_tn_ex`."""
+    if isinstance(opts, dict):
+        opts = make_options(**opts)
+    p = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_tn_strided_ex(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn,
+                                    accum_dtype, stream, p)
 
 
 def gemm_tn_last_kernels() -> str:

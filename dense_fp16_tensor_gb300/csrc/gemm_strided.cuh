@@ -7,9 +7,10 @@
 // copy the same:
 //
 //   warps 0-3   copy producer: each thread gathers 16-byte K-chunks (8 fp16
-//               along K) of A and B rows through the strides -- one 16-byte
-//               vector load when the chunk is contiguous and aligned, else
-//               eight 2-byte loads -- and writes them to the 128B-swizzled
+//               along K) of A and B rows through the strides, four chunks in
+//               flight at a time -- for a contiguous chunk the widest loads
+//               its alignment allows, else eight 2-byte loads -- and writes
+//               them to the 128B-swizzled
 //               K-major layout the TMA unit would produce (row r, chunk j at
 //               byte r*128 + 16*(j ^ (r%8))), zero outside the matrix; then
 //               fence.proxy.async and one arrival per thread on `full`.
@@ -60,6 +61,32 @@ struct StridedSmem {
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
 };
 
+// 16 contiguous bytes at a 2-byte aligned address, with the widest loads
+// the alignment allows (never touching bytes outside [src, src + 16)).
+__device__ __forceinline__ uint4 load16_contiguous(const __half* src) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+  if ((a & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(src));
+  uint4 v;
+  if ((a & 7u) == 0) {
+    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(src));
+    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(src + 4));
+    v = make_uint4(lo.x, lo.y, hi.x, hi.y);
+  } else if ((a & 3u) == 0) {
+    const unsigned* w = reinterpret_cast<const unsigned*>(src);
+    v = make_uint4(__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3));
+  } else {  // 2 mod 4: one halfword, three words, one halfword
+    const unsigned short* hs = reinterpret_cast<const unsigned short*>(src);
+    const unsigned* w = reinterpret_cast<const unsigned*>(src + 1);
+    const uint32_t h0 = __ldg(hs), h7 = __ldg(hs + 7);
+    const uint32_t w0 = __ldg(w), w1 = __ldg(w + 1), w2 = __ldg(w + 2);
+    v.x = h0 | (w0 << 16);
+    v.y = (w0 >> 16) | (w1 << 16);
+    v.z = (w1 >> 16) | (w2 << 16);
+    v.w = (w2 >> 16) | (h7 << 16);
+  }
+  return v;
+}
+
 // Eight consecutive-k elements X(row, k0..k0+7) of a (rows, K) view with
 // strides (s_row, s_k); zeros outside the matrix.
 __device__ __forceinline__ uint4 gather_chunk(const __half* X, int64_t s_row, int64_t s_k,
@@ -67,9 +94,7 @@ __device__ __forceinline__ uint4 gather_chunk(const __half* X, int64_t s_row, in
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
   if (row >= rows || k0 >= K) return v;
   const __half* src = X + static_cast<int64_t>(row) * s_row + static_cast<int64_t>(k0) * s_k;
-  if (s_k == 1 && k0 + 8 <= K && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-    return __ldg(reinterpret_cast<const uint4*>(src));
-  }
+  if (s_k == 1 && k0 + 8 <= K) return load16_contiguous(src);
   unsigned short h[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
@@ -84,16 +109,31 @@ __device__ __forceinline__ uint4 gather_chunk(const __half* X, int64_t s_row, in
 // Fill `rows` x 64 of one operand's stage in the K-major 128B-swizzled
 // layout.  Chunk q of this thread's share covers row (q / 8) and K-chunk
 // (q % 8) when K is the contiguous mode, else row (q % rows) so that
-// neighbouring threads read neighbouring rows.
+// neighbouring threads read neighbouring rows.  Chunks are gathered four at
+// a time so that their loads are in flight together.
 __device__ __forceinline__ void fill_operand(uint8_t* dst, const __half* X, int64_t s_row,
                                              int64_t s_k, int rows_total, int K, int row0,
                                              int k0, int rows, int tid) {
   const bool k_fast = (s_k == 1) || (s_row != 1 && s_k <= s_row);
-  for (int q = tid; q < rows * 8; q += kStrProducers) {
-    const int r = k_fast ? q >> 3 : q % rows;
-    const int j = k_fast ? q & 7 : q / rows;
-    const uint4 v = gather_chunk(X, s_row, s_k, rows_total, K, row0 + r, k0 + 8 * j);
-    *reinterpret_cast<uint4*>(dst + r * 128 + 16 * (j ^ (r & 7))) = v;
+  constexpr int kBatch = 4;
+  for (int q0 = tid; q0 < rows * 8; q0 += kBatch * kStrProducers) {
+    uint4 v[kBatch];
+    int off[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int q = q0 + b * kStrProducers;
+      off[b] = -1;
+      v[b] = make_uint4(0u, 0u, 0u, 0u);
+      if (q < rows * 8) {
+        const int r = k_fast ? q >> 3 : q % rows;
+        const int j = k_fast ? q & 7 : q / rows;
+        v[b] = gather_chunk(X, s_row, s_k, rows_total, K, row0 + r, k0 + 8 * j);
+        off[b] = r * 128 + 16 * (j ^ (r & 7));
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+      if (off[b] >= 0) *reinterpret_cast<uint4*>(dst + off[b]) = v[b];
   }
 }
 

@@ -15,6 +15,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -25,6 +26,7 @@
 #include "gemm_wide.cuh"
 #include "gemm_skinny.cuh"
 #include "gemm_strided.cuh"
+#include "repack.cuh"
 
 namespace {
 
@@ -562,13 +564,153 @@ bool injective2(int64_t rows, int64_t cols, int64_t s_r, int64_t s_c) {
 
 }  // namespace
 
-extern "C" GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K, const void* A,
-                                           int64_t sAm, int64_t sAk, const void* B, int64_t sBn,
-                                           int64_t sBk, void* CD, int64_t sCm, int64_t sCn,
-                                           int accum_dtype, void* stream) {
+namespace {
+
+cudaError_t repack2d(const void* src, int64_t s_sr, int64_t s_sc, void* dst, int64_t s_dr,
+                     int64_t s_dc, int64_t rows, int64_t cols, cudaStream_t stream) {
+  if (s_sc == 1 && s_dc == 1 && rows <= 65535) {
+    const int64_t chunks = (cols + 7) / 8;
+    const dim3 grid(static_cast<unsigned>(
+                        std::min<int64_t>((chunks + kRepackThreads - 1) / kRepackThreads, 64)),
+                    static_cast<unsigned>(rows), 1);
+    repack_rows_kernel<<<grid, kRepackThreads, 0, stream>>>(static_cast<const __half*>(src), s_sr,
+                                                            static_cast<__half*>(dst), s_dr,
+                                                            static_cast<int>(rows),
+                                                            static_cast<int>(cols));
+    return cudaGetLastError();
+  }
+  const dim3 grid(static_cast<unsigned>((cols + kRepackTile - 1) / kRepackTile),
+                  static_cast<unsigned>((rows + kRepackTile - 1) / kRepackTile), 1);
+  repack2d_kernel<<<grid, kRepackThreads, 0, stream>>>(
+      static_cast<const __half*>(src), s_sr, s_sc, static_cast<__half*>(dst), s_dr, s_dc,
+      static_cast<int>(rows), static_cast<int>(cols));
+  return cudaGetLastError();
+}
+
+int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+
+// A (rows, K) view that TMA can read directly: (major, ld) or false.
+bool tma_view(const void* p, int64_t rows, int64_t K, int64_t s_r, int64_t s_k, int& major,
+              int64_t& ld) {
+  if (reinterpret_cast<uintptr_t>(p) & 15u) return false;
+  if (s_k == 1 && (rows == 1 || (s_r % 8 == 0 && s_r >= K))) {
+    major = GEMM_TN_MAJOR_K;
+    ld = rows == 1 ? round8(K) : s_r;
+    return true;
+  }
+  if (s_r == 1 && (K == 1 || (s_k % 8 == 0 && s_k >= rows))) {
+    major = GEMM_TN_MAJOR_MN;
+    ld = K == 1 ? round8(rows) : s_k;
+    return true;
+  }
+  return false;
+}
+
+int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream_t stream) {
+  StridedArgs p = base;
+  const int grid = std::min(p.num_tiles, st.num_sms);
+  gemm_tn_strided_kernel<<<grid, kStrThreads, StridedSmem::kDynamicBytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  t_last_launches = 1;
+  t_last_kernels = "gemm_tn_strided_kernel";
+  return GEMM_TN_OK;
+}
+
+// Repack the views TMA cannot read into row-major buffers from the stream's
+// memory pool, run the tile kernels, scatter D back if needed.  Returns
+// GEMM_TN_ERR_NO_MEMORY (nothing enqueued) when the pool cannot serve it.
+int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t sAm,
+                        int64_t sAk, const void* B, int64_t sBn, int64_t sBk, void* CD,
+                        int64_t sCm, int64_t sCn, int accum, const DeviceState& st,
+                        cudaStream_t stream) {
+  int a_major = 0, b_major = 0, c_major = 0;
+  int64_t ldA = 0, ldB = 0, ldC = 0;
+  const bool a_direct = tma_view(A, M, K, sAm, sAk, a_major, ldA);
+  const bool b_direct = tma_view(B, N, K, sBn, sBk, b_major, ldB);
+  // C/D must be row-major for the tile kernels: (M,N):(ldC,1)
+  const bool c_direct = tma_view(CD, M, N, sCm, sCn, c_major, ldC) && c_major == GEMM_TN_MAJOR_K;
+  const int64_t Kp = round8(K), Np = round8(N);
+  const size_t a_elems = a_direct ? 0 : static_cast<size_t>(M) * Kp;
+  const size_t b_elems = b_direct ? 0 : static_cast<size_t>(N) * Kp;
+  const size_t c_elems = c_direct ? 0 : static_cast<size_t>(M) * Np;
+  const size_t total = (a_elems + b_elems + c_elems) * 2;
+  void* ws = nullptr;
+  if (total > 0 && cudaMallocAsync(&ws, total, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_NO_MEMORY;
+  }
+  __half* wa = static_cast<__half*>(ws);
+  __half* wb = wa + a_elems;
+  __half* wc = wb + b_elems;
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  const void* Ause = A;
+  const void* Buse = B;
+  void* Cuse = CD;
+  if (!a_direct) {
+    e = repack2d(A, sAm, sAk, wa, Kp, 1, M, K, stream);
+    Ause = wa, a_major = GEMM_TN_MAJOR_K, ldA = Kp, ++launches;
+  }
+  if (e == cudaSuccess && !b_direct) {
+    e = repack2d(B, sBn, sBk, wb, Kp, 1, N, K, stream);
+    Buse = wb, b_major = GEMM_TN_MAJOR_K, ldB = Kp, ++launches;
+  }
+  if (e == cudaSuccess && !c_direct) {
+    e = repack2d(CD, sCm, sCn, wc, Np, 1, M, N, stream);
+    Cuse = wc, ldC = Np, ++launches;
+  }
+  int s = GEMM_TN_OK;
+  const char* gemm_kernels = "";
+  if (e == cudaSuccess) {
+    gemm_tn_options o;
+    std::memset(&o, 0, sizeof o);
+    const int path = plan(M, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
+    if (path == GEMM_TN_PATH_SKINNY) {
+      s = launch_skinny(M, N, K, Ause, ldA, Buse, ldB, Cuse, ldC, stream, o, st);
+    } else {
+      s = launch_large(M, N, K, Ause, ldA, a_major, Buse, ldB, b_major, Cuse, ldC, accum, stream,
+                       o, st);
+    }
+    launches += t_last_launches;
+    gemm_kernels = t_last_kernels;
+  } else {
+    s = GEMM_TN_ERR_CUDA;
+  }
+  if (s == GEMM_TN_OK && !c_direct) {
+    e = repack2d(wc, Np, 1, CD, sCm, sCn, M, N, stream);
+    if (e != cudaSuccess) s = GEMM_TN_ERR_CUDA;
+    ++launches;
+  }
+  if (ws && cudaFreeAsync(ws, stream) != cudaSuccess && s == GEMM_TN_OK) s = GEMM_TN_ERR_CUDA;
+  if (s != GEMM_TN_OK) {
+    cudaGetLastError();
+    t_last_launches = 0;
+    t_last_kernels = "";
+    return s;
+  }
+  t_last_launches = launches;
+  // the repack kernels run around the tile kernel(s) named here
+  static thread_local char names[160];
+  std::snprintf(names, sizeof names, "%s%s", (a_direct && b_direct && c_direct) ? "" : "repack2d_kernel+",
+                gemm_kernels);
+  t_last_kernels = names;
+  return GEMM_TN_OK;
+}
+
+}  // namespace
+
+extern "C" GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K, const void* A,
+                                              int64_t sAm, int64_t sAk, const void* B,
+                                              int64_t sBn, int64_t sBk, void* CD, int64_t sCm,
+                                              int64_t sCn, int accum_dtype, void* stream,
+                                              const gemm_tn_options* opts) {
   t_last_launches = 0;
   t_last_kernels = "";
   const int64_t kMax = 0x7FFFFFFF;
+  const int route = opts ? opts->path : GEMM_TN_PATH_AUTO;
+  if (route != GEMM_TN_PATH_AUTO && route != GEMM_TN_PATH_STRIDED_COPY &&
+      route != GEMM_TN_PATH_STRIDED_REPACK)
+    return GEMM_TN_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM_TN_ERR_INVALID_ARG;
   if (sAm < 0 || sAk < 0 || sBn < 0 || sBk < 0 || sCm < 0 || sCn < 0)
     return GEMM_TN_ERR_INVALID_ARG;
@@ -596,6 +738,17 @@ extern "C" GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K, cons
     s = device_setup(dev, st);
   }
   if (s != GEMM_TN_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  // Repacking costs two extra passes over the operands and an allocation;
+  // below ~2^24 multiply-adds the copy-producer kernel is as fast.
+  const bool big = static_cast<double>(M) * N * K >= 16777216.0;
+  if (route == GEMM_TN_PATH_STRIDED_REPACK || (route == GEMM_TN_PATH_AUTO && big)) {
+    s = strided_repack_path(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype, *st,
+                            cs);
+    if (s != GEMM_TN_ERR_NO_MEMORY || route == GEMM_TN_PATH_STRIDED_REPACK) return s;
+    // pool exhausted: the copy producer needs no workspace
+  }
 
   StridedArgs p;
   std::memset(&p, 0, sizeof p);
@@ -617,12 +770,14 @@ extern "C" GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K, cons
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.k_blocks = static_cast<int>((K + kStrBK - 1) / kStrBK);
   p.group_m = 16;
-  p.timeout_ns = kDefaultTimeoutNs;
-  const int grid = std::min(p.num_tiles, st->num_sms);
-  gemm_tn_strided_kernel<<<grid, kStrThreads, StridedSmem::kDynamicBytes,
-                           static_cast<cudaStream_t>(stream)>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
-  t_last_launches = 1;
-  t_last_kernels = "gemm_tn_strided_kernel";
-  return GEMM_TN_OK;
+  p.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+  return strided_copy_path(p, *st, cs);
+}
+
+extern "C" GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K, const void* A,
+                                           int64_t sAm, int64_t sAk, const void* B, int64_t sBn,
+                                           int64_t sBk, void* CD, int64_t sCm, int64_t sCn,
+                                           int accum_dtype, void* stream) {
+  return gemm_tn_strided_ex(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype, stream,
+                            nullptr);
 }

@@ -98,8 +98,14 @@ typedef enum {
                                persistent tile path otherwise */
   GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernels: 256x256 tiles on one
                                CTA or on a CTA pair, or 128xBN tiles */
-  GEMM_TN_PATH_SKINNY = 2   /* swapped-operand split-K kernel + reduction;
+  GEMM_TN_PATH_SKINNY = 2,  /* swapped-operand split-K kernel + reduction;
                                needs M <= 64 and K-major A and B */
+  GEMM_TN_PATH_STRIDED_COPY = 3,   /* gemm_tn_strided_ex only: threads gather
+                                      operands into shared memory; no
+                                      workspace */
+  GEMM_TN_PATH_STRIDED_REPACK = 4  /* gemm_tn_strided_ex only: repack views
+                                      TMA cannot read into pooled buffers,
+                                      then the tile kernels */
 } gemm_tn_path;
 
 /* Extra controls for gemm_tn_ex.  Zero-initialise and set what you need;
@@ -163,21 +169,40 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
  *   A(m,k) = A[m*sAm + k*sAk],  B(n,k) = B[n*sBn + k*sBk],
  *   C/D(m,n) = CD[m*sCm + n*sCn]     (strides in elements, all >= 0)
  * The accumulation modes and in-place semantics are those of gemm_tn.
- * Always runs the copy-producer kernel (threads gather 16-byte K chunks into
- * shared memory instead of TMA), so it accepts layouts gemm_tn rejects:
- * leading dimensions that are not multiples of 8, pointers that are only
- * 2-byte aligned, and views with no stride-1 mode; gemm_tn is faster when
- * its requirements hold.
+ * It accepts layouts gemm_tn rejects: leading dimensions that are not
+ * multiples of 8, pointers that are only 2-byte aligned, and views with no
+ * stride-1 mode.  Two routes:
+ *   - repack: operands whose view TMA cannot read are first copied into
+ *     row-major buffers taken from the device's stream-ordered memory pool
+ *     (cudaMallocAsync / cudaFreeAsync on `stream`), the tile kernels run
+ *     on them, and D is scattered back when its view needed a copy;
+ *   - copy producer: one kernel whose threads gather 16-byte K chunks
+ *     through the strides straight into shared memory; no workspace.
+ * gemm_tn_strided picks repack for problems of at least 2^24 multiply-adds
+ * and falls back to the copy producer when the pool cannot serve the
+ * workspace; gemm_tn_strided_ex can force either (gemm_tn_options.path =
+ * GEMM_TN_PATH_STRIDED_REPACK / _COPY; timeout_ns also applies).
  * Errors: GEMM_TN_ERR_INVALID_ARG for negative sizes or strides, NULL with a
  * nonzero extent, a C/D view in which two coordinates share an element, or
  * C/D overlapping A or B; GEMM_TN_ERR_ALIGNMENT for a pointer that is not
- * 2-byte aligned.  M == 0, N == 0 or K == 0 enqueue nothing.
+ * 2-byte aligned; GEMM_TN_ERR_NO_MEMORY when the repack route is forced and
+ * the pool cannot serve it.  M == 0, N == 0 or K == 0 enqueue nothing.
  */
 GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K,
                                 const void* A, int64_t sAm, int64_t sAk,
                                 const void* B, int64_t sBn, int64_t sBk,
                                 void* CD, int64_t sCm, int64_t sCn,
                                 int accum_dtype, void* stream);
+
+/* gemm_tn_strided with explicit controls (opts may be NULL); only `path`
+ * (0, GEMM_TN_PATH_STRIDED_COPY or GEMM_TN_PATH_STRIDED_REPACK) and
+ * `timeout_ns` are read. */
+GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K,
+                                   const void* A, int64_t sAm, int64_t sAk,
+                                   const void* B, int64_t sBn, int64_t sBk,
+                                   void* CD, int64_t sCm, int64_t sCn,
+                                   int accum_dtype, void* stream,
+                                   const gemm_tn_options* opts);
 
 /* Synchronise `stream`, then read and clear the device error word that a
  * kernel sets when one of its bounded waits expires.  Returns GEMM_TN_OK,

@@ -135,3 +135,9 @@ def test_strided_noop_sizes(lib):
     assert scall(M=0) == gb.OK
     assert scall(K=0, A=0, B=0) == gb.OK
     assert scall(M=1, sCm=0, K=0) == gb.OK  # one row: a zero row stride is fine
+
+
+def test_strided_ex_rejects_tile_paths(lib):
+    for path in (gb.PATH_LARGE, gb.PATH_SKINNY, 9):
+        assert gb.gemm_tn_strided_ex(64, 64, 64, P, 64, 1, P + (1 << 20), 64, 1, P + (2 << 20),
+                                     64, 1, 0, None, {"path": path}) == gb.ERR_INVALID_ARG

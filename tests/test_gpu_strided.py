@@ -43,7 +43,7 @@ VIEWS = {
 }
 
 
-def run_case(M, N, K, view, accum, dist_ab, dist_c, seed):
+def run_case(M, N, K, view, accum, dist_ab, dist_c, seed, route=gb.PATH_STRIDED_COPY):
     (sAm, sAk), (sBn, sBk), (sCm, sCn), (oA, oB, oC) = VIEWS[view](M, N, K)
     XA = wl.draw((oA + extent(M, K, sAm, sAk),), dist_ab, seed)
     XB = wl.draw((oB + extent(N, K, sBn, sBk),), dist_ab, seed + 1)
@@ -51,10 +51,15 @@ def run_case(M, N, K, view, accum, dist_ab, dist_c, seed):
     dev = torch.device("cuda")
     dA, dB, dC = XA.to(dev), XB.to(dev), XC.to(dev)
     s = torch.cuda.current_stream().cuda_stream
-    st = gb.gemm_tn_strided(M, N, K, dA.data_ptr() + 2 * oA, sAm, sAk, dB.data_ptr() + 2 * oB,
-                            sBn, sBk, dC.data_ptr() + 2 * oC, sCm, sCn, accum, s)
+    st = gb.gemm_tn_strided_ex(M, N, K, dA.data_ptr() + 2 * oA, sAm, sAk, dB.data_ptr() + 2 * oB,
+                               sBn, sBk, dC.data_ptr() + 2 * oC, sCm, sCn, accum, s,
+                               {"path": route})
     assert st == gb.OK, gb.gemm_tn_status_string(st)
-    assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel"
+    kernels = gb.gemm_tn_last_kernels()
+    if route == gb.PATH_STRIDED_COPY:
+        assert kernels == "gemm_tn_strided_kernel"
+    elif route == gb.PATH_STRIDED_REPACK:
+        assert "gemm_tn_strided_kernel" not in kernels and kernels
     torch.cuda.synchronize()
     out = np_bits(dC.cpu())
     d64, d16 = oracle.gemm_tn_strided(M, N, K, np_bits(XA)[oA:], sAm, sAk, np_bits(XB)[oB:],
@@ -67,17 +72,29 @@ def run_case(M, N, K, view, accum, dist_ab, dist_c, seed):
     return got, d64, d16
 
 
+ROUTES = [gb.PATH_STRIDED_COPY, gb.PATH_STRIDED_REPACK]
+
+
+@pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("view", sorted(VIEWS))
 @pytest.mark.parametrize("accum", [0, 1])
-def test_strided_views_integer_bit_exact(view, accum):
+def test_strided_views_integer_bit_exact(view, accum, route):
     for i, (M, N, K) in enumerate([(1, 1, 1), (17, 129, 65), (200, 300, 130), (130, 260, 513)]):
-        got, d64, d16 = run_case(M, N, K, view, accum, "int2", "int4", 500 + 10 * i)
+        got, d64, d16 = run_case(M, N, K, view, accum, "int2", "int4", 500 + 10 * i, route)
         check(got, d64, d16, K, accum, True, f"{view} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("route", ROUTES)
 @pytest.mark.parametrize("accum", [0, 1])
-def test_strided_real_values_tolerance(accum):
+def test_strided_real_values_tolerance(accum, route):
     M, N, K = 384, 520, 1000
     for view in ("no_unit_stride", "odd_ld_mn_major"):
-        got, d64, d16 = run_case(M, N, K, view, accum, "u11", "u11", 900)
+        got, d64, d16 = run_case(M, N, K, view, accum, "u11", "u11", 900, route)
         check(got, d64, d16, K, accum, False, f"{view} real")
+
+
+def test_strided_auto_route_picks_repack_for_large_problems():
+    M, N, K = 256, 512, 768
+    got, d64, d16 = run_case(M, N, K, "odd_ld_k_major", 0, "int1", "int4", 950, gb.PATH_AUTO)
+    assert gb.gemm_tn_last_kernels().startswith("repack2d_kernel+")
+    check(got, d64, d16, K, 0, True, "auto route")
