@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--stream-k", type=int, default=0,
+                    help="256x256 kernel: 0 auto, 1 split any partial last wave, -1 never")
     ap.add_argument("--tile-kernel", type=int, default=0,
                     help="large path: 0 choose, 1 single-CTA 128xN, 2 CTA-pair 256x256, "
                          "3 single-CTA 256x256")
@@ -278,8 +280,9 @@ def run_ours(args):
     A, Bm, CD = A_st.to(dev), B_st.to(dev), C_st.to(dev)
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
-    opts = (gb.make_options(tile_n=args.tile_n, tile_kernel=args.tile_kernel)
-            if (args.tile_n or args.tile_kernel) else None)
+    opts = (gb.make_options(tile_n=args.tile_n, tile_kernel=args.tile_kernel,
+                            stream_k=args.stream_k)
+            if (args.tile_n or args.tile_kernel or args.stream_k) else None)
 
     def step(a_ptr=None, b_ptr=None, cd_ptr=None):
         st = gb.gemm_tn_ex(w.M, w.N, w.K, a_ptr or A.data_ptr(), w.ldA, w.a_major,
@@ -375,7 +378,7 @@ def run_ours(args):
     peak = float(peaks["bf16_tflops"])  # fp16 dense rate = bf16 dense rate
     path = gb.gemm_tn_plan_path(w.M, w.N, w.K, w.a_major, w.b_major)
     # the dominant kernel of one step, as reported by the library
-    kkey = kernels_run.split("+")[0].split("<")[0]
+    kkey = next((k for k in kernels_run.split("+") if k.startswith("gemm_tn")), "").split("<")[0]
     traffic = traffic_for(kkey, w.name) if kkey in KERNEL_SOURCES else None
     if path == gb.PATH_LARGE:
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -394,6 +397,7 @@ def run_ours(args):
     if not args.no_extra and w.name != "skinny":
         extra["skinny_m16"] = bench_skinny(dev, stream)
         extra["strided_4096"] = bench_strided(dev, stream)
+        extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -507,6 +511,58 @@ def bench_strided(dev, stream, steps=20):
     return {"workload": "M=N=K=4096, ld = K+1 (A, B), ldC = N+1, fp32 accumulate",
             "kernels": gb.gemm_tn_last_kernels(), "ms_per_call": ms, "TFLOP_per_s": tf,
             "frac_of_peak": tf / float(peaks["bf16_tflops"]), "peak_kind": kind}
+
+
+def bench_stream_k(dev, stream, steps=50, rounds=3):
+    """Stream-K split of the 256 x 256 tile kernel against the unsplit kernel on
+    M=3072 N=4096 K=4096 (192 tiles: one full wave of 152 plus 40), fp32
+    accumulation; the two are timed in alternating rounds."""
+    import torch
+
+    from dense_fp16_tensor_gb300 import binding as gb
+    from dense_fp16_tensor_gb300 import workloads as wl
+    M, N, K = 3072, 4096, 4096
+    A = wl.draw((M * K,), "u11", 7101).to(dev)
+    Bm = wl.draw((N * K,), "u11", 7102).to(dev)
+    CD = torch.zeros(M * N, dtype=torch.float16, device=dev)
+    sp = stream.cuda_stream
+    kernels = {}
+
+    def step(sk):
+        st = gb.gemm_tn_ex(M, N, K, A.data_ptr(), K, 0, Bm.data_ptr(), K, 0, CD.data_ptr(), N, 0,
+                           sp, {"path": gb.PATH_LARGE, "tile_kernel": gb.TILE_WIDE,
+                                "stream_k": sk})
+        if st != gb.OK:
+            raise gb.GemmTnError(st)
+        kernels[sk] = gb.gemm_tn_last_kernels()
+
+    def timed(sk):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                step(sk)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    with torch.cuda.stream(stream):
+        for sk in (1, -1, 1, -1):
+            step(sk)
+    torch.cuda.synchronize()
+    t = {1: [], -1: []}
+    for _ in range(rounds):
+        for sk in (1, -1):
+            t[sk].append(timed(sk))
+    fl = 2.0 * M * N * K
+    ms_sk, ms_plain = statistics.median(t[1]), statistics.median(t[-1])
+    return {"workload": "M=3072 N=4096 K=4096 (192 tiles of 256x256 on 152 SMs), fp32 accumulate",
+            "stream_k": {"kernels": kernels[1], "ms_per_call": ms_sk,
+                         "TFLOP_per_s": fl / (ms_sk * 1e-3) / 1e12},
+            "unsplit": {"kernels": kernels[-1], "ms_per_call": ms_plain,
+                        "TFLOP_per_s": fl / (ms_plain * 1e-3) / 1e12},
+            "speedup": ms_plain / ms_sk}
 
 
 def main():

@@ -63,4 +63,18 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / rows;
 }
 
+// Contiguous split of `units` work units over `grid` CTAs: CTA c owns
+// [unit_begin(c), unit_begin(c+1)).
+__device__ __forceinline__ int64_t unit_begin(int64_t units, int cta, int grid) {
+  return units * cta / grid;
+}
+
+// CTA whose unit range holds unit u (ranges from unit_begin are monotone).
+__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t units, int grid) {
+  int c = static_cast<int>(u * grid / units);
+  while (c + 1 < grid && unit_begin(units, c + 1, grid) <= u) ++c;
+  while (c > 0 && unit_begin(units, c, grid) > u) --c;
+  return c;
+}
+
 }  // namespace gemm_tn_dev

@@ -46,6 +46,16 @@ struct LargeArgs {
   int group_m;
   uint64_t timeout_ns;
   int test_stall;
+  // Stream-K (256 x 256 kernel only): tiles [sk_tile0, num_tiles) are cut
+  // into contiguous (tile, K-block) ranges of sk_per units, CTA c owning
+  // units [c * sk_per, min((c + 1) * sk_per, sk_units)).  sk_tile0 ==
+  // num_tiles means no split tiles.  (sk_per * (gridDim.x + 1) < 2^31.)
+  int sk_tile0;
+  int sk_max_segs;     // split-tile segments one CTA can hold
+  int sk_units;        // (num_tiles - sk_tile0) * k_blocks
+  int sk_per;          // units per CTA
+  float* sk_partials;  // [gridDim.x * sk_max_segs] slots of 256 x 256 fp32
+  int* sk_counters;    // [(num_tiles - sk_tile0) * 8], zero on entry
 };
 
 template <int BN>

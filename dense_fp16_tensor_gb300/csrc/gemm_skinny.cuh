@@ -59,10 +59,6 @@ struct SkinnySmem {
   static constexpr uint32_t kTmemCols = MP <= 16 ? 32 : (MP <= 32 ? 64 : 128);
 };
 
-__device__ __forceinline__ int64_t unit_begin(int64_t units, int cta, int grid) {
-  return units * cta / grid;
-}
-
 // Segments of CTA `cta`: consecutive pieces of [begin, end) that stay inside
 // one tile.  seg j covers [max(begin, (first_tile + j) * kb), min(end, ...)).
 struct SegIter {
@@ -261,14 +257,6 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L::kTmemCols);
   }
-}
-
-// CTA whose unit range holds unit u (ranges from unit_begin are monotone).
-__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t units, int grid) {
-  int c = static_cast<int>(u * grid / units);
-  while (c + 1 < grid && unit_begin(units, c + 1, grid) <= u) ++c;
-  while (c > 0 && unit_begin(units, c, grid) > u) --c;
-  return c;
 }
 
 // D(m,n) = fp16( sum over the CTAs that touched tile n/128, in CTA order, of

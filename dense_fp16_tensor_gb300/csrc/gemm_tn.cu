@@ -45,7 +45,13 @@ struct DeviceState {
   int num_sms = 0;
   bool attrs_set = false;
   int max_pairs = 0;  // CTA pairs of gemm_tn_large2_kernel that fit at once
+  cudaMemPool_t pool = nullptr;  // library-owned stream-ordered workspace pool
 };
+
+// Workspaces come from a pool owned by the library (one per device) that
+// keeps up to this much memory cached between calls, so a call's workspace
+// is normally served without new physical allocation.
+constexpr uint64_t kPoolKeepBytes = 1ull << 30;
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -123,7 +129,27 @@ int device_setup(int dev, DeviceState*& st) {
     st->attrs_set = true;
   }
   if (resolve_encoder() != GEMM_TN_OK) return GEMM_TN_ERR_CUDA;
+  if (st->pool == nullptr) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+    uint64_t keep = kPoolKeepBytes;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return GEMM_TN_ERR_CUDA;
+    }
+    st->pool = pool;
+  }
   return GEMM_TN_OK;
+}
+
+// Stream-ordered workspace from the device's library pool.
+cudaError_t ws_alloc(void** p, size_t bytes, const DeviceState& st, cudaStream_t stream) {
+  return cudaMallocFromPoolAsync(p, bytes, st.pool, stream);
 }
 
 // Tensor map over a (rows, K) operand.  K-major: dims {K, rows}, box
@@ -243,13 +269,53 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   p.group_m = (pair || wide) ? 8 : 16;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
+  p.sk_tile0 = p.num_tiles;  // no split tiles unless stream-K is set up below
+  void* sk_ws = nullptr;
   if (wide) {
     CUtensorMap tmD;
     s = encode_cd(&tmD, CD, M, N, ldC);
     if (s != GEMM_TN_OK) return s;
-    const int grid = std::min(p.num_tiles, st.num_sms);
+    int grid = std::min(p.num_tiles, st.num_sms);
+    // Stream-K for the last, partial wave, on request only (fp32
+    // accumulation only: a split fp16 accumulation would round at different
+    // places).
+    const int G = st.num_sms;
+    const int full = p.num_tiles / G, rem = p.num_tiles - full * G;
+    const int64_t units = static_cast<int64_t>(rem) * p.k_blocks;
+    const int64_t per = (units + G - 1) / G;
+    const bool want = !p.acc_f16 && rem > 0 && p.k_blocks >= 2 &&
+                      per * (G + 1) < (int64_t{1} << 31) && o.stream_k == 1;
+    if (want) {
+      const int max_segs = static_cast<int>(per / p.k_blocks + 2);
+      const size_t part_bytes = static_cast<size_t>(G) * max_segs * kWideBM * kWideBN * 4;
+      const size_t cnt_bytes = static_cast<size_t>(rem) * 8 * sizeof(int);
+      if (ws_alloc(&sk_ws, part_bytes + cnt_bytes, st, stream) == cudaSuccess) {
+        int* counters = reinterpret_cast<int*>(static_cast<char*>(sk_ws) + part_bytes);
+        if (cudaMemsetAsync(counters, 0, cnt_bytes, stream) == cudaSuccess) {
+          p.sk_tile0 = full * G;
+          p.sk_units = static_cast<int>(units);
+          p.sk_per = static_cast<int>(per);
+          p.sk_max_segs = max_segs;
+          p.sk_partials = static_cast<float*>(sk_ws);
+          p.sk_counters = counters;
+          grid = G;
+        } else {
+          cudaGetLastError();
+          cudaFreeAsync(sk_ws, stream);
+          sk_ws = nullptr;
+        }
+      } else {
+        cudaGetLastError();  // no workspace: run unsplit
+        sk_ws = nullptr;
+      }
+    }
     gemm_tn_wide_kernel<<<grid, kWideThreads, WideSmem::kDynamicBytes, stream>>>(tmA, tmB, tmD,
                                                                                p);
+    if (sk_ws) {
+      const cudaError_t le = cudaGetLastError();
+      cudaFreeAsync(sk_ws, stream);
+      if (le != cudaSuccess) return GEMM_TN_ERR_CUDA;
+    }
   } else if (pair) {
     const int pairs = std::min(p.num_tiles, st.max_pairs);
     gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(tmA, tmB,
@@ -265,8 +331,8 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
     }
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
-  t_last_launches = 1;
-  t_last_kernels = wide ? "gemm_tn_wide_kernel"
+  t_last_launches = sk_ws ? 2 : 1;  // the counters' memset counts as a launch
+  t_last_kernels = wide ? (sk_ws ? "memset+gemm_tn_wide_kernel" : "gemm_tn_wide_kernel")
                  : pair ? "gemm_tn_large2_kernel"
                         : (bn == 256 ? "gemm_tn_large_kernel<256>" : "gemm_tn_large_kernel<128>");
   return GEMM_TN_OK;
@@ -340,7 +406,7 @@ int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, c
   // Stream-ordered workspace: concurrent calls on different streams never
   // share it, and the pool keeps the memory for the next call.
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+  if (ws_alloc(&ws, need, st, stream) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_TN_ERR_NO_MEMORY;
   }
@@ -635,7 +701,7 @@ int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   const size_t c_elems = c_direct ? 0 : static_cast<size_t>(M) * Np;
   const size_t total = (a_elems + b_elems + c_elems) * 2;
   void* ws = nullptr;
-  if (total > 0 && cudaMallocAsync(&ws, total, stream) != cudaSuccess) {
+  if (total > 0 && ws_alloc(&ws, total, st, stream) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_TN_ERR_NO_MEMORY;
   }

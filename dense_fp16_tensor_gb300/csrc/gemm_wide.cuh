@@ -22,6 +22,21 @@
 //     The next tile's C rows are prefetched into L2 during its main loop, and
 //     the TMA ring keeps loading the next tile's first stages meanwhile.
 //
+// Stream-K (the make_tiled_mma page's K split across workers, "Thread groups
+// along K, and the loop along K": partial sums must be reduced and C added
+// once): whole tiles go round-robin; the tiles of the last, partial wave
+// (t >= sk_tile0) are cut into contiguous (tile, K-block) ranges of equal
+// length, one per CTA.  A CTA whose range covers a whole tile finishes it directly.
+// Otherwise each of its epilogue warps writes its 32 x 256 slab of the fp32
+// partial sum, fences, and takes a ticket on the (tile, slab) counter; the
+// warp that takes the last ticket adds the slab's partials of all
+// contributors in CTA order (deterministic), adds C once, rounds and stores
+// D.  A warp that finds every other contributor already done skips its own
+// partial and finishes from TMEM; the sum, and its order, are the same.  No
+// CTA ever waits for another.  Partials are stored in 4-column groups
+// (float4 per lane, lanes on consecutive rows) so that every store and load
+// moves whole lines.
+//
 // Waits are bounded and abort as in gemm_large.cuh.
 #pragma once
 
@@ -40,6 +55,10 @@ constexpr uint32_t kWideTmemCols = 512;
 
 constexpr int kWideEpiWarps = 8;
 constexpr uint32_t kWideStagingBytes = 32 * 128;  // 32 rows x 64 fp16, 128-byte swizzle
+// Stream-K partials: one 32-row x 64-column fp32 block of a warp's slab is
+// 8 KiB, stored as [column group g (16)][lane (32)] float4.
+constexpr uint32_t kSkBlockBytes = 32 * 64 * 4;
+constexpr int kFinBufs = 3;  // finisher landing buffers per epilogue warp
 
 struct WideSmem {
   static constexpr uint32_t kABytes = kWideBM * kWideBK * 2;  // 32 KiB
@@ -47,8 +66,10 @@ struct WideSmem {
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kStagingOffset = kWideStages * kStageBytes;  // 1024-aligned
   static constexpr uint32_t kBarOffset = kStagingOffset + kWideEpiWarps * kWideStagingBytes;
-  // full[S], empty[S], tmem_full, tmem_empty, drain
-  static constexpr uint32_t kNumBars = 2 * kWideStages + 3;
+  // full[S], empty[S], tmem_full, tmem_empty, drain, then the stream-K
+  // finisher's landing-zone barriers (kFinBufs per epilogue warp)
+  static constexpr uint32_t kFinBar0 = 2 * kWideStages + 3;
+  static constexpr uint32_t kNumBars = kFinBar0 + kWideEpiWarps * kFinBufs;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
@@ -96,6 +117,45 @@ __device__ __forceinline__ uint4 load_c_piece(const LargeArgs& p, int m, int n) 
   return v;
 }
 
+// One item of CTA c's work list: whole tiles first (round-robin), then the
+// pieces of split tiles in its stream-K range.  slot < 0: the CTA computes
+// the whole tile (direct epilogue); slot >= 0: partial sum, stored in slot.
+struct WideItem {
+  int tile, kb0, kb1, slot;
+};
+
+// First unit of CTA c's stream-K range.
+__device__ __forceinline__ int sk_begin(const LargeArgs& p, int c) {
+  return min(c * p.sk_per, p.sk_units);
+}
+
+__device__ __forceinline__ bool wide_item(const LargeArgs& p, int c, int G, int idx,
+                                          WideItem& it) {
+  const int n_dp = c < p.sk_tile0 ? (p.sk_tile0 - 1 - c) / G + 1 : 0;
+  if (idx < n_dp) {
+    it.tile = c + idx * G;
+    it.kb0 = 0;
+    it.kb1 = p.k_blocks;
+    it.slot = -1;
+    return true;
+  }
+  if (p.sk_units == 0) return false;
+  const int j = idx - n_dp;
+  const int ub = sk_begin(p, c), ue = sk_begin(p, c + 1);
+  if (ue <= ub) return false;
+  const int kb = p.k_blocks;
+  const int ft = ub / kb;
+  if (j > (ue - 1) / kb - ft) return false;
+  const int rt = ft + j;
+  const int t0 = rt * kb;
+  const int lo = max(ub, t0), hi = min(ue, t0 + kb);
+  it.tile = p.sk_tile0 + rt;
+  it.kb0 = lo - t0;
+  it.kb1 = hi - t0;
+  it.slot = (it.kb0 == 0 && it.kb1 == kb) ? -1 : c * p.sk_max_segs + j;
+  return true;
+}
+
 __global__ void __launch_bounds__(kWideThreads, 1)
     gemm_tn_wide_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
@@ -117,6 +177,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
+  const int cta = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWideStages; ++s) {
@@ -126,6 +187,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, 8);  // eight epilogue warps
     mbar_init(drain, 1);
+    for (int b = 0; b < kWideEpiWarps * kFinBufs; ++b) mbar_init(smem_u32(bars + L::kFinBar0 + b), 1);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -148,17 +210,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
       bool ok = true;
-      int local = 0;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+      WideItem it;
+      for (int idx = 0; ok && wide_item(p, cta, G, idx, it); ++idx) {
         int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        tile_coords(it.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
                             timeout_code(kRoleProducer, stage))) {
             ok = false;
             break;
           }
-          if (!(p.test_stall && local == 0 && kb == 0)) {
+          if (!(p.test_stall && idx == 0 && kb == it.kb0)) {
             const uint32_t fb = full0 + 8 * stage;
             const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t b_dst = a_dst + L::kABytes;
@@ -200,14 +262,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const uint32_t idesc = make_idesc_f16(128, kWideBN, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      WideItem it;
+      for (int idx = 0; ok && wide_item(p, cta, G, idx, it); ++idx) {
         if (!wait_bounded(tempty, acc_phase ^ 1u, abort_flag, p.timeout_ns,
                           timeout_code(kRoleMma, 0x200))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
                             timeout_code(kRoleMma, stage))) {
             ok = false;
@@ -226,7 +289,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               const uint32_t ah = a_base + h * 16384;
               const uint64_t ad = p.a_mn ? make_sw128_desc(ah + k * 2048, 8192, 1024)
                                          : make_sw128_desc(ah + k * 32, 16, 1024);
-              mma_f16(tmem_base + h * kWideBN, ad, bd, idesc, (kb | k) != 0);
+              mma_f16(tmem_base + h * kWideBN, ad, bd, idesc, (kb != it.kb0) || (k != 0));
             }
           }
           mma_commit(empty0 + 8 * stage);
@@ -246,18 +309,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;                                // 0..7
+    const int ew = warp - 2;                                // 0..7: the warp's slab
     const int half = ew >> 2;                               // 128-row half of the tile
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes 32*quad ..
     const int row0 = half * 128 + static_cast<int>(quad * 32);  // first tile row of this warp
+    const int trow = row0 + static_cast<int>(lane);             // this lane's tile row
     uint8_t* stg = smem + L::kStagingOffset + ew * kWideStagingBytes;
     const uint32_t stg_u32 = smem_u32(stg);
     // coalesced pattern: piece i of lane l is row 4i + l/8, 16-byte segment l%8
     const int prow = static_cast<int>(lane >> 3), pseg = static_cast<int>(lane & 7);
-    auto load_chunk = [&](int tm, int tn, int c, uint4 (&v)[8]) {
+    int tm = 0, tn = 0;
+    uint4 cnext[8];
+    auto load_chunk = [&](int c, uint4 (&v)[8]) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        v[i] = load_c_piece(p, tm * kWideBM + row0 + 4 * i + prow, tn * kWideBN + 64 * c + 8 * pseg);
+        v[i] = load_c_piece(p, tm * kWideBM + row0 + 4 * i + prow,
+                            tn * kWideBN + 64 * c + 8 * pseg);
     };
     auto stage_chunk = [&](const uint4 (&v)[8]) {
 #pragma unroll
@@ -266,76 +333,265 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         *reinterpret_cast<uint4*>(stg + r * 128 + 16 * (pseg ^ (r & 7))) = v[i];
       }
     };
-    // Warm L2 with this warp's C rows of a tile (one row per lane).
-    auto prefetch_c = [&](int t2) {
-      if (t2 >= p.num_tiles) return;
+    // C of chunks 0 and 1 (0 staged, 1 in registers), once the previous
+    // tile's last store has finished reading the staging buffer.
+    auto preload_c = [&]() {
+      load_chunk(0, cnext);
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+      stage_chunk(cnext);
+      load_chunk(1, cnext);
+      __syncwarp();
+    };
+    // D = C + acc for chunk c (64 columns) of this warp's slab; acc words are
+    // fp32 (or fp16 in the low half) in r[0..64).
+    auto emit_chunk = [&](int c, const uint32_t (&r)[64]) {
+      if (c > 0) {
+        if (lane == 0) bulk_wait_group_read0();  // previous store has read staging
+        __syncwarp();
+        stage_chunk(cnext);
+        if (c + 1 < kWideBN / 64) load_chunk(c + 1, cnext);
+        __syncwarp();
+      }
+      uint8_t* my_row = stg + lane * 128;
+#pragma unroll
+      for (int s8 = 0; s8 < 8; ++s8) {
+        uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
+        *q = add_c8(p.acc_f16, r + 8 * s8, *q);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int m_row0 = tm * kWideBM + row0;
+      const int n0 = tn * kWideBN + 64 * c;
+      if (lane == 0 && m_row0 < p.M && n0 < p.N) {
+        tma_store_2d(&tmD, stg_u32, n0, m_row0);
+        bulk_commit_group();
+      }
+    };
+    auto load_tmem_chunk = [&](int c, uint32_t (&r)[64]) {
+      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + half * kWideBN;
+      tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+      tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+      tmem_wait_ld();
+      if (c == kWideBN / 64 - 1) {
+        // every TMEM column of this warp is in registers: hand the
+        // accumulator back so the next item's MMAs can start
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty);
+      }
+    };
+    // Warm L2 with this warp's C rows of a whole tile (one row per lane).
+    auto prefetch_c = [&](int idx2) {
+      WideItem nx;
+      if (!wide_item(p, cta, G, idx2, nx)) return;
       int tm2, tn2;
-      tile_coords(t2, p.tiles_m, p.tiles_n, p.group_m, tm2, tn2);
-      const int m2 = tm2 * kWideBM + row0 + static_cast<int>(lane);
+      tile_coords(nx.tile, p.tiles_m, p.tiles_n, p.group_m, tm2, tn2);
+      const int m2 = tm2 * kWideBM + trow;
       const int n2 = tn2 * kWideBN;
       if (m2 < p.M && n2 < p.N) {
         const uint32_t bytes = static_cast<uint32_t>(min(kWideBN, p.N - n2) * 2) & ~15u;
         if (bytes) prefetch_l2(p.CD + static_cast<int64_t>(m2) * p.ldC + n2, bytes);
       }
     };
-    prefetch_c(static_cast<int>(blockIdx.x));
+    prefetch_c(0);
     uint32_t acc_phase = 0;
-    uint4 cnext[8];
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-      // C of the first two chunks does not depend on the MMAs: fetch it now
-      // (once the previous tile's last store has finished reading staging).
-      load_chunk(tm, tn, 0, cnext);
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
-      stage_chunk(cnext);
-      load_chunk(tm, tn, 1, cnext);
-      __syncwarp();
+    WideItem it;
+    for (int idx = 0; wide_item(p, cta, G, idx, it); ++idx) {
+      tile_coords(it.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      // C does not depend on the MMAs: fetch it now (for a partial tile too,
+      // in case this warp turns out to finish it; the staging buffer is
+      // otherwise idle on such an item)
+      preload_c();
+      WideItem nx;
+      const bool last_item = !wide_item(p, cta, G, idx + 1, nx);
       if (!wait_bounded(tfull, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, 0)))
         break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + half * kWideBN;
-      const int m_row0 = tm * kWideBM + row0;
+      if (it.slot < 0) {
+#pragma unroll 1
+        for (int c = 0; c < kWideBN / 64; ++c) {
+          uint32_t r[64];
+          load_tmem_chunk(c, r);
+          emit_chunk(c, r);
+        }
+        acc_phase ^= 1u;
+        prefetch_c(idx + 1);
+        continue;
+      }
+      // Stream-K state of a partial tile.
+      int rt = 0, c_first = 0, c_last = 0, n_mem = 0, n_loads = 0;
+      bool own_in_tmem = true, staged = false;
+      const uint32_t zone = smem_u32(smem + ew * (kFinBufs * kSkBlockBytes));
+      const uint32_t fbar = smem_u32(bars + L::kFinBar0 + ew * kFinBufs);
+      // this warp's 8 KiB block (slab ew, chunk c) of contributor c2's slot
+      auto block_of = [&](int c2, int c) -> const float4* {
+        const int j2 = rt - (c2 * p.sk_per) / p.k_blocks;
+        return reinterpret_cast<const float4*>(p.sk_partials) +
+               static_cast<int64_t>(c2 * p.sk_max_segs + j2) * (kWideBM * kWideBN / 4) +
+               (ew * 4 + c) * (kSkBlockBytes / 16);
+      };
+      // bulk load i: chunk i / n_mem of the (i % n_mem)-th contributor kept in memory
+      auto issue = [&](int i) {
+        const int c = i / n_mem;
+        int c2 = c_first + (i - c * n_mem);
+        if (own_in_tmem && c2 >= cta) ++c2;  // skip this CTA's own term
+        const int buf = i % kFinBufs;
+        mbar_arrive_expect_tx(fbar + 8 * buf, kSkBlockBytes);
+        bulk_load_g2s(zone + buf * kSkBlockBytes, block_of(c2, c), kSkBlockBytes, fbar + 8 * buf);
+      };
+      {
+        // partial tile.  Contributors: CTAs c_first..c_last, every one with
+        // a non-empty share.
+        rt = it.tile - p.sk_tile0;
+        const int u0 = rt * p.k_blocks;
+        c_first = u0 / p.sk_per;
+        c_last = (u0 + p.k_blocks - 1) / p.sk_per;
+        const int n_contrib = c_last - c_first + 1;
+        int* counter = p.sk_counters + rt * 8 + ew;
+        // If every other contributor has already published its slab, this
+        // warp finishes the slab straight from TMEM (no partial of its own
+        // goes through memory); no other warp can then reach the last ticket.
+        const int done = ld_acquire_gpu(counter);  // every lane acquires for its own loads
+        bool finish = done == n_contrib - 1;
+        own_in_tmem = finish;
+        if (!finish) {
+          // publish this slab's fp32 partial sum, then take a ticket
+          float4* part = reinterpret_cast<float4*>(p.sk_partials) +
+                         static_cast<int64_t>(it.slot) * (kWideBM * kWideBN / 4);
+#pragma unroll 1
+          for (int c = 0; c < kWideBN / 64; ++c) {
+            uint32_t r[64];
+            load_tmem_chunk(c, r);
+            float4* dst = part + (ew * 4 + c) * (kSkBlockBytes / 16) + lane;
+#pragma unroll
+            for (int g = 0; g < 16; ++g)
+              dst[32 * g] = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+          }
+          __threadfence();
+          __syncwarp();
+          int ticket = 0;
+          if (lane == 0) ticket = atomicAdd(counter, 1);
+          ticket = __shfl_sync(0xffffffffu, ticket, 0);
+          finish = ticket == n_contrib - 1;
+          if (finish) __threadfence();
+        }
+        if (!finish) {
+          acc_phase ^= 1u;
+          prefetch_c(idx + 1);
+          continue;
+        }
+        // This warp finishes the slab: every other contributor's slab is in
+        // memory.  On the CTA's last item the main-loop stages are idle (its
+        // MMAs have completed), so the blocks come in by bulk copy, three in
+        // flight per warp; otherwise by plain loads.
+        staged = last_item;
+        n_mem = n_contrib - (own_in_tmem ? 1 : 0);
+        n_loads = n_mem * (kWideBN / 64);
+        if (staged && lane == 0) {
+          fence_proxy_async_global();
+          for (int i = 0; i < min(kFinBufs, n_loads); ++i) issue(i);
+        }
+      }
+      bool ok = true;
+      int next = 0;  // next bulk load to consume
 #pragma unroll 1
       for (int c = 0; c < kWideBN / 64; ++c) {
         uint32_t r[64];
-        tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
-        tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-        tmem_wait_ld();
-        if (c == kWideBN / 64 - 1) {
-          // every TMEM column of this warp is in registers: hand the
-          // accumulator back so the next tile's MMAs can start
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty);
-        }
-        if (c > 0) {
-          // the previous chunk's store must have read the staging buffer
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-          stage_chunk(cnext);
-          if (c + 1 < kWideBN / 64) load_chunk(tm, tn, c + 1, cnext);
-          __syncwarp();
-        }
-        // row `lane` of the chunk: D = C + acc in the swizzled layout
-        uint8_t* my_row = stg + lane * 128;
+        {
+          // all terms in CTA order (this CTA's own from TMEM or from memory)
+          float4 acc[16];
 #pragma unroll
-        for (int s8 = 0; s8 < 8; ++s8) {
-          uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
-          *q = add_c8(p.acc_f16, r + 8 * s8, *q);
+          for (int g = 0; g < 16; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+          for (int c2 = c_first; c2 <= c_last; ++c2) {
+            if (own_in_tmem && c2 == cta) {
+              // 16 columns at a time: a whole 64-column chunk next to acc
+              // and the held C chunk would not fit the register budget
+              const uint32_t t_row = tmem_base + ((quad * 32) << 16) + half * kWideBN + c * 64;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t t[16];
+                tmem_ld_32x32b_x16(t_row + 16 * q, t);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                  acc[4 * q + g].x += __uint_as_float(t[4 * g]);
+                  acc[4 * q + g].y += __uint_as_float(t[4 * g + 1]);
+                  acc[4 * q + g].z += __uint_as_float(t[4 * g + 2]);
+                  acc[4 * q + g].w += __uint_as_float(t[4 * g + 3]);
+                }
+              }
+              if (c == kWideBN / 64 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty);
+              }
+            } else if (staged) {
+              const int buf = next % kFinBufs;
+              if (!wait_bounded(fbar + 8 * buf, static_cast<uint32_t>(next / kFinBufs) & 1u,
+                                abort_flag, p.timeout_ns, timeout_code(kRoleEpilogue, 0x10),
+                                false)) {
+                // give the copies still in flight a bounded chance to land
+                for (int i = next + 1; i < min(next + kFinBufs, n_loads); ++i)
+                  wait_bounded(fbar + 8 * (i % kFinBufs), static_cast<uint32_t>(i / kFinBufs) & 1u,
+                               abort_flag, p.timeout_ns, timeout_code(kRoleEpilogue, 0x11), false);
+                ok = false;
+                break;
+              }
+              const float4* blk =
+                  reinterpret_cast<const float4*>(smem + ew * (kFinBufs * kSkBlockBytes) +
+                                                  buf * kSkBlockBytes) +
+                  lane;
+#pragma unroll
+              for (int g = 0; g < 16; ++g) {
+                const float4 v = blk[32 * g];
+                acc[g].x += v.x;
+                acc[g].y += v.y;
+                acc[g].z += v.z;
+                acc[g].w += v.w;
+              }
+              __syncwarp();  // every lane has read the buffer before it is refilled
+              if (lane == 0 && next + kFinBufs < n_loads) {
+                fence_proxy_async_smem();
+                issue(next + kFinBufs);
+              }
+              ++next;
+            } else {
+              const float4* src = block_of(c2, c) + lane;
+              // two halves of eight column groups keep the registers in
+              // budget next to the C chunk held for the next store
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                float4 v[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) v[g] = __ldcg(src + 32 * (8 * h + g));
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                  acc[8 * h + g].x += v[g].x;
+                  acc[8 * h + g].y += v[g].y;
+                  acc[8 * h + g].z += v[g].z;
+                  acc[8 * h + g].w += v[g].w;
+                }
+              }
+            }
+          }
+          if (!ok) break;
+#pragma unroll
+          for (int g = 0; g < 16; ++g) {
+            r[4 * g] = __float_as_uint(acc[g].x);
+            r[4 * g + 1] = __float_as_uint(acc[g].y);
+            r[4 * g + 2] = __float_as_uint(acc[g].z);
+            r[4 * g + 3] = __float_as_uint(acc[g].w);
+          }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int n0 = tn * kWideBN + 64 * c;
-        if (lane == 0 && m_row0 < p.M && n0 < p.N) {
-          tma_store_2d(&tmD, stg_u32, n0, m_row0);
-          bulk_commit_group();
-        }
+        emit_chunk(c, r);
       }
+      if (!ok) break;
       acc_phase ^= 1u;
-      prefetch_c(t + static_cast<int>(gridDim.x));
+      prefetch_c(idx + 1);
     }
     if (lane == 0) bulk_wait_group0();  // all D stores performed before exit
     __syncwarp();

@@ -37,11 +37,14 @@
  *                    added in fp16: the F16F16F16F16 form.
  *
  * Ownership: the caller owns A, B and CD (device memory); the library never
- * frees or retains caller memory.  The skinny path's split-K partial sums
- * live in a workspace taken from the current device's default memory pool
- * with cudaMallocAsync on the call's stream and returned with cudaFreeAsync
- * on the same stream, so calls on different streams never share it (see
- * gemm_tn_skinny_noalloc for a variant that allocates nothing).
+ * frees or retains caller memory.  Workspaces (the skinny path's split-K
+ * partial sums, stream-K partial tiles, repacked strided operands) come from
+ * a memory pool the library creates for each device on first use: taken with
+ * cudaMallocFromPoolAsync on the call's stream and returned with
+ * cudaFreeAsync on the same stream, so calls on different streams never
+ * share them.  The pool keeps up to 1 GiB cached between calls and lives
+ * until process exit (see gemm_tn_skinny_noalloc for a variant that
+ * allocates nothing).
  *
  * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream).  It returns once the kernels are enqueued; D is
@@ -130,6 +133,17 @@ typedef struct {
                            tiles, 2 = CTA-pair 256 x 256 tiles (two SMs per
                            tile, tcgen05 cta_group::2), 3 = single-CTA
                            256 x 256 tiles (tile_n is ignored by 2 and 3) */
+  int stream_k;         /* single-CTA 256 x 256 kernel, fp32 accumulation:
+                           1 = split the last, partial wave of tiles over all
+                           SMs (stream-K: K ranges of equal length, partial
+                           sums through a workspace, added in a fixed order),
+                           0 (default) or -1 = never.  The default is off
+                           because the split's finishing work (partials
+                           pulled through one SM per tile at the end of the
+                           kernel) cost about as much as the balanced wave
+                           saved on every shape measured.  The split needs a
+                           workspace from the library's pool; without one
+                           the call runs unsplit. */
 } gemm_tn_options;
 
 /*
@@ -173,8 +187,8 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
  * multiples of 8, pointers that are only 2-byte aligned, and views with no
  * stride-1 mode.  Two routes:
  *   - repack: operands whose view TMA cannot read are first copied into
- *     row-major buffers taken from the device's stream-ordered memory pool
- *     (cudaMallocAsync / cudaFreeAsync on `stream`), the tile kernels run
+ *     row-major buffers from the library's stream-ordered pool (see
+ *     Ownership at the top of this file), the tile kernels run
  *     on them, and D is scattered back when its view needed a copy;
  *   - copy producer: one kernel whose threads gather 16-byte K chunks
  *     through the strides straight into shared memory; no workspace.
@@ -244,7 +258,7 @@ GEMM_TN_API const char* gemm_tn_status_string(int status);
  *     unpredictable moment;
  *   - programs that must fix their device-memory footprint up front.
  * gemm_tn's skinny path takes its split-K partial sums' workspace from the
- * device memory pool on every call.  This entry point computes the same
+ * library's memory pool on every call.  This entry point computes the same
  * thing with the same kernels, but keeps the partial sums in one fixed
  * array of GEMM_TN_NOALLOC_SCRATCH_BYTES compiled into the library, so no
  * call ever allocates or frees device memory.
