@@ -12,6 +12,11 @@ library route for full-size checks:
 * ``gemm_tn_blas`` -- the same definition with float64 BLAS matmul as its
   one step (used where the triple loop would take minutes, e.g. 8192^3).
 
+``gemm_tn_general`` is the scaled, batched form D = alpha A.B^T + beta C over
+a batch of (ld, major) views ("cute(7) simple_gemm", section 8.1's cuBLAS
+call and section 4's extra modes), with the BLAS conventions for alpha == 0
+and beta == 0.
+
 Operand convention ("Reading CuTe's make_tiled_mma", section "Fix the
 matrices and directions first"): A is (M,K), B is (N,K), C/D are (M,N) and
 D(m,n) = C(m,n) + sum_k A(m,k) B(n,k).  Memory views ("CuTe Layout to Tensor
@@ -78,6 +83,11 @@ def _load():
         lib.oracle_gemm_tn_sampled.restype = i32
         lib.oracle_gemm_tn_sampled.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64,
                                                i32, vp, i64, i64, vp, vp, vp, vp, i32]
+        lib.oracle_gemm_tn_general.restype = i32
+        lib.oracle_gemm_tn_general.argtypes = [i64, i64, i64, i64, ctypes.c_double,
+                                               vp, i64, i64, i64, vp, i64, i64, i64,
+                                               ctypes.c_double, vp, i64, i64, i64,
+                                               vp, vp, i32]
         _lib = lib
         return lib
 
@@ -250,6 +260,39 @@ def gemm_tn_sampled(M, N, K, A, ldA, a_major, B, ldB, b_major, C, ldC,
     d16 = np.empty(len(rows), np.uint16)
     lib.oracle_gemm_tn_sampled(M, N, K, _ptr(A), ldA, a_major, _ptr(B), ldB, b_major,
                                _ptr(C), ldC or 0, len(rows), _ptr(rows), _ptr(cols),
+                               _ptr(d64), _ptr(d16), nthreads or default_threads())
+    return d64, d16
+
+
+def gemm_tn_general(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C=None,
+                    ldC=None, batch=1, strideA=0, strideB=0, strideC=0, want_f16=True,
+                    nthreads=None):
+    """D(l) = alpha * A(l).B(l)^T + beta * C(l) for l < batch.
+
+    Operand l's view is the (ld, major) view of the storage starting at
+    element l * stride (a stride may be 0: the operand is shared).  alpha == 0
+    leaves A and B unread, beta == 0 leaves C unread (C may be None).
+    Returns ``(d64, d16bits)`` of shape (batch, M, N)."""
+    lib = _load()
+    A, B = _bits(A), _bits(B)
+    C = None if C is None else _bits(C)
+    if beta != 0 and C is None:
+        raise ValueError("beta != 0 needs C")
+    vA = (ldA, 1) if a_major == MAJOR_K else (1, ldA)
+    vB = (ldB, 1) if b_major == MAJOR_K else (1, ldB)
+    ldC = N if ldC is None else ldC
+    for l in (0, batch - 1) if batch > 0 else ():
+        if alpha != 0:
+            _check_strided(M, K, A[l * strideA:], vA[0], vA[1], "A")
+            _check_strided(N, K, B[l * strideB:], vB[0], vB[1], "B")
+        if beta != 0:
+            _check_strided(M, N, C[l * strideC:], ldC, 1, "C")
+    d64 = np.empty((batch, M, N), np.float64)
+    d16 = np.empty((batch, M, N), np.uint16) if want_f16 else None
+    lib.oracle_gemm_tn_general(M, N, K, batch, float(alpha),
+                               _ptr(A), vA[0], vA[1], strideA,
+                               _ptr(B), vB[0], vB[1], strideB,
+                               float(beta), _ptr(C), ldC, 1, strideC,
                                _ptr(d64), _ptr(d16), nthreads or default_threads())
     return d64, d16
 

@@ -31,6 +31,12 @@
  * leading dimensions), a library special case (float64 BLAS matmul) and, for
  * the fp16 codec, numpy's IEEE binary16 conversion over every bit pattern.
  *
+ * The scaled, batched form (oracle_gemm_tn_general) follows the
+ * "cute(7) simple_gemm" page, section 8.1: its cuBLAS comparison computes
+ * D = alpha * A.B^T + beta * C, and local_tile's extra modes there (section
+ * 4) carry a batch coordinate; see that function's comment for the
+ * conventions taken where the page is silent.
+ *
  * Arithmetic: fp16 inputs are decoded exactly to fp64; every fp16 x fp16
  * product is exact in fp64 (22 significant bits), and the k-sum runs in
  * ascending k from the initial C(m,n) with no blocking or reordering, so
@@ -319,4 +325,97 @@ ORACLE_EXPORT int oracle_gemm_tn_sampled(int64_t M, int64_t N, int64_t K,
   j.sm = sm;
   j.sn = sn;
   return run_threads(&j, nthreads, count, 1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scaled and batched form                                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  int64_t M, N, K, L;
+  double alpha, beta;
+  const uint16_t *A, *B, *C;
+  int64_t sAm, sAk, sAl, sBn, sBk, sBl, sCm, sCn, sCl;
+  const double* lut;
+  double* out_f64;   /* (L,M,N) row-major, may be NULL */
+  uint16_t* out_f16; /* (L,M,N) row-major, may be NULL */
+  int64_t begin, end; /* range of (l, m) rows */
+} gjob_t;
+
+static void* general_worker(void* arg) {
+  const gjob_t* j = (const gjob_t*)arg;
+  for (int64_t lm = j->begin; lm < j->end; ++lm) {
+    const int64_t l = lm / j->M, m = lm % j->M;
+    for (int64_t n = 0; n < j->N; ++n) {
+      double d = 0.0;
+      if (j->alpha != 0.0) {
+        /* the product term: exact fp16 x fp16 products, ascending k */
+        double s = 0.0;
+        for (int64_t k = 0; k < j->K; ++k) {
+          const double a = j->lut[j->A[l * j->sAl + m * j->sAm + k * j->sAk]];
+          const double b = j->lut[j->B[l * j->sBl + n * j->sBn + k * j->sBk]];
+          s += a * b;
+        }
+        d = j->alpha * s;
+      }
+      if (j->beta != 0.0) d += j->beta * j->lut[j->C[l * j->sCl + m * j->sCm + n * j->sCn]];
+      const int64_t o = (l * j->M + m) * j->N + n;
+      if (j->out_f64) j->out_f64[o] = d;
+      if (j->out_f16) j->out_f16[o] = oracle_double_to_half_rne(d);
+    }
+  }
+  return NULL;
+}
+
+/*
+ * D(l,m,n) = alpha * sum_{k<K} A(l,m,k) * B(l,n,k) + beta * C(l,m,n)
+ * for l < L (the batch), with
+ *   A(l,m,k) = A[l*sAl + m*sAm + k*sAk],  B(l,n,k) = B[l*sBl + n*sBn + k*sBk],
+ *   C(l,m,n) = C[l*sCl + m*sCm + n*sCn]   (a batch stride may be 0).
+ * The sum is formed in fp64 (exact products, ascending k), scaled by alpha,
+ * and beta * C is added; the fp16 result is that fp64 value rounded once.
+ * Where the pages are silent the BLAS conventions hold: alpha == 0 leaves
+ * A and B unread (and K == 0 gives an empty sum), beta == 0 leaves C
+ * unread (C may be NULL), so NaN or Inf there does not reach D.
+ * out_f64 / out_f16 are (L,M,N) row-major (either may be NULL).
+ * Returns the number of threads used.
+ */
+ORACLE_EXPORT int oracle_gemm_tn_general(int64_t M, int64_t N, int64_t K, int64_t L,
+                                         double alpha,
+                                         const uint16_t* A, int64_t sAm, int64_t sAk, int64_t sAl,
+                                         const uint16_t* B, int64_t sBn, int64_t sBk, int64_t sBl,
+                                         double beta,
+                                         const uint16_t* C, int64_t sCm, int64_t sCn, int64_t sCl,
+                                         double* out_f64, uint16_t* out_f16, int nthreads) {
+  gjob_t proto;
+  memset(&proto, 0, sizeof proto);
+  proto.M = M; proto.N = N; proto.K = K; proto.L = L;
+  proto.alpha = alpha; proto.beta = beta;
+  proto.A = A; proto.B = B; proto.C = C;
+  proto.sAm = sAm; proto.sAk = sAk; proto.sAl = sAl;
+  proto.sBn = sBn; proto.sBk = sBk; proto.sBl = sBl;
+  proto.sCm = sCm; proto.sCn = sCn; proto.sCl = sCl;
+  proto.lut = half_lut();
+  proto.out_f64 = out_f64;
+  proto.out_f16 = out_f16;
+  const int64_t total = L * M;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if (total < nthreads) nthreads = total > 0 ? (int)total : 1;
+  pthread_t th[256];
+  gjob_t jobs[256];
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = proto;
+    jobs[t].begin = total * t / nthreads;
+    jobs[t].end = total * (t + 1) / nthreads;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, general_worker, &jobs[t]) != 0) break;
+    started = t;
+  }
+  general_worker(&jobs[0]);
+  for (int t = started + 1; t < nthreads; ++t) general_worker(&jobs[t]);
+  for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+  return nthreads;
 }
