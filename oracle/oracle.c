@@ -347,18 +347,24 @@ static void* general_worker(void* arg) {
   for (int64_t lm = j->begin; lm < j->end; ++lm) {
     const int64_t l = lm / j->M, m = lm % j->M;
     for (int64_t n = 0; n < j->N; ++n) {
-      double d = 0.0;
-      if (j->alpha != 0.0) {
-        /* the product term: exact fp16 x fp16 products, ascending k */
+      /* the product term P = alpha * sum and the C term Q = beta * C, each
+       * present only when its scalar is nonzero (and K > 0 for P) */
+      const int has_p = j->alpha != 0.0 && j->K > 0, has_q = j->beta != 0.0;
+      double p = 0.0, q = 0.0;
+      if (has_p) {
+        /* exact fp16 x fp16 products, ascending k */
         double s = 0.0;
         for (int64_t k = 0; k < j->K; ++k) {
           const double a = j->lut[j->A[l * j->sAl + m * j->sAm + k * j->sAk]];
           const double b = j->lut[j->B[l * j->sBl + n * j->sBn + k * j->sBk]];
           s += a * b;
         }
-        d = j->alpha * s;
+        p = j->alpha * s;
       }
-      if (j->beta != 0.0) d += j->beta * j->lut[j->C[l * j->sCl + m * j->sCm + n * j->sCn]];
+      if (has_q) q = j->beta * j->lut[j->C[l * j->sCl + m * j->sCm + n * j->sCn]];
+      /* an absent term is left out, not added as zero: a lone term keeps its
+       * sign of zero; with neither term D is +0 */
+      const double d = has_p ? (has_q ? p + q : p) : (has_q ? q : 0.0);
       const int64_t o = (l * j->M + m) * j->N + n;
       if (j->out_f64) j->out_f64[o] = d;
       if (j->out_f16) j->out_f16[o] = oracle_double_to_half_rne(d);
@@ -374,9 +380,11 @@ static void* general_worker(void* arg) {
  *   C(l,m,n) = C[l*sCl + m*sCm + n*sCn]   (a batch stride may be 0).
  * The sum is formed in fp64 (exact products, ascending k), scaled by alpha,
  * and beta * C is added; the fp16 result is that fp64 value rounded once.
- * Where the pages are silent the BLAS conventions hold: alpha == 0 leaves
- * A and B unread (and K == 0 gives an empty sum), beta == 0 leaves C
- * unread (C may be NULL), so NaN or Inf there does not reach D.
+ * Where the pages are silent the BLAS conventions hold: alpha == 0 or
+ * K == 0 leaves out the product term and A, B unread; beta == 0 leaves out
+ * the C term and C unread (C may be NULL), so NaN or Inf there does not
+ * reach D.  A term left out is not added as a zero: D is the other term
+ * alone (its sign of zero kept), or +0 when both are left out.
  * out_f64 / out_f16 are (L,M,N) row-major (either may be NULL).
  * Returns the number of threads used.
  */

@@ -169,3 +169,26 @@ def test_degenerate_sizes():
     A, B = h(np.zeros((0, 3, 4))), h(np.zeros((0, 2, 4)))
     d, d16 = run(1.0, A, B, 0.0, None)
     assert d.shape == (0, 3, 2)
+
+
+def test_signed_zero_of_a_lone_term():
+    # A zero sum scaled by a negative alpha with no C term is -0 (P alone);
+    # adding a +0 C term (beta != 0) gives +0 by IEEE addition; beta * C alone
+    # keeps -0 when alpha == 0; with both terms absent D is +0.
+    M, N, K = 3, 4, 5
+    A = h(np.zeros((1, M, K)))
+    B = ints((1, N, K), 19)
+    C = h(np.zeros((1, M, N)))
+    neg0 = np.float16(-0.0).view(np.uint16)
+    pos0 = np.float16(0.0).view(np.uint16)
+    _, d16 = run(-1.0, A, B, 0.0, None)
+    assert (d16 == neg0).all()
+    _, d16 = run(-1.0, A, B, 1.0, C)
+    assert (d16 == pos0).all()
+    _, d16 = run(0.0, A, B, -2.0, C)
+    assert (d16 == neg0).all()
+    _, d16 = run(0.0, A, B, 0.0, None)
+    assert (d16 == pos0).all()
+    # K == 0 leaves the product term out even for a negative alpha
+    _, d16 = run(-3.0, h(np.zeros((1, M, 0))), h(np.zeros((1, N, 0))), 0.0, None)
+    assert (d16 == pos0).all()
