@@ -29,7 +29,8 @@ ERR_NO_MEMORY = 6
 # Every symbol declared in include/gemm_tn.h.
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
             "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc",
-            "gemm_tn_last_kernels", "gemm_tn_strided", "gemm_tn_strided_ex")
+            "gemm_tn_last_kernels", "gemm_tn_strided", "gemm_tn_strided_ex",
+            "gemm_tn_scaled", "gemm_tn_batched", "gemm_tn_batched_ex")
 
 # Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -91,6 +92,16 @@ def lib() -> ctypes.CDLL:
         L.gemm_tn_last_kernels.argtypes = []
         L.gemm_tn_skinny_noalloc.restype = i32
         L.gemm_tn_skinny_noalloc.argtypes = gemm_args
+        f32 = ctypes.c_float
+        batched_args = [i64, i64, i64, i64, f32, vp, i64, i64, i32, vp, i64, i64, i32,
+                        f32, vp, i64, i64, vp, i64, i64, i32, vp]
+        L.gemm_tn_batched.restype = i32
+        L.gemm_tn_batched.argtypes = batched_args
+        L.gemm_tn_batched_ex.restype = i32
+        L.gemm_tn_batched_ex.argtypes = batched_args + [ctypes.POINTER(GemmTnOptions)]
+        L.gemm_tn_scaled.restype = i32
+        L.gemm_tn_scaled.argtypes = [i64, i64, i64, f32, vp, i64, i32, vp, i64, i32, f32,
+                                     vp, i64, vp, i64, i32, vp]
         _lib = L
         return L
 
@@ -119,6 +130,35 @@ def gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, 
     p = ctypes.byref(opts) if opts is not None else None
     return lib().gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype,
                             stream, p)
+
+
+def gemm_tn_scaled(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ldC, D, ldD,
+                   accum_dtype, stream) -> int:
+    """C ``gemm_tn_scaled``: D = alpha * A.B^T + beta * C (C may be 0 when
+    beta == 0)."""
+    return lib().gemm_tn_scaled(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ldC,
+                                D, ldD, accum_dtype, stream)
+
+
+def gemm_tn_batched(M, N, K, batch, alpha, A, ldA, strideA, a_major, B, ldB, strideB, b_major,
+                    beta, C, ldC, strideC, D, ldD, strideD, accum_dtype, stream) -> int:
+    """C ``gemm_tn_batched``: D_l = alpha * A_l.B_l^T + beta * C_l, operand l
+    starting l * stride elements after the base pointer."""
+    return lib().gemm_tn_batched(M, N, K, batch, alpha, A, ldA, strideA, a_major, B, ldB,
+                                 strideB, b_major, beta, C, ldC, strideC, D, ldD, strideD,
+                                 accum_dtype, stream)
+
+
+def gemm_tn_batched_ex(M, N, K, batch, alpha, A, ldA, strideA, a_major, B, ldB, strideB,
+                       b_major, beta, C, ldC, strideC, D, ldD, strideD, accum_dtype, stream,
+                       opts=None) -> int:
+    """C ``gemm_tn_batched_ex``; ``opts`` as for :func:`gemm_tn_ex`."""
+    if isinstance(opts, dict):
+        opts = make_options(**opts)
+    p = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_tn_batched_ex(M, N, K, batch, alpha, A, ldA, strideA, a_major, B, ldB,
+                                    strideB, b_major, beta, C, ldC, strideC, D, ldD, strideD,
+                                    accum_dtype, stream, p)
 
 
 def gemm_tn_check_device_error(stream) -> tuple[int, int]:

@@ -4,6 +4,8 @@
 
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "ptx.cuh"
 
 namespace gemm_tn_dev {
@@ -47,6 +49,55 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+// Epilogue operands and scalars, shared by every kernel:
+//   D(l,m,n) = fp16( alpha * acc(l,m,n) + beta * C(l,m,n) )
+// for batch l (the simple_gemm page's cuBLAS comparison, section 8.1, uses
+// this alpha / beta form).  With scaled == 0 (alpha = beta = 1) the sum is
+// acc + C in the accumulator's precision (fp32, or fp16 for fp16
+// accumulation); otherwise it is formed in fp32 as fma(alpha, acc, beta * C)
+// and rounded once.  With read_c == 0 (beta == 0) the C term is left out:
+// D = alpha * acc, C is not read, and NaN or Inf stored there cannot reach
+// D (an absent term is not added as +0, so a lone -0 stays -0).
+struct EpiArgs {
+  const __half* C;
+  int64_t ldC, sC;  // row and batch strides of C (elements)
+  __half* D;
+  int64_t ldD, sD;  // row and batch strides of D
+  float alpha, beta;
+  int scaled;       // (alpha, beta) != (1, 1)
+  int read_c;       // beta != 0
+};
+
+// Two outputs from fp32 accumulator values and two C values.
+__device__ __forceinline__ __half2 epi_f32x2(const EpiArgs& e, float a0, float a1, __half2 c) {
+  const float2 cf = __half22float2(c);
+  if (!e.scaled) return __floats2half2_rn(a0 + cf.x, a1 + cf.y);
+  if (!e.read_c) return __floats2half2_rn(e.alpha * a0, e.alpha * a1);
+  return __floats2half2_rn(fmaf(e.alpha, a0, e.beta * cf.x), fmaf(e.alpha, a1, e.beta * cf.y));
+}
+
+// Two outputs from an fp16 accumulator pair and two C values.
+__device__ __forceinline__ __half2 epi_f16x2(const EpiArgs& e, __half2 acc, __half2 c) {
+  if (!e.scaled) return __hadd2(acc, c);
+  const float2 af = __half22float2(acc), cf = __half22float2(c);
+  if (!e.read_c) return __floats2half2_rn(e.alpha * af.x, e.alpha * af.y);
+  return __floats2half2_rn(fmaf(e.alpha, af.x, e.beta * cf.x), fmaf(e.alpha, af.y, e.beta * cf.y));
+}
+
+// One output from one accumulator word (fp32, or fp16 in the low half).
+__device__ __forceinline__ __half epi_one(const EpiArgs& e, bool acc_f16, uint32_t a, __half c) {
+  if (acc_f16) {
+    const __half ah = __ushort_as_half(static_cast<unsigned short>(a));
+    if (!e.scaled) return __hadd(ah, c);
+    if (!e.read_c) return __float2half_rn(e.alpha * __half2float(ah));
+    return __float2half_rn(fmaf(e.alpha, __half2float(ah), e.beta * __half2float(c)));
+  }
+  const float af = __uint_as_float(a);
+  if (!e.scaled) return __float2half_rn(af + __half2float(c));
+  if (!e.read_c) return __float2half_rn(e.alpha * af);
+  return __float2half_rn(fmaf(e.alpha, af, e.beta * __half2float(c)));
 }
 
 // Grouped raster over output tiles: runs of `group_m` tile-rows are walked

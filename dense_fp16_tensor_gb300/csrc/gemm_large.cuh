@@ -1,6 +1,8 @@
 // gemm_large.cuh -- persistent, warp-specialised tcgen05 TN GEMM for sm_103a.
 //
 // Computes D(m,n) = C(m,n) + sum_k A(m,k) B(n,k) over 128 x BN output tiles
+// (in general D = alpha * A.B^T + beta * C, over a batch of problems; see
+// EpiArgs)
 // (the CTA tiling and K-block loop of "CuTe Layout to Tensor Core", section
 // 4 "local_tile", and "cute(7) simple_gemm", section "3.4 the K loop"), with
 // the data movement redone for GB300:
@@ -38,11 +40,13 @@ constexpr int kLargeThreads = 192;
 
 struct LargeArgs {
   int M, N, K;
-  __half* CD;
-  int64_t ldC;
+  EpiArgs e;           // C, D, alpha, beta
+  int batch;           // problems; tile t belongs to problem t / tiles_per_batch
+  int tiles_per_batch;  // tiles_m * tiles_n
+  int a_batched, b_batched;  // operand maps carry a batch coordinate (else it is 0)
   int acc_f16;
   int a_mn, b_mn;
-  int tiles_m, tiles_n, num_tiles, k_blocks;
+  int tiles_m, tiles_n, num_tiles, k_blocks;  // num_tiles = batch * tiles_per_batch
   int group_m;
   uint64_t timeout_ns;
   int test_stall;
@@ -71,16 +75,27 @@ struct LargeSmem {
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;  // + alignment slack
 };
 
-// Epilogue of one 32-column chunk for one row: D = C + acc, fp16 out.
-__device__ __forceinline__ void store_chunk(const LargeArgs& p, int m, int n0,
+// Batch and tile coordinates of tile t (grouped raster inside each problem).
+__device__ __forceinline__ void batch_tile(const LargeArgs& p, int t, int& tb, int& tm,
+                                           int& tn) {
+  tb = p.batch > 1 ? t / p.tiles_per_batch : 0;
+  tile_coords(t - tb * p.tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+}
+
+// Epilogue of one 32-column chunk for one row of problem tb:
+// D = alpha * acc + beta * C, fp16 out.
+__device__ __forceinline__ void store_chunk(const LargeArgs& p, int tb, int m, int n0,
                                             const uint32_t (&r)[32]) {
   if (m >= p.M || n0 >= p.N) return;
-  __half* row = p.CD + static_cast<int64_t>(m) * p.ldC;
+  const EpiArgs& e = p.e;
+  const __half* crow = e.C + tb * e.sC + static_cast<int64_t>(m) * e.ldC;
+  __half* drow = e.D + tb * e.sD + static_cast<int64_t>(m) * e.ldD;
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     const int n = n0 + 8 * v;
     if (n + 8 <= p.N) {
-      uint4 c = *reinterpret_cast<const uint4*>(row + n);
+      uint4 c = make_uint4(0u, 0u, 0u, 0u);
+      if (e.read_c) c = *reinterpret_cast<const uint4*>(crow + n);
       const __half2* ch = reinterpret_cast<const __half2*>(&c);
       uint4 o;
       __half2* oh = reinterpret_cast<__half2*>(&o);
@@ -90,21 +105,16 @@ __device__ __forceinline__ void store_chunk(const LargeArgs& p, int m, int n0,
         if (p.acc_f16) {
           const __half2 acc = __halves2half2(__ushort_as_half(static_cast<unsigned short>(lo)),
                                              __ushort_as_half(static_cast<unsigned short>(hi)));
-          oh[j] = __hadd2(acc, ch[j]);
+          oh[j] = epi_f16x2(e, acc, ch[j]);
         } else {
-          const float2 cf = __half22float2(ch[j]);
-          oh[j] = __floats2half2_rn(__uint_as_float(lo) + cf.x, __uint_as_float(hi) + cf.y);
+          oh[j] = epi_f32x2(e, __uint_as_float(lo), __uint_as_float(hi), ch[j]);
         }
       }
-      *reinterpret_cast<uint4*>(row + n) = o;
+      *reinterpret_cast<uint4*>(drow + n) = o;
     } else {
       for (int j = 0; j < 8 && n + j < p.N; ++j) {
-        const uint32_t a = r[8 * v + j];
-        if (p.acc_f16) {
-          row[n + j] = __hadd(__ushort_as_half(static_cast<unsigned short>(a)), row[n + j]);
-        } else {
-          row[n + j] = __float2half_rn(__uint_as_float(a) + __half2float(row[n + j]));
-        }
+        const __half c = e.read_c ? crow[n + j] : __ushort_as_half(0);
+        drow[n + j] = epi_one(e, p.acc_f16, r[8 * v + j], c);
       }
     }
   }
@@ -167,8 +177,9 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       bool ok = true;
       int local = 0;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
-        int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        int tb, tm, tn;
+        batch_tile(p, t, tb, tm, tn);
+        const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
                             timeout_code(kRoleProducer, stage))) {
@@ -183,18 +194,18 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
             mbar_arrive_expect_tx(fb, L::kStageBytes);
             const int k0 = kb * kLargeBK;
             if (!p.a_mn) {
-              tma_load_2d(a_dst, &tmA, fb, k0, tm * kLargeBM);
+              tma_load_3d(a_dst, &tmA, fb, k0, tm * kLargeBM, za);
             } else {
 #pragma unroll
               for (int i = 0; i < kLargeBM / 64; ++i)
-                tma_load_2d(a_dst + i * 8192, &tmA, fb, tm * kLargeBM + 64 * i, k0);
+                tma_load_3d(a_dst + i * 8192, &tmA, fb, tm * kLargeBM + 64 * i, k0, za);
             }
             if (!p.b_mn) {
-              tma_load_2d(b_dst, &tmB, fb, k0, tn * BN);
+              tma_load_3d(b_dst, &tmB, fb, k0, tn * BN, zb);
             } else {
 #pragma unroll
               for (int i = 0; i < BN / 64; ++i)
-                tma_load_2d(b_dst + i * 8192, &tmB, fb, tn * BN + 64 * i, k0);
+                tma_load_3d(b_dst + i * 8192, &tmB, fb, tn * BN + 64 * i, k0, zb);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -267,8 +278,8 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     const int row_in_tile = static_cast<int>(quad * 32 + lane);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      int tb, tm, tn;
+      batch_tile(p, t, tb, tm, tn);
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, acc)))
         break;
@@ -280,7 +291,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_wait_ld();
-        store_chunk(p, m, tn * BN + c * 32, r);
+        store_chunk(p, tb, m, tn * BN + c * 32, r);
       }
       tc_fence_before();
       __syncwarp();

@@ -105,8 +105,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       bool ok = true;
       int local = 0;
       for (int t = pair; ok && t < p.num_tiles; t += num_pairs, ++local) {
-        int tm, tn;
-        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        int tb, tm, tn;
+        batch_tile(p, t, tb, tm, tn);
+        const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
         const int a_row = tm * kPairBM + 128 * static_cast<int>(rank);
         const int b_row = tn * kPairBN + 128 * static_cast<int>(rank);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -122,16 +123,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_arrive_expect_tx(fb, L::kStageBytes);
             const int k0 = kb * kPairBK;
             if (!p.a_mn) {
-              tma_load_2d(a_dst, &tmA, fb, k0, a_row);
+              tma_load_3d(a_dst, &tmA, fb, k0, a_row, za);
             } else {
-              tma_load_2d(a_dst, &tmA, fb, a_row, k0);
-              tma_load_2d(a_dst + 8192, &tmA, fb, a_row + 64, k0);
+              tma_load_3d(a_dst, &tmA, fb, a_row, k0, za);
+              tma_load_3d(a_dst + 8192, &tmA, fb, a_row + 64, k0, za);
             }
             if (!p.b_mn) {
-              tma_load_2d(b_dst, &tmB, fb, k0, b_row);
+              tma_load_3d(b_dst, &tmB, fb, k0, b_row, zb);
             } else {
-              tma_load_2d(b_dst, &tmB, fb, b_row, k0);
-              tma_load_2d(b_dst + 8192, &tmB, fb, b_row + 64, k0);
+              tma_load_3d(b_dst, &tmB, fb, b_row, k0, zb);
+              tma_load_3d(b_dst + 8192, &tmB, fb, b_row + 64, k0, zb);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -224,8 +225,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < p.num_tiles; t += num_pairs) {
-      int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      int tb, tm, tn;
+      batch_tile(p, t, tb, tm, tn);
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, acc), true, peer_abort))
         break;
@@ -237,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_wait_ld();
-        store_chunk(p, m, tn * kPairBN + c * 32, r);
+        store_chunk(p, tb, m, tn * kPairBN + c * 32, r);
       }
       tc_fence_before();
       __syncwarp();

@@ -259,8 +259,9 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   }
 }
 
-// D(m,n) = fp16( sum over the CTAs that touched tile n/128, in CTA order, of
-// their partial (n%128, m)  +  C(m,n) ).  Block (tile, y) has 512 threads;
+// D(m,n) = fp16( alpha * (sum over the CTAs that touched tile n/128, in CTA
+// order, of their partial (n%128, m))  +  beta * C(m,n) ) -- see EpiArgs;
+// with alpha = beta = 1 the sum plus C.  Block (tile, y) has 512 threads;
 // thread (g, r) owns column n = 128*tile + r and rows 4g..4g+3 with
 // g = 4y + threadIdx.x/128, reads one 16-byte vector of partials per
 // contributing CTA, and adds C once.  The kernel is
@@ -271,7 +272,7 @@ constexpr int kReduceThreads = 4 * kSkinnyBN;  // four 4-row groups per block
 
 template <int MP>
 __global__ void __launch_bounds__(kReduceThreads)
-    gemm_tn_splitk_reduce_kernel(const SkinnyArgs p, __half* CD, int64_t ldC) {
+    gemm_tn_splitk_reduce_kernel(const SkinnyArgs p, const EpiArgs e) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tile = static_cast<int>(blockIdx.x);
   const int r = static_cast<int>(threadIdx.x) % kSkinnyBN;
@@ -299,8 +300,8 @@ __global__ void __launch_bounds__(kReduceThreads)
   for (int j = 0; j < 4; ++j) {
     const int m = 4 * g + j;
     if (m < p.M) {
-      __half* d = CD + static_cast<int64_t>(m) * ldC + n;
-      *d = __float2half_rn(v[j] + __half2float(*d));
+      const __half c = e.read_c ? e.C[static_cast<int64_t>(m) * e.ldC + n] : __ushort_as_half(0);
+      e.D[static_cast<int64_t>(m) * e.ldD + n] = epi_one(e, false, __float_as_uint(v[j]), c);
     }
   }
 }

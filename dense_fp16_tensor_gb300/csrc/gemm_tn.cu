@@ -10,6 +10,9 @@
 //   * the choice between the persistent tile kernel and the skinny split-K
 //     kernel, and their grid sizes (one CTA per SM);
 //   * the skinny path's stream-ordered split-K workspace.
+// Every entry point describes its call as one Problem (a batch of
+// D = alpha * A.B^T + beta * C); gemm_tn itself is the case batch 1,
+// alpha = beta = 1, D = C in place.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -27,6 +30,7 @@
 #include "gemm_skinny.cuh"
 #include "gemm_strided.cuh"
 #include "repack.cuh"
+#include "scale.cuh"
 
 namespace {
 
@@ -178,17 +182,79 @@ int encode_operand(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, i
   return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
 }
 
-// Tensor map over C/D (M,N):(ldC,1) for 32-row x 64-column epilogue boxes
-// with the 128-byte swizzle (the staging layout); out-of-range rows and
-// columns of a stored box are not written.
-int encode_cd(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int64_t ldC) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldC) * 2};
-  cuuint32_t box[2] = {64, 32}, estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides, box, estr,
+// The same over a batch: dims {inner, outer, L} with batch stride `bstride`
+// elements.  A shared operand (bstride 0) or a single problem gets a batch
+// extent of 1 (its coordinate is always 0) and a nominal stride.
+int encode_operand_batched(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K,
+                           int64_t ld, int64_t bstride, int64_t L, int mn_major,
+                           uint32_t box_rows) {
+  const int64_t inner = mn_major ? rows : K, outer = mn_major ? K : rows;
+  const bool batched = L > 1 && bstride != 0;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer),
+                        static_cast<cuuint64_t>(batched ? L : 1)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+                           static_cast<cuuint64_t>(batched ? bstride : outer * ld) * 2};
+  cuuint32_t box[3] = {64, mn_major ? 64u : box_rows, 1}, estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
+}
+
+// Tensor map over D, a batch of (M,N):(ldD,1) views sD elements apart, for
+// 32-row x 64-column epilogue boxes with the 128-byte swizzle (the staging
+// layout); out-of-range rows and columns of a stored box are not written.
+int encode_d(CUtensorMap* map, void* ptr, int64_t M, int64_t N, int64_t ldD, int64_t sD,
+             int64_t L) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M),
+                        static_cast<cuuint64_t>(L > 1 ? L : 1)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldD) * 2,
+                           static_cast<cuuint64_t>(L > 1 ? sD : M * ldD) * 2};
+  cuuint32_t box[3] = {64, 32, 1}, estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ptr, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
+}
+
+// One call: a batch of L problems D = alpha * A.B^T + beta * C, operand l's
+// view starting l * stride elements after the base pointer.
+struct Problem {
+  int64_t M, N, K, L;
+  float alpha, beta;
+  const void* A;
+  int64_t ldA, sA;
+  int a_major;
+  const void* B;
+  int64_t ldB, sB;
+  int b_major;
+  const void* C;
+  int64_t ldC, sC;
+  void* D;
+  int64_t ldD, sD;
+  int accum;
+  bool use_ab() const { return alpha != 0.f && K > 0; }
+  bool read_c() const { return beta != 0.f; }
+  bool in_place() const {
+    return C == D && ldC == ldD && (L <= 1 || sC == sD);
+  }
+};
+
+EpiArgs epi_of(const Problem& q) {
+  EpiArgs e;
+  std::memset(&e, 0, sizeof e);
+  e.read_c = q.read_c() ? 1 : 0;
+  e.C = e.read_c ? static_cast<const __half*>(q.C) : nullptr;
+  e.ldC = q.ldC;
+  e.sC = q.L > 1 ? q.sC : 0;
+  e.D = static_cast<__half*>(q.D);
+  e.ldD = q.ldD;
+  e.sD = q.L > 1 ? q.sD : 0;
+  e.alpha = q.alpha;
+  e.beta = q.beta;
+  e.scaled = (q.alpha != 1.f || q.beta != 1.f) ? 1 : 0;
+  return e;
 }
 
 // Byte range [lo, hi) touched by a (rows, cols) view with the given major.
@@ -200,44 +266,102 @@ void extent(const void* p, int64_t rows, int64_t cols, int64_t ld, int mn_major,
   hi = lo + static_cast<uintptr_t>(((outer - 1) * ld + inner) * 2);
 }
 
-int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
-             const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum) {
+// Byte range [lo, hi) touched by L views of (rows, cols) `stride` elements apart.
+void extent_batched(const void* p, int64_t rows, int64_t cols, int64_t ld, int mn_major,
+                    int64_t stride, int64_t L, uintptr_t& lo, uintptr_t& hi) {
+  extent(p, rows, cols, ld, mn_major, lo, hi);
+  if (L > 1) hi += static_cast<uintptr_t>((L - 1) * stride * 2);
+}
+
+bool overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+int validate(const Problem& q) {
   const int64_t kMax = 0x7FFFFFFF;
-  if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM_TN_ERR_INVALID_ARG;
-  if ((a_major != GEMM_TN_MAJOR_K && a_major != GEMM_TN_MAJOR_MN) ||
-      (b_major != GEMM_TN_MAJOR_K && b_major != GEMM_TN_MAJOR_MN))
+  if (q.M < 0 || q.N < 0 || q.K < 0 || q.L < 0 || q.M > kMax || q.N > kMax || q.K > kMax ||
+      q.L > kMax)
     return GEMM_TN_ERR_INVALID_ARG;
-  if (accum != GEMM_TN_ACC_F32 && accum != GEMM_TN_ACC_F16) return GEMM_TN_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return GEMM_TN_OK;
-  if (CD == nullptr || ldC < N || ldC > kMax) return GEMM_TN_ERR_INVALID_ARG;
-  if (K > 0) {
-    if (A == nullptr || B == nullptr) return GEMM_TN_ERR_INVALID_ARG;
-    if (ldA < (a_major ? M : K) || ldB < (b_major ? N : K) || ldA > kMax || ldB > kMax)
+  if ((q.a_major != GEMM_TN_MAJOR_K && q.a_major != GEMM_TN_MAJOR_MN) ||
+      (q.b_major != GEMM_TN_MAJOR_K && q.b_major != GEMM_TN_MAJOR_MN))
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (q.accum != GEMM_TN_ACC_F32 && q.accum != GEMM_TN_ACC_F16) return GEMM_TN_ERR_INVALID_ARG;
+  if (q.M == 0 || q.N == 0 || q.L == 0) return GEMM_TN_OK;
+  const bool batched = q.L > 1;
+  // D: written; batches may not overlap one another
+  if (q.D == nullptr || q.ldD < q.N || q.ldD > kMax) return GEMM_TN_ERR_INVALID_ARG;
+  if (batched && q.sD < q.M * q.ldD) return GEMM_TN_ERR_INVALID_ARG;
+  uintptr_t d0, d1;
+  extent_batched(q.D, q.M, q.N, q.ldD, 0, q.sD, q.L, d0, d1);
+  if (q.read_c()) {
+    if (q.C == nullptr || q.ldC < q.N || q.ldC > kMax || (batched && q.sC < 0))
       return GEMM_TN_ERR_INVALID_ARG;
-    uintptr_t a0, a1, b0, b1, c0, c1;
-    extent(A, M, K, ldA, a_major, a0, a1);
-    extent(B, N, K, ldB, b_major, b0, b1);
-    extent(CD, M, N, ldC, 0, c0, c1);
-    if ((c0 < a1 && a0 < c1) || (c0 < b1 && b0 < c1)) return GEMM_TN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
-      return GEMM_TN_ERR_ALIGNMENT;
-    if ((ldA | ldB) & 7) return GEMM_TN_ERR_ALIGNMENT;
+    if (!q.in_place()) {
+      uintptr_t c0, c1;
+      extent_batched(q.C, q.M, q.N, q.ldC, 0, q.sC, q.L, c0, c1);
+      if (overlap(c0, c1, d0, d1)) return GEMM_TN_ERR_INVALID_ARG;
+    }
   }
-  if ((reinterpret_cast<uintptr_t>(CD) & 15u) || (ldC & 7)) return GEMM_TN_ERR_ALIGNMENT;
+  if (q.use_ab()) {
+    if (q.A == nullptr || q.B == nullptr) return GEMM_TN_ERR_INVALID_ARG;
+    const int64_t a_outer = q.a_major ? q.K : q.M, b_outer = q.b_major ? q.K : q.N;
+    if (q.ldA < (q.a_major ? q.M : q.K) || q.ldB < (q.b_major ? q.N : q.K) || q.ldA > kMax ||
+        q.ldB > kMax)
+      return GEMM_TN_ERR_INVALID_ARG;
+    // batch strides: 0 (one operand for every problem) or whole views apart
+    if (batched && ((q.sA != 0 && q.sA < a_outer * q.ldA) || (q.sB != 0 && q.sB < b_outer * q.ldB) ||
+                    q.sA < 0 || q.sB < 0))
+      return GEMM_TN_ERR_INVALID_ARG;
+    uintptr_t a0, a1, b0, b1;
+    extent_batched(q.A, q.M, q.K, q.ldA, q.a_major, q.sA, q.L, a0, a1);
+    extent_batched(q.B, q.N, q.K, q.ldB, q.b_major, q.sB, q.L, b0, b1);
+    if (overlap(d0, d1, a0, a1) || overlap(d0, d1, b0, b1)) return GEMM_TN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q.A) | reinterpret_cast<uintptr_t>(q.B)) & 15u)
+      return GEMM_TN_ERR_ALIGNMENT;
+    if ((q.ldA | q.ldB) & 7) return GEMM_TN_ERR_ALIGNMENT;
+    if (batched && ((q.sA | q.sB) & 7)) return GEMM_TN_ERR_ALIGNMENT;
+  }
+  if ((reinterpret_cast<uintptr_t>(q.D) & 15u) || (q.ldD & 7) || (batched && (q.sD & 7)))
+    return GEMM_TN_ERR_ALIGNMENT;
+  if (q.read_c() && ((reinterpret_cast<uintptr_t>(q.C) & 15u) || (q.ldC & 7) ||
+                     (batched && (q.sC & 7))))
+    return GEMM_TN_ERR_ALIGNMENT;
   return GEMM_TN_OK;
 }
 
-int plan(int64_t M, int a_major, int b_major, int accum, int requested) {
+// The legacy in-place description: one problem, D = C + A.B^T in CD.
+Problem in_place_problem(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA,
+                         int a_major, const void* B, int64_t ldB, int b_major, void* CD,
+                         int64_t ldC, int accum) {
+  Problem q;
+  std::memset(&q, 0, sizeof q);
+  q.M = M; q.N = N; q.K = K; q.L = 1;
+  q.alpha = 1.f; q.beta = 1.f;
+  q.A = A; q.ldA = ldA; q.a_major = a_major;
+  q.B = B; q.ldB = ldB; q.b_major = b_major;
+  q.C = CD; q.ldC = ldC;
+  q.D = CD; q.ldD = ldC;
+  q.accum = accum;
+  return q;
+}
+
+// Argument checks of the in-place form (the allocation-free entry point
+// uses them too).
+int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
+             const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum) {
+  return validate(in_place_problem(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum));
+}
+
+int plan(int64_t M, int a_major, int b_major, int accum, int requested, int64_t L = 1) {
   const bool skinny_ok = M <= kSkinnyMaxM && a_major == GEMM_TN_MAJOR_K &&
-                         b_major == GEMM_TN_MAJOR_K && accum == GEMM_TN_ACC_F32;
+                         b_major == GEMM_TN_MAJOR_K && accum == GEMM_TN_ACC_F32 && L <= 1;
   if (requested == GEMM_TN_PATH_SKINNY) return skinny_ok ? GEMM_TN_PATH_SKINNY : -1;
   if (requested == GEMM_TN_PATH_LARGE) return GEMM_TN_PATH_LARGE;
   return skinny_ok ? GEMM_TN_PATH_SKINNY : GEMM_TN_PATH_LARGE;
 }
 
-int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_major,
-                 const void* B, int64_t ldB, int b_major, void* CD, int64_t ldC, int accum,
-                 cudaStream_t stream, const gemm_tn_options& o, const DeviceState& st) {
+int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
+                 const DeviceState& st) {
+  const int64_t M = q.M, N = q.N, K = q.K;
+  const int a_major = q.a_major, b_major = q.b_major, accum = q.accum;
   // Kernel choice: 256 x 256 single-CTA tiles (fewest operand bytes per
   // flop per SM) unless the problem is too small to fill them or the caller
   // asked for another tile kernel.
@@ -248,23 +372,30 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   const int bn = (pair || wide) ? 256 : ((o.tile_n == 128) ? 128 : 256);
   const int bm = (pair || wide) ? 256 : kLargeBM;
   CUtensorMap tmA, tmB;
-  int s = encode_operand(&tmA, A, M, K, ldA, a_major, wide ? 256 : kLargeBM);
+  int s = encode_operand_batched(&tmA, q.A, M, K, q.ldA, q.sA, q.L, a_major,
+                                 wide ? 256 : kLargeBM);
   if (s == GEMM_TN_OK)
-    s = encode_operand(&tmB, B, N, K, ldB, b_major, static_cast<uint32_t>(pair ? 128 : bn));
+    s = encode_operand_batched(&tmB, q.B, N, K, q.ldB, q.sB, q.L, b_major,
+                               static_cast<uint32_t>(pair ? 128 : bn));
   if (s != GEMM_TN_OK) return s;
   LargeArgs p;
   std::memset(&p, 0, sizeof p);
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.CD = static_cast<__half*>(CD);
-  p.ldC = ldC;
+  p.e = epi_of(q);
   p.acc_f16 = accum == GEMM_TN_ACC_F16;
   p.a_mn = a_major;
   p.b_mn = b_major;
   p.tiles_m = static_cast<int>((M + bm - 1) / bm);
   p.tiles_n = static_cast<int>((N + bn - 1) / bn);
-  p.num_tiles = p.tiles_m * p.tiles_n;
+  const int64_t per_batch = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (per_batch * q.L > 0x7FFFFFFF) return GEMM_TN_ERR_UNSUPPORTED;
+  p.batch = static_cast<int>(q.L);
+  p.tiles_per_batch = static_cast<int>(per_batch);
+  p.a_batched = q.L > 1 && q.sA != 0;
+  p.b_batched = q.L > 1 && q.sB != 0;
+  p.num_tiles = static_cast<int>(per_batch * q.L);
   p.k_blocks = static_cast<int>((K + kLargeBK - 1) / kLargeBK);
   p.group_m = (pair || wide) ? 8 : 16;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
@@ -273,7 +404,7 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
   void* sk_ws = nullptr;
   if (wide) {
     CUtensorMap tmD;
-    s = encode_cd(&tmD, CD, M, N, ldC);
+    s = encode_d(&tmD, q.D, M, N, q.ldD, q.sD, q.L);
     if (s != GEMM_TN_OK) return s;
     int grid = std::min(p.num_tiles, st.num_sms);
     // Stream-K for the last, partial wave, on request only (fp32
@@ -341,7 +472,7 @@ int launch_large(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, in
 // Split-K kernel and its reduction for one MMA width MP.
 template <int MP>
 cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const SkinnyArgs& p, __half* CD, int64_t ldC, cudaStream_t stream) {
+                             const SkinnyArgs& p, const EpiArgs& ep, cudaStream_t stream) {
   gemm_tn_skinny_kernel<kSkinnyStages, MP>
       <<<grid, kSkinnyThreads, SkinnySmem<kSkinnyStages, MP>::kDynamicBytes, stream>>>(tmA, tmB,
                                                                                       p);
@@ -358,26 +489,26 @@ cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm_tn_splitk_reduce_kernel<MP>, p, CD, ldC);
+  e = cudaLaunchKernelEx(&cfg, gemm_tn_splitk_reduce_kernel<MP>, p, ep);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_skinny_kernels(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                  const SkinnyArgs& p, void* CD, int64_t ldC,
+                                  const SkinnyArgs& p, const EpiArgs& ep,
                                   cudaStream_t stream) {
-  __half* cd = static_cast<__half*>(CD);
   switch (p.mp) {
-    case 16: return launch_skinny_mp<16>(grid, tmA, tmB, p, cd, ldC, stream);
-    case 32: return launch_skinny_mp<32>(grid, tmA, tmB, p, cd, ldC, stream);
-    case 48: return launch_skinny_mp<48>(grid, tmA, tmB, p, cd, ldC, stream);
-    default: return launch_skinny_mp<64>(grid, tmA, tmB, p, cd, ldC, stream);
+    case 16: return launch_skinny_mp<16>(grid, tmA, tmB, p, ep, stream);
+    case 32: return launch_skinny_mp<32>(grid, tmA, tmB, p, ep, stream);
+    case 48: return launch_skinny_mp<48>(grid, tmA, tmB, p, ep, stream);
+    default: return launch_skinny_mp<64>(grid, tmA, tmB, p, ep, stream);
   }
 }
 
-int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, const void* B,
-                  int64_t ldB, void* CD, int64_t ldC, cudaStream_t stream,
-                  const gemm_tn_options& o, const DeviceState& st) {
+int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
+                  const DeviceState& st) {
+  const int64_t M = q.M, N = q.N, K = q.K, ldA = q.ldA, ldB = q.ldB;
+  const void *A = q.A, *B = q.B;
   SkinnyArgs p;
   std::memset(&p, 0, sizeof p);
   p.M = static_cast<int>(M);
@@ -411,7 +542,7 @@ int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, c
     return GEMM_TN_ERR_NO_MEMORY;
   }
   p.ws = static_cast<float*>(ws);
-  const cudaError_t e = launch_skinny_kernels(grid, tmA, tmB, p, CD, ldC, stream);
+  const cudaError_t e = launch_skinny_kernels(grid, tmA, tmB, p, epi_of(q), stream);
   const cudaError_t f = cudaFreeAsync(ws, stream);
   if (e != cudaSuccess || f != cudaSuccess) {
     cudaGetLastError();
@@ -419,6 +550,65 @@ int launch_skinny(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, c
   }
   t_last_launches = 2;
   t_last_kernels = "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel";
+  return GEMM_TN_OK;
+}
+
+// D = beta * C (or zero) when the product term is absent.
+int launch_scale(const Problem& q, cudaStream_t stream, const DeviceState& st) {
+  const int64_t groups = (q.N + 7) / 8;
+  const int64_t total = q.L * q.M * groups;
+  const int64_t want = (total + kScaleThreads - 1) / kScaleThreads;
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 8LL * st.num_sms)));
+  gemm_tn_scale_kernel<<<grid, kScaleThreads, 0, stream>>>(
+      static_cast<int>(q.M), static_cast<int>(q.N), static_cast<int>(q.L), epi_of(q));
+  if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  t_last_launches = 1;
+  t_last_kernels = "gemm_tn_scale_kernel";
+  return GEMM_TN_OK;
+}
+
+bool options_ok(const gemm_tn_options& o) {
+  return !(o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
+           (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) || o.tile_kernel < 0 ||
+           o.tile_kernel > 3);
+}
+
+int device_state(DeviceState*& st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return device_setup(dev, st);
+}
+
+// Every entry point but the strided and allocation-free ones ends here.
+int run_problem(const Problem& q, void* stream, const gemm_tn_options* opts) {
+  t_last_launches = 0;
+  t_last_kernels = "";
+  gemm_tn_options o;
+  std::memset(&o, 0, sizeof o);
+  if (opts) o = *opts;
+  if (!options_ok(o)) return GEMM_TN_ERR_INVALID_ARG;
+  int s = validate(q);
+  if (s != GEMM_TN_OK) return s;
+  if (q.M == 0 || q.N == 0 || q.L == 0) return GEMM_TN_OK;
+  // D = beta * C: nothing to do in place with beta == 1
+  if (!q.use_ab() && q.beta == 1.f && q.in_place()) return GEMM_TN_OK;
+
+  const int path = plan(q.M, q.a_major, q.b_major, q.accum, o.path, q.L);
+  if (path < 0) return GEMM_TN_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  s = device_state(st);
+  if (s != GEMM_TN_OK) return s;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (!q.use_ab())
+    s = launch_scale(q, cs, *st);
+  else if (path == GEMM_TN_PATH_SKINNY)
+    s = launch_skinny(q, cs, o, *st);
+  else
+    s = launch_large(q, cs, o, *st);
+  if (s != GEMM_TN_OK) return s;
+  if (o.sync_check) return gemm_tn_check_device_error(stream, nullptr);
   return GEMM_TN_OK;
 }
 
@@ -448,39 +638,45 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64
                            int a_major, const void* B, int64_t ldB, int b_major, void* CD,
                            int64_t ldC, int accum_dtype, void* stream,
                            const gemm_tn_options* opts) {
-  t_last_launches = 0;
-  t_last_kernels = "";
-  gemm_tn_options o;
-  std::memset(&o, 0, sizeof o);
-  if (opts) o = *opts;
-  if (o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
-      (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) || o.tile_kernel < 0 ||
-      o.tile_kernel > 3)
-    return GEMM_TN_ERR_INVALID_ARG;
-  int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
-  if (s != GEMM_TN_OK) return s;
-  if (M == 0 || N == 0 || K == 0) return GEMM_TN_OK;  // D = C: nothing to do
+  return run_problem(
+      in_place_problem(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype), stream,
+      opts);
+}
 
-  const int path = plan(M, a_major, b_major, accum_dtype, o.path);
-  if (path < 0) return GEMM_TN_ERR_INVALID_ARG;
+GEMM_TN_API int gemm_tn_batched_ex(int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+                                   const void* A, int64_t ldA, int64_t strideA, int a_major,
+                                   const void* B, int64_t ldB, int64_t strideB, int b_major,
+                                   float beta, const void* C, int64_t ldC, int64_t strideC,
+                                   void* D, int64_t ldD, int64_t strideD, int accum_dtype,
+                                   void* stream, const gemm_tn_options* opts) {
+  Problem q;
+  std::memset(&q, 0, sizeof q);
+  q.M = M; q.N = N; q.K = K; q.L = batch;
+  q.alpha = alpha; q.beta = beta;
+  q.A = A; q.ldA = ldA; q.sA = strideA; q.a_major = a_major;
+  q.B = B; q.ldB = ldB; q.sB = strideB; q.b_major = b_major;
+  q.C = C; q.ldC = ldC; q.sC = strideC;
+  q.D = D; q.ldD = ldD; q.sD = strideD;
+  q.accum = accum_dtype;
+  return run_problem(q, stream, opts);
+}
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
-  DeviceState* st = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    s = device_setup(dev, st);
-  }
-  if (s != GEMM_TN_OK) return s;
+GEMM_TN_API int gemm_tn_batched(int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+                                const void* A, int64_t ldA, int64_t strideA, int a_major,
+                                const void* B, int64_t ldB, int64_t strideB, int b_major,
+                                float beta, const void* C, int64_t ldC, int64_t strideC, void* D,
+                                int64_t ldD, int64_t strideD, int accum_dtype, void* stream) {
+  return gemm_tn_batched_ex(M, N, K, batch, alpha, A, ldA, strideA, a_major, B, ldB, strideB,
+                            b_major, beta, C, ldC, strideC, D, ldD, strideD, accum_dtype, stream,
+                            nullptr);
+}
 
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (path == GEMM_TN_PATH_SKINNY)
-    s = launch_skinny(M, N, K, A, ldA, B, ldB, CD, ldC, cs, o, *st);
-  else
-    s = launch_large(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, cs, o, *st);
-  if (s != GEMM_TN_OK) return s;
-  if (o.sync_check) return gemm_tn_check_device_error(stream, nullptr);
-  return GEMM_TN_OK;
+GEMM_TN_API int gemm_tn_scaled(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                               int64_t ldA, int a_major, const void* B, int64_t ldB, int b_major,
+                               float beta, const void* C, int64_t ldC, void* D, int64_t ldD,
+                               int accum_dtype, void* stream) {
+  return gemm_tn_batched_ex(M, N, K, 1, alpha, A, ldA, 0, a_major, B, ldB, 0, b_major, beta, C,
+                            ldC, 0, D, ldD, 0, accum_dtype, stream, nullptr);
 }
 
 GEMM_TN_API int gemm_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA,
@@ -598,7 +794,9 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   if (s != GEMM_TN_OK) return s;
 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (launch_skinny_kernels(grid, tmA, tmB, p, CD, ldC, cs) != cudaSuccess) {
+  const EpiArgs ep =
+      epi_of(in_place_problem(M, N, K, A, ldA, 0, B, ldB, 0, CD, ldC, GEMM_TN_ACC_F32));
+  if (launch_skinny_kernels(grid, tmA, tmB, p, ep, cs) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_TN_ERR_CUDA;
   }
@@ -731,12 +929,10 @@ int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
     gemm_tn_options o;
     std::memset(&o, 0, sizeof o);
     const int path = plan(M, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
-    if (path == GEMM_TN_PATH_SKINNY) {
-      s = launch_skinny(M, N, K, Ause, ldA, Buse, ldB, Cuse, ldC, stream, o, st);
-    } else {
-      s = launch_large(M, N, K, Ause, ldA, a_major, Buse, ldB, b_major, Cuse, ldC, accum, stream,
-                       o, st);
-    }
+    const Problem q =
+        in_place_problem(M, N, K, Ause, ldA, a_major, Buse, ldB, b_major, Cuse, ldC, accum);
+    s = path == GEMM_TN_PATH_SKINNY ? launch_skinny(q, stream, o, st)
+                                    : launch_large(q, stream, o, st);
     launches += t_last_launches;
     gemm_kernels = t_last_kernels;
   } else {

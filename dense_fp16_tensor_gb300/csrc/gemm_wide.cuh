@@ -18,7 +18,9 @@
 //     with the 128-byte swizzle: C rows arrive with coalesced 128-byte loads
 //     (the first chunk's before the accumulator is even ready, the others
 //     one chunk ahead), each lane adds its TMEM row in the swizzled layout
-//     (conflict-free), and D leaves by TMA store, which also clips the tails.
+//     (conflict-free), and D leaves by TMA store, which also clips the tails
+//     (all but a right edge with N % 8 != 0: the TMA store writes whole
+//     16-byte pieces, so that chunk is copied out with plain stores).
 //     The next tile's C rows are prefetched into L2 during its main loop, and
 //     the TMA ring keeps loading the next tile's first stages meanwhile.
 //
@@ -81,21 +83,21 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
                : "memory");
 }
 
-// Eight fp16 values of C (uint4) plus eight accumulator words -> eight fp16 of D.
-__device__ __forceinline__ uint4 add_c8(bool acc_f16, const uint32_t* r, uint4 c) {
+// Eight fp16 values of C (uint4) plus eight accumulator words -> eight fp16
+// of D = alpha * acc + beta * C.
+__device__ __forceinline__ uint4 add_c8(const LargeArgs& p, const uint32_t* r, uint4 c) {
   const __half2* ch = reinterpret_cast<const __half2*>(&c);
   uint4 o;
   __half2* oh = reinterpret_cast<__half2*>(&o);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t lo = r[2 * j], hi = r[2 * j + 1];
-    if (acc_f16) {
+    if (p.acc_f16) {
       const __half2 acc = __halves2half2(__ushort_as_half(static_cast<unsigned short>(lo)),
                                          __ushort_as_half(static_cast<unsigned short>(hi)));
-      oh[j] = __hadd2(acc, ch[j]);
+      oh[j] = epi_f16x2(p.e, acc, ch[j]);
     } else {
-      const float2 cf = __half22float2(ch[j]);
-      oh[j] = __floats2half2_rn(__uint_as_float(lo) + cf.x, __uint_as_float(hi) + cf.y);
+      oh[j] = epi_f32x2(p.e, __uint_as_float(lo), __uint_as_float(hi), ch[j]);
     }
   }
   return o;
@@ -103,10 +105,11 @@ __device__ __forceinline__ uint4 add_c8(bool acc_f16, const uint32_t* r, uint4 c
 
 // One 16-byte piece of a 32 x 64 C chunk for the coalesced load pattern:
 // load i (0..7) of lane l covers row 4i + l/8, columns 8*(l%8) .. +8.
-__device__ __forceinline__ uint4 load_c_piece(const LargeArgs& p, int m, int n) {
+// cb is problem tb's C; zeros when C is not read.
+__device__ __forceinline__ uint4 load_c_piece(const LargeArgs& p, const __half* cb, int m, int n) {
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (m < p.M && n < p.N) {
-    const __half* src = p.CD + static_cast<int64_t>(m) * p.ldC + n;
+  if (p.e.read_c && m < p.M && n < p.N) {
+    const __half* src = cb + static_cast<int64_t>(m) * p.e.ldC + n;
     if (n + 8 <= p.N) {
       v = *reinterpret_cast<const uint4*>(src);
     } else {
@@ -212,8 +215,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       bool ok = true;
       WideItem it;
       for (int idx = 0; ok && wide_item(p, cta, G, idx, it); ++idx) {
-        int tm, tn;
-        tile_coords(it.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        int tb, tm, tn;
+        batch_tile(p, it.tile, tb, tm, tn);
+        const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
                             timeout_code(kRoleProducer, stage))) {
@@ -227,18 +231,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             mbar_arrive_expect_tx(fb, L::kStageBytes);
             const int k0 = kb * kWideBK;
             if (!p.a_mn) {
-              tma_load_2d(a_dst, &tmA, fb, k0, tm * kWideBM);
+              tma_load_3d(a_dst, &tmA, fb, k0, tm * kWideBM, za);
             } else {
 #pragma unroll
               for (int i = 0; i < kWideBM / 64; ++i)
-                tma_load_2d(a_dst + i * 8192, &tmA, fb, tm * kWideBM + 64 * i, k0);
+                tma_load_3d(a_dst + i * 8192, &tmA, fb, tm * kWideBM + 64 * i, k0, za);
             }
             if (!p.b_mn) {
-              tma_load_2d(b_dst, &tmB, fb, k0, tn * kWideBN);
+              tma_load_3d(b_dst, &tmB, fb, k0, tn * kWideBN, zb);
             } else {
 #pragma unroll
               for (int i = 0; i < kWideBN / 64; ++i)
-                tma_load_2d(b_dst + i * 8192, &tmB, fb, tn * kWideBN + 64 * i, k0);
+                tma_load_3d(b_dst + i * 8192, &tmB, fb, tn * kWideBN + 64 * i, k0, zb);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -318,12 +322,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const uint32_t stg_u32 = smem_u32(stg);
     // coalesced pattern: piece i of lane l is row 4i + l/8, 16-byte segment l%8
     const int prow = static_cast<int>(lane >> 3), pseg = static_cast<int>(lane & 7);
-    int tm = 0, tn = 0;
+    int tb = 0, tm = 0, tn = 0;
+    const __half* cb = p.e.C;  // problem tb's C
     uint4 cnext[8];
     auto load_chunk = [&](int c, uint4 (&v)[8]) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        v[i] = load_c_piece(p, tm * kWideBM + row0 + 4 * i + prow,
+        v[i] = load_c_piece(p, cb, tm * kWideBM + row0 + 4 * i + prow,
                             tn * kWideBN + 64 * c + 8 * pseg);
     };
     auto stage_chunk = [&](const uint4 (&v)[8]) {
@@ -357,14 +362,32 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
       for (int s8 = 0; s8 < 8; ++s8) {
         uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
-        *q = add_c8(p.acc_f16, r + 8 * s8, *q);
+        *q = add_c8(p, r + 8 * s8, *q);
       }
       fence_proxy_async_smem();
       __syncwarp();
       const int m_row0 = tm * kWideBM + row0;
       const int n0 = tn * kWideBN + 64 * c;
-      if (lane == 0 && m_row0 < p.M && n0 < p.N) {
-        tma_store_2d(&tmD, stg_u32, n0, m_row0);
+      if (n0 + 64 > p.N && (p.N & 7)) {
+        // D's ragged right edge with N not a multiple of 8: a TMA store
+        // writes whole 16-byte pieces past column N, so each lane copies its
+        // own row's valid columns out of the staging buffer instead.
+        const int m = m_row0 + static_cast<int>(lane), ncols = p.N - n0;
+        if (m < p.M && ncols > 0) {
+          __half* drow = p.e.D + tb * p.e.sD + static_cast<int64_t>(m) * p.e.ldD + n0;
+          for (int s8 = 0; 8 * s8 < ncols; ++s8) {
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
+            if (8 * s8 + 8 <= ncols) {
+              *reinterpret_cast<uint4*>(drow + 8 * s8) = v;
+            } else {
+              const __half* vh = reinterpret_cast<const __half*>(&v);
+              for (int j = 0; 8 * s8 + j < ncols; ++j) drow[8 * s8 + j] = vh[j];
+            }
+          }
+        }
+      } else if (lane == 0 && m_row0 < p.M && n0 < p.N) {
+        tma_store_3d(&tmD, stg_u32, n0, m_row0, tb);
         bulk_commit_group();
       }
     };
@@ -385,20 +408,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     auto prefetch_c = [&](int idx2) {
       WideItem nx;
       if (!wide_item(p, cta, G, idx2, nx)) return;
-      int tm2, tn2;
-      tile_coords(nx.tile, p.tiles_m, p.tiles_n, p.group_m, tm2, tn2);
+      int tb2, tm2, tn2;
+      batch_tile(p, nx.tile, tb2, tm2, tn2);
       const int m2 = tm2 * kWideBM + trow;
       const int n2 = tn2 * kWideBN;
-      if (m2 < p.M && n2 < p.N) {
+      if (p.e.read_c && m2 < p.M && n2 < p.N) {
         const uint32_t bytes = static_cast<uint32_t>(min(kWideBN, p.N - n2) * 2) & ~15u;
-        if (bytes) prefetch_l2(p.CD + static_cast<int64_t>(m2) * p.ldC + n2, bytes);
+        if (bytes)
+          prefetch_l2(p.e.C + tb2 * p.e.sC + static_cast<int64_t>(m2) * p.e.ldC + n2, bytes);
       }
     };
     prefetch_c(0);
     uint32_t acc_phase = 0;
     WideItem it;
     for (int idx = 0; wide_item(p, cta, G, idx, it); ++idx) {
-      tile_coords(it.tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      batch_tile(p, it.tile, tb, tm, tn);
+      cb = p.e.C + tb * p.e.sC;
       // C does not depend on the MMAs: fetch it now (for a partial tile too,
       // in case this warp turns out to finish it; the staging buffer is
       // otherwise idle on such an item)

@@ -118,6 +118,20 @@ def operand(rows: int, cols: int, ld: int, major: int, dist: str, seed: int,
     return st
 
 
+def batched_operand(L: int, rows: int, cols: int, ld: int, major: int, stride: int, dist: str,
+                    seed: int, K: int = 1, poison: bool = True) -> torch.Tensor:
+    """Flat storage of L (rows, cols) operands, operand l at element l * stride
+    (stride 0: one operand shared by all).  Slack and gaps are NaN."""
+    outer, _ = storage_shape(rows, cols, ld, major)
+    per = outer * ld
+    n = max(per, (L - 1) * stride + per) if L > 0 else per
+    st = torch.full((n,), float("nan") if poison else 0.0, dtype=torch.float16)
+    for l in range(L if stride else 1):
+        st[l * stride:l * stride + per] = operand(rows, cols, ld, major, dist, seed + 7919 * l, K,
+                                                 poison).reshape(-1)
+    return st
+
+
 def view(storage: torch.Tensor, rows: int, cols: int, ld: int, major: int) -> torch.Tensor:
     """The logical (rows, cols) view of a stored operand (no copy)."""
     strides = (ld, 1) if major == MAJOR_K else (1, ld)

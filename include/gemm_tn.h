@@ -25,8 +25,8 @@
  * C and D share one buffer: each element of C is read before the element of
  * D at the same position is written.  (Page "Reading CuTe's retile_D",
  * section "How the two fragments are handed to the MMA", accumulates the
- * product onto C in place.)  There is no alpha/beta; to compute D = A.B^T,
- * zero the buffer first.
+ * product onto C in place.)  gemm_tn_scaled and gemm_tn_batched below add
+ * the alpha / beta form with a separate D, and a batch of problems.
  *
  * Accumulation (same page, section "From CuTe's name to the instruction";
  * make_tiled_mma page, section "Fix the matrices and directions first"):
@@ -36,7 +36,7 @@
  *   GEMM_TN_ACC_F16: the products are summed in an fp16 accumulator and C is
  *                    added in fp16: the F16F16F16F16 form.
  *
- * Ownership: the caller owns A, B and CD (device memory); the library never
+ * Ownership: the caller owns A, B, C and D (device memory); the library never
  * frees or retains caller memory.  Workspaces (the skinny path's split-K
  * partial sums, stream-K partial tiles, repacked strided operands) come from
  * a memory pool the library creates for each device on first use: taken with
@@ -49,8 +49,8 @@
  * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream).  It returns once the kernels are enqueued; D is
  * valid after the stream has been synchronised.  Calls on one stream are
- * ordered; calls that may overlap on different streams must not share the
- * CD buffer.  All pointers are device pointers of the current device.
+ * ordered; calls that may overlap on different streams must not share an
+ * output buffer.  All pointers are device pointers of the current device.
  *
  * Errors: every function returns a gemm_tn_status and never aborts or throws.
  * Argument checks run before anything is enqueued, so an error return from
@@ -177,6 +177,68 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
                            const gemm_tn_options* opts);
 
 /*
+ * Scaled, batched form:
+ *
+ *     D_l = alpha * A_l . B_l^T + beta * C_l        for l < batch
+ *
+ * Page "cute(7) simple_gemm", section 8.1, checks the kernel against
+ * cuBLAS's alpha / beta GEMM (D = alpha A.B^T + beta C); page "CuTe Layout
+ * to Tensor Core", section 4 (local_tile), gives the extra coordinate that
+ * indexes a batch.  Per problem the views are those of gemm_tn, with a
+ * separate D: (M,N):(ldD,1).  Problem l's operand X starts strideX elements
+ * after problem l-1's:  A_l = A + l*strideA, and so on.
+ *
+ *   alpha, beta  fp32 scalars.  alpha == 0 or K == 0: the product term is
+ *                absent and A, B are not read (D = beta * C); beta == 0: C is
+ *                not read and may be NULL (NaN or Inf stored there cannot
+ *                reach D).  These are the BLAS conventions.
+ *   precision    fp32 accumulation: fma(alpha, acc, beta * C) in fp32,
+ *                rounded once to fp16.  fp16 accumulation: the products are
+ *                summed in fp16 as in gemm_tn; with alpha = beta = 1, C is
+ *                added in fp16 (exactly gemm_tn), otherwise the fp16 sum is
+ *                scaled and C added in fp32 and rounded once.
+ *   strides      used only when batch > 1, in elements, multiples of 8:
+ *                strideA: 0 (one A for every problem) or at least one view
+ *                  (M*ldA K-major, K*ldA M-major); strideB likewise;
+ *                strideC: any value >= 0 (0 = one C for every problem);
+ *                strideD: at least M*ldD (the problems' D do not overlap).
+ *   aliasing     D may be C itself (same pointer, ldD == ldC, strideD ==
+ *                strideC): each C element is read before the D element at
+ *                its position is written.  Otherwise D must not overlap C;
+ *                D must never overlap A or B.
+ *   alignment    A, B, C, D 16-byte aligned, ld* multiples of 8
+ *                (GEMM_TN_ERR_ALIGNMENT otherwise; gemm_tn_strided takes
+ *                arbitrary strides for the unscaled, single-problem form).
+ *   paths        one problem with M <= 64, K-major operands and fp32
+ *                accumulation takes the skinny split-K path; everything else
+ *                runs the tile kernels with the batch folded into the tile
+ *                list (tile t belongs to problem t / tiles-per-problem).
+ *   returns      as gemm_tn; M, N or batch == 0 is a no-op.
+ */
+GEMM_TN_API int gemm_tn_batched(int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+                                const void* A, int64_t ldA, int64_t strideA, int a_major,
+                                const void* B, int64_t ldB, int64_t strideB, int b_major,
+                                float beta, const void* C, int64_t ldC, int64_t strideC,
+                                void* D, int64_t ldD, int64_t strideD, int accum_dtype,
+                                void* stream);
+
+/* gemm_tn_batched with explicit controls (opts may be NULL); the controls
+ * mean what they mean for gemm_tn_ex. */
+GEMM_TN_API int gemm_tn_batched_ex(int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+                                   const void* A, int64_t ldA, int64_t strideA, int a_major,
+                                   const void* B, int64_t ldB, int64_t strideB, int b_major,
+                                   float beta, const void* C, int64_t ldC, int64_t strideC,
+                                   void* D, int64_t ldD, int64_t strideD, int accum_dtype,
+                                   void* stream, const gemm_tn_options* opts);
+
+/* One problem of the scaled form: D = alpha * A.B^T + beta * C
+ * (gemm_tn_batched with batch 1). */
+GEMM_TN_API int gemm_tn_scaled(int64_t M, int64_t N, int64_t K, float alpha, const void* A,
+                               int64_t ldA, int a_major, const void* B, int64_t ldB, int b_major,
+                               float beta, const void* C, int64_t ldC, void* D, int64_t ldD,
+                               int accum_dtype, void* stream);
+
+/*
  * D = C + A.B^T for operand views with arbitrary element strides (the layout
  * page, sections 1-2: a matrix is any shape:stride view; neither mode needs
  * to be stride-1):
@@ -229,12 +291,13 @@ GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail);
 GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major,
                                   int b_major);
 
-/* Number of kernel launches the last successful gemm_tn / gemm_tn_ex call on
- * this host thread enqueued (0 for the no-op cases). */
+/* Number of kernel launches the last successful gemm_tn, gemm_tn_ex,
+ * gemm_tn_scaled, gemm_tn_batched[_ex] or gemm_tn_strided[_ex] call on this
+ * host thread enqueued (0 for the no-op cases). */
 GEMM_TN_API int gemm_tn_last_launch_count(void);
 
-/* Names of the kernels the last successful gemm_tn / gemm_tn_ex /
- * gemm_tn_skinny_noalloc call on this host thread enqueued, '+'-separated
+/* Names of the kernels the last successful call of any entry point above or
+ * gemm_tn_skinny_noalloc on this host thread enqueued, '+'-separated
  * ("" after a no-op call).  Static storage; never NULL. */
 GEMM_TN_API const char* gemm_tn_last_kernels(void);
 

@@ -141,3 +141,59 @@ def test_strided_ex_rejects_tile_paths(lib):
     for path in (gb.PATH_LARGE, gb.PATH_SKINNY, 9):
         assert gb.gemm_tn_strided_ex(64, 64, 64, P, 64, 1, P + (1 << 20), 64, 1, P + (2 << 20),
                                      64, 1, 0, None, {"path": path}) == gb.ERR_INVALID_ARG
+
+
+# --- scaled / batched form: argument checks (no device needed) -------------
+
+MB = 1 << 20
+
+
+def bcall(M=64, N=64, K=64, L=2, alpha=1.0, A=P, ldA=64, sA=64 * 64, am=0, B=P + 4 * MB,
+          ldB=64, sB=64 * 64, bm=0, beta=1.0, C=P + 8 * MB, ldC=64, sC=64 * 64,
+          D=P + 12 * MB, ldD=64, sD=64 * 64, acc=0):
+    return gb.gemm_tn_batched_ex(M, N, K, L, alpha, A, ldA, sA, am, B, ldB, sB, bm, beta, C,
+                                 ldC, sC, D, ldD, sD, acc, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(L=-1), gb.ERR_INVALID_ARG),
+    (dict(C=0), gb.ERR_INVALID_ARG),                      # beta != 0 needs C
+    (dict(D=0), gb.ERR_INVALID_ARG),
+    (dict(sD=64 * 64 - 8), gb.ERR_INVALID_ARG),           # the problems' D overlap
+    (dict(sA=64 * 63), gb.ERR_INVALID_ARG),               # A views overlap (not 0)
+    (dict(sB=-64 * 64), gb.ERR_INVALID_ARG),
+    (dict(sC=-8), gb.ERR_INVALID_ARG),
+    (dict(D=P + 8 * MB + 128), gb.ERR_INVALID_ARG),       # D overlaps C, not in place
+    (dict(D=P + 8 * MB, ldD=72, sD=72 * 64), gb.ERR_INVALID_ARG),  # same base, other view
+    (dict(D=P + 4096 * 2), gb.ERR_INVALID_ARG),           # D overlaps problem 1's A
+    (dict(D=P + 4 * MB + 64 * 64 * 2), gb.ERR_INVALID_ARG),  # D overlaps problem 1's B
+    (dict(sA=64 * 64 + 4), gb.ERR_ALIGNMENT),
+    (dict(sC=12), gb.ERR_ALIGNMENT),
+    (dict(sD=64 * 64 + 4), gb.ERR_ALIGNMENT),
+    (dict(C=P + 8 * MB + 2, L=1), gb.ERR_ALIGNMENT),
+    (dict(ldD=60), gb.ERR_INVALID_ARG),
+])
+def test_batched_argument_checks(lib, kw, status):
+    assert bcall(**kw) == status
+
+
+def test_batched_checks_that_pass_reach_the_device(lib):
+    # Arguments that validate: without a GPU the call fails at device setup
+    # (GEMM_TN_ERR_CUDA), not at an argument check.
+    ok_like = {gb.OK, gb.ERR_CUDA}
+    assert bcall() in ok_like
+    assert bcall(beta=0.0, C=0) in ok_like                  # C unused when beta == 0
+    assert bcall(alpha=0.0, A=0, B=0) in ok_like            # A, B unused when alpha == 0
+    assert bcall(K=0, A=0, B=0) in ok_like                  # empty sum
+    assert bcall(C=P + 12 * MB) in ok_like                  # D == C in place
+    assert bcall(sA=0, sB=0, sC=0) in ok_like               # shared A, B, C
+    assert bcall(L=1, sD=0, sA=8, sB=8) in ok_like          # strides unused for one problem
+
+
+def test_scaled_is_one_problem(lib):
+    st = gb.gemm_tn_scaled(64, 64, 64, 2.0, P, 64, 0, P + 4 * MB, 64, 0, 0.5, P + 8 * MB, 64,
+                           P + 8 * MB + 64, 64, 0, None)
+    assert st == gb.ERR_INVALID_ARG                          # D overlaps C
+    st = gb.gemm_tn_scaled(0, 64, 64, 2.0, P, 64, 0, P + 4 * MB, 64, 0, 0.5, 0, 64, 0, 64, 0,
+                           None)
+    assert st == gb.OK                                       # M == 0: no-op

@@ -126,7 +126,8 @@ def test_ragged_sweep(accum, a_major, b_major, tile_kernel):
         ldC = (N + 7) // 8 * 8 + 8
         A_st = wl.operand(M, K, ldA, a_major, "int2", int(rng.integers(1 << 30)))
         B_st = wl.operand(N, K, ldB, b_major, "int2", int(rng.integers(1 << 30)))
-        C_st = wl.operand(M, N, ldC, 0, "int4", int(rng.integers(1 << 30)), poison=False)
+        # NaN in C's slack: the kernels must neither read it nor write it
+        C_st = wl.operand(M, N, ldC, 0, "int4", int(rng.integers(1 << 30)))
         D_st, st = run_gpu(M, N, K, A_st, ldA, a_major, B_st, ldB, b_major, C_st, ldC, accum,
                            opts={"path": gb.PATH_LARGE, "tile_kernel": tile_kernel},
                            guard_rows=2)
