@@ -398,6 +398,7 @@ def run_ours(args):
         extra["skinny_m16"] = bench_skinny(dev, stream)
         extra["strided_4096"] = bench_strided(dev, stream)
         extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
+        extra["scaled_batched"] = bench_general(dev, stream)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -563,6 +564,54 @@ def bench_stream_k(dev, stream, steps=50, rounds=3):
             "unsplit": {"kernels": kernels[-1], "ms_per_call": ms_plain,
                         "TFLOP_per_s": fl / (ms_plain * 1e-3) / 1e12},
             "speedup": ms_plain / ms_sk}
+
+
+def bench_general(dev, stream, steps=20):
+    """The scaled and batched entry point (gemm_tn_batched): D = alpha A.B^T +
+    beta C with a separate D at 8192^3, and two batches of smaller problems
+    (64 of 1024^3; 256 of 512^3 with beta = 0), fp32 accumulation, K-major
+    operands, calls back to back."""
+    import torch
+
+    from dense_fp16_tensor_gb300 import binding as gb
+    from dense_fp16_tensor_gb300 import workloads as wl
+    peaks, kind = load_peaks()
+    out = {}
+    for name, M, N, K, L, alpha, beta in (("scaled_8192", 8192, 8192, 8192, 1, 0.5, 2.0),
+                                          ("batched_64x1024", 1024, 1024, 1024, 64, 1.0, 1.0),
+                                          ("batched_256x512", 512, 512, 512, 256, 1.0, 0.0)):
+        A = wl.draw((L * M * K,), "u11", 7201).to(dev)
+        Bm = wl.draw((L * N * K,), "u11", 7202).to(dev)
+        C = wl.draw((L * M * N,), "u11", 7203).to(dev)
+        D = torch.empty(L * M * N, dtype=torch.float16, device=dev)
+        sp = stream.cuda_stream
+
+        def step():
+            st = gb.gemm_tn_batched(M, N, K, L, alpha, A.data_ptr(), K, M * K, 0, Bm.data_ptr(),
+                                    K, N * K, 0, beta, C.data_ptr(), N, M * N, D.data_ptr(), N,
+                                    M * N, 0, sp)
+            if st != gb.OK:
+                raise gb.GemmTnError(st)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        tf = 2.0 * L * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"M": M, "N": N, "K": K, "batch": L, "alpha": alpha, "beta": beta,
+                     "kernels": gb.gemm_tn_last_kernels(), "ms_per_call": ms,
+                     "TFLOP_per_s": tf, "frac_of_peak": tf / float(peaks["bf16_tflops"]),
+                     "peak_kind": kind}
+        del A, Bm, C, D
+    return out
 
 
 def main():

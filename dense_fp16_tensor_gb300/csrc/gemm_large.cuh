@@ -67,7 +67,9 @@ struct LargeSmem {
   static constexpr uint32_t kABytes = kLargeBM * kLargeBK * 2;  // 16 KiB
   static constexpr uint32_t kBBytes = BN * kLargeBK * 2;        // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kBarOffset = kLargeStages * kStageBytes;
+  // epilogue staging: 4 warps x 32 rows x 64 fp16 (1024-aligned)
+  static constexpr uint32_t kStagingOffset = kLargeStages * kStageBytes;
+  static constexpr uint32_t kBarOffset = kStagingOffset + 4 * 32 * 128;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
   static constexpr uint32_t kNumBars = 2 * kLargeStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
@@ -120,10 +122,112 @@ __device__ __forceinline__ void store_chunk(const LargeArgs& p, int tb, int m, i
   }
 }
 
+// Eight fp16 values of C (uint4) plus eight accumulator words -> eight fp16
+// of D = alpha * acc + beta * C.
+__device__ __forceinline__ uint4 add_c8(const LargeArgs& p, const uint32_t* r, uint4 c) {
+  const __half2* ch = reinterpret_cast<const __half2*>(&c);
+  uint4 o;
+  __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = r[2 * j], hi = r[2 * j + 1];
+    if (p.acc_f16) {
+      const __half2 acc = __halves2half2(__ushort_as_half(static_cast<unsigned short>(lo)),
+                                         __ushort_as_half(static_cast<unsigned short>(hi)));
+      oh[j] = epi_f16x2(p.e, acc, ch[j]);
+    } else {
+      oh[j] = epi_f32x2(p.e, __uint_as_float(lo), __uint_as_float(hi), ch[j]);
+    }
+  }
+  return o;
+}
+
+// One 16-byte piece of a 32 x 64 C chunk for the coalesced load pattern:
+// load i (0..7) of lane l covers row 4i + l/8, columns 8*(l%8) .. +8.
+// cb is problem tb's C; zeros when C is not read.
+__device__ __forceinline__ uint4 load_c_piece(const LargeArgs& p, const __half* cb, int m, int n) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (p.e.read_c && m < p.M && n < p.N) {
+    const __half* src = cb + static_cast<int64_t>(m) * p.e.ldC + n;
+    if (n + 8 <= p.N) {
+      v = *reinterpret_cast<const uint4*>(src);
+    } else {
+      __half* vh = reinterpret_cast<__half*>(&v);
+      for (int j = 0; j < 8 && n + j < p.N; ++j) vh[j] = src[j];
+    }
+  }
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Staged epilogue of one warp: 32 rows x 64 columns per chunk.
+//
+// C arrives in a coalesced pattern (8 lanes per 128-byte row segment) into a
+// 128-byte-swizzled staging buffer; each lane then adds its own TMEM row to
+// its staged row (conflict-free thanks to the swizzle) and the chunk leaves
+// by one TMA store, which also clips the row tail.  A right edge with N not
+// a multiple of 8 is copied out with plain stores instead, because a TMA
+// store writes whole 16-byte pieces.
+constexpr uint32_t kStagingBytes = 32 * 128;  // 32 rows x 64 fp16
+
+// C pieces of the chunk with rows m_base.., columns n_base..: piece i of lane
+// l is row 4i + l/8, 16-byte segment l%8.
+__device__ __forceinline__ void epi_load_c(const LargeArgs& p, const __half* cb, int m_base,
+                                           int n_base, uint32_t lane, uint4 (&v)[8]) {
+  const int prow = static_cast<int>(lane >> 3), pseg = static_cast<int>(lane & 7);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = load_c_piece(p, cb, m_base + 4 * i + prow, n_base + 8 * pseg);
+}
+
+__device__ __forceinline__ void epi_stage_c(uint8_t* stg, uint32_t lane, const uint4 (&v)[8]) {
+  const int prow = static_cast<int>(lane >> 3), pseg = static_cast<int>(lane & 7);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + prow;
+    *reinterpret_cast<uint4*>(stg + r * 128 + 16 * (pseg ^ (r & 7))) = v[i];
+  }
+}
+
+// Combine this lane's accumulator row r (64 words) with its staged C row,
+// then store the chunk whose first element is D(m_row0, n0) of problem tb.
+__device__ __forceinline__ void epi_store_chunk(const LargeArgs& p, const CUtensorMap* tmD,
+                                                uint8_t* stg, uint32_t stg_u32, uint32_t lane,
+                                                int tb, int m_row0, int n0,
+                                                const uint32_t (&r)[64]) {
+  uint8_t* my_row = stg + lane * 128;
+#pragma unroll
+  for (int s8 = 0; s8 < 8; ++s8) {
+    uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
+    *q = add_c8(p, r + 8 * s8, *q);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (n0 + 64 > p.N && (p.N & 7)) {
+    const int m = m_row0 + static_cast<int>(lane), ncols = p.N - n0;
+    if (m < p.M && ncols > 0) {
+      __half* drow = p.e.D + tb * p.e.sD + static_cast<int64_t>(m) * p.e.ldD + n0;
+      for (int s8 = 0; 8 * s8 < ncols; ++s8) {
+        const uint4 v =
+            *reinterpret_cast<const uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
+        if (8 * s8 + 8 <= ncols) {
+          *reinterpret_cast<uint4*>(drow + 8 * s8) = v;
+        } else {
+          const __half* vh = reinterpret_cast<const __half*>(&v);
+          for (int j = 0; 8 * s8 + j < ncols; ++j) drow[8 * s8 + j] = vh[j];
+        }
+      }
+    }
+  } else if (lane == 0 && m_row0 < p.M && n0 < p.N) {
+    tma_store_3d(tmD, stg_u32, n0, m_row0, tb);
+    bulk_commit_group();
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kLargeThreads, 1)
     gemm_tn_large_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const LargeArgs p) {
+                         const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmD, const LargeArgs p) {
   using L = LargeSmem<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -159,6 +263,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 2 * BN);
@@ -274,31 +379,60 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Staged: C of the next tile is fetched (coalesced) while its MMAs run;
+    // per 64-column chunk the accumulator row is added to the staged C row
+    // and the chunk leaves by TMA store.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes 32*quad ..
-    const int row_in_tile = static_cast<int>(quad * 32 + lane);
+    const int row0 = static_cast<int>(quad * 32);            // first tile row of this warp
+    uint8_t* stg = smem + L::kStagingOffset + (warp - 2) * kStagingBytes;
+    const uint32_t stg_u32 = smem_u32(stg);
+    constexpr int kChunks = BN / 64;
     uint32_t acc = 0, acc_phase = 0;
+    uint4 cnext[8];
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
+      const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
+      const int m_base = tm * kLargeBM + row0, n_base = tn * BN;
+      // chunk 0 of C staged and chunk 1 in registers, once the previous
+      // tile's last store has read the staging buffer
+      epi_load_c(p, cb, m_base, n_base, lane, cnext);
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+      epi_stage_c(stg, lane, cnext);
+      if (kChunks > 1) epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
+      __syncwarp();
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, acc)))
         break;
       tc_fence_after();
-      const int m = tm * kLargeBM + row_in_tile;
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
+      for (int c = 0; c < kChunks; ++c) {
+        if (c > 0) {
+          if (lane == 0) bulk_wait_group_read0();  // previous store has read staging
+          __syncwarp();
+          epi_stage_c(stg, lane, cnext);
+          if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
+          __syncwarp();
+        }
+        uint32_t r[64];
+        tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        store_chunk(p, tb, m, tn * BN + c * 32, r);
+        if (c == kChunks - 1) {
+          // every column of this accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        }
+        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_group0();  // all D stores performed before exit
+    __syncwarp();
   }
 
   __syncwarp();

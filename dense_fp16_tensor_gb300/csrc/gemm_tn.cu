@@ -402,10 +402,12 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.test_stall = o.test_stall;
   p.sk_tile0 = p.num_tiles;  // no split tiles unless stream-K is set up below
   void* sk_ws = nullptr;
-  if (wide) {
-    CUtensorMap tmD;
+  CUtensorMap tmD;
+  if (!pair) {
     s = encode_d(&tmD, q.D, M, N, q.ldD, q.sD, q.L);
     if (s != GEMM_TN_OK) return s;
+  }
+  if (wide) {
     int grid = std::min(p.num_tiles, st.num_sms);
     // Stream-K for the last, partial wave, on request only (fp32
     // accumulation only: a split fp16 accumulation would round at different
@@ -455,10 +457,10 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     const int grid = std::min(p.num_tiles, st.num_sms);
     if (bn == 256) {
       gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
-          tmA, tmB, p);
+          tmA, tmB, tmD, p);
     } else {
       gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
-          tmA, tmB, p);
+          tmA, tmB, tmD, p);
     }
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;

@@ -56,7 +56,7 @@ constexpr int kWideThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kWideTmemCols = 512;
 
 constexpr int kWideEpiWarps = 8;
-constexpr uint32_t kWideStagingBytes = 32 * 128;  // 32 rows x 64 fp16, 128-byte swizzle
+constexpr uint32_t kWideStagingBytes = kStagingBytes;
 // Stream-K partials: one 32-row x 64-column fp32 block of a warp's slab is
 // 8 KiB, stored as [column group g (16)][lane (32)] float4.
 constexpr uint32_t kSkBlockBytes = 32 * 64 * 4;
@@ -81,43 +81,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
                "r"(bytes)
                : "memory");
-}
-
-// Eight fp16 values of C (uint4) plus eight accumulator words -> eight fp16
-// of D = alpha * acc + beta * C.
-__device__ __forceinline__ uint4 add_c8(const LargeArgs& p, const uint32_t* r, uint4 c) {
-  const __half2* ch = reinterpret_cast<const __half2*>(&c);
-  uint4 o;
-  __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t lo = r[2 * j], hi = r[2 * j + 1];
-    if (p.acc_f16) {
-      const __half2 acc = __halves2half2(__ushort_as_half(static_cast<unsigned short>(lo)),
-                                         __ushort_as_half(static_cast<unsigned short>(hi)));
-      oh[j] = epi_f16x2(p.e, acc, ch[j]);
-    } else {
-      oh[j] = epi_f32x2(p.e, __uint_as_float(lo), __uint_as_float(hi), ch[j]);
-    }
-  }
-  return o;
-}
-
-// One 16-byte piece of a 32 x 64 C chunk for the coalesced load pattern:
-// load i (0..7) of lane l covers row 4i + l/8, columns 8*(l%8) .. +8.
-// cb is problem tb's C; zeros when C is not read.
-__device__ __forceinline__ uint4 load_c_piece(const LargeArgs& p, const __half* cb, int m, int n) {
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (p.e.read_c && m < p.M && n < p.N) {
-    const __half* src = cb + static_cast<int64_t>(m) * p.e.ldC + n;
-    if (n + 8 <= p.N) {
-      v = *reinterpret_cast<const uint4*>(src);
-    } else {
-      __half* vh = reinterpret_cast<__half*>(&v);
-      for (int j = 0; j < 8 && n + j < p.N; ++j) vh[j] = src[j];
-    }
-  }
-  return v;
 }
 
 // One item of CTA c's work list: whole tiles first (round-robin), then the
@@ -326,18 +289,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const __half* cb = p.e.C;  // problem tb's C
     uint4 cnext[8];
     auto load_chunk = [&](int c, uint4 (&v)[8]) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        v[i] = load_c_piece(p, cb, tm * kWideBM + row0 + 4 * i + prow,
-                            tn * kWideBN + 64 * c + 8 * pseg);
+      epi_load_c(p, cb, tm * kWideBM + row0, tn * kWideBN + 64 * c, lane, v);
     };
-    auto stage_chunk = [&](const uint4 (&v)[8]) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 4 * i + prow;
-        *reinterpret_cast<uint4*>(stg + r * 128 + 16 * (pseg ^ (r & 7))) = v[i];
-      }
-    };
+    auto stage_chunk = [&](const uint4 (&v)[8]) { epi_stage_c(stg, lane, v); };
     // C of chunks 0 and 1 (0 staged, 1 in registers), once the previous
     // tile's last store has finished reading the staging buffer.
     auto preload_c = [&]() {
@@ -348,8 +302,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       load_chunk(1, cnext);
       __syncwarp();
     };
-    // D = C + acc for chunk c (64 columns) of this warp's slab; acc words are
-    // fp32 (or fp16 in the low half) in r[0..64).
+    // D = alpha * acc + beta * C for chunk c (64 columns) of this warp's
+    // slab; acc words are fp32 (or fp16 in the low half) in r[0..64).
     auto emit_chunk = [&](int c, const uint32_t (&r)[64]) {
       if (c > 0) {
         if (lane == 0) bulk_wait_group_read0();  // previous store has read staging
@@ -358,38 +312,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (c + 1 < kWideBN / 64) load_chunk(c + 1, cnext);
         __syncwarp();
       }
-      uint8_t* my_row = stg + lane * 128;
-#pragma unroll
-      for (int s8 = 0; s8 < 8; ++s8) {
-        uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
-        *q = add_c8(p, r + 8 * s8, *q);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      const int m_row0 = tm * kWideBM + row0;
-      const int n0 = tn * kWideBN + 64 * c;
-      if (n0 + 64 > p.N && (p.N & 7)) {
-        // D's ragged right edge with N not a multiple of 8: a TMA store
-        // writes whole 16-byte pieces past column N, so each lane copies its
-        // own row's valid columns out of the staging buffer instead.
-        const int m = m_row0 + static_cast<int>(lane), ncols = p.N - n0;
-        if (m < p.M && ncols > 0) {
-          __half* drow = p.e.D + tb * p.e.sD + static_cast<int64_t>(m) * p.e.ldD + n0;
-          for (int s8 = 0; 8 * s8 < ncols; ++s8) {
-            const uint4 v =
-                *reinterpret_cast<const uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
-            if (8 * s8 + 8 <= ncols) {
-              *reinterpret_cast<uint4*>(drow + 8 * s8) = v;
-            } else {
-              const __half* vh = reinterpret_cast<const __half*>(&v);
-              for (int j = 0; 8 * s8 + j < ncols; ++j) drow[8 * s8 + j] = vh[j];
-            }
-          }
-        }
-      } else if (lane == 0 && m_row0 < p.M && n0 < p.N) {
-        tma_store_3d(&tmD, stg_u32, n0, m_row0, tb);
-        bulk_commit_group();
-      }
+      epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, tm * kWideBM + row0, tn * kWideBN + 64 * c,
+                      r);
     };
     auto load_tmem_chunk = [&](int c, uint32_t (&r)[64]) {
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + half * kWideBN;
@@ -423,7 +347,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     WideItem it;
     for (int idx = 0; wide_item(p, cta, G, idx, it); ++idx) {
       batch_tile(p, it.tile, tb, tm, tn);
-      cb = p.e.C + tb * p.e.sC;
+      cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
       // C does not depend on the MMAs: fetch it now (for a partial tile too,
       // in case this warp turns out to finish it; the staging buffer is
       // otherwise idle on such an item)
