@@ -188,6 +188,26 @@ __device__ __forceinline__ void epi_stage_c(uint8_t* stg, uint32_t lane, const u
   }
 }
 
+// Plain-store copy of this lane's staged row, columns [n0, N), for a right
+// edge that a TMA store would overrun (kept out of line: it runs once per
+// tile row at most and only when N % 8 != 0).
+__device__ __noinline__ void epi_store_ragged(const LargeArgs& p, const uint8_t* my_row,
+                                              uint32_t lane, int tb, int m, int n0) {
+  const int ncols = p.N - n0;
+  if (m >= p.M || ncols <= 0) return;
+  __half* drow = p.e.D + tb * p.e.sD + static_cast<int64_t>(m) * p.e.ldD + n0;
+  for (int s8 = 0; 8 * s8 < ncols; ++s8) {
+    const uint4 v =
+        *reinterpret_cast<const uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
+    if (8 * s8 + 8 <= ncols) {
+      *reinterpret_cast<uint4*>(drow + 8 * s8) = v;
+    } else {
+      const __half* vh = reinterpret_cast<const __half*>(&v);
+      for (int j = 0; 8 * s8 + j < ncols; ++j) drow[8 * s8 + j] = vh[j];
+    }
+  }
+}
+
 // Combine this lane's accumulator row r (64 words) with its staged C row,
 // then store the chunk whose first element is D(m_row0, n0) of problem tb.
 __device__ __forceinline__ void epi_store_chunk(const LargeArgs& p, const CUtensorMap* tmD,
@@ -203,20 +223,7 @@ __device__ __forceinline__ void epi_store_chunk(const LargeArgs& p, const CUtens
   fence_proxy_async_smem();
   __syncwarp();
   if (n0 + 64 > p.N && (p.N & 7)) {
-    const int m = m_row0 + static_cast<int>(lane), ncols = p.N - n0;
-    if (m < p.M && ncols > 0) {
-      __half* drow = p.e.D + tb * p.e.sD + static_cast<int64_t>(m) * p.e.ldD + n0;
-      for (int s8 = 0; 8 * s8 < ncols; ++s8) {
-        const uint4 v =
-            *reinterpret_cast<const uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
-        if (8 * s8 + 8 <= ncols) {
-          *reinterpret_cast<uint4*>(drow + 8 * s8) = v;
-        } else {
-          const __half* vh = reinterpret_cast<const __half*>(&v);
-          for (int j = 0; 8 * s8 + j < ncols; ++j) drow[8 * s8 + j] = vh[j];
-        }
-      }
-    }
+    epi_store_ragged(p, my_row, lane, tb, m_row0 + static_cast<int>(lane), n0);
   } else if (lane == 0 && m_row0 < p.M && n0 < p.N) {
     tma_store_3d(tmD, stg_u32, n0, m_row0, tb);
     bulk_commit_group();
