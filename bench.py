@@ -186,18 +186,27 @@ class ClockSampler:
                 "power_w_max": max((num(p[3]) or 0.0) for p in use)}
 
 
+_ORACLE_INPUTS = {}
+
+
+def oracle_inputs(w):
+    """Bits of workload w's operands (generated once per process)."""
+    if w.name not in _ORACLE_INPUTS:
+        import numpy as np
+        import torch
+
+        from dense_fp16_tensor_gb300 import workloads as wl
+
+        def bits(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        _ORACLE_INPUTS[w.name] = tuple(bits(t) for t in wl.make_inputs(w))
+    return _ORACLE_INPUTS[w.name]
+
+
 def oracle_sample_rate(w, rows: int, nthreads: int):
     """Time the CPU oracle on the first `rows` rows of workload w (fp64 triple loop)."""
-    import numpy as np
-    import torch
-
     import oracle
-    from dense_fp16_tensor_gb300 import workloads as wl
-    A_st, B_st, C_st = wl.make_inputs(w)
-
-    def bits(t):
-        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    a, b, c = bits(A_st), bits(B_st), bits(C_st)
+    a, b, c = oracle_inputs(w)
     t0 = time.perf_counter()
     oracle.gemm_tn(rows, w.N, w.K, a, w.ldA, w.a_major, b, w.ldB, w.b_major, c, w.ldC,
                    want_f16=True, nthreads=nthreads)
@@ -214,9 +223,16 @@ def cpu_baseline(w, target_s=12.0):
     rows = int(min(w.M, max(probe_rows, probe_rows * target_s / max(dt, 1e-3))))
     rows = max(cores, rows // cores * cores) if rows >= cores else rows
     rate, dt = oracle_sample_rate(w, rows, cores)
+    # one thread on a small fixed slice, for the per-core rate
+    one_rows = min(w.M, 8)
+    one_rate, one_dt = oracle_sample_rate(w, one_rows, 1)
     return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {rows} of {w.M} output rows of the {w.M}x{w.N}x{w.K} problem "
-                      f"(fp64 triple loop, {rows * w.N} outputs, {dt:.1f} s)"}
+                      f"(fp64 triple loop, {rows * w.N} outputs, {dt:.1f} s)",
+            "single_core": {"value": one_rate, "unit": UNIT, "cores": 1,
+                            "sample": f"first {one_rows} rows on one thread ({one_dt:.1f} s); "
+                                      f"the whole problem would take "
+                                      f"{one_dt * w.M / one_rows / 3600:.1f} h at this rate"}}
 
 
 # ---------------------------------------------------------------- reference arm
