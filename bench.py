@@ -9,7 +9,8 @@ fp16 epilogue).  The metric is TFLOP/s (2*M*N*K per step).
 Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
   e2e           the same metric through the C ABI with host buffers: every
                 step copies A, B and C from pinned host memory to the device
-                and D back, inside the timed region
+                and D back, inside the timed region (steps pipelined over two
+                buffer sets and three streams; the serial figure beside it)
   roofline      the main kernel against the measured dense bf16/fp16 peak
   cpu_baseline  the CPU oracle (fp64 triple loop) timed on a bounded sample
                 of the same workload on this host's cores
@@ -49,7 +50,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--tile-n", type=int, default=0)
@@ -348,39 +349,65 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = ws * w.flops * args.steps / (total_ms * 1e-3) / 1e12
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers.  Every step copies
+    # its A, B and C from pinned host memory and its D back.  The steps are
+    # pipelined over two device buffer sets: step i's host-to-device copies
+    # (one copy stream), its GEMM (the compute stream) and its device-to-host
+    # copy (a second copy stream) overlap the neighbouring steps.  The
+    # serial form (one stream, nothing overlapped) is reported beside it.
     hA = A_st.pin_memory()
     hB = B_st.pin_memory()
     hC = C_st.pin_memory()
-    hD = torch.empty_like(C_st).pin_memory()
-    dA, dB, dCD = torch.empty_like(A), torch.empty_like(Bm), torch.empty_like(CD)
+    hD = [torch.empty_like(C_st).pin_memory() for _ in range(2)]
+    bufs = [(torch.empty_like(A), torch.empty_like(Bm), torch.empty_like(CD)) for _ in range(2)]
     h2d = (hA.numel() + hB.numel() + hC.numel()) * 2
-    d2h = hD.numel() * 2
+    d2h = hD[0].numel() * 2
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            dCD.copy_(hC, non_blocking=True)
-            step(dA.data_ptr(), dB.data_ptr(), dCD.data_ptr())
-            hD.copy_(dCD, non_blocking=True)
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
+    def e2e_run(nsteps, pipelined):
+        first = torch.cuda.Event(enable_timing=True)
+        last = torch.cuda.Event(enable_timing=True)
+        out_done = []
+        cin = s_in if pipelined else stream
+        cout = s_out if pipelined else stream
+        first.record(cin)
+        for i in range(nsteps):
+            dA, dB, dCD = bufs[i % 2 if pipelined else 0]
+            if pipelined and i >= 2:
+                cin.wait_event(out_done[i - 2])  # buffer set free again
+            with torch.cuda.stream(cin):
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                dCD.copy_(hC, non_blocking=True)
+            if pipelined:
+                ev = torch.cuda.Event()
+                ev.record(cin)
+                stream.wait_event(ev)
+            with torch.cuda.stream(stream):
+                step(dA.data_ptr(), dB.data_ptr(), dCD.data_ptr())
+            if pipelined:
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                cout.wait_event(ev)
+            with torch.cuda.stream(cout):
+                hD[i % 2].copy_(dCD, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cout)
+            out_done.append(ev)
+        last.record(cout)
+        torch.cuda.synchronize()
+        return first.elapsed_time(last) / nsteps
+
+    e2e_run(2, True)
+    e2e_run(2, False)
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    te = torch.tensor([e2e_ms], device=dev)
+    e2e_ms = e2e_run(args.e2e_steps, True)
+    e2e_serial_ms = e2e_run(max(2, args.e2e_steps // 2), False)
+    te = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
     if ws > 1:
         dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms = float(te.item())
-    del dA, dB, dCD
+    e2e_ms, e2e_serial_ms = (float(x) for x in te.tolist())
+    del bufs
 
     if rank != 0:
         if ws > 1:
@@ -436,7 +463,10 @@ def run_ours(args):
                    "path": "large" if path == gb.PATH_LARGE else "skinny"},
         "e2e": {"value": ws * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+                "pipelining": "two buffer sets; H2D, GEMM and D2H on three streams",
+                "serial_ms_per_step": e2e_serial_ms,
+                "serial_value": ws * w.flops / (e2e_serial_ms * 1e-3) / 1e12},
         "gpu_launches": launches,
         "roofline": roofline,
         "cpu_baseline": cpu,
