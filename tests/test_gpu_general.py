@@ -244,3 +244,70 @@ def test_unscaled_entry_point_unchanged_by_general_form():
     D, _ = cs.run(1.0, 1.0, 0)
     torch.cuda.synchronize()
     assert torch.equal(CD.cpu().view(torch.int16), D.view(torch.int16))
+
+
+def test_batched_large_sampled_rows():
+    """Two 4096^3 problems (16 x 16 tiles each, several waves), scaled, separate
+    D, real values: whole rows of D checked against the oracle's general form
+    evaluated on those rows only."""
+    M = N = K = 4096
+    L = 2
+    dev = torch.device("cuda")
+    A_st = wl.draw((L * M * K,), "u11", 501)
+    B_st = wl.draw((L * N * K,), "u11", 502)
+    C_st = wl.draw((L * M * N,), "u11", 503)
+    A, B, C = A_st.to(dev), B_st.to(dev), C_st.to(dev)
+    D = torch.empty(L * M * N, dtype=torch.float16, device=dev)
+    st = gb.gemm_tn_batched(M, N, K, L, 0.5, A.data_ptr(), K, M * K, 0, B.data_ptr(), K, N * K,
+                            0, -1.0, C.data_ptr(), N, M * N, D.data_ptr(), N, M * N, 0,
+                            torch.cuda.current_stream().cuda_stream)
+    assert st == gb.OK
+    torch.cuda.synchronize()
+    d = np_bits(D.cpu())
+    a, b, c = np_bits(A_st), np_bits(B_st), np_bits(C_st)
+    rng = np.random.default_rng(7)
+    for l in range(L):
+        for m0 in sorted(rng.choice(M - 1, 3, replace=False)):
+            rows = 2
+            ao = l * M * K + m0 * K
+            co = l * M * N + m0 * N
+            d64, d16 = oracle.gemm_tn_general(rows, N, K, 0.5, a[ao:ao + rows * K], K, 0,
+                                              b[l * N * K:(l + 1) * N * K], K, 0, -1.0,
+                                              c[co:co + rows * N], N)
+            got = d[co:co + rows * N].reshape(1, rows, N)
+            check(got, d64, d16, K, 0, False, f"problem {l} rows {m0}..{m0 + rows}")
+
+
+@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny"])
+def test_graph_capture_replays_match_eager(case):
+    """A call captured into a CUDA graph (after one eager call has set the
+    library up) replays to the same bits as the eager call.  The tile-kernel
+    and scale-only paths allocate nothing per call; the skinny path's
+    workspace comes from the library's pool in stream order, which capture
+    records as graph memory nodes."""
+    M, N, K, L = (16, 1000, 3000, 1) if case == "skinny" else (520, 392, 328, 2)
+    tile = {"wide": gb.TILE_WIDE, "single": gb.TILE_SINGLE, "scale": gb.TILE_WIDE,
+            "skinny": 0}[case]
+    path = gb.PATH_SKINNY if case == "skinny" else gb.PATH_LARGE
+    alpha = 0.0 if case == "scale" else -2.0
+    cs = Case(M, N, K, L, seed=20)
+    dev = torch.device("cuda")
+    A, B, C = cs.A.to(dev), cs.B.to(dev), cs.C.to(dev)
+    D_eager, D_graph = cs.D0.to(dev), cs.D0.to(dev)
+
+    def call(D, stream):
+        return gb.gemm_tn_batched_ex(M, N, K, L, alpha, A.data_ptr(), cs.ldA, cs.sA, 0,
+                                     B.data_ptr(), cs.ldB, cs.sB, 0, 0.5, C.data_ptr(), cs.ldC,
+                                     cs.sC, D.data_ptr(), cs.ldD, cs.sD, 0, stream,
+                                     dict(path=path, tile_kernel=tile))
+    assert call(D_eager, torch.cuda.current_stream().cuda_stream) == gb.OK
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        assert call(D_graph, torch.cuda.current_stream().cuda_stream) == gb.OK
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(D_graph.view(torch.int16), D_eager.view(torch.int16))
+    cs.verify(D_graph.cpu(), alpha, 0.5, 0, True, f"graph replay {case}")
