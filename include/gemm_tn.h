@@ -46,6 +46,11 @@
  * until process exit (see gemm_tn_skinny_noalloc for a variant that
  * allocates nothing).
  *
+ * Graphs: the first call on a device sets the library up (kernel attributes,
+ * the workspace pool); after that, calls can be recorded by stream capture
+ * and replayed (the workspace of the skinny and stream-K paths is then a
+ * graph memory node).
+ *
  * Ordering: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream).  It returns once the kernels are enqueued; D is
  * valid after the stream has been synchronised.  Calls on one stream are
