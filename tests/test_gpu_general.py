@@ -278,7 +278,7 @@ def test_batched_large_sampled_rows():
             check(got, d64, d16, K, 0, False, f"problem {l} rows {m0}..{m0 + rows}")
 
 
-@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny"])
+@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "streamk"])
 def test_graph_capture_replays_match_eager(case):
     """A call captured into a CUDA graph (after one eager call has set the
     library up) replays to the same bits as the eager call.  The tile-kernel
@@ -287,7 +287,7 @@ def test_graph_capture_replays_match_eager(case):
     records as graph memory nodes."""
     M, N, K, L = (16, 1000, 3000, 1) if case == "skinny" else (520, 392, 328, 2)
     tile = {"wide": gb.TILE_WIDE, "single": gb.TILE_SINGLE, "scale": gb.TILE_WIDE,
-            "skinny": 0}[case]
+            "skinny": 0, "streamk": gb.TILE_WIDE}[case]
     path = gb.PATH_SKINNY if case == "skinny" else gb.PATH_LARGE
     alpha = 0.0 if case == "scale" else -2.0
     cs = Case(M, N, K, L, seed=20)
@@ -299,7 +299,8 @@ def test_graph_capture_replays_match_eager(case):
         return gb.gemm_tn_batched_ex(M, N, K, L, alpha, A.data_ptr(), cs.ldA, cs.sA, 0,
                                      B.data_ptr(), cs.ldB, cs.sB, 0, 0.5, C.data_ptr(), cs.ldC,
                                      cs.sC, D.data_ptr(), cs.ldD, cs.sD, 0, stream,
-                                     dict(path=path, tile_kernel=tile))
+                                     dict(path=path, tile_kernel=tile,
+                                          stream_k=1 if case == "streamk" else 0))
     assert call(D_eager, torch.cuda.current_stream().cuda_stream) == gb.OK
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
@@ -311,3 +312,37 @@ def test_graph_capture_replays_match_eager(case):
     torch.cuda.synchronize()
     assert torch.equal(D_graph.view(torch.int16), D_eager.view(torch.int16))
     cs.verify(D_graph.cpu(), alpha, 0.5, 0, True, f"graph replay {case}")
+
+
+@pytest.mark.parametrize("route", ["repack", "copy"])
+def test_graph_capture_of_the_strided_routes(route):
+    """gemm_tn_strided captured and replayed: the repack route (pooled
+    buffers, copy kernels, tile kernel, scatter of D) and the copy-producer
+    kernel."""
+    M, N, K = 300, 260, 200
+    dev = torch.device("cuda")
+    ld = K + 1  # not TMA-expressible: forces the repack route
+    A_st = wl.draw((M * ld,), "int1", 31)
+    B_st = wl.draw((N * ld,), "int1", 32)
+    C_st = wl.draw((M * (N + 1),), "int4", 33)
+    A, B = A_st.to(dev), B_st.to(dev)
+    D1, D2 = C_st.to(dev), C_st.to(dev)
+
+    path = gb.PATH_STRIDED_REPACK if route == "repack" else gb.PATH_STRIDED_COPY
+
+    def call(D, stream):
+        return gb.gemm_tn_strided_ex(M, N, K, A.data_ptr(), ld, 1, B.data_ptr(), ld, 1,
+                                     D.data_ptr(), N + 1, 1, 0, stream, {"path": path})
+    assert call(D1, torch.cuda.current_stream().cuda_stream) == gb.OK
+    assert ("repack" in gb.gemm_tn_last_kernels()) == (route == "repack")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        assert call(D2, torch.cuda.current_stream().cuda_stream) == gb.OK
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(D1.view(torch.int16), D2.view(torch.int16))
+    d64, d16 = oracle.gemm_tn_strided(M, N, K, np_bits(A_st), ld, 1, np_bits(B_st), ld, 1,
+                                      np_bits(C_st), N + 1, 1)
+    got = np_bits(D2.cpu())[:M * (N + 1)].reshape(M, N + 1)[:, :N]
+    check(got, d64, d16, K, 0, True, f"strided graph replay ({route})")
