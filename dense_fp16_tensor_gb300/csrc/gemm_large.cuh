@@ -84,44 +84,6 @@ __device__ __forceinline__ void batch_tile(const LargeArgs& p, int t, int& tb, i
   tile_coords(t - tb * p.tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
 }
 
-// Epilogue of one 32-column chunk for one row of problem tb:
-// D = alpha * acc + beta * C, fp16 out.
-__device__ __forceinline__ void store_chunk(const LargeArgs& p, int tb, int m, int n0,
-                                            const uint32_t (&r)[32]) {
-  if (m >= p.M || n0 >= p.N) return;
-  const EpiArgs& e = p.e;
-  const __half* crow = e.C + tb * e.sC + static_cast<int64_t>(m) * e.ldC;
-  __half* drow = e.D + tb * e.sD + static_cast<int64_t>(m) * e.ldD;
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    const int n = n0 + 8 * v;
-    if (n + 8 <= p.N) {
-      uint4 c = make_uint4(0u, 0u, 0u, 0u);
-      if (e.read_c) c = *reinterpret_cast<const uint4*>(crow + n);
-      const __half2* ch = reinterpret_cast<const __half2*>(&c);
-      uint4 o;
-      __half2* oh = reinterpret_cast<__half2*>(&o);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = r[8 * v + 2 * j], hi = r[8 * v + 2 * j + 1];
-        if (p.acc_f16) {
-          const __half2 acc = __halves2half2(__ushort_as_half(static_cast<unsigned short>(lo)),
-                                             __ushort_as_half(static_cast<unsigned short>(hi)));
-          oh[j] = epi_f16x2(e, acc, ch[j]);
-        } else {
-          oh[j] = epi_f32x2(e, __uint_as_float(lo), __uint_as_float(hi), ch[j]);
-        }
-      }
-      *reinterpret_cast<uint4*>(drow + n) = o;
-    } else {
-      for (int j = 0; j < 8 && n + j < p.N; ++j) {
-        const __half c = e.read_c ? crow[n + j] : __ushort_as_half(0);
-        drow[n + j] = epi_one(e, p.acc_f16, r[8 * v + j], c);
-      }
-    }
-  }
-}
-
 // Eight fp16 values of C (uint4) plus eight accumulator words -> eight fp16
 // of D = alpha * acc + beta * C.
 __device__ __forceinline__ uint4 add_c8(const LargeArgs& p, const uint32_t* r, uint4 c) {

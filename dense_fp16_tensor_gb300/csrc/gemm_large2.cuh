@@ -38,7 +38,9 @@ struct PairSmem {
   static constexpr uint32_t kABytes = 128 * kPairBK * 2;  // 16 KiB
   static constexpr uint32_t kBBytes = 128 * kPairBK * 2;  // 16 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kBarOffset = kPairStages * kStageBytes;
+  // epilogue staging: 4 warps x 32 rows x 64 fp16 (1024-aligned)
+  static constexpr uint32_t kStagingOffset = kPairStages * kStageBytes;
+  static constexpr uint32_t kBarOffset = kStagingOffset + 4 * kStagingBytes;
   static constexpr uint32_t kNumBars = 2 * kPairStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
@@ -47,7 +49,8 @@ struct PairSmem {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tn_large2_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const LargeArgs p) {
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmD, const LargeArgs p) {
   using L = PairSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -86,6 +89,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), kPairTmemCols);
@@ -220,32 +224,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Staged as in the single-CTA kernels: this CTA's 128 rows of the pair
+    // tile, C fetched while the tile's MMAs run, 64-column chunks stored by
+    // TMA; the accumulator goes back to the even CTA's MMA thread.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const int row_in_tile = static_cast<int>(rank * 128 + quad * 32 + lane);
+    const int row0 = static_cast<int>(rank * 128 + quad * 32);  // first tile row of this warp
+    uint8_t* stg = smem + L::kStagingOffset + (warp - 2) * kStagingBytes;
+    const uint32_t stg_u32 = smem_u32(stg);
+    constexpr int kChunks = kPairBN / 64;
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     uint32_t acc = 0, acc_phase = 0;
+    uint4 cnext[8];
     for (int t = pair; t < p.num_tiles; t += num_pairs) {
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
+      const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
+      const int m_base = tm * kPairBM + row0, n_base = tn * kPairBN;
+      epi_load_c(p, cb, m_base, n_base, lane, cnext);
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+      epi_stage_c(stg, lane, cnext);
+      epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
+      __syncwarp();
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, acc), true, peer_abort))
         break;
       tc_fence_after();
-      const int m = tm * kPairBM + row_in_tile;
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN;
 #pragma unroll 1
-      for (int c = 0; c < kPairBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
+      for (int c = 0; c < kChunks; ++c) {
+        if (c > 0) {
+          if (lane == 0) bulk_wait_group_read0();  // previous store has read staging
+          __syncwarp();
+          epi_stage_c(stg, lane, cnext);
+          if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
+          __syncwarp();
+        }
+        uint32_t r[64];
+        tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        store_chunk(p, tb, m, tn * kPairBN + c * 32, r);
+        if (c == kChunks - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
+        }
+        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_group0();  // all D stores performed before exit
+    __syncwarp();
   }
 
   __syncwarp();

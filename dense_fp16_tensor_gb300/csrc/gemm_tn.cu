@@ -366,7 +366,20 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   // flop per SM) unless the problem is too small to fill them or the caller
   // asked for another tile kernel.
   int kind = o.tile_kernel;
-  if (kind == 0) kind = (M > kLargeBM && N > 128) ? 3 : 1;
+  if (kind == 0) {
+    // 256 x 256 tiles on one CTA need the fewest operand bytes per flop, but
+    // their accumulator cannot be double-buffered: they win when K is long
+    // enough to hide the drain and there are enough tiles to fill at least
+    // half the SMs.  Otherwise the CTA pair (double-buffered, 256 x 256 per
+    // two SMs), or 128-row tiles when a side is too short for 256.
+    if (M > kLargeBM && N > 128) {
+      const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
+      const bool wide_ok = K > 1024 && 2 * tiles256 >= st.num_sms;
+      kind = wide_ok ? 3 : (st.max_pairs > 0 ? 2 : 1);
+    } else {
+      kind = 1;
+    }
+  }
   if (kind == 2 && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
   const bool pair = kind == 2, wide = kind == 3;
   const int bn = (pair || wide) ? 256 : ((o.tile_n == 128) ? 128 : 256);
@@ -403,10 +416,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.sk_tile0 = p.num_tiles;  // no split tiles unless stream-K is set up below
   void* sk_ws = nullptr;
   CUtensorMap tmD;
-  if (!pair) {
-    s = encode_d(&tmD, q.D, M, N, q.ldD, q.sD, q.L);
-    if (s != GEMM_TN_OK) return s;
-  }
+  s = encode_d(&tmD, q.D, M, N, q.ldD, q.sD, q.L);
+  if (s != GEMM_TN_OK) return s;
   if (wide) {
     int grid = std::min(p.num_tiles, st.num_sms);
     // Stream-K for the last, partial wave, on request only (fp32
@@ -451,8 +462,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     }
   } else if (pair) {
     const int pairs = std::min(p.num_tiles, st.max_pairs);
-    gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(tmA, tmB,
-                                                                                     p);
+    gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(
+        tmA, tmB, tmD, p);
   } else {
     const int grid = std::min(p.num_tiles, st.num_sms);
     if (bn == 256) {
