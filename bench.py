@@ -43,7 +43,7 @@ METRIC = "fp16 TN GEMM TFLOP/s at 8192³ and % of GB300 dense FP16 tensor peak"
 UNIT = "TFLOP/s"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--tile-kernel", type=int, default=0,
                     help="large path: 0 choose, 1 single-CTA 128xN, 2 CTA-pair 256x256, "
                          "3 single-CTA 256x256")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -70,6 +70,25 @@ def dist_env():
 
 
 # ---------------------------------------------------------------- helpers
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank values over all ranks (the values
+    themselves with one rank).  device: where the reduction tensor lives
+    ('cuda' for NCCL, 'cpu' for gloo)."""
+    import torch
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor(list(values), dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return [float(x) for x in t.tolist()]
+    return [float(x) for x in values]
+
+
+def whole_job_tflops(world_size, flops_per_step, steps, max_total_ms):
+    """Throughput of the whole job: every rank's work over the slowest rank's
+    time (replicas: each rank runs the same problem on its own GPU)."""
+    return world_size * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -342,12 +361,9 @@ def run_ours(args):
         sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1) if rank == 0 else None
 
-    t = torch.tensor([total_ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    (total_ms,) = max_over_ranks([total_ms], dev)
     ms_per_step = total_ms / args.steps
-    value = ws * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(ws, w.flops, args.steps, total_ms)
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its A, B and C from pinned host memory and its D back.  The steps are
@@ -403,10 +419,7 @@ def run_ours(args):
     barrier()
     e2e_ms = e2e_run(args.e2e_steps, True)
     e2e_serial_ms = e2e_run(max(2, args.e2e_steps // 2), False)
-    te = torch.tensor([e2e_ms, e2e_serial_ms], device=dev)
-    if ws > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_ms, e2e_serial_ms = (float(x) for x in te.tolist())
+    e2e_ms, e2e_serial_ms = max_over_ranks([e2e_ms, e2e_serial_ms], dev)
     del bufs
 
     if rank != 0:
@@ -461,12 +474,12 @@ def run_ours(args):
                           "> 129 MB), no flush" if w.min_bytes > 129e6 else
                           "inputs smaller than L2, no flush"),
                    "path": "large" if path == gb.PATH_LARGE else "skinny"},
-        "e2e": {"value": ws * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_tflops(ws, w.flops, 1, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                 "pipelining": "two buffer sets; H2D, GEMM and D2H on three streams",
                 "serial_ms_per_step": e2e_serial_ms,
-                "serial_value": ws * w.flops / (e2e_serial_ms * 1e-3) / 1e12},
+                "serial_value": whole_job_tflops(ws, w.flops, 1, e2e_serial_ms)},
         "gpu_launches": launches,
         "roofline": roofline,
         "cpu_baseline": cpu,
