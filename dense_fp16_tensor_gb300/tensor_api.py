@@ -70,3 +70,67 @@ def gemm(A: torch.Tensor, Bm: torch.Tensor, CD: torch.Tensor, accum: str = "f32"
     if st != B.OK:
         raise B.GemmTnError(st)
     return CD
+
+
+def _per_problem(t: torch.Tensor | None, name: str):
+    """(2-D view of problem 0, batch stride, batch size or None) of a 2-D or 3-D tensor."""
+    if t is None:
+        return None, 0, None
+    if t.dim() == 3:
+        return t[0], t.stride(0) if t.shape[0] > 1 else 0, t.shape[0]
+    if t.dim() == 2:
+        return t, 0, None
+    raise TypeError(f"{name} must be 2-D or 3-D")
+
+
+def gemm_scaled(A: torch.Tensor, Bm: torch.Tensor, C: torch.Tensor | None = None, *,
+                alpha: float = 1.0, beta: float | None = None, out: torch.Tensor | None = None,
+                accum: str = "f32", stream: torch.cuda.Stream | None = None,
+                **options) -> torch.Tensor:
+    """out <- alpha * A . Bm^T + beta * C (gemm_tn_batched).
+
+    2-D operands are one problem: A (M,K), Bm (N,K), C and out (M,N).  Any
+    3-D operand makes a batch: A (L,M,K), Bm (L,N,K), C and out (L,M,N); a
+    2-D operand (or a 3-D one expanded along the batch, stride 0) is shared
+    by every problem.  beta defaults to 1 with C and 0 without; out is
+    allocated when not given (and may be C itself, for in place).
+    """
+    A2, sA, LA = _per_problem(A, "A")
+    B2, sB, LB = _per_problem(Bm, "B")
+    C2, sC, LC = _per_problem(C, "C")
+    O2, sO, LO = _per_problem(out, "out")
+    sizes = {x for x in (LA, LB, LC, LO) if x is not None}
+    if len(sizes) > 1:
+        raise ValueError(f"batch sizes disagree: {sorted(sizes)}")
+    L = sizes.pop() if sizes else None
+    M, K = A2.shape
+    N, K2 = B2.shape
+    if K2 != K:
+        raise ValueError(f"K mismatch: A {tuple(A.shape)}, B {tuple(Bm.shape)}")
+    if beta is None:
+        beta = 1.0 if C is not None else 0.0
+    if beta != 0 and C is None:
+        raise ValueError("beta != 0 needs C")
+    if out is None:
+        shape = (L, M, N) if L is not None else (M, N)
+        out = torch.empty(shape, dtype=torch.float16, device=A.device)
+        O2, sO, _ = _per_problem(out, "out")
+    for t, name in ((A, "A"), (Bm, "B"), (C, "C"), (out, "out")):
+        if t is not None and (t.dtype != torch.float16 or not t.is_cuda):
+            raise TypeError(f"{name} must be a float16 CUDA tensor")
+    for t2, name in ((C2, "C"), (O2, "out")):
+        if t2 is not None and (tuple(t2.shape) != (M, N) or (t2.stride(1) != 1 and N > 1)):
+            raise ValueError(f"{name} must be (M, N) row-major per problem")
+    a_major, ldA = operand_view(A2, "A")
+    b_major, ldB = operand_view(B2, "B")
+    ldC = (C2.stride(0) if M > 1 else _round8(N)) if C2 is not None else N
+    ldD = O2.stride(0) if M > 1 else _round8(N)
+    s = stream if stream is not None else torch.cuda.current_stream(out.device)
+    acc = _ACC[accum] if isinstance(accum, str) else int(accum)
+    st = B.gemm_tn_batched_ex(M, N, K, L if L is not None else 1, float(alpha), A2.data_ptr(),
+                              ldA, sA, a_major, B2.data_ptr(), ldB, sB, b_major, float(beta),
+                              C2.data_ptr() if C2 is not None else 0, ldC, sC, O2.data_ptr(),
+                              ldD, sO, acc, s.cuda_stream, options or None)
+    if st != B.OK:
+        raise B.GemmTnError(st)
+    return out

@@ -274,8 +274,8 @@ def gemm_tn_general(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C=No
     leaves A and B unread, beta == 0 leaves C unread (C may be None).
     Returns ``(d64, d16bits)`` of shape (batch, M, N)."""
     lib = _load()
-    A, B = _bits(A), _bits(B)
-    C = None if C is None else _bits(C)
+    A, B = _bits(A).reshape(-1), _bits(B).reshape(-1)
+    C = None if C is None else _bits(C).reshape(-1)
     if beta != 0 and C is None:
         raise ValueError("beta != 0 needs C")
     vA = (ldA, 1) if a_major == MAJOR_K else (1, ldA)

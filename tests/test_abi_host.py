@@ -197,3 +197,18 @@ def test_scaled_is_one_problem(lib):
     st = gb.gemm_tn_scaled(0, 64, 64, 2.0, P, 64, 0, P + 4 * MB, 64, 0, 0.5, 0, 64, 0, 64, 0,
                            None)
     assert st == gb.OK                                       # M == 0: no-op
+
+
+def test_tensor_front_end_checks_before_the_device():
+    import torch
+    from dense_fp16_tensor_gb300 import tensor_api
+    A = torch.zeros((2, 16, 32), dtype=torch.float16)
+    B = torch.zeros((3, 24, 32), dtype=torch.float16)
+    with pytest.raises(ValueError, match="batch sizes disagree"):
+        tensor_api.gemm_scaled(A, B)
+    with pytest.raises(ValueError, match="K mismatch"):
+        tensor_api.gemm_scaled(A, torch.zeros((2, 24, 16), dtype=torch.float16))
+    with pytest.raises(ValueError, match="beta != 0 needs C"):
+        tensor_api.gemm_scaled(A, B[:2], beta=1.0)
+    with pytest.raises(TypeError, match="CUDA"):
+        tensor_api.gemm_scaled(A, B[:2], out=torch.zeros((2, 16, 24), dtype=torch.float16))

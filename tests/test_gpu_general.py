@@ -346,3 +346,29 @@ def test_graph_capture_of_the_strided_routes(route):
                                       np_bits(C_st), N + 1, 1)
     got = np_bits(D2.cpu())[:M * (N + 1)].reshape(M, N + 1)[:, :N]
     check(got, d64, d16, K, 0, True, f"strided graph replay ({route})")
+
+
+def test_tensor_front_end_scaled_and_batched():
+    """dense_fp16_tensor_gb300.gemm_scaled: 3-D batches (B shared through
+    expand, stride 0), a separate output allocated by the call, and a 2-D
+    in-place call with out = C."""
+    import dense_fp16_tensor_gb300 as g
+    dev = torch.device("cuda")
+    L, M, N, K = 3, 136, 200, 96
+    A = wl.draw((L, M, K), "int1", 41).to(dev)
+    B1 = wl.draw((N, K), "int1", 42).to(dev)
+    C = wl.draw((L, M, N), "int4", 43).to(dev)
+    D = g.gemm_scaled(A, B1.unsqueeze(0).expand(L, N, K), C, alpha=2.0, beta=-1.0)
+    torch.cuda.synchronize()
+    assert D.shape == (L, M, N)
+    _, ref16 = oracle.gemm_tn_general(M, N, K, 2.0, np_bits(A.cpu()), K, 0, np_bits(B1.cpu()), K,
+                                      0, -1.0, np_bits(C.cpu()), N, L, M * K, 0, M * N)
+    assert np.array_equal(np_bits(D.cpu()).reshape(L, M, N), ref16)
+    # one problem, in place: C <- 0.5 * A0 . B1^T + 1 * C
+    C0 = C[1].clone()
+    out = g.gemm_scaled(A[0], B1, C0, alpha=0.5, out=C0)
+    torch.cuda.synchronize()
+    assert out.data_ptr() == C0.data_ptr()
+    _, ref16 = oracle.gemm_tn_general(M, N, K, 0.5, np_bits(A[0].cpu()), K, 0, np_bits(B1.cpu()),
+                                      K, 0, 1.0, np_bits(C[1].cpu()), N)
+    assert np.array_equal(np_bits(C0.cpu()), ref16[0])
