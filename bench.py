@@ -479,6 +479,7 @@ def run_ours(args):
                 "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                 "pipelining": "two buffer sets; H2D, GEMM and D2H on three streams",
                 "serial_ms_per_step": e2e_serial_ms,
+                "h2d_gb_per_s": h2d / (e2e_ms * 1e-3) / 1e9,
                 "serial_value": whole_job_tflops(ws, w.flops, 1, e2e_serial_ms)},
         "gpu_launches": launches,
         "roofline": roofline,
