@@ -437,10 +437,13 @@ def run_ours(args):
     kkey = next((k for k in kernels_run.split("+") if k.startswith("gemm_tn")), "").split("<")[0]
     traffic = traffic_for(kkey, w.name) if kkey in KERNEL_SOURCES else None
     if path == gb.PATH_LARGE:
+        sustained = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic,
                     "kernel": kernels_run,
                     "peak_kind": f"{peak_kind} bf16 dense burst (fp16 dense rate is equal)",
+                    "peak_sustained": sustained,
+                    "frac_of_sustained": achieved / sustained if sustained else None,
                     "algorithmic_flops_per_launch": w.flops}
     else:
         gbs = w.min_bytes / (kernel_ms * 1e-3) / 1e9
