@@ -366,13 +366,19 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   // flop per SM) unless the problem is too small to fill them or the caller
   // asked for another tile kernel.
   int kind = o.tile_kernel;
+  int tile_n = o.tile_n;
   if (kind == 0) {
     // 256 x 256 tiles on one CTA need the fewest operand bytes per flop, but
     // their accumulator cannot be double-buffered: they win when K is long
     // enough to hide the drain and there are enough tiles to fill at least
     // half the SMs.  Otherwise the CTA pair (double-buffered, 256 x 256 per
-    // two SMs), or 128-row tiles when a side is too short for 256.
-    if (M > kLargeBM && N > 128) {
+    // two SMs); 128-row tiles when a side is too short for 256, and
+    // 128 x 128 tiles when even 128 x 256 tiles would leave half the SMs idle.
+    const int64_t tiles_128x256 = ((M + 127) / 128) * ((N + 255) / 256) * q.L;
+    if (2 * tiles_128x256 <= st.num_sms) {
+      kind = 1;
+      if (tile_n == 0) tile_n = 128;
+    } else if (M > kLargeBM && N > 128) {
       const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
       const bool wide_ok = K > 1024 && 2 * tiles256 >= st.num_sms;
       kind = wide_ok ? 3 : (st.max_pairs > 0 ? 2 : 1);
@@ -382,7 +388,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   }
   if (kind == 2 && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
   const bool pair = kind == 2, wide = kind == 3;
-  const int bn = (pair || wide) ? 256 : ((o.tile_n == 128) ? 128 : 256);
+  const int bn = (pair || wide) ? 256 : ((tile_n == 128) ? 128 : 256);
   const int bm = (pair || wide) ? 256 : kLargeBM;
   CUtensorMap tmA, tmB;
   int s = encode_operand_batched(&tmA, q.A, M, K, q.ldA, q.sA, q.L, a_major,

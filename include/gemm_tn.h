@@ -133,10 +133,12 @@ typedef struct {
                            consumer's bounded wait expires and the kernel
                            reports GEMM_TN_ERR_DEVICE_TIMEOUT instead of
                            hanging */
-  int tile_kernel;      /* large path: 0 = choose (when M and N exceed 128:
-                           3 if K > 1024 and the 256 x 256 tiles of all
-                           problems fill at least half the SMs, else 2;
-                           otherwise 1), 1 = single-CTA 128 x tile_n
+  int tile_kernel;      /* large path: 0 = choose (1 with 128 x 128 tiles
+                           when 128 x 256 tiles would fill at most half the
+                           SMs; else, when M and N exceed 128, 3 if K > 1024
+                           and the 256 x 256 tiles of all problems fill at
+                           least half the SMs, otherwise 2; else 1),
+                           1 = single-CTA 128 x tile_n
                            tiles, 2 = CTA-pair 256 x 256 tiles (two SMs per
                            tile, tcgen05 cta_group::2), 3 = single-CTA
                            256 x 256 tiles (tile_n is ignored by 2 and 3) */
