@@ -458,6 +458,7 @@ def run_ours(args):
         extra["strided_4096"] = bench_strided(dev, stream)
         extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
         extra["scaled_batched"] = bench_general(dev, stream)
+        extra["tile_split_k"] = bench_tile_split(dev, stream)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -627,6 +628,49 @@ def bench_stream_k(dev, stream, steps=50, rounds=3):
             "unsplit": {"kernels": kernels[-1], "ms_per_call": ms_plain,
                         "TFLOP_per_s": fl / (ms_plain * 1e-3) / 1e12},
             "speedup": ms_plain / ms_sk}
+
+
+def bench_tile_split(dev, stream, steps=100):
+    """K split of the 128-row tile kernel on shapes whose tiles leave most SMs
+    idle: the automatic choice (split, with its reduction) against the same
+    kernel unsplit; fp32 accumulation."""
+    import torch
+
+    from dense_fp16_tensor_gb300 import binding as gb
+    from dense_fp16_tensor_gb300 import workloads as wl
+    out = {}
+    for M, N, K in ((512, 512, 8192), (256, 1024, 16384), (1024, 1024, 8192)):
+        A = wl.draw((M * K,), "u11", 7301).to(dev)
+        Bm = wl.draw((N * K,), "u11", 7302).to(dev)
+        CD = torch.zeros(M * N, dtype=torch.float16, device=dev)
+        sp = stream.cuda_stream
+        row = {}
+        for name, opts in (("split", None), ("unsplit", {"path": gb.PATH_LARGE, "tile_kernel": 1,
+                                                         "tile_n": 128})):
+            def step():
+                st = gb.gemm_tn_ex(M, N, K, A.data_ptr(), K, 0, Bm.data_ptr(), K, 0, CD.data_ptr(),
+                                   N, 0, sp, opts)
+                if st != gb.OK:
+                    raise gb.GemmTnError(st)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    step()
+            torch.cuda.synchronize()
+            kernels = gb.gemm_tn_last_kernels()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(steps):
+                    step()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / steps * 1e3
+            row[name] = {"kernels": kernels, "us_per_call": us,
+                         "TFLOP_per_s": 2.0 * M * N * K / (us * 1e-6) / 1e12}
+        row["speedup"] = row["unsplit"]["us_per_call"] / row["split"]["us_per_call"]
+        out[f"{M}x{N}x{K}"] = row
+    return out
 
 
 def bench_general(dev, stream, steps=20):

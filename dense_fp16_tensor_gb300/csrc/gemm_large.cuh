@@ -60,6 +60,14 @@ struct LargeArgs {
   int sk_per;          // units per CTA
   float* sk_partials;  // [gridDim.x * sk_max_segs] slots of 256 x 256 fp32
   int* sk_counters;    // [(num_tiles - sk_tile0) * 8], zero on entry
+  // Split-K of the 128-row kernel: each tile's K blocks are cut into
+  // ks_splits ranges of ks_kb_per blocks (the last may be shorter); work
+  // unit u is split u % ks_splits of tile u / ks_splits.  With ks_splits > 1
+  // each unit stores its fp32 partial tile to ks_ws (layout at
+  // ks_partial_index) and gemm_tn_tile_reduce_kernel adds the splits.
+  int ks_splits;       // 1 = no split
+  int ks_kb_per;
+  float* ks_ws;
 };
 
 template <int BN>
@@ -82,6 +90,15 @@ __device__ __forceinline__ void batch_tile(const LargeArgs& p, int t, int& tb, i
                                            int& tn) {
   tb = p.batch > 1 ? t / p.tiles_per_batch : 0;
   tile_coords(t - tb * p.tiles_per_batch, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+}
+
+// Split-K partial tile of unit u (128 x bn fp32): float4 of row 32q + lane,
+// columns 64c + 4g .. +3 (q: TMEM lane quadrant, c: 64-column chunk, g: group
+// of 4 columns) at this index, so that a warp's stores and the reduction's
+// loads move whole 512-byte lines.
+__device__ __forceinline__ int64_t ks_partial_index(int64_t u, int bn, int q, int c, int g,
+                                                    int lane) {
+  return (((u * 4 + q) * (bn / 64) + c) * 16 + g) * 32 + lane;
 }
 
 // Eight fp16 values of C (uint4) plus eight accumulator words -> eight fp16
@@ -215,6 +232,9 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
+  // a split-K reduction launched as a programmatic dependent may become
+  // resident now; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLargeStages; ++s) {
@@ -250,17 +270,20 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: loads issued, their parity
       bool ok = true;
       int local = 0;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++local) {
+      const int units = p.num_tiles * p.ks_splits;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++local) {
+        const int t = u / p.ks_splits, sp = u - t * p.ks_splits;
+        const int kb0 = sp * p.ks_kb_per, kb1 = min(kb0 + p.ks_kb_per, p.k_blocks);
         int tb, tm, tn;
         batch_tile(p, t, tb, tm, tn);
         const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
                             timeout_code(kRoleProducer, stage))) {
             ok = false;
             break;
           }
-          const bool withhold = p.test_stall && local == 0 && kb == 0;
+          const bool withhold = p.test_stall && local == 0 && kb == kb0;
           if (!withhold) {
             const uint32_t fb = full0 + 8 * stage;
             const uint32_t a_dst = smem_u32(sA + stage * L::kABytes);
@@ -304,7 +327,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       const uint32_t idesc = make_idesc_f16(kLargeBM, BN, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      const int units = p.num_tiles * p.ks_splits;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int sp = u % p.ks_splits;
+        const int kb0 = sp * p.ks_kb_per, kb1 = min(kb0 + p.ks_kb_per, p.k_blocks);
         if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
                           timeout_code(kRoleMma, 0x200 + acc))) {
           ok = false;
@@ -312,7 +338,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
                             timeout_code(kRoleMma, stage))) {
             ok = false;
@@ -327,7 +353,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
                                        : make_sw128_desc(a_base + k * 32, 16, 1024);
             const uint64_t bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
                                        : make_sw128_desc(b_base + k * 32, 16, 1024);
-            mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            mma_f16(d_tmem, ad, bd, idesc, (kb != kb0) || (k != 0));
           }
           mma_commit(empty0 + 8 * stage);  // stage free once these MMAs have read it
           if (++stage == kLargeStages) {
@@ -358,7 +384,38 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     constexpr int kChunks = BN / 64;
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    const int units = p.num_tiles * p.ks_splits;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      if (p.ks_splits > 1) {
+        // split-K unit: this warp's 32 rows of the fp32 partial tile -> ks_ws
+        if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
+                          timeout_code(kRoleEpilogue, acc)))
+          break;
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN;
+        float4* ws4 = reinterpret_cast<float4*>(p.ks_ws);
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+          tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+          tmem_wait_ld();
+          if (c == kChunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+          }
+#pragma unroll
+          for (int g = 0; g < 16; ++g)
+            ws4[ks_partial_index(u, BN, static_cast<int>(quad), c, g, static_cast<int>(lane))] =
+                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
+      const int t = u;
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
@@ -410,6 +467,68 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * BN);
+  }
+}
+
+// Sum of the split-K partials of one 32 x 64 piece of a tile, in split order,
+// then the epilogue: D = alpha * sum + beta * C (see EpiArgs).  Block
+// (piece, tile): piece = quadrant q (32 rows) x chunk c (64 columns).  The
+// partial float4s are read in their stored order (whole lines), the sums go
+// through shared memory, and C / D move as 16-byte row segments.  Launched
+// as a programmatic dependent of the split kernel.
+constexpr int kTileReduceThreads = 256;
+
+template <int BN>
+__global__ void __launch_bounds__(kTileReduceThreads)
+    gemm_tn_tile_reduce_kernel(const LargeArgs p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float sum[32][64 + 4];
+  const int t = static_cast<int>(blockIdx.y);
+  const int piece = static_cast<int>(blockIdx.x);
+  const int q = piece / (BN / 64), c = piece - q * (BN / 64);
+  const float4* ws4 = reinterpret_cast<const float4*>(p.ks_ws);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int f = static_cast<int>(threadIdx.x) + h * kTileReduceThreads;  // 0..511
+    const int g = f >> 5, lane = f & 31;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < p.ks_splits; ++sp) {
+      const float4 v = __ldcg(ws4 + ks_partial_index(static_cast<int64_t>(t) * p.ks_splits + sp,
+                                                     BN, q, c, g, lane));
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    sum[lane][4 * g] = a.x;
+    sum[lane][4 * g + 1] = a.y;
+    sum[lane][4 * g + 2] = a.z;
+    sum[lane][4 * g + 3] = a.w;
+  }
+  __syncthreads();
+  int tb, tm, tn;
+  batch_tile(p, t, tb, tm, tn);
+  const int r = static_cast<int>(threadIdx.x) >> 3, seg = static_cast<int>(threadIdx.x) & 7;
+  const int m = tm * kLargeBM + 32 * q + r, n = tn * BN + 64 * c + 8 * seg;
+  if (m >= p.M || n >= p.N) return;
+  const EpiArgs& e = p.e;
+  const __half* crow = e.read_c ? e.C + tb * e.sC + static_cast<int64_t>(m) * e.ldC : nullptr;
+  __half* drow = e.D + tb * e.sD + static_cast<int64_t>(m) * e.ldD;
+  if (n + 8 <= p.N) {
+    uint4 cv = make_uint4(0u, 0u, 0u, 0u);
+    if (e.read_c) cv = *reinterpret_cast<const uint4*>(crow + n);
+    const __half2* ch = reinterpret_cast<const __half2*>(&cv);
+    uint4 o;
+    __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      oh[j] = epi_f32x2(e, sum[r][8 * seg + 2 * j], sum[r][8 * seg + 2 * j + 1], ch[j]);
+    *reinterpret_cast<uint4*>(drow + n) = o;
+  } else {
+    for (int j = 0; n + j < p.N; ++j) {
+      const __half cj = e.read_c ? crow[n + j] : __ushort_as_half(0);
+      drow[n + j] = epi_one(e, false, __float_as_uint(sum[r][8 * seg + j]), cj);
+    }
   }
 }
 

@@ -420,6 +420,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
   p.sk_tile0 = p.num_tiles;  // no split tiles unless stream-K is set up below
+  p.ks_splits = 1;           // no K split of the 128-row kernel unless set up below
+  p.ks_kb_per = p.k_blocks;
   void* sk_ws = nullptr;
   CUtensorMap tmD;
   s = encode_d(&tmD, q.D, M, N, q.ldD, q.sD, q.L);
@@ -471,13 +473,69 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(
         tmA, tmB, tmD, p);
   } else {
-    const int grid = std::min(p.num_tiles, st.num_sms);
+    // K split over several CTAs per tile (fp32 accumulation only: a split
+    // fp16 accumulation would round at different places): on request
+    // (split_k with tile_kernel 1), or automatically when the kernel was
+    // chosen automatically, its tiles leave more than half the SMs idle and
+    // K is long enough (>= 2048, >= 512 per split) to pay for the partials
+    // and the reduction.
+    int splits = 1;
+    if (!p.acc_f16) {
+      if (o.tile_kernel == 1 && o.split_k > 0)
+        splits = o.split_k;
+      else if (o.tile_kernel == 0 && o.split_k == 0 && 2 * p.num_tiles <= st.num_sms &&
+               p.k_blocks >= 32)
+        splits = std::min(st.num_sms / p.num_tiles, p.k_blocks / 8);
+      splits = std::max(1, std::min(splits, p.k_blocks));
+    }
+    void* ks_ws = nullptr;
+    if (splits > 1) {
+      p.ks_kb_per = (p.k_blocks + splits - 1) / splits;
+      p.ks_splits = (p.k_blocks + p.ks_kb_per - 1) / p.ks_kb_per;  // no empty split
+      const size_t bytes = static_cast<size_t>(p.num_tiles) * p.ks_splits * kLargeBM * bn * 4;
+      if (static_cast<int64_t>(p.num_tiles) * p.ks_splits > 0x7FFFFFFF ||
+          ws_alloc(&ks_ws, bytes, st, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_TN_ERR_NO_MEMORY;
+      }
+      p.ks_ws = static_cast<float*>(ks_ws);
+    }
+    const int grid = static_cast<int>(
+        std::min<int64_t>(static_cast<int64_t>(p.num_tiles) * p.ks_splits, st.num_sms));
     if (bn == 256) {
       gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
           tmA, tmB, tmD, p);
     } else {
       gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
           tmA, tmB, tmD, p);
+    }
+    if (ks_ws) {
+      cudaError_t e = cudaGetLastError();
+      if (e == cudaSuccess) {
+        // the reduction as a programmatic dependent: resident early, it waits
+        // in griddepcontrol.wait for the split kernel's partials
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(static_cast<unsigned>(4 * (bn / 64)), static_cast<unsigned>(p.num_tiles), 1);
+        cfg.blockDim = dim3(kTileReduceThreads, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = bn == 256 ? cudaLaunchKernelEx(&cfg, gemm_tn_tile_reduce_kernel<256>, p)
+                      : cudaLaunchKernelEx(&cfg, gemm_tn_tile_reduce_kernel<128>, p);
+      }
+      const cudaError_t f = cudaFreeAsync(ks_ws, stream);
+      if (e != cudaSuccess || f != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_TN_ERR_CUDA;
+      }
+      t_last_launches = 2;
+      t_last_kernels = bn == 256 ? "gemm_tn_large_kernel<256>+gemm_tn_tile_reduce_kernel"
+                                 : "gemm_tn_large_kernel<128>+gemm_tn_tile_reduce_kernel";
+      return GEMM_TN_OK;
     }
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;

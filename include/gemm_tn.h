@@ -121,7 +121,12 @@ typedef enum {
 typedef struct {
   int path;             /* gemm_tn_path */
   int split_k;          /* skinny path: number of CTAs sharing the K loop of
-                           the output tiles (0 = one per SM) */
+                           the output tiles (0 = one per SM).  Large path
+                           with tile_kernel 1: K splits per 128-row tile,
+                           fp32 accumulation only (0 = none; with
+                           tile_kernel 0 the library splits by itself when
+                           the tiles would leave more than half the SMs
+                           idle and K >= 2048) */
   int tile_n;           /* large path: output tile width, 0 (= 256), 128 or 256 */
   int sync_check;       /* nonzero: synchronise `stream` after the launch and
                            return GEMM_TN_ERR_DEVICE_TIMEOUT if a kernel gave
