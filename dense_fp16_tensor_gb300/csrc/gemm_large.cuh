@@ -1,11 +1,10 @@
 // gemm_large.cuh -- persistent, warp-specialised tcgen05 TN GEMM for sm_103a.
 //
 // Computes D(m,n) = C(m,n) + sum_k A(m,k) B(n,k) over 128 x BN output tiles
-// (in general D = alpha * A.B^T + beta * C, over a batch of problems; see
-// EpiArgs)
-// (the CTA tiling and K-block loop of "CuTe Layout to Tensor Core", section
-// 4 "local_tile", and "cute(7) simple_gemm", section "3.4 the K loop"), with
-// the data movement redone for GB300:
+// (in general D = alpha * A.B^T + beta * C over a batch of problems, see
+// EpiArgs; the CTA tiling and K-block loop of "CuTe Layout to Tensor Core",
+// section 4 "local_tile", and "cute(7) simple_gemm", section "3.4 the K
+// loop"), with the data movement redone for GB300:
 //
 //   warp 0      TMA producer: per K block of 64, one A box (128 x 64) and one
 //               B box (BN x 64) into a 128B-swizzled stage of a kStages ring,
@@ -16,15 +15,20 @@
 //               issues tcgen05.mma (M=128, N=BN, K=16, four per stage); each
 //               stage is released with tcgen05.commit -> `empty`, each tile
 //               with tcgen05.commit -> `tmem_full`.
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, add C in the
-//               accumulator's precision, round to fp16, predicated 16-byte
-//               stores; arrive `tmem_empty` so the MMA warp can reuse the
-//               accumulator while the next tile's main loop runs.
+//   warps 2-5   epilogue (staged, shared with the other tile kernels): C of
+//               the next tile arrives in coalesced 32 x 64 chunks into a
+//               128-byte-swizzled staging buffer while its MMAs run; per
+//               chunk tcgen05.ld 64 columns, combine with the staged C
+//               (epi_f32x2 / epi_f16x2), TMA-store the chunk; arrive
+//               `tmem_empty` once all columns are read, so the MMA warp
+//               reuses the accumulator while the epilogue finishes.
 //
-// Tiles are handed out round-robin (t = blockIdx.x, += gridDim.x) in a
-// grouped raster.  Every wait is bounded (see wait_bounded); on expiry the
-// kernel records the failure, drains its own copies and MMAs in flight,
-// frees its TMEM and returns.
+// Work units (tiles, or (tile, K range) pairs when ks_splits > 1) are handed
+// out round-robin (u = blockIdx.x, += gridDim.x) in a grouped raster; a
+// split unit stores its fp32 partial tile for gemm_tn_tile_reduce_kernel.
+// Every wait is bounded (see wait_bounded); on expiry the kernel records the
+// failure, drains its own copies and MMAs in flight, frees its TMEM and
+// returns.
 #pragma once
 
 #include <cuda_fp16.h>

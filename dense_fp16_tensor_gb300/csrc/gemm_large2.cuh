@@ -18,6 +18,9 @@
 //     both CTAs with one multicast tcgen05.commit; accumulators are handed to
 //     both CTAs' epilogues the same way, and the eight epilogue warps of the
 //     pair return an accumulator by arriving on the even CTA's `tmem_empty`.
+//   * Each CTA's epilogue is the staged one of gemm_large.cuh on its 128
+//     rows of the tile, with two accumulators so it overlaps the next
+//     tile's main loop.
 //
 // Every wait is bounded; a CTA that gives up raises its own and its peer's
 // abort flag, both drain what they issued, free the pair's TMEM and return.
