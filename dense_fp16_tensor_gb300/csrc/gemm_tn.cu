@@ -5,11 +5,14 @@
 // header.  This file owns:
 //   * validation (sizes, leading dimensions, alignment, aliasing) before any
 //     work is enqueued;
-//   * tensor maps for A and B (128-byte swizzle, zero fill out of range),
-//     built with cuTensorMapEncodeTiled from the driver entry point;
-//   * the choice between the persistent tile kernel and the skinny split-K
-//     kernel, and their grid sizes (one CTA per SM);
-//   * the skinny path's stream-ordered split-K workspace.
+//   * tensor maps for A, B and D (128-byte swizzle, zero fill out of range,
+//     a batch coordinate), built with cuTensorMapEncodeTiled from the
+//     driver entry point;
+//   * the choice of path (tile kernels, skinny split-K, scale-only) and of
+//     tile kernel, K splits and stream-K, and the grid sizes (one CTA per
+//     SM, persistent);
+//   * stream-ordered workspaces from a library-owned memory pool (split-K
+//     partials, stream-K partials, repacked strided operands).
 // Every entry point describes its call as one Problem (a batch of
 // D = alpha * A.B^T + beta * C); gemm_tn itself is the case batch 1,
 // alpha = beta = 1, D = C in place.
