@@ -15,7 +15,11 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
   cpu_baseline  the CPU oracle (fp64 triple loop) timed on a bounded sample
                 of the same workload on this host's cores
   clocks        SM clocks and throttle reasons sampled during the timed region
-  extra         the skinny M=16 workload's achieved HBM bandwidth
+  extra         other paths, each timed on its own: the skinny M=16 workload's
+                HBM bandwidth, 4096^3 with K+1 leading dimensions (strided
+                route), stream-K against the unsplit kernel, the scaled and
+                batched entry point, and the 128-row kernel's K split on
+                few-tile shapes
 
 Multi-GPU: the GEMM is one problem per GPU here (replicas only): with
 torchrun each rank runs the same workload on its own GPU, and the value is
