@@ -278,16 +278,17 @@ def test_batched_large_sampled_rows():
             check(got, d64, d16, K, 0, False, f"problem {l} rows {m0}..{m0 + rows}")
 
 
-@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "streamk"])
+@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "streamk", "tile_split"])
 def test_graph_capture_replays_match_eager(case):
     """A call captured into a CUDA graph (after one eager call has set the
     library up) replays to the same bits as the eager call.  The tile-kernel
     and scale-only paths allocate nothing per call; the skinny path's
     workspace comes from the library's pool in stream order, which capture
     records as graph memory nodes."""
-    M, N, K, L = (16, 1000, 3000, 1) if case == "skinny" else (520, 392, 328, 2)
+    M, N, K, L = {"skinny": (16, 1000, 3000, 1),
+                  "tile_split": (300, 200, 4000, 1)}.get(case, (520, 392, 328, 2))
     tile = {"wide": gb.TILE_WIDE, "single": gb.TILE_SINGLE, "scale": gb.TILE_WIDE,
-            "skinny": 0, "streamk": gb.TILE_WIDE}[case]
+            "skinny": 0, "streamk": gb.TILE_WIDE, "tile_split": gb.TILE_SINGLE}[case]
     path = gb.PATH_SKINNY if case == "skinny" else gb.PATH_LARGE
     alpha = 0.0 if case == "scale" else -2.0
     cs = Case(M, N, K, L, seed=20)
@@ -300,7 +301,8 @@ def test_graph_capture_replays_match_eager(case):
                                      B.data_ptr(), cs.ldB, cs.sB, 0, 0.5, C.data_ptr(), cs.ldC,
                                      cs.sC, D.data_ptr(), cs.ldD, cs.sD, 0, stream,
                                      dict(path=path, tile_kernel=tile,
-                                          stream_k=1 if case == "streamk" else 0))
+                                          stream_k=1 if case == "streamk" else 0,
+                                          split_k=3 if case == "tile_split" else 0))
     assert call(D_eager, torch.cuda.current_stream().cuda_stream) == gb.OK
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
