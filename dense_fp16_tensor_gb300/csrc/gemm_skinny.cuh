@@ -56,7 +56,8 @@ struct SkinnySmem {
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = MP <= 16 ? 32 : (MP <= 32 ? 64 : 128);
+  // two accumulators of MP fp32 columns, rounded up to a power of two
+  static constexpr uint32_t kTmemCols = MP <= 16 ? 32 : (MP <= 32 ? 64 : (MP <= 64 ? 128 : 256));
 };
 
 // Segments of CTA `cta`: consecutive pieces of [begin, end) that stay inside

@@ -40,7 +40,8 @@ namespace {
 using namespace gemm_tn_dev;
 
 constexpr int kMaxDevices = 64;
-constexpr int kSkinnyMaxM = 64;
+constexpr int kSkinnyMaxM = 128;   // skinny path for M <= 128
+constexpr int kNoallocMaxM = 64;   // the allocation-free entry point's limit
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per wait
 
 thread_local int t_last_launches = 0;
@@ -83,7 +84,14 @@ cudaError_t set_skinny_attr() {
                               SkinnySmem<STAGES, MP>::kDynamicBytes);
 }
 
-constexpr int kSkinnyStages = 8;
+// Ring depth of the skinny kernel: 8 stages up to MP = 64 (16 KiB of B plus
+// at most 8 KiB of A each); 6 above (up to 32 KiB each).
+constexpr int skinny_stages(int mp) { return mp <= 64 ? 8 : 6; }
+
+// MMA width for M rows of A: M rounded up to 16 up to 64, then 96 or 128.
+int skinny_mp(int64_t M) {
+  return M <= 64 ? static_cast<int>((M + 15) / 16 * 16) : (M <= 96 ? 96 : 128);
+}
 
 // Per-device set-up (under g_mu): capability check, SM count, kernel
 // attributes.  Returns a status.
@@ -128,10 +136,12 @@ int device_setup(int dev, DeviceState*& st) {
       e = cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_large2_kernel, &cfg);
       st->max_pairs = clusters;
     }
-    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 16>();
-    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 32>();
-    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 48>();
-    if (e == cudaSuccess) e = set_skinny_attr<kSkinnyStages, 64>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(16), 16>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(32), 32>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(48), 48>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(64), 64>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(96), 96>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(128), 128>();
     if (e != cudaSuccess) return GEMM_TN_ERR_CUDA;
     st->attrs_set = true;
   }
@@ -553,8 +563,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
 template <int MP>
 cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const SkinnyArgs& p, const EpiArgs& ep, cudaStream_t stream) {
-  gemm_tn_skinny_kernel<kSkinnyStages, MP>
-      <<<grid, kSkinnyThreads, SkinnySmem<kSkinnyStages, MP>::kDynamicBytes, stream>>>(tmA, tmB,
+  gemm_tn_skinny_kernel<skinny_stages(MP), MP>
+      <<<grid, kSkinnyThreads, SkinnySmem<skinny_stages(MP), MP>::kDynamicBytes, stream>>>(tmA, tmB,
                                                                                       p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -581,7 +591,9 @@ cudaError_t launch_skinny_kernels(int grid, const CUtensorMap& tmA, const CUtens
     case 16: return launch_skinny_mp<16>(grid, tmA, tmB, p, ep, stream);
     case 32: return launch_skinny_mp<32>(grid, tmA, tmB, p, ep, stream);
     case 48: return launch_skinny_mp<48>(grid, tmA, tmB, p, ep, stream);
-    default: return launch_skinny_mp<64>(grid, tmA, tmB, p, ep, stream);
+    case 64: return launch_skinny_mp<64>(grid, tmA, tmB, p, ep, stream);
+    case 96: return launch_skinny_mp<96>(grid, tmA, tmB, p, ep, stream);
+    default: return launch_skinny_mp<128>(grid, tmA, tmB, p, ep, stream);
   }
 }
 
@@ -594,7 +606,7 @@ int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& 
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.mp = static_cast<int>((M + 15) / 16 * 16);
+  p.mp = skinny_mp(M);
   p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
   p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
   p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
@@ -832,7 +844,7 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   t_last_kernels = "";
   int s = validate(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype);
   if (s != GEMM_TN_OK) return s;
-  if (M > kSkinnyMaxM || a_major != GEMM_TN_MAJOR_K || b_major != GEMM_TN_MAJOR_K ||
+  if (M > kNoallocMaxM || a_major != GEMM_TN_MAJOR_K || b_major != GEMM_TN_MAJOR_K ||
       accum_dtype != GEMM_TN_ACC_F32)
     return GEMM_TN_ERR_INVALID_ARG;
   if (M == 0 || N == 0 || K == 0) return GEMM_TN_OK;  // D = C: nothing to do
@@ -852,7 +864,7 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.mp = static_cast<int>((M + 15) / 16 * 16);
+  p.mp = skinny_mp(M);
   p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
   p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
   p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;

@@ -97,17 +97,20 @@ typedef enum {
   GEMM_TN_ERR_CUDA = 4,            /* a CUDA runtime / driver call failed */
   GEMM_TN_ERR_DEVICE_TIMEOUT = 5,  /* a bounded wait inside a kernel expired;
                                       that launch's D is not valid */
-  GEMM_TN_ERR_NO_MEMORY = 6        /* the skinny path's workspace could not be
+  GEMM_TN_ERR_NO_MEMORY = 6        /* a workspace (split-K or stream-K partial
+                                      sums, repacked operands) could not be
                                       allocated */
 } gemm_tn_status;
 
 typedef enum {
-  GEMM_TN_PATH_AUTO = 0,    /* skinny path for M <= 64 with K-major A and B,
-                               persistent tile path otherwise */
+  GEMM_TN_PATH_AUTO = 0,    /* skinny path for M <= 128 with K-major A and B
+                               and fp32 accumulation, persistent tile path
+                               otherwise */
   GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernels: 256x256 tiles on one
                                CTA or on a CTA pair, or 128xBN tiles */
   GEMM_TN_PATH_SKINNY = 2,  /* swapped-operand split-K kernel + reduction;
-                               needs M <= 64 and K-major A and B */
+                               needs M <= 128, K-major A and B and fp32
+                               accumulation */
   GEMM_TN_PATH_STRIDED_COPY = 3,   /* gemm_tn_strided_ex only: threads gather
                                       operands into shared memory; no
                                       workspace */
@@ -223,7 +226,7 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
  *   alignment    A, B, C, D 16-byte aligned, ld* multiples of 8
  *                (GEMM_TN_ERR_ALIGNMENT otherwise; gemm_tn_strided takes
  *                arbitrary strides for the unscaled, single-problem form).
- *   paths        one problem with M <= 64, K-major operands and fp32
+ *   paths        one problem with M <= 128, K-major operands and fp32
  *                accumulation takes the skinny split-K path; everything else
  *                runs the tile kernels with the batch folded into the tile
  *                list (tile t belongs to problem t / tiles-per-problem).

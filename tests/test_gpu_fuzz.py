@@ -58,7 +58,7 @@ def draw_case(rng):
     elif mode == "wide_sk":
         opts = dict(path=gb.PATH_LARGE, tile_kernel=3, stream_k=1)
     elif mode == "skinny":
-        if M <= 64 and am == 0 and bm == 0 and acc == 0 and L == 1:
+        if M <= 128 and am == 0 and bm == 0 and acc == 0 and L == 1:
             opts = dict(path=gb.PATH_SKINNY)
     shared = {x: L > 1 and rng.random() < 0.25 for x in "ABC"}
     return M, N, K, L, am, bm, acc, alpha, beta, opts, shared, str(mode)

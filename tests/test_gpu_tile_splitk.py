@@ -74,7 +74,8 @@ SPLIT = "gemm_tn_large_kernel<128>+gemm_tn_tile_reduce_kernel"
                                    (128, 128, 64 * 40), (100, 260, 2600)])
 def test_automatic_split_integers_bit_exact(shape):
     M, N, K = shape
-    got, d64, d16, k = run(M, N, K, 1, 1.0, 1.0, seed=1)
+    # the tile path (M <= 128 would otherwise take the skinny path)
+    got, d64, d16, k = run(M, N, K, 1, 1.0, 1.0, seed=1, opts=dict(path=gb.PATH_LARGE))
     assert k == SPLIT, k
     check(got, d64, d16, K, 0, True, f"split {shape}")
 
