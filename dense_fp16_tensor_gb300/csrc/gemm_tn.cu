@@ -667,7 +667,11 @@ bool options_ok(const gemm_tn_options& o) {
 
 int device_state(DeviceState*& st) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  // The current device of this host thread; cudaSetDevice makes its primary
+  // context current here too, which the driver calls below (tensor-map
+  // encoding) need on a thread that has not used CUDA yet.
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
+    return GEMM_TN_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
   return device_setup(dev, st);
 }
@@ -850,7 +854,11 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   if (M == 0 || N == 0 || K == 0) return GEMM_TN_OK;  // D = C: nothing to do
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  // The current device of this host thread; cudaSetDevice makes its primary
+  // context current here too, which the driver calls below (tensor-map
+  // encoding) need on a thread that has not used CUDA yet.
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
+    return GEMM_TN_ERR_CUDA;
   DeviceState* st = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1084,7 +1092,11 @@ extern "C" GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K, c
   if ((c0 < a1 && a0 < c1) || (c0 < b1 && b0 < c1)) return GEMM_TN_ERR_INVALID_ARG;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  // The current device of this host thread; cudaSetDevice makes its primary
+  // context current here too, which the driver calls below (tensor-map
+  // encoding) need on a thread that has not used CUDA yet.
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
+    return GEMM_TN_ERR_CUDA;
   DeviceState* st = nullptr;
   int s;
   {

@@ -374,3 +374,41 @@ def test_tensor_front_end_scaled_and_batched():
     _, ref16 = oracle.gemm_tn_general(M, N, K, 0.5, np_bits(A[0].cpu()), K, 0, np_bits(B1.cpu()),
                                       K, 0, 1.0, np_bits(C[1].cpu()), N)
     assert np.array_equal(np_bits(C0.cpu()), ref16[0])
+
+
+def test_concurrent_calls_from_host_threads():
+    """Four host threads, each with its own stream, call the scaled entry point
+    (tile path with K split, skinny path, 256x256 tiles) at the same time;
+    every result matches the oracle (workspaces are per call, the library's
+    per-thread state is thread-local)."""
+    import threading
+    dev = torch.device("cuda")
+    shapes = [(512, 512, 8192), (48, 2000, 3000), (600, 700, 2048), (300, 260, 5000)]
+    cases = [Case(M, N, K, 1, seed=60 + i) for i, (M, N, K) in enumerate(shapes)]
+    inputs = [(cs.A.to(dev), cs.B.to(dev), cs.C.to(dev), cs.D0.to(dev)) for cs in cases]
+    torch.cuda.synchronize()
+    errors, kernels = [], {}
+
+    def work(i):
+        try:
+            cs = cases[i]
+            A, B, C, D = inputs[i]
+            s = torch.cuda.Stream()
+            for _ in range(5):
+                st = gb.gemm_tn_batched_ex(cs.M, cs.N, cs.K, 1, -1.0, A.data_ptr(), cs.ldA, 0, 0,
+                                           B.data_ptr(), cs.ldB, 0, 0, 2.0, C.data_ptr(), cs.ldC,
+                                           0, D.data_ptr(), cs.ldD, 0, 0, s.cuda_stream, None)
+                assert st == gb.OK, gb.gemm_tn_status_string(st)
+            kernels[i] = gb.gemm_tn_last_kernels()
+            s.synchronize()
+        except Exception as e:  # reported below
+            errors.append((i, repr(e)))
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert "tile_reduce" in kernels[0] and "skinny" in kernels[1], kernels
+    for i, cs in enumerate(cases):
+        cs.verify(inputs[i][3].cpu(), -1.0, 2.0, 0, True, f"thread {i}")
