@@ -412,3 +412,35 @@ def test_concurrent_calls_from_host_threads():
     assert "tile_reduce" in kernels[0] and "skinny" in kernels[1], kernels
     for i, cs in enumerate(cases):
         cs.verify(inputs[i][3].cpu(), -1.0, 2.0, 0, True, f"thread {i}")
+
+
+def test_batch_strides_beyond_32_bits():
+    """Problem 1's A and D start more than 2^31 elements (4 GiB) after
+    problem 0's: the batch offsets go through 64-bit arithmetic in the tensor
+    maps, the epilogue and the checks."""
+    M, N, K, L = 256, 264, 128, 2
+    big = (1 << 31) + 64            # elements, a multiple of 8
+    dev = torch.device("cuda")
+    A = torch.zeros(big + M * K, dtype=torch.float16, device=dev)
+    Dbuf = torch.zeros(big + 64 + M * N, dtype=torch.float16, device=dev)
+    A0 = wl.draw((M * K,), "int1", 71)
+    A1 = wl.draw((M * K,), "int1", 72)
+    A[:M * K] = A0.to(dev)
+    A[big:big + M * K] = A1.to(dev)
+    B = wl.draw((N * K,), "int1", 73).to(dev)
+    C = wl.draw((M * N,), "int4", 74).to(dev)
+    sD = big + 64
+    for tile in (gb.TILE_SINGLE, gb.TILE_PAIR, gb.TILE_WIDE):
+        st = gb.gemm_tn_batched_ex(M, N, K, L, 2.0, A.data_ptr(), K, big, 0, B.data_ptr(), K, 0, 0,
+                                   -1.0, C.data_ptr(), N, 0, Dbuf.data_ptr(), N, sD, 0,
+                                   torch.cuda.current_stream().cuda_stream,
+                                   dict(path=gb.PATH_LARGE, tile_kernel=tile, sync_check=1))
+        assert st == gb.OK, gb.gemm_tn_status_string(st)
+        torch.cuda.synchronize()
+        for l, Al in enumerate((A0, A1)):
+            got = np_bits(Dbuf[l * sD:l * sD + M * N].cpu()).reshape(1, M, N)
+            d64, d16 = oracle.gemm_tn_general(M, N, K, 2.0, np_bits(Al), K, 0, np_bits(B.cpu()),
+                                              K, 0, -1.0, np_bits(C.cpu()), N)
+            check(got, d64, d16, K, 0, True, f"problem {l} tile {tile}")
+    del A, Dbuf
+    torch.cuda.empty_cache()
