@@ -15,8 +15,9 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
   cpu_baseline  the CPU oracle (fp64 triple loop) timed on a bounded sample
                 of the same workload on this host's cores
   clocks        SM clocks and throttle reasons sampled during the timed region
-  extra         other paths, each timed on its own: the skinny M=16 workload's
-                HBM bandwidth, 4096^3 with K+1 leading dimensions (strided
+  extra         other paths, each timed on its own: cuBLAS (torch.addmm) on
+                the headline's inputs beside gemm_tn_scaled (context only),
+                the skinny M=16 workload's HBM bandwidth, 4096^3 with K+1 leading dimensions (strided
                 route), stream-K against the unsplit kernel, the scaled and
                 batched entry point, and the 128-row kernel's K split on
                 few-tile shapes
@@ -458,6 +459,8 @@ def run_ours(args):
 
     extra = {}
     if not args.no_extra and w.name != "skinny":
+        if w.name == "large":
+            extra["cublas_same_inputs"] = bench_cublas(dev, stream, w, A, Bm)
         extra["skinny_m16"] = bench_skinny(dev, stream)
         extra["strided_4096"] = bench_strided(dev, stream)
         extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
@@ -501,6 +504,63 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def bench_cublas(dev, stream, w, A, Bm, steps=400, rounds=2):
+    """Context, not the product path: the headline problem with the same A and
+    B, D = A.B^T + C with a separate D and a uniform [-1,1] C, through
+    gemm_tn_scaled and through cuBLAS (torch.addmm), timed in alternating
+    blocks of back-to-back calls.  Both sit at the board's power limit on
+    these operands, so the ratio compares energy per FLOP as much as kernels."""
+    import torch
+
+    from dense_fp16_tensor_gb300 import binding as gb
+    from dense_fp16_tensor_gb300 import workloads as wl
+    M, N, K = w.M, w.N, w.K
+    C = wl.draw((M * N,), "u11", 7301).to(dev).view(M, N)
+    D = torch.empty_like(C)
+    A2, B2 = A.view(M, K), Bm.view(N, K)
+    sp = stream.cuda_stream
+
+    def ours():
+        st = gb.gemm_tn_scaled(M, N, K, 1.0, A.data_ptr(), K, 0, Bm.data_ptr(), K, 0, 1.0,
+                               C.data_ptr(), N, D.data_ptr(), N, gb.ACC_F32, sp)
+        if st != gb.OK:
+            raise gb.GemmTnError(st)
+
+    def cublas():
+        torch.addmm(C, A2, B2.t(), out=D)
+
+    def timed(fn):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            ours()
+            cublas()
+    torch.cuda.synchronize()
+    t = {"ours": [], "cublas": []}
+    for _ in range(rounds):
+        t["ours"].append(timed(ours))
+        t["cublas"].append(timed(cublas))
+    fl = 2.0 * M * N * K
+    out = {"workload": f"M=N=K={M}, D = A.B^T + C (separate D), fp32 accumulate, "
+                       f"{rounds} alternating blocks of {steps} calls",
+           "cublas_entry": "torch.addmm (cuBLAS)"}
+    for k, v in t.items():
+        ms = statistics.median(v)
+        out[k] = {"ms_per_call": ms, "TFLOP_per_s": fl / (ms * 1e-3) / 1e12}
+    out["ratio_ours_over_cublas"] = out["ours"]["TFLOP_per_s"] / out["cublas"]["TFLOP_per_s"]
+    del C, D
+    return out
 
 
 def bench_skinny(dev, stream, steps=200):

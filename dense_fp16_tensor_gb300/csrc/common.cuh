@@ -114,18 +114,25 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   tn = r / rows;
 }
 
-// Contiguous split of `units` work units over `grid` CTAs: CTA c owns
-// [unit_begin(c), unit_begin(c+1)).
-__device__ __forceinline__ int64_t unit_begin(int64_t units, int cta, int grid) {
-  return units * cta / grid;
+// Quotient of two non-negative 64-bit values, in 32-bit arithmetic when both
+// fit (a 64-bit division is a long software routine; the unit indices of a
+// real problem are far below 2^31).
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+  if ((static_cast<uint64_t>(a) | static_cast<uint64_t>(b)) >> 31 == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
 }
 
-// CTA whose unit range holds unit u (ranges from unit_begin are monotone).
-__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t units, int grid) {
-  int c = static_cast<int>(u * grid / units);
-  while (c + 1 < grid && unit_begin(units, c + 1, grid) <= u) ++c;
-  while (c > 0 && unit_begin(units, c, grid) > u) --c;
-  return c;
+// Contiguous split of `units` work units into ranges of `per` units: CTA c
+// owns [c*per, min((c+1)*per, units)); the last non-empty range may be
+// shorter, and the grid has ceil(units/per) CTAs.
+__device__ __forceinline__ int64_t unit_begin(int64_t units, int cta, int64_t per) {
+  return min(static_cast<int64_t>(cta) * per, units);
+}
+
+// CTA whose unit range holds unit u.
+__device__ __forceinline__ int cta_of_unit(int64_t u, int64_t per) {
+  return static_cast<int>(div_nonneg(u, per));
 }
 
 }  // namespace gemm_tn_dev

@@ -1,4 +1,4 @@
-// gemm_skinny.cuh -- HBM-streaming path for skinny M (M <= 64), sm_103a.
+// gemm_skinny.cuh -- HBM-streaming path for skinny M (M <= 128), sm_103a.
 //
 // With M this small the work is one pass over B (N x K fp16), so the kernel
 // is bound by HBM, not by the tensor cores.  The roles of the operands are
@@ -12,8 +12,8 @@
 // symmetric in the roles of A and B up to a transpose).
 //
 // N/128 output tiles are far fewer than the SMs, so the K loop is split.
-// The (tile, K-block) units are laid out tile-major and cut into gridDim.x
-// equal contiguous ranges, one per CTA (persistent, one CTA per SM).  A range
+// The (tile, K-block) units are laid out tile-major and cut into contiguous
+// ranges of equal length, one per CTA (persistent, one CTA per SM).  A range
 // covers whole or partial K loops of one or more tiles; each maximal piece
 // inside one tile is a segment whose fp32 partial sum (128 x MP) goes to the
 // workspace.  A second kernel adds, for every output, the partials of the
@@ -39,9 +39,10 @@ struct SkinnyArgs {
   int mp;            // M rounded up to 16 (the MMA's N)
   int tiles, k_blocks;
   int64_t units;     // tiles * k_blocks
+  int64_t per;       // units per CTA: CTA c owns [c*per, min((c+1)*per, units))
   int max_segs;      // segments one CTA can produce
-  int grid;          // CTAs of the split kernel
-  float* ws;         // [gridDim.x * max_segs][128][mp] fp32 partials
+  int grid;          // CTAs of the split kernel (ceil(units / per))
+  float* ws;         // [grid * max_segs][mp/4][128] float4 partials (see skinny_partial)
   uint64_t timeout_ns;
   int test_stall;
 };
@@ -60,18 +61,27 @@ struct SkinnySmem {
   static constexpr uint32_t kTmemCols = MP <= 16 ? 32 : (MP <= 32 ? 64 : (MP <= 64 ? 128 : 256));
 };
 
+// Partial sums of one segment slot: 128 rows (n) x MP columns (m) of fp32,
+// stored column-quad-major -- float4 q of row r at (slot * MP/4 + q) * 128 + r
+// -- so that 32 consecutive rows' quad is 512 contiguous bytes: the epilogue
+// warps store and the reduction reads whole lines.
+template <int MP>
+__device__ __forceinline__ int64_t skinny_partial(int64_t slot, int q, int row) {
+  return (slot * (MP / 4) + q) * kSkinnyBN + row;
+}
+
 // Segments of CTA `cta`: consecutive pieces of [begin, end) that stay inside
 // one tile.  seg j covers [max(begin, (first_tile + j) * kb), min(end, ...)).
 struct SegIter {
   int64_t begin, end;
   int kb;
-  __device__ SegIter(int64_t units, int cta, int grid, int k_blocks)
-      : begin(unit_begin(units, cta, grid)), end(unit_begin(units, cta + 1, grid)),
+  __device__ SegIter(int64_t units, int cta, int64_t per, int k_blocks)
+      : begin(unit_begin(units, cta, per)), end(unit_begin(units, cta + 1, per)),
         kb(k_blocks) {}
-  __device__ int first_tile() const { return static_cast<int>(begin / kb); }
+  __device__ int first_tile() const { return static_cast<int>(div_nonneg(begin, kb)); }
   __device__ int count() const {
     if (end <= begin) return 0;
-    return static_cast<int>((end - 1) / kb) - first_tile() + 1;
+    return static_cast<int>(div_nonneg(end - 1, kb)) - first_tile() + 1;
   }
   __device__ void seg(int j, int& tile, int& kb0, int& kb1) const {
     tile = first_tile() + j;
@@ -103,7 +113,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const SegIter segs(p.units, blockIdx.x, gridDim.x, p.k_blocks);
+  const SegIter segs(p.units, blockIdx.x, p.per, p.k_blocks);
   // The reduction kernel may be scheduled now; it waits for this grid's
   // completion before it reads anything.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -134,6 +144,10 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent: the kernel before this one in the
+  // stream (which may write A, B or C, or read the workspace) must be
+  // complete before any global memory is touched.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -230,18 +244,18 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
         break;
       tc_fence_after();
       const int64_t slot = static_cast<int64_t>(blockIdx.x) * p.max_segs + j;
-      float* dst = p.ws + (slot * kSkinnyBN + row) * MP;
+      float4* dst = reinterpret_cast<float4*>(p.ws) + skinny_partial<MP>(slot, 0, row);
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * MP;
 #pragma unroll
       for (int c = 0; c < MP / 16; ++c) {
         uint32_t r[16];
         tmem_ld_32x32b_x16(t_row + c * 16, r);
         tmem_wait_ld();
-        float4* d4 = reinterpret_cast<float4*>(dst + c * 16);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          d4[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          dst[(4 * c + v) * kSkinnyBN] =
+              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
       }
       tc_fence_before();
       __syncwarp();
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
 // with alpha = beta = 1 the sum plus C.  Block (tile, y) has 512 threads;
 // thread (g, r) owns column n = 128*tile + r and rows 4g..4g+3 with
 // g = 4y + threadIdx.x/128, reads one 16-byte vector of partials per
-// contributing CTA, and adds C once.  The kernel is
+// contributing CTA (a warp reads 512 contiguous bytes), and adds C once.  The kernel is
 // launched as a programmatic dependent of the split-K kernel: its blocks
 // become resident while the split-K kernel runs and wait for its completion
 // (and the visibility of its partial sums) in griddepcontrol.wait.
@@ -274,23 +288,26 @@ constexpr int kReduceThreads = 4 * kSkinnyBN;  // four 4-row groups per block
 template <int MP>
 __global__ void __launch_bounds__(kReduceThreads)
     gemm_tn_splitk_reduce_kernel(const SkinnyArgs p, const EpiArgs e) {
+  // The next call's kernels may become resident now (they wait for this
+  // grid's completion before touching memory).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tile = static_cast<int>(blockIdx.x);
   const int r = static_cast<int>(threadIdx.x) % kSkinnyBN;
   const int g = 4 * static_cast<int>(blockIdx.y) + static_cast<int>(threadIdx.x) / kSkinnyBN;
   const int n = tile * kSkinnyBN + r;
   if (n >= p.N || 4 * g >= p.M) return;
-  const int grid = p.grid;
   const int64_t u0 = static_cast<int64_t>(tile) * p.k_blocks;
-  const int c_first = cta_of_unit(u0, p.units, grid);
-  const int c_last = cta_of_unit(u0 + p.k_blocks - 1, p.units, grid);
+  const int c_first = cta_of_unit(u0, p.per);
+  const int c_last = cta_of_unit(u0 + p.k_blocks - 1, p.per);
+  const float4* ws = reinterpret_cast<const float4*>(p.ws);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // every CTA from c_first to c_last has a non-empty range inside this tile
   for (int c = c_first; c <= c_last; ++c) {
-    const int64_t b = unit_begin(p.units, c, grid);
-    if (unit_begin(p.units, c + 1, grid) <= b) continue;  // empty range
-    const int j = tile - static_cast<int>(b / p.k_blocks);
+    const int64_t b = static_cast<int64_t>(c) * p.per;
+    const int j = tile - static_cast<int>(div_nonneg(b, p.k_blocks));
     const int64_t slot = static_cast<int64_t>(c) * p.max_segs + j;
-    const float4 x = *reinterpret_cast<const float4*>(p.ws + (slot * kSkinnyBN + r) * MP + 4 * g);
+    const float4 x = ws[skinny_partial<MP>(slot, g, r)];
     acc.x += x.x;
     acc.y += x.y;
     acc.z += x.z;

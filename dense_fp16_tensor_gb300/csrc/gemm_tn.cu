@@ -563,22 +563,27 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
 template <int MP>
 cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const SkinnyArgs& p, const EpiArgs& ep, cudaStream_t stream) {
-  gemm_tn_skinny_kernel<skinny_stages(MP), MP>
-      <<<grid, kSkinnyThreads, SkinnySmem<skinny_stages(MP), MP>::kDynamicBytes, stream>>>(tmA, tmB,
-                                                                                      p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // programmatic dependent launch: resident early, waits in griddepcontrol.wait
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles), MP / 16, 1);
-  cfg.blockDim = dim3(kReduceThreads, 1, 1);
-  cfg.stream = stream;
+  // Both kernels are programmatic dependent launches: each becomes resident
+  // while the kernel before it in the stream finishes, sets up its barriers
+  // and tensor memory, and waits in griddepcontrol.wait before it touches
+  // global memory.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kSkinnyThreads, 1, 1);
+  cfg.dynamicSmemBytes = SkinnySmem<skinny_stages(MP), MP>::kDynamicBytes;
+  cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<skinny_stages(MP), MP>, tmA, tmB, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles), MP / 16, 1);
+  cfg.blockDim = dim3(kReduceThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, gemm_tn_splitk_reduce_kernel<MP>, p, ep);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -610,11 +615,13 @@ int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& 
   p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
   p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
   p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
-  int grid = o.split_k > 0 ? o.split_k : st.num_sms;
-  grid = static_cast<int>(std::min<int64_t>(grid, p.units));
+  // Ranges of ceil(units / CTAs) units; a range spans at most per / k_blocks
+  // + 2 tiles.  Recomputing the grid from per drops CTAs left without work.
+  const int64_t want = std::min<int64_t>(o.split_k > 0 ? o.split_k : st.num_sms, p.units);
+  const int64_t per = (p.units + want - 1) / want;
+  const int grid = static_cast<int>((p.units + per - 1) / per);
+  p.per = per;
   p.grid = grid;
-  // A range of ceil(units/grid) units spans at most that many / k_blocks + 2 tiles.
-  const int64_t per = (p.units + grid - 1) / grid;
   p.max_segs = static_cast<int>(per / p.k_blocks + 2);
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
@@ -876,9 +883,11 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
   p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
   p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
-  const int grid = static_cast<int>(std::min<int64_t>(st->num_sms, p.units));
+  const int64_t want = std::min<int64_t>(st->num_sms, p.units);
+  const int64_t per = (p.units + want - 1) / want;
+  const int grid = static_cast<int>((p.units + per - 1) / per);
+  p.per = per;
   p.grid = grid;
-  const int64_t per = (p.units + grid - 1) / grid;
   p.max_segs = static_cast<int>(per / p.k_blocks + 2);
   p.timeout_ns = kDefaultTimeoutNs;
   const uint64_t need =

@@ -123,8 +123,9 @@ typedef enum {
  * every zero field means "the library's default". */
 typedef struct {
   int path;             /* gemm_tn_path */
-  int split_k;          /* skinny path: number of CTAs sharing the K loop of
-                           the output tiles (0 = one per SM).  Large path
+  int split_k;          /* skinny path: at most this many CTAs share the K
+                           loops of the output tiles, in ranges of equal
+                           length (0 = one per SM).  Large path
                            with tile_kernel 1: K splits per 128-row tile,
                            fp32 accumulation only (0 = none; with
                            tile_kernel 0 the library splits by itself when
