@@ -1,4 +1,4 @@
-// gemm_skinny.cuh -- HBM-streaming path for skinny M (M <= 128), sm_103a.
+// gemm_skinny.cuh -- HBM-streaming path for skinny M (M <= 256), sm_103a.
 //
 // With M this small the work is one pass over B (N x K fp16), so the kernel
 // is bound by HBM, not by the tensor cores.  The roles of the operands are
@@ -58,7 +58,8 @@ struct SkinnySmem {
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
   // two accumulators of MP fp32 columns, rounded up to a power of two
-  static constexpr uint32_t kTmemCols = MP <= 16 ? 32 : (MP <= 32 ? 64 : (MP <= 64 ? 128 : 256));
+  static constexpr uint32_t kTmemCols =
+      MP <= 16 ? 32 : (MP <= 32 ? 64 : (MP <= 64 ? 128 : (MP <= 128 ? 256 : 512)));
 };
 
 // Partial sums of one segment slot: 128 rows (n) x MP columns (m) of fp32,

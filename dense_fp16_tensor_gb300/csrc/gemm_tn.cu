@@ -40,7 +40,13 @@ namespace {
 using namespace gemm_tn_dev;
 
 constexpr int kMaxDevices = 64;
-constexpr int kSkinnyMaxM = 128;   // skinny path for M <= 128
+constexpr int kSkinnyMaxM = 256;  // the skinny kernel serves M <= 256
+// The automatic choice takes the skinny path for M <= 192 and, for M up to
+// 256, while N is at most this: 56 CTA-pair tiles of 256 columns, under 3/4
+// of the pairs a GB300 runs at once.  Wider N keeps the pair kernel busy
+// enough to stream B faster than the skinny kernel's 4-stage ring at MMA
+// width 256.
+constexpr int64_t kSkinnyWideMaxN = 56 * 256;
 constexpr int kNoallocMaxM = 64;   // the allocation-free entry point's limit
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per wait
 
@@ -85,12 +91,17 @@ cudaError_t set_skinny_attr() {
 }
 
 // Ring depth of the skinny kernel: 8 stages up to MP = 64 (16 KiB of B plus
-// at most 8 KiB of A each); 6 above (up to 32 KiB each).
-constexpr int skinny_stages(int mp) { return mp <= 64 ? 8 : 6; }
+// at most 8 KiB of A each), 6 up to 128 (32 KiB), 5 at 192 (40 KiB) and 4
+// at 256 (48 KiB).
+constexpr int skinny_stages(int mp) {
+  return mp <= 64 ? 8 : (mp <= 128 ? 6 : (mp <= 192 ? 5 : 4));
+}
 
-// MMA width for M rows of A: M rounded up to 16 up to 64, then 96 or 128.
+// MMA width for M rows of A: M rounded up to 16 up to 64, then 96, 128, 192
+// or 256.
 int skinny_mp(int64_t M) {
-  return M <= 64 ? static_cast<int>((M + 15) / 16 * 16) : (M <= 96 ? 96 : 128);
+  if (M <= 64) return static_cast<int>((M + 15) / 16 * 16);
+  return M <= 96 ? 96 : (M <= 128 ? 128 : (M <= 192 ? 192 : 256));
 }
 
 // Per-device set-up (under g_mu): capability check, SM count, kernel
@@ -142,6 +153,8 @@ int device_setup(int dev, DeviceState*& st) {
     if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(64), 64>();
     if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(96), 96>();
     if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(128), 128>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(192), 192>();
+    if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(256), 256>();
     if (e != cudaSuccess) return GEMM_TN_ERR_CUDA;
     st->attrs_set = true;
   }
@@ -363,12 +376,14 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_
   return validate(in_place_problem(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum));
 }
 
-int plan(int64_t M, int a_major, int b_major, int accum, int requested, int64_t L = 1) {
+int plan(int64_t M, int64_t N, int a_major, int b_major, int accum, int requested,
+         int64_t L = 1) {
   const bool skinny_ok = M <= kSkinnyMaxM && a_major == GEMM_TN_MAJOR_K &&
                          b_major == GEMM_TN_MAJOR_K && accum == GEMM_TN_ACC_F32 && L <= 1;
   if (requested == GEMM_TN_PATH_SKINNY) return skinny_ok ? GEMM_TN_PATH_SKINNY : -1;
   if (requested == GEMM_TN_PATH_LARGE) return GEMM_TN_PATH_LARGE;
-  return skinny_ok ? GEMM_TN_PATH_SKINNY : GEMM_TN_PATH_LARGE;
+  const bool auto_ok = M <= 192 || N <= kSkinnyWideMaxN;
+  return skinny_ok && auto_ok ? GEMM_TN_PATH_SKINNY : GEMM_TN_PATH_LARGE;
 }
 
 int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
@@ -598,7 +613,9 @@ cudaError_t launch_skinny_kernels(int grid, const CUtensorMap& tmA, const CUtens
     case 48: return launch_skinny_mp<48>(grid, tmA, tmB, p, ep, stream);
     case 64: return launch_skinny_mp<64>(grid, tmA, tmB, p, ep, stream);
     case 96: return launch_skinny_mp<96>(grid, tmA, tmB, p, ep, stream);
-    default: return launch_skinny_mp<128>(grid, tmA, tmB, p, ep, stream);
+    case 128: return launch_skinny_mp<128>(grid, tmA, tmB, p, ep, stream);
+    case 192: return launch_skinny_mp<192>(grid, tmA, tmB, p, ep, stream);
+    default: return launch_skinny_mp<256>(grid, tmA, tmB, p, ep, stream);
   }
 }
 
@@ -697,7 +714,7 @@ int run_problem(const Problem& q, void* stream, const gemm_tn_options* opts) {
   // D = beta * C: nothing to do in place with beta == 1
   if (!q.use_ab() && q.beta == 1.f && q.in_place()) return GEMM_TN_OK;
 
-  const int path = plan(q.M, q.a_major, q.b_major, q.accum, o.path, q.L);
+  const int path = plan(q.M, q.N, q.a_major, q.b_major, q.accum, o.path, q.L);
   if (path < 0) return GEMM_TN_ERR_INVALID_ARG;
   DeviceState* st = nullptr;
   s = device_state(st);
@@ -790,9 +807,8 @@ GEMM_TN_API int gemm_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 }
 
 GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major, int b_major) {
-  (void)N;
   (void)K;
-  return plan(M, a_major, b_major, GEMM_TN_ACC_F32, GEMM_TN_PATH_AUTO);
+  return plan(M, N, a_major, b_major, GEMM_TN_ACC_F32, GEMM_TN_PATH_AUTO);
 }
 
 GEMM_TN_API int gemm_tn_last_launch_count(void) { return t_last_launches; }
@@ -1037,7 +1053,7 @@ int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if (e == cudaSuccess) {
     gemm_tn_options o;
     std::memset(&o, 0, sizeof o);
-    const int path = plan(M, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
+    const int path = plan(M, N, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
     const Problem q =
         in_place_problem(M, N, K, Ause, ldA, a_major, Buse, ldB, b_major, Cuse, ldC, accum);
     s = path == GEMM_TN_PATH_SKINNY ? launch_skinny(q, stream, o, st)

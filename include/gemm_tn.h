@@ -103,13 +103,14 @@ typedef enum {
 } gemm_tn_status;
 
 typedef enum {
-  GEMM_TN_PATH_AUTO = 0,    /* skinny path for M <= 128 with K-major A and B
-                               and fp32 accumulation, persistent tile path
+  GEMM_TN_PATH_AUTO = 0,    /* skinny path with K-major A and B and fp32
+                               accumulation for M <= 192, and for M <= 256
+                               when N <= 14336; persistent tile path
                                otherwise */
   GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernels: 256x256 tiles on one
                                CTA or on a CTA pair, or 128xBN tiles */
   GEMM_TN_PATH_SKINNY = 2,  /* swapped-operand split-K kernel + reduction;
-                               needs M <= 128, K-major A and B and fp32
+                               needs M <= 256, K-major A and B and fp32
                                accumulation */
   GEMM_TN_PATH_STRIDED_COPY = 3,   /* gemm_tn_strided_ex only: threads gather
                                       operands into shared memory; no

@@ -47,7 +47,11 @@ def test_plan_path(lib):
     assert gb.gemm_tn_plan_path(16, 16384, 16384, 0, 0) == gb.PATH_SKINNY
     assert gb.gemm_tn_plan_path(64, 100, 100, 0, 0) == gb.PATH_SKINNY
     assert gb.gemm_tn_plan_path(128, 100, 100, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(129, 100, 100, 0, 0) == gb.PATH_LARGE
+    assert gb.gemm_tn_plan_path(192, 65536, 100, 0, 0) == gb.PATH_SKINNY
+    assert gb.gemm_tn_plan_path(193, 14336, 100, 0, 0) == gb.PATH_SKINNY
+    assert gb.gemm_tn_plan_path(256, 14336, 100, 0, 0) == gb.PATH_SKINNY
+    assert gb.gemm_tn_plan_path(193, 14337, 100, 0, 0) == gb.PATH_LARGE
+    assert gb.gemm_tn_plan_path(257, 100, 100, 0, 0) == gb.PATH_LARGE
     assert gb.gemm_tn_plan_path(16, 100, 100, 1, 0) == gb.PATH_LARGE
     assert gb.gemm_tn_plan_path(8192, 8192, 8192, 0, 0) == gb.PATH_LARGE
 
@@ -79,7 +83,7 @@ def call(M=64, N=64, K=64, A=P, ldA=64, am=0, B=P + (1 << 20), ldB=64, bm=0,
     (dict(ldC=68), gb.ERR_ALIGNMENT),
     (dict(opts=gb.make_options(path=7)), gb.ERR_INVALID_ARG),
     (dict(opts=gb.make_options(tile_n=96)), gb.ERR_INVALID_ARG),
-    (dict(M=136, opts=gb.make_options(path=2)), gb.ERR_INVALID_ARG),  # skinny needs M <= 128
+    (dict(M=264, opts=gb.make_options(path=2)), gb.ERR_INVALID_ARG),  # skinny needs M <= 256
 ])
 def test_argument_errors_return_before_any_device_work(lib, kw, status):
     assert call(**kw) == status

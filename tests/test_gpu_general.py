@@ -158,7 +158,7 @@ def test_batched_small_m_runs_the_tile_kernel():
 
 
 def test_skinny_path_scaled_separate_d():
-    for M in (16, 40, 64):
+    for M in (16, 40, 64, 160, 256):
         cs = Case(M, 1000, 3000, 1, seed=7 + M)
         D, k = cs.run(0.5, -2.0, 0)
         assert k == "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel", k

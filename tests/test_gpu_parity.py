@@ -156,7 +156,7 @@ def test_large_path_real_values_every_tile_kernel(tile_n, tile_kernel):
         check(result_view(D_st, M, N), d64, d16, K, accum, False, f"tile_n={tile_n}")
 
 
-@pytest.mark.parametrize("M", [1, 16, 17, 40, 64, 65, 96, 100, 128])
+@pytest.mark.parametrize("M", [1, 16, 17, 40, 64, 65, 96, 100, 128, 129, 192, 200, 256])
 def test_skinny_path_shapes_and_splits(M):
     """Skinny path: every M bucket, ragged N and K, several split counts;
     integer values so that every split must give the same bits (C once)."""

@@ -74,7 +74,7 @@ SPLIT = "gemm_tn_large_kernel<128>+gemm_tn_tile_reduce_kernel"
                                    (128, 128, 64 * 40), (100, 260, 2600)])
 def test_automatic_split_integers_bit_exact(shape):
     M, N, K = shape
-    # the tile path (M <= 128 would otherwise take the skinny path)
+    # the tile path (M <= 256 would otherwise take the skinny path)
     got, d64, d16, k = run(M, N, K, 1, 1.0, 1.0, seed=1, opts=dict(path=gb.PATH_LARGE))
     assert k == SPLIT, k
     check(got, d64, d16, K, 0, True, f"split {shape}")
@@ -88,8 +88,10 @@ def test_split_with_scalars_batches_and_majors(am, bm):
 
 
 def test_split_beta_zero_and_real_values_deterministic():
-    a = run(256, 384, 6000, 1, 0.75, 0.0, dist="u11", cdist="u11", seed=3)
-    b = run(256, 384, 6000, 1, 0.75, 0.0, dist="u11", cdist="u11", seed=3)
+    # the tile path (M <= 256 with this N would otherwise take the skinny path)
+    o = dict(path=gb.PATH_LARGE)
+    a = run(256, 384, 6000, 1, 0.75, 0.0, dist="u11", cdist="u11", seed=3, opts=o)
+    b = run(256, 384, 6000, 1, 0.75, 0.0, dist="u11", cdist="u11", seed=3, opts=o)
     assert a[3] == SPLIT
     assert np.array_equal(a[0], b[0])  # fixed summation order
     check(a[0], a[1], a[2], 6000, 0, False, "split real")
