@@ -7,10 +7,15 @@
 // loop"), with the data movement redone for GB300:
 //
 //   warp 0      TMA producer: per K block of 64, one A box (128 x 64) and one
-//               B box (BN x 64) into a 128B-swizzled stage of a kStages ring,
+//               B box (BN x 64) into a 128B-swizzled stage of a 4-stage ring,
 //               completion counted on the stage's `full` mbarrier.  Out-of-
 //               range rows / columns / K are zero-filled by the TMA unit, so
 //               ragged M, N and K need no special case in the main loop.
+//               With KO (BN = 128, K-major A and B, K a multiple of 64) a
+//               stage covers 128 of K and each operand arrives as one
+//               {64, 128, 2} box over a map whose third dimension steps K by
+//               64: three stages of two 32 KiB boxes, which a GB300 SM takes
+//               in about twice as fast as four 16 KiB boxes.
 //   warp 1      allocates 2*BN TMEM columns (two accumulators) and one lane
 //               issues tcgen05.mma (M=128, N=BN, K=16, four per stage); each
 //               stage is released with tcgen05.commit -> `empty`, each tile
@@ -38,8 +43,7 @@
 namespace gemm_tn_dev {
 
 constexpr int kLargeBM = 128;
-constexpr int kLargeBK = 64;
-constexpr int kLargeStages = 4;
+constexpr int kLargeBK = 64;   // K per stage (and per p.k_blocks unit) without KO
 constexpr int kLargeThreads = 192;
 
 struct LargeArgs {
@@ -74,16 +78,19 @@ struct LargeArgs {
   float* ks_ws;
 };
 
-template <int BN>
+template <int BN, bool KO = false>
 struct LargeSmem {
-  static constexpr uint32_t kABytes = kLargeBM * kLargeBK * 2;  // 16 KiB
-  static constexpr uint32_t kBBytes = BN * kLargeBK * 2;        // 16 / 32 KiB
+  static_assert(!KO || BN == 128, "K-chunk boxes only with 128 x 128 tiles");
+  static constexpr int kBK = KO ? 128 : kLargeBK;    // K per stage
+  static constexpr int kStages = KO ? 3 : 4;
+  static constexpr uint32_t kABytes = kLargeBM * kBK * 2;  // 16 / 32 KiB
+  static constexpr uint32_t kBBytes = BN * kBK * 2;        // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   // epilogue staging: 4 warps x 32 rows x 64 fp16 (1024-aligned)
-  static constexpr uint32_t kStagingOffset = kLargeStages * kStageBytes;
+  static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
   static constexpr uint32_t kBarOffset = kStagingOffset + 4 * 32 * 128;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
-  static constexpr uint32_t kNumBars = 2 * kLargeStages + 5;
+  static constexpr uint32_t kNumBars = 2 * kStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;  // + alignment slack
@@ -213,26 +220,29 @@ __device__ __forceinline__ void epi_store_chunk(const LargeArgs& p, const CUtens
   }
 }
 
-template <int BN>
+// KO: stages of 128 of K loaded as K-chunk boxes (see the header); p.k_blocks
+// then counts blocks of 128.
+template <int BN, bool KO = false>
 __global__ void __launch_bounds__(kLargeThreads, 1)
     gemm_tn_large_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmD, const LargeArgs p) {
-  using L = LargeSmem<BN>;
+  using L = LargeSmem<BN, KO>;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                                  // stage s at s * kABytes
-  uint8_t* sB = smem + kLargeStages * L::kABytes;      // stage s at s * kBBytes
+  uint8_t* sA = smem;                             // stage s at s * kABytes
+  uint8_t* sB = smem + kStages * L::kABytes;      // stage s at s * kBBytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOffset + 4);
 
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + kLargeStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kLargeStages);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kLargeStages + 2);
-  const uint32_t drain = smem_u32(bars + 2 * kLargeStages + 4);
+  const uint32_t empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kLargeStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -293,25 +303,31 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
             const uint32_t a_dst = smem_u32(sA + stage * L::kABytes);
             const uint32_t b_dst = smem_u32(sB + stage * L::kBBytes);
             mbar_arrive_expect_tx(fb, L::kStageBytes);
-            const int k0 = kb * kLargeBK;
-            if (!p.a_mn) {
-              tma_load_3d(a_dst, &tmA, fb, k0, tm * kLargeBM, za);
+            if constexpr (KO) {
+              // K chunks 2kb and 2kb+1 (the second zero-filled past K)
+              tma_load_4d(a_dst, &tmA, fb, 0, tm * kLargeBM, 2 * kb, za);
+              tma_load_4d(b_dst, &tmB, fb, 0, tn * BN, 2 * kb, zb);
             } else {
+              const int k0 = kb * kLargeBK;
+              if (!p.a_mn) {
+                tma_load_3d(a_dst, &tmA, fb, k0, tm * kLargeBM, za);
+              } else {
 #pragma unroll
-              for (int i = 0; i < kLargeBM / 64; ++i)
-                tma_load_3d(a_dst + i * 8192, &tmA, fb, tm * kLargeBM + 64 * i, k0, za);
-            }
-            if (!p.b_mn) {
-              tma_load_3d(b_dst, &tmB, fb, k0, tn * BN, zb);
-            } else {
+                for (int i = 0; i < kLargeBM / 64; ++i)
+                  tma_load_3d(a_dst + i * 8192, &tmA, fb, tm * kLargeBM + 64 * i, k0, za);
+              }
+              if (!p.b_mn) {
+                tma_load_3d(b_dst, &tmB, fb, k0, tn * BN, zb);
+              } else {
 #pragma unroll
-              for (int i = 0; i < BN / 64; ++i)
-                tma_load_3d(b_dst + i * 8192, &tmB, fb, tn * BN + 64 * i, k0, zb);
+                for (int i = 0; i < BN / 64; ++i)
+                  tma_load_3d(b_dst + i * 8192, &tmB, fb, tn * BN + 64 * i, k0, zb);
+              }
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
-          if (++stage == kLargeStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -319,7 +335,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       }
       if (!ok || *abort_flag) {
         // Let every copy this thread issued land before the CTA can exit.
-        for (int s = 0; s < kLargeStages; ++s)
+        for (int s = 0; s < kStages; ++s)
           if (issued_mask >> s & 1u)
             wait_bounded(full0 + 8 * s, issued_parity >> s & 1u, abort_flag, p.timeout_ns,
                          timeout_code(kRoleProducer, 0x100 + s), false);
@@ -352,15 +368,22 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
           const uint32_t a_base = smem_u32(sA + stage * L::kABytes);
           const uint32_t b_base = smem_u32(sB + stage * L::kBBytes);
 #pragma unroll
-          for (int k = 0; k < kLargeBK / 16; ++k) {
-            const uint64_t ad = p.a_mn ? make_sw128_desc(a_base + k * 2048, 8192, 1024)
-                                       : make_sw128_desc(a_base + k * 32, 16, 1024);
-            const uint64_t bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
-                                       : make_sw128_desc(b_base + k * 32, 16, 1024);
+          for (int k = 0; k < L::kBK / 16; ++k) {
+            uint64_t ad, bd;
+            if constexpr (KO) {
+              // K chunk k/4 of each operand is a 128-row SW128 block
+              ad = make_sw128_desc(a_base + (k >> 2) * (kLargeBM * 128) + (k & 3) * 32, 16, 1024);
+              bd = make_sw128_desc(b_base + (k >> 2) * (BN * 128) + (k & 3) * 32, 16, 1024);
+            } else {
+              ad = p.a_mn ? make_sw128_desc(a_base + k * 2048, 8192, 1024)
+                          : make_sw128_desc(a_base + k * 32, 16, 1024);
+              bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
+                          : make_sw128_desc(b_base + k * 32, 16, 1024);
+            }
             mma_f16(d_tmem, ad, bd, idesc, (kb != kb0) || (k != 0));
           }
           mma_commit(empty0 + 8 * stage);  // stage free once these MMAs have read it
-          if (++stage == kLargeStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }

@@ -4,9 +4,13 @@
 // SMs (a cluster of 2) compute one 256 x 256 output tile together:
 //
 //   * CTA r of the pair TMA-loads rows [128r, 128r+128) of the tile's A block
-//     and rows [128r, 128r+128) of its B block into its own 6-stage ring
-//     (32 KiB per 64-deep K block), so each SM pulls 64 B per clock of
-//     tensor work instead of 96 B with 128 x 256 single-CTA tiles.
+//     and rows [128r, 128r+128) of its B block into its own ring, so each SM
+//     pulls 64 B per clock of tensor work instead of 96 B with 128 x 256
+//     single-CTA tiles.  Without KO the ring has 6 stages of one 64-deep K
+//     block (two 16 KiB boxes); with KO (K-major A and B, K a multiple of
+//     64) it has 3 stages of 128 of K, each operand one {64, 128, 2} box over
+//     a map whose third dimension steps K by 64 -- a GB300 SM takes in two
+//     32 KiB boxes per stage about twice as fast as two 16 KiB boxes.
 //   * One thread of the even CTA issues tcgen05.mma.cta_group::2 with
 //     M = 256, N = 256, K = 16: the instruction reads A from both CTAs'
 //     shared memory (split along M) and B from both (split along N), and
@@ -32,29 +36,32 @@ namespace gemm_tn_dev {
 
 constexpr int kPairBM = 256;   // output rows per tile (128 per CTA)
 constexpr int kPairBN = 256;   // output columns per tile (B rows: 128 per CTA)
-constexpr int kPairBK = 64;
-constexpr int kPairStages = 6;
 constexpr int kPairThreads = 192;
 constexpr uint32_t kPairTmemCols = 512;  // two 256-column fp32 accumulators
 
+template <bool KO = false>
 struct PairSmem {
-  static constexpr uint32_t kABytes = 128 * kPairBK * 2;  // 16 KiB
-  static constexpr uint32_t kBBytes = 128 * kPairBK * 2;  // 16 KiB
+  static constexpr int kBK = KO ? 128 : 64;  // K per stage (and per p.k_blocks unit)
+  static constexpr int kStages = KO ? 3 : 6;
+  static constexpr uint32_t kABytes = 128 * kBK * 2;  // 16 / 32 KiB
+  static constexpr uint32_t kBBytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   // epilogue staging: 4 warps x 32 rows x 64 fp16 (1024-aligned)
-  static constexpr uint32_t kStagingOffset = kPairStages * kStageBytes;
+  static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
   static constexpr uint32_t kBarOffset = kStagingOffset + 4 * kStagingBytes;
-  static constexpr uint32_t kNumBars = 2 * kPairStages + 5;
+  static constexpr uint32_t kNumBars = 2 * kStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
 };
 
+template <bool KO = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tn_large2_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmD, const LargeArgs p) {
-  using L = PairSmem;
+  using L = PairSmem<KO>;
+  constexpr int kPairStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -128,18 +135,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t b_dst = a_dst + L::kABytes;
             mbar_arrive_expect_tx(fb, L::kStageBytes);
-            const int k0 = kb * kPairBK;
-            if (!p.a_mn) {
-              tma_load_3d(a_dst, &tmA, fb, k0, a_row, za);
+            if constexpr (KO) {
+              // K chunks 2kb and 2kb+1 (the second zero-filled past K)
+              tma_load_4d(a_dst, &tmA, fb, 0, a_row, 2 * kb, za);
+              tma_load_4d(b_dst, &tmB, fb, 0, b_row, 2 * kb, zb);
             } else {
-              tma_load_3d(a_dst, &tmA, fb, a_row, k0, za);
-              tma_load_3d(a_dst + 8192, &tmA, fb, a_row + 64, k0, za);
-            }
-            if (!p.b_mn) {
-              tma_load_3d(b_dst, &tmB, fb, k0, b_row, zb);
-            } else {
-              tma_load_3d(b_dst, &tmB, fb, b_row, k0, zb);
-              tma_load_3d(b_dst + 8192, &tmB, fb, b_row + 64, k0, zb);
+              const int k0 = kb * L::kBK;
+              if (!p.a_mn) {
+                tma_load_3d(a_dst, &tmA, fb, k0, a_row, za);
+              } else {
+                tma_load_3d(a_dst, &tmA, fb, a_row, k0, za);
+                tma_load_3d(a_dst + 8192, &tmA, fb, a_row + 64, k0, za);
+              }
+              if (!p.b_mn) {
+                tma_load_3d(b_dst, &tmB, fb, k0, b_row, zb);
+              } else {
+                tma_load_3d(b_dst, &tmB, fb, b_row, k0, zb);
+                tma_load_3d(b_dst + 8192, &tmB, fb, b_row + 64, k0, zb);
+              }
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -181,11 +194,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           const uint32_t a_base = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t b_base = a_base + L::kABytes;
 #pragma unroll
-          for (int k = 0; k < kPairBK / 16; ++k) {
-            const uint64_t ad = p.a_mn ? make_sw128_desc(a_base + k * 2048, 8192, 1024)
-                                       : make_sw128_desc(a_base + k * 32, 16, 1024);
-            const uint64_t bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
-                                       : make_sw128_desc(b_base + k * 32, 16, 1024);
+          for (int k = 0; k < L::kBK / 16; ++k) {
+            uint64_t ad, bd;
+            if constexpr (KO) {
+              // K chunk k/4 of each operand is a 128-row SW128 block
+              ad = make_sw128_desc(a_base + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024);
+              bd = make_sw128_desc(b_base + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024);
+            } else {
+              ad = p.a_mn ? make_sw128_desc(a_base + k * 2048, 8192, 1024)
+                          : make_sw128_desc(a_base + k * 32, 16, 1024);
+              bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
+                          : make_sw128_desc(b_base + k * 32, 16, 1024);
+            }
             mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // free the stage in both CTAs

@@ -129,8 +129,17 @@ int device_setup(int dev, DeviceState*& st) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                LargeSmem<128>::kDynamicBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tn_large2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               PairSmem::kDynamicBytes);
+      e = cudaFuncSetAttribute(gemm_tn_large_kernel<128, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               LargeSmem<128, true>::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_large2_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairSmem<false>::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_large2_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairSmem<true>::kDynamicBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_tn_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                WideSmem::kDynamicBytes);
@@ -142,9 +151,11 @@ int device_setup(int dev, DeviceState*& st) {
       std::memset(&cfg, 0, sizeof cfg);
       cfg.gridDim = dim3(2 * static_cast<unsigned>(st->num_sms / 2), 1, 1);
       cfg.blockDim = dim3(kPairThreads, 1, 1);
-      cfg.dynamicSmemBytes = PairSmem::kDynamicBytes;
+      static_assert(PairSmem<false>::kDynamicBytes >= PairSmem<true>::kDynamicBytes,
+                    "pair occupancy is taken from the larger layout");
+      cfg.dynamicSmemBytes = PairSmem<false>::kDynamicBytes;
       int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_large2_kernel, &cfg);
+      e = cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_large2_kernel<false>, &cfg);
       st->max_pairs = clusters;
     }
     if (e == cudaSuccess) e = set_skinny_attr<skinny_stages(16), 16>();
@@ -222,6 +233,26 @@ int encode_operand_batched(CUtensorMap* map, const void* ptr, int64_t rows, int6
                            static_cast<cuuint64_t>(batched ? bstride : outer * ld) * 2};
   cuuint32_t box[3] = {64, mn_major ? 64u : box_rows, 1}, estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_TN_OK : GEMM_TN_ERR_CUDA;
+}
+
+// K-major operand as K chunks: dims {64, rows, K/64, L}, the third stepping
+// K by 64 elements (128 bytes), box {64, box_rows, 2, 1}: one box brings 128
+// of K for box_rows rows, as two consecutive 128B-swizzled blocks.  Needs K
+// a multiple of 64 (the inner dimension is never clipped, so a partial last
+// chunk would read past K); the chunk past the last one is zero-filled.
+int encode_operand_ko(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld,
+                      int64_t bstride, int64_t L, uint32_t box_rows) {
+  const bool batched = L > 1 && bstride != 0;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 64),
+                        static_cast<cuuint64_t>(batched ? L : 1)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld) * 2, 128,
+                           static_cast<cuuint64_t>(batched ? bstride : rows * ld) * 2};
+  cuuint32_t box[4] = {64, box_rows, 2, 1}, estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -418,12 +449,23 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   const bool pair = kind == 2, wide = kind == 3;
   const int bn = (pair || wide) ? 256 : ((tile_n == 128) ? 128 : 256);
   const int bm = (pair || wide) ? 256 : kLargeBM;
+  // K-chunk boxes (stages of 128 of K) for the CTA pair and 128 x 128 tiles
+  // when both operands are K-major and K is a multiple of 64, from K = 1024
+  // on (shorter K loops fill and drain the 3-stage ring too often: 6-8 %
+  // slower at K = 512).
+  const bool ko = (pair || (kind == 1 && bn == 128)) && a_major == GEMM_TN_MAJOR_K &&
+                  b_major == GEMM_TN_MAJOR_K && K % 64 == 0 && K >= 1024;
   CUtensorMap tmA, tmB;
-  int s = encode_operand_batched(&tmA, q.A, M, K, q.ldA, q.sA, q.L, a_major,
-                                 wide ? 256 : kLargeBM);
-  if (s == GEMM_TN_OK)
-    s = encode_operand_batched(&tmB, q.B, N, K, q.ldB, q.sB, q.L, b_major,
-                               static_cast<uint32_t>(pair ? 128 : bn));
+  int s;
+  if (ko) {
+    s = encode_operand_ko(&tmA, q.A, M, K, q.ldA, q.sA, q.L, 128);
+    if (s == GEMM_TN_OK) s = encode_operand_ko(&tmB, q.B, N, K, q.ldB, q.sB, q.L, 128);
+  } else {
+    s = encode_operand_batched(&tmA, q.A, M, K, q.ldA, q.sA, q.L, a_major, wide ? 256 : kLargeBM);
+    if (s == GEMM_TN_OK)
+      s = encode_operand_batched(&tmB, q.B, N, K, q.ldB, q.sB, q.L, b_major,
+                                 static_cast<uint32_t>(pair ? 128 : bn));
+  }
   if (s != GEMM_TN_OK) return s;
   LargeArgs p;
   std::memset(&p, 0, sizeof p);
@@ -443,7 +485,10 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.a_batched = q.L > 1 && q.sA != 0;
   p.b_batched = q.L > 1 && q.sB != 0;
   p.num_tiles = static_cast<int>(per_batch * q.L);
-  p.k_blocks = static_cast<int>((K + kLargeBK - 1) / kLargeBK);
+  // K blocks of the kernel's stage depth: 128 with K-chunk boxes, else 64
+  const int64_t bk = ko ? 128 : kLargeBK;
+  p.k_blocks = static_cast<int>((K + bk - 1) / bk);
+  const int64_t kb64 = (K + kLargeBK - 1) / kLargeBK;
   p.group_m = (pair || wide) ? 8 : 16;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
@@ -498,8 +543,13 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     }
   } else if (pair) {
     const int pairs = std::min(p.num_tiles, st.max_pairs);
-    gemm_tn_large2_kernel<<<2 * pairs, kPairThreads, PairSmem::kDynamicBytes, stream>>>(
-        tmA, tmB, tmD, p);
+    if (ko) {
+      gemm_tn_large2_kernel<true><<<2 * pairs, kPairThreads, PairSmem<true>::kDynamicBytes,
+                                    stream>>>(tmA, tmB, tmD, p);
+    } else {
+      gemm_tn_large2_kernel<false><<<2 * pairs, kPairThreads, PairSmem<false>::kDynamicBytes,
+                                     stream>>>(tmA, tmB, tmD, p);
+    }
   } else {
     // K split over several CTAs per tile (fp32 accumulation only: a split
     // fp16 accumulation would round at different places): on request
@@ -512,8 +562,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
       if (o.tile_kernel == 1 && o.split_k > 0)
         splits = o.split_k;
       else if (o.tile_kernel == 0 && o.split_k == 0 && 2 * p.num_tiles <= st.num_sms &&
-               p.k_blocks >= 32)
-        splits = std::min(st.num_sms / p.num_tiles, p.k_blocks / 8);
+               kb64 >= 32)
+        splits = static_cast<int>(std::min<int64_t>(st.num_sms / p.num_tiles, kb64 / 8));
       splits = std::max(1, std::min(splits, p.k_blocks));
     }
     void* ks_ws = nullptr;
@@ -533,6 +583,9 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     if (bn == 256) {
       gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
           tmA, tmB, tmD, p);
+    } else if (ko) {
+      gemm_tn_large_kernel<128, true>
+          <<<grid, kLargeThreads, LargeSmem<128, true>::kDynamicBytes, stream>>>(tmA, tmB, tmD, p);
     } else {
       gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
           tmA, tmB, tmD, p);

@@ -283,8 +283,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int trow = row0 + static_cast<int>(lane);             // this lane's tile row
     uint8_t* stg = smem + L::kStagingOffset + ew * kWideStagingBytes;
     const uint32_t stg_u32 = smem_u32(stg);
-    // coalesced pattern: piece i of lane l is row 4i + l/8, 16-byte segment l%8
-    const int prow = static_cast<int>(lane >> 3), pseg = static_cast<int>(lane & 7);
     int tb = 0, tm = 0, tn = 0;
     const __half* cb = p.e.C;  // problem tb's C
     uint4 cnext[8];
