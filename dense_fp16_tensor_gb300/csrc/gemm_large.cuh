@@ -86,14 +86,15 @@ struct LargeSmem {
   static constexpr uint32_t kABytes = kLargeBM * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kBBytes = BN * kBK * 2;        // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // epilogue staging: 4 warps x 32 rows x 64 fp16 (1024-aligned)
+  // epilogue staging: 4 warps x 2 buffers x 32 rows x 64 fp16 (1024-aligned)
   static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
-  static constexpr uint32_t kBarOffset = kStagingOffset + 4 * 32 * 128;
+  static constexpr uint32_t kBarOffset = kStagingOffset + 8 * 32 * 128;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
   static constexpr uint32_t kNumBars = 2 * kStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;  // + alignment slack
+  static_assert(kDynamicBytes <= 232448, "over the 227 KiB of shared memory per CTA");
 };
 
 // Batch and tile coordinates of tile t (grouped raster inside each problem).
@@ -200,7 +201,9 @@ __device__ __noinline__ void epi_store_ragged(const LargeArgs& p, const uint8_t*
 
 // Combine this lane's accumulator row r (64 words) with its staged C row,
 // then store the chunk whose first element is D(m_row0, n0) of problem tb.
-__device__ __forceinline__ void epi_store_chunk(const LargeArgs& p, const CUtensorMap* tmD,
+// Returns (in lane 0) whether the chunk left by a TMA store, i.e. whether
+// one bulk group now reads the staging buffer.
+__device__ __forceinline__ bool epi_store_chunk(const LargeArgs& p, const CUtensorMap* tmD,
                                                 uint8_t* stg, uint32_t stg_u32, uint32_t lane,
                                                 int tb, int m_row0, int n0,
                                                 const uint32_t (&r)[64]) {
@@ -217,8 +220,35 @@ __device__ __forceinline__ void epi_store_chunk(const LargeArgs& p, const CUtens
   } else if (lane == 0 && m_row0 < p.M && n0 < p.N) {
     tma_store_3d(tmD, stg_u32, n0, m_row0, tb);
     bulk_commit_group();
+    return true;
   }
+  return false;
 }
+
+// Two staging buffers of one epilogue warp: a chunk is staged and combined
+// in one while the TMA store of the previous chunk may still read the other.
+struct StagingPair {
+  uint8_t* base;          // two kStagingBytes buffers
+  uint32_t buf = 0;       // buffer of the next chunk
+  bool last_tma = false;  // lane 0: the previous chunk's store is a pending bulk group
+  // The buffer for the next chunk, once the store that last read it is done:
+  // all bulk groups but the most recent (the other buffer's) when the
+  // previous chunk left by TMA, else all of them.
+  __device__ __forceinline__ uint8_t* acquire(uint32_t lane) {
+    if (lane == 0) {
+      if (last_tma)
+        bulk_wait_group_read1();
+      else
+        bulk_wait_group_read0();
+    }
+    __syncwarp();
+    return base + buf * kStagingBytes;
+  }
+  __device__ __forceinline__ void release(bool tma) {
+    last_tma = tma;
+    buf ^= 1u;
+  }
+};
 
 // KO: stages of 128 of K loaded as K-chunk boxes (see the header); p.k_blocks
 // then counts blocks of 128.
@@ -406,8 +436,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     // and the chunk leaves by TMA store.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes 32*quad ..
     const int row0 = static_cast<int>(quad * 32);            // first tile row of this warp
-    uint8_t* stg = smem + L::kStagingOffset + (warp - 2) * kStagingBytes;
-    const uint32_t stg_u32 = smem_u32(stg);
+    StagingPair staging{smem + L::kStagingOffset + (warp - 2) * 2 * kStagingBytes};
     constexpr int kChunks = BN / 64;
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
@@ -447,11 +476,9 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       batch_tile(p, t, tb, tm, tn);
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
       const int m_base = tm * kLargeBM + row0, n_base = tn * BN;
-      // chunk 0 of C staged and chunk 1 in registers, once the previous
-      // tile's last store has read the staging buffer
+      // chunk 0 of C staged and chunk 1 in registers
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
+      uint8_t* stg = staging.acquire(lane);
       epi_stage_c(stg, lane, cnext);
       if (kChunks > 1) epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
@@ -463,8 +490,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         if (c > 0) {
-          if (lane == 0) bulk_wait_group_read0();  // previous store has read staging
-          __syncwarp();
+          stg = staging.acquire(lane);
           epi_stage_c(stg, lane, cnext);
           if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
@@ -479,7 +505,8 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
         }
-        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
+        staging.release(
+            epi_store_chunk(p, &tmD, stg, smem_u32(stg), lane, tb, m_base, n_base + 64 * c, r));
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;

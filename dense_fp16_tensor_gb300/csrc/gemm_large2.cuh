@@ -46,13 +46,14 @@ struct PairSmem {
   static constexpr uint32_t kABytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kBBytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // epilogue staging: 4 warps x 32 rows x 64 fp16 (1024-aligned)
+  // epilogue staging: 4 warps x 2 buffers x 32 rows x 64 fp16 (1024-aligned)
   static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
-  static constexpr uint32_t kBarOffset = kStagingOffset + 4 * kStagingBytes;
+  static constexpr uint32_t kBarOffset = kStagingOffset + 8 * kStagingBytes;
   static constexpr uint32_t kNumBars = 2 * kStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
+  static_assert(kDynamicBytes <= 232448, "over the 227 KiB of shared memory per CTA");
 };
 
 template <bool KO = false>
@@ -252,8 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // TMA; the accumulator goes back to the even CTA's MMA thread.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
     const int row0 = static_cast<int>(rank * 128 + quad * 32);  // first tile row of this warp
-    uint8_t* stg = smem + L::kStagingOffset + (warp - 2) * kStagingBytes;
-    const uint32_t stg_u32 = smem_u32(stg);
+    StagingPair staging{smem + L::kStagingOffset + (warp - 2) * 2 * kStagingBytes};
     constexpr int kChunks = kPairBN / 64;
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     uint32_t acc = 0, acc_phase = 0;
@@ -264,8 +264,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
       const int m_base = tm * kPairBM + row0, n_base = tn * kPairBN;
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
+      uint8_t* stg = staging.acquire(lane);
       epi_stage_c(stg, lane, cnext);
       epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
@@ -277,8 +276,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         if (c > 0) {
-          if (lane == 0) bulk_wait_group_read0();  // previous store has read staging
-          __syncwarp();
+          stg = staging.acquire(lane);
           epi_stage_c(stg, lane, cnext);
           if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
@@ -292,7 +290,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
         }
-        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
+        staging.release(
+            epi_store_chunk(p, &tmD, stg, smem_u32(stg), lane, tb, m_base, n_base + 64 * c, r));
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;

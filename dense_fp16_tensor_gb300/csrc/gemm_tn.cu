@@ -443,6 +443,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
       kind = wide_ok ? 3 : (st.max_pairs > 0 ? 2 : 1);
     } else {
       kind = 1;
+      if (tile_n == 0 && N <= 128) tile_n = 128;  // a 256-wide tile would be half empty
     }
   }
   if (kind == 2 && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;

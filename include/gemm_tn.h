@@ -132,7 +132,10 @@ typedef struct {
                            tile_kernel 0 the library splits by itself when
                            the tiles would leave more than half the SMs
                            idle and K >= 2048) */
-  int tile_n;           /* large path: output tile width, 0 (= 256), 128 or 256 */
+  int tile_n;           /* large path, 128-row tiles: output tile width, 128
+                           or 256 (0: the library's choice -- 128 when N <=
+                           128 or when 128 x 256 tiles would leave half the
+                           SMs idle, else 256) */
   int sync_check;       /* nonzero: synchronise `stream` after the launch and
                            return GEMM_TN_ERR_DEVICE_TIMEOUT if a kernel gave
                            up waiting (the sticky device error word is read
