@@ -427,19 +427,22 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   int kind = o.tile_kernel;
   int tile_n = o.tile_n;
   if (kind == 0) {
-    // 256 x 256 tiles on one CTA need the fewest operand bytes per flop, but
-    // their accumulator cannot be double-buffered: they win when K is long
-    // enough to hide the drain and there are enough tiles to fill at least
-    // half the SMs.  Otherwise the CTA pair (double-buffered, 256 x 256 per
-    // two SMs); 128-row tiles when a side is too short for 256, and
-    // 128 x 128 tiles when even 128 x 256 tiles would leave half the SMs idle.
+    // The CTA pair (256 x 256 per two SMs, double-buffered accumulators,
+    // K-chunk loads) is the fastest kernel on everything but the largest
+    // problems; 256 x 256 tiles on one CTA (undoubled accumulator) do a few
+    // per cent more work per joule, which wins once a stream of such calls
+    // runs at the board's power limit: from M*N*K*L >= 2^39 (one 8192^3
+    // problem) with K > 1024 and enough tiles to fill half the SMs.  128-row
+    // tiles when a side is too short for 256, and 128 x 128 tiles when even
+    // 128 x 256 tiles would leave half the SMs idle.
     const int64_t tiles_128x256 = ((M + 127) / 128) * ((N + 255) / 256) * q.L;
     if (2 * tiles_128x256 <= st.num_sms) {
       kind = 1;
       if (tile_n == 0) tile_n = 128;
     } else if (M > kLargeBM && N > 128) {
       const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
-      const bool wide_ok = K > 1024 && 2 * tiles256 >= st.num_sms;
+      const double mnkl = static_cast<double>(M) * N * K * q.L;
+      const bool wide_ok = K > 1024 && 2 * tiles256 >= st.num_sms && mnkl >= 549755813888.0;
       kind = wide_ok ? 3 : (st.max_pairs > 0 ? 2 : 1);
     } else {
       kind = 1;

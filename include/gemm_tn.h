@@ -148,9 +148,10 @@ typedef struct {
                            hanging */
   int tile_kernel;      /* large path: 0 = choose (1 with 128 x 128 tiles
                            when 128 x 256 tiles would fill at most half the
-                           SMs; else, when M and N exceed 128, 3 if K > 1024
-                           and the 256 x 256 tiles of all problems fill at
-                           least half the SMs, otherwise 2; else 1),
+                           SMs; else, when M and N exceed 128, 3 if
+                           M*N*K*batch >= 2^39, K > 1024 and the 256 x 256
+                           tiles of all problems fill at least half the SMs,
+                           otherwise 2; else 1),
                            1 = single-CTA 128 x tile_n
                            tiles, 2 = CTA-pair 256 x 256 tiles (two SMs per
                            tile, tcgen05 cta_group::2), 3 = single-CTA
