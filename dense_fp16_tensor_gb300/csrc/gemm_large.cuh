@@ -276,8 +276,9 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  // a split-K reduction launched as a programmatic dependent may become
-  // resident now; it waits for this grid's completion before reading
+  // The next kernel in the stream (this call's reduction, or the next
+  // call's kernel) may become resident now; it waits for this grid's
+  // completion before it touches memory.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
@@ -306,6 +307,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: the kernel before this one in the stream
+  // (which may write A, B or C, or read a workspace this call reuses) must
+  // be complete before any global memory is touched.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -535,6 +540,9 @@ constexpr int kTileReduceThreads = 256;
 template <int BN>
 __global__ void __launch_bounds__(kTileReduceThreads)
     gemm_tn_tile_reduce_kernel(const LargeArgs p) {
+  // The next call's kernels may become resident now (they wait for this
+  // grid's completion before touching memory).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float sum[32][64 + 4];
   const int t = static_cast<int>(blockIdx.y);

@@ -83,6 +83,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const bool leader = rank == 0;
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  // The next kernel in the stream (this call's reduction, or the next
+  // call's kernel) may become resident now; it waits for this grid's
+  // completion before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
@@ -112,6 +116,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t peer_abort = mapa_shared(smem_u32(smem + L::kCtlOffset), rank ^ 1u);
+  // Programmatic dependent launch: the kernel before this one in the stream
+  // (which may write A, B or C, or read a workspace this call reuses) must
+  // be complete before any global memory is touched.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -25,6 +25,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "../../include/gemm_tn.h"
 #include "gemm_large.cuh"
@@ -417,6 +418,27 @@ int plan(int64_t M, int64_t N, int a_major, int b_major, int accum, int requeste
   return skinny_ok && auto_ok ? GEMM_TN_PATH_SKINNY : GEMM_TN_PATH_LARGE;
 }
 
+// Every kernel of the library is a programmatic dependent launch: it may
+// become resident while the kernel before it in the stream finishes, sets
+// up its barriers and tensor memory, and waits in griddepcontrol.wait before
+// it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
                  const DeviceState& st) {
   const int64_t M = q.M, N = q.N, K = q.K;
@@ -538,21 +560,23 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
         sk_ws = nullptr;
       }
     }
-    gemm_tn_wide_kernel<<<grid, kWideThreads, WideSmem::kDynamicBytes, stream>>>(tmA, tmB, tmD,
-                                                                               p);
-    if (sk_ws) {
-      const cudaError_t le = cudaGetLastError();
-      cudaFreeAsync(sk_ws, stream);
-      if (le != cudaSuccess) return GEMM_TN_ERR_CUDA;
+    const cudaError_t le = launch_pdl(gemm_tn_wide_kernel, dim3(grid), dim3(kWideThreads),
+                                      WideSmem::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    if (sk_ws) cudaFreeAsync(sk_ws, stream);
+    if (le != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_CUDA;
     }
   } else if (pair) {
     const int pairs = std::min(p.num_tiles, st.max_pairs);
-    if (ko) {
-      gemm_tn_large2_kernel<true><<<2 * pairs, kPairThreads, PairSmem<true>::kDynamicBytes,
-                                    stream>>>(tmA, tmB, tmD, p);
-    } else {
-      gemm_tn_large2_kernel<false><<<2 * pairs, kPairThreads, PairSmem<false>::kDynamicBytes,
-                                     stream>>>(tmA, tmB, tmD, p);
+    const cudaError_t le =
+        ko ? launch_pdl(gemm_tn_large2_kernel<true>, dim3(2 * pairs), dim3(kPairThreads),
+                        PairSmem<true>::kDynamicBytes, stream, tmA, tmB, tmD, p)
+           : launch_pdl(gemm_tn_large2_kernel<false>, dim3(2 * pairs), dim3(kPairThreads),
+                        PairSmem<false>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    if (le != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_CUDA;
     }
   } else {
     // K split over several CTAs per tile (fp32 accumulation only: a split
@@ -584,33 +608,30 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     }
     const int grid = static_cast<int>(
         std::min<int64_t>(static_cast<int64_t>(p.num_tiles) * p.ks_splits, st.num_sms));
-    if (bn == 256) {
-      gemm_tn_large_kernel<256><<<grid, kLargeThreads, LargeSmem<256>::kDynamicBytes, stream>>>(
-          tmA, tmB, tmD, p);
-    } else if (ko) {
-      gemm_tn_large_kernel<128, true>
-          <<<grid, kLargeThreads, LargeSmem<128, true>::kDynamicBytes, stream>>>(tmA, tmB, tmD, p);
-    } else {
-      gemm_tn_large_kernel<128><<<grid, kLargeThreads, LargeSmem<128>::kDynamicBytes, stream>>>(
-          tmA, tmB, tmD, p);
+    cudaError_t le;
+    if (bn == 256)
+      le = launch_pdl(gemm_tn_large_kernel<256>, dim3(grid), dim3(kLargeThreads),
+                      LargeSmem<256>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    else if (ko)
+      le = launch_pdl(gemm_tn_large_kernel<128, true>, dim3(grid), dim3(kLargeThreads),
+                      LargeSmem<128, true>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    else
+      le = launch_pdl(gemm_tn_large_kernel<128>, dim3(grid), dim3(kLargeThreads),
+                      LargeSmem<128>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    if (le != cudaSuccess && !ks_ws) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_CUDA;
     }
     if (ks_ws) {
-      cudaError_t e = cudaGetLastError();
+      cudaError_t e = le;
       if (e == cudaSuccess) {
-        // the reduction as a programmatic dependent: resident early, it waits
-        // in griddepcontrol.wait for the split kernel's partials
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(static_cast<unsigned>(4 * (bn / 64)), static_cast<unsigned>(p.num_tiles), 1);
-        cfg.blockDim = dim3(kTileReduceThreads, 1, 1);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = bn == 256 ? cudaLaunchKernelEx(&cfg, gemm_tn_tile_reduce_kernel<256>, p)
-                      : cudaLaunchKernelEx(&cfg, gemm_tn_tile_reduce_kernel<128>, p);
+        // the reduction: resident early, it waits in griddepcontrol.wait for
+        // the split kernel's partials
+        const dim3 rgrid(static_cast<unsigned>(4 * (bn / 64)), static_cast<unsigned>(p.num_tiles));
+        e = bn == 256 ? launch_pdl(gemm_tn_tile_reduce_kernel<256>, rgrid,
+                                   dim3(kTileReduceThreads), 0, stream, p)
+                      : launch_pdl(gemm_tn_tile_reduce_kernel<128>, rgrid,
+                                   dim3(kTileReduceThreads), 0, stream, p);
       }
       const cudaError_t f = cudaFreeAsync(ks_ws, stream);
       if (e != cudaSuccess || f != cudaSuccess) {
@@ -635,28 +656,13 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
 template <int MP>
 cudaError_t launch_skinny_mp(int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
                              const SkinnyArgs& p, const EpiArgs& ep, cudaStream_t stream) {
-  // Both kernels are programmatic dependent launches: each becomes resident
-  // while the kernel before it in the stream finishes, sets up its barriers
-  // and tensor memory, and waits in griddepcontrol.wait before it touches
-  // global memory.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kSkinnyThreads, 1, 1);
-  cfg.dynamicSmemBytes = SkinnySmem<skinny_stages(MP), MP>::kDynamicBytes;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e =
-      cudaLaunchKernelEx(&cfg, gemm_tn_skinny_kernel<skinny_stages(MP), MP>, tmA, tmB, p);
+  cudaError_t e = launch_pdl(gemm_tn_skinny_kernel<skinny_stages(MP), MP>, dim3(grid),
+                             dim3(kSkinnyThreads),
+                             SkinnySmem<skinny_stages(MP), MP>::kDynamicBytes, stream, tmA, tmB,
+                             p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles), MP / 16, 1);
-  cfg.blockDim = dim3(kReduceThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, gemm_tn_splitk_reduce_kernel<MP>, p, ep);
+  e = launch_pdl(gemm_tn_splitk_reduce_kernel<MP>, dim3(static_cast<unsigned>(p.tiles), MP / 16),
+                 dim3(kReduceThreads), 0, stream, p, ep);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -144,6 +144,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const int cta = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+  // The next kernel in the stream (this call's reduction, or the next
+  // call's kernel) may become resident now; it waits for this grid's
+  // completion before it touches memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWideStages; ++s) {
@@ -170,6 +174,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Programmatic dependent launch: the kernel before this one in the stream
+  // (which may write A, B or C, or read a workspace this call reuses) must
+  // be complete before any global memory is touched.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
