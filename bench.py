@@ -460,7 +460,8 @@ def run_ours(args):
     extra = {}
     if not args.no_extra and w.name != "skinny":
         if w.name == "large":
-            extra["cublas_same_inputs"] = bench_cublas(dev, stream, w, A, Bm)
+            extra["cublas_same_inputs"] = bench_cublas(dev, stream, w, A, Bm,
+                                                       steps=max(20, min(400, args.steps)))
         extra["skinny_m16"] = bench_skinny(dev, stream)
         extra["strided_4096"] = bench_strided(dev, stream)
         extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
@@ -696,8 +697,9 @@ def bench_stream_k(dev, stream, steps=50, rounds=3):
 
 def bench_tile_split(dev, stream, steps=100):
     """K split of the 128-row tile kernel on shapes whose tiles leave most SMs
-    idle: the automatic choice (split, with its reduction) against the same
-    kernel unsplit; fp32 accumulation."""
+    idle: the tile path's automatic choice (split, with its reduction)
+    against the same kernel unsplit; fp32 accumulation.  (M = 256 with this
+    N would otherwise take the skinny path.)"""
     import torch
 
     from dense_fp16_tensor_gb300 import binding as gb
@@ -709,8 +711,8 @@ def bench_tile_split(dev, stream, steps=100):
         CD = torch.zeros(M * N, dtype=torch.float16, device=dev)
         sp = stream.cuda_stream
         row = {}
-        for name, opts in (("split", None), ("unsplit", {"path": gb.PATH_LARGE, "tile_kernel": 1,
-                                                         "tile_n": 128})):
+        for name, opts in (("split", {"path": gb.PATH_LARGE}),
+                           ("unsplit", {"path": gb.PATH_LARGE, "tile_kernel": 1, "tile_n": 128})):
             def step():
                 st = gb.gemm_tn_ex(M, N, K, A.data_ptr(), K, 0, Bm.data_ptr(), K, 0, CD.data_ptr(),
                                    N, 0, sp, opts)
