@@ -15,13 +15,15 @@
 //     M = 256, N = 256, K = 16: the instruction reads A from both CTAs'
 //     shared memory (split along M) and B from both (split along N), and
 //     writes rows [128r, 128r+128) of D into CTA r's tensor memory.
-//   * Stage completion: each CTA's copies signal its own `full` barrier, so
-//     each CTA can always drain its own copies.  One thread of the odd CTA
-//     forwards each completed stage to the even CTA's `full` barrier (which
-//     therefore expects two arrivals).  The MMA thread releases a stage in
-//     both CTAs with one multicast tcgen05.commit; accumulators are handed to
-//     both CTAs' epilogues the same way, and the eight epilogue warps of the
-//     pair return an accumulator by arriving on the even CTA's `tmem_empty`.
+//   * Stage completion: both CTAs' copies of a stage count their bytes on
+//     the even CTA's `full` barrier (cta_group::2 loads may signal a barrier
+//     in the peer CTA), which the even CTA's producer arms with the bytes of
+//     the whole pair stage; so the MMA thread sees a stage as soon as the
+//     last of its four boxes has landed, with no hop through the odd CTA.
+//     The MMA thread releases a stage in both CTAs with one multicast
+//     tcgen05.commit; accumulators are handed to both CTAs' epilogues the
+//     same way, and the eight epilogue warps of the pair return an
+//     accumulator by arriving on the even CTA's `tmem_empty`.
 //   * Each CTA's epilogue is the staged one of gemm_large.cuh on its 128
 //     rows of the tile, with two accumulators so it overlaps the next
 //     tile's main loop.
@@ -90,7 +92,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
-      mbar_init(full0 + 8 * s, leader ? 2 : 1);  // own copies (+ the peer's forward)
+      mbar_init(full0 + 8 * s, 1);  // the even CTA's arming; both CTAs' bytes (odd: unused)
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -124,6 +126,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // Both CTAs' copies signal the even CTA's full barrier; only the even
+      // CTA arms it (arrival plus the pair stage's bytes).  A copy of the odd
+      // CTA may land before the arming: the barrier's transaction count then
+      // runs below zero for a while, and the phase still cannot complete
+      // without the arrival.  Neither CTA can start a stage's next phase
+      // before the MMA thread has released the stage in both (the multicast
+      // commit on `empty`), which it does only after the phase completed, so
+      // no copy can count against the wrong phase.
+      const uint32_t full_pair0 = mapa_shared(full0, 0);
       uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
       bool ok = true;
       int local = 0;
@@ -140,27 +151,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             break;
           }
           if (!(p.test_stall && local == 0 && kb == 0)) {
-            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t fb = full_pair0 + 8 * stage;
             const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t b_dst = a_dst + L::kABytes;
-            mbar_arrive_expect_tx(fb, L::kStageBytes);
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * L::kStageBytes);
             if constexpr (KO) {
               // K chunks 2kb and 2kb+1 (the second zero-filled past K)
-              tma_load_4d(a_dst, &tmA, fb, 0, a_row, 2 * kb, za);
-              tma_load_4d(b_dst, &tmB, fb, 0, b_row, 2 * kb, zb);
+              tma_load_4d_pair(a_dst, &tmA, fb, 0, a_row, 2 * kb, za);
+              tma_load_4d_pair(b_dst, &tmB, fb, 0, b_row, 2 * kb, zb);
             } else {
               const int k0 = kb * L::kBK;
               if (!p.a_mn) {
-                tma_load_3d(a_dst, &tmA, fb, k0, a_row, za);
+                tma_load_3d_pair(a_dst, &tmA, fb, k0, a_row, za);
               } else {
-                tma_load_3d(a_dst, &tmA, fb, a_row, k0, za);
-                tma_load_3d(a_dst + 8192, &tmA, fb, a_row + 64, k0, za);
+                tma_load_3d_pair(a_dst, &tmA, fb, a_row, k0, za);
+                tma_load_3d_pair(a_dst + 8192, &tmA, fb, a_row + 64, k0, za);
               }
               if (!p.b_mn) {
-                tma_load_3d(b_dst, &tmB, fb, k0, b_row, zb);
+                tma_load_3d_pair(b_dst, &tmB, fb, k0, b_row, zb);
               } else {
-                tma_load_3d(b_dst, &tmB, fb, b_row, k0, zb);
-                tma_load_3d(b_dst + 8192, &tmB, fb, b_row + 64, k0, zb);
+                tma_load_3d_pair(b_dst, &tmB, fb, b_row, k0, zb);
+                tma_load_3d_pair(b_dst + 8192, &tmB, fb, b_row + 64, k0, zb);
               }
             }
             issued_mask |= 1u << stage;
@@ -173,10 +184,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
       }
       if (!ok || *abort_flag) {
+        // Give every copy still in flight time to land before the CTA can
+        // leave.  The even CTA sees its stages complete on `full` (which
+        // also counts the odd CTA's bytes, so a phase the odd CTA never
+        // loaded runs to the limit).  The odd CTA cannot watch its copies
+        // directly; a stage it loaded is known landed once the MMA thread
+        // has released it (`empty`), else it waits out the limit.
         for (int s = 0; s < kPairStages; ++s)
           if (issued_mask >> s & 1u)
-            wait_bounded(full0 + 8 * s, issued_parity >> s & 1u, abort_flag, p.timeout_ns,
-                         timeout_code(kRoleProducer, 0x100 + s), false, peer_abort);
+            wait_bounded(leader ? full0 + 8 * s : empty0 + 8 * s, issued_parity >> s & 1u,
+                         abort_flag, p.timeout_ns, timeout_code(kRoleProducer, 0x100 + s), false,
+                         peer_abort);
       }
     }
   } else if (warp == 1) {
@@ -232,26 +250,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         mma_commit_pair(drain);
         wait_bounded(drain, 0, abort_flag, p.timeout_ns, timeout_code(kRoleMma, 0x300), false,
                      peer_abort);
-      }
-    } else if (lane == 0) {
-      // ---------------------------------------------------------- forwarder
-      // Tell the even CTA when this CTA's half of a stage has landed.
-      const uint32_t leader_full0 = mapa_shared(full0, 0);
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!wait_bounded(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
-                            timeout_code(kRoleMma, 0x400 + stage), true, peer_abort)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_cluster(leader_full0 + 8 * stage);
-          if (++stage == kPairStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
       }
     }
   } else {
