@@ -6,11 +6,13 @@
 //   * CTA r of the pair TMA-loads rows [128r, 128r+128) of the tile's A block
 //     and rows [128r, 128r+128) of its B block into its own ring, so each SM
 //     pulls 64 B per clock of tensor work instead of 96 B with 128 x 256
-//     single-CTA tiles.  Without KO the ring has 6 stages of one 64-deep K
-//     block (two 16 KiB boxes); with KO (K-major A and B, K a multiple of
-//     64) it has 3 stages of 128 of K, each operand one {64, 128, 2} box over
-//     a map whose third dimension steps K by 64 -- a GB300 SM takes in two
-//     32 KiB boxes per stage about twice as fast as two 16 KiB boxes.
+//     single-CTA tiles.  With DEEP the ring has 3 stages of 128 of K (two
+//     64-deep sub-blocks per operand, each loaded as in the 64-deep layout;
+//     64 KiB per CTA), and a sub-block past K is zero-filled by the copy;
+//     otherwise 6 stages of one 64-deep K block.  Deep stages halve the
+//     stage hand-offs per byte and win from K = 1024 on, except when a
+//     K-major operand's rows are not 128-byte aligned: then the shallow
+//     ring is faster.
 //   * One thread of the even CTA issues tcgen05.mma.cta_group::2 with
 //     M = 256, N = 256, K = 16: the instruction reads A from both CTAs'
 //     shared memory (split along M) and B from both (split along N), and
@@ -41,10 +43,10 @@ constexpr int kPairBN = 256;   // output columns per tile (B rows: 128 per CTA)
 constexpr int kPairThreads = 192;
 constexpr uint32_t kPairTmemCols = 512;  // two 256-column fp32 accumulators
 
-template <bool KO = false>
+template <bool DEEP = false>
 struct PairSmem {
-  static constexpr int kBK = KO ? 128 : 64;  // K per stage (and per p.k_blocks unit)
-  static constexpr int kStages = KO ? 3 : 6;
+  static constexpr int kBK = DEEP ? 128 : 64;  // K per stage (= p.k_blocks unit)
+  static constexpr int kStages = DEEP ? 3 : 6;
   static constexpr uint32_t kABytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kBBytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
@@ -58,12 +60,12 @@ struct PairSmem {
   static_assert(kDynamicBytes <= 232448, "over the 227 KiB of shared memory per CTA");
 };
 
-template <bool KO = false>
+template <bool DEEP = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tn_large2_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmD, const LargeArgs p) {
-  using L = PairSmem<KO>;
+  using L = PairSmem<DEEP>;
   constexpr int kPairStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -155,23 +157,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t b_dst = a_dst + L::kABytes;
             if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * L::kStageBytes);
-            if constexpr (KO) {
-              // K chunks 2kb and 2kb+1 (the second zero-filled past K)
-              tma_load_4d_pair(a_dst, &tmA, fb, 0, a_row, 2 * kb, za);
-              tma_load_4d_pair(b_dst, &tmB, fb, 0, b_row, 2 * kb, zb);
-            } else {
-              const int k0 = kb * L::kBK;
+            // 64-deep sub-blocks, 16 KiB apart; rows past M / N and K past the
+            // end (up to a whole sub-block) are zero-filled
+#pragma unroll
+            for (int sub = 0; sub < L::kBK / 64; ++sub) {
+              const int k0 = kb * L::kBK + 64 * sub;
+              const uint32_t as = a_dst + sub * 16384, bs = b_dst + sub * 16384;
               if (!p.a_mn) {
-                tma_load_3d_pair(a_dst, &tmA, fb, k0, a_row, za);
+                tma_load_3d_pair(as, &tmA, fb, k0, a_row, za);
               } else {
-                tma_load_3d_pair(a_dst, &tmA, fb, a_row, k0, za);
-                tma_load_3d_pair(a_dst + 8192, &tmA, fb, a_row + 64, k0, za);
+                tma_load_3d_pair(as, &tmA, fb, a_row, k0, za);
+                tma_load_3d_pair(as + 8192, &tmA, fb, a_row + 64, k0, za);
               }
               if (!p.b_mn) {
-                tma_load_3d_pair(b_dst, &tmB, fb, k0, b_row, zb);
+                tma_load_3d_pair(bs, &tmB, fb, k0, b_row, zb);
               } else {
-                tma_load_3d_pair(b_dst, &tmB, fb, b_row, k0, zb);
-                tma_load_3d_pair(b_dst + 8192, &tmB, fb, b_row + 64, k0, zb);
+                tma_load_3d_pair(bs, &tmB, fb, b_row, k0, zb);
+                tma_load_3d_pair(bs + 8192, &tmB, fb, b_row + 64, k0, zb);
               }
             }
             issued_mask |= 1u << stage;
@@ -222,17 +224,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           const uint32_t b_base = a_base + L::kABytes;
 #pragma unroll
           for (int k = 0; k < L::kBK / 16; ++k) {
-            uint64_t ad, bd;
-            if constexpr (KO) {
-              // K chunk k/4 of each operand is a 128-row SW128 block
-              ad = make_sw128_desc(a_base + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024);
-              bd = make_sw128_desc(b_base + (k >> 2) * (128 * 128) + (k & 3) * 32, 16, 1024);
-            } else {
-              ad = p.a_mn ? make_sw128_desc(a_base + k * 2048, 8192, 1024)
-                          : make_sw128_desc(a_base + k * 32, 16, 1024);
-              bd = p.b_mn ? make_sw128_desc(b_base + k * 2048, 8192, 1024)
-                          : make_sw128_desc(b_base + k * 32, 16, 1024);
-            }
+            // 16-deep step k: sub-block k / 4 (16 KiB further per sub-block),
+            // step k % 4 in it
+            const uint32_t as = a_base + (k >> 2) * 16384, bs = b_base + (k >> 2) * 16384;
+            const int kk = k & 3;
+            const uint64_t ad = p.a_mn ? make_sw128_desc(as + kk * 2048, 8192, 1024)
+                                       : make_sw128_desc(as + kk * 32, 16, 1024);
+            const uint64_t bd = p.b_mn ? make_sw128_desc(bs + kk * 2048, 8192, 1024)
+                                       : make_sw128_desc(bs + kk * 32, 16, 1024);
             mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
           mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // free the stage in both CTAs

@@ -450,7 +450,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   int tile_n = o.tile_n;
   if (kind == 0) {
     // The CTA pair (256 x 256 per two SMs, double-buffered accumulators,
-    // K-chunk loads) is the fastest kernel on everything but the largest
+    // 128-deep stages) is the fastest kernel on everything but the largest
     // problems; 256 x 256 tiles on one CTA (undoubled accumulator) do a few
     // per cent more work per joule, which wins once a stream of such calls
     // runs at the board's power limit: from M*N*K*L >= 2^39 (one 8192^3
@@ -475,12 +475,18 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   const bool pair = kind == 2, wide = kind == 3;
   const int bn = (pair || wide) ? 256 : ((tile_n == 128) ? 128 : 256);
   const int bm = (pair || wide) ? 256 : kLargeBM;
-  // K-chunk boxes (stages of 128 of K) for the CTA pair and 128 x 128 tiles
-  // when both operands are K-major and K is a multiple of 64, from K = 1024
-  // on (shorter K loops fill and drain the 3-stage ring too often: 6-8 %
-  // slower at K = 512).
-  const bool ko = (pair || (kind == 1 && bn == 128)) && a_major == GEMM_TN_MAJOR_K &&
+  // K-chunk boxes (stages of 128 of K) for 128 x 128 tiles when both
+  // operands are K-major and K is a multiple of 64, from K = 1024 on
+  // (shorter K loops fill and drain the 3-stage ring too often: 6-8 % slower
+  // at K = 512).  The CTA pair takes 128-deep stages of plain 64-deep boxes
+  // from K = 1024 on (1-2 % faster than K-chunk boxes from K = 2048 on, even
+  // at K = 1024, and 5-17 % faster than 64-deep stages at 8192^3 with an
+  // M-major A), unless a K-major operand's rows are not 128-byte aligned
+  // (3-5 % slower there than 64-deep stages).
+  const bool ko = kind == 1 && bn == 128 && a_major == GEMM_TN_MAJOR_K &&
                   b_major == GEMM_TN_MAJOR_K && K % 64 == 0 && K >= 1024;
+  const bool deep = ko || (pair && K >= 1024 && (a_major == GEMM_TN_MAJOR_MN || q.ldA % 64 == 0) &&
+                           (b_major == GEMM_TN_MAJOR_MN || q.ldB % 64 == 0));
   CUtensorMap tmA, tmB;
   int s;
   if (ko) {
@@ -511,8 +517,9 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.a_batched = q.L > 1 && q.sA != 0;
   p.b_batched = q.L > 1 && q.sB != 0;
   p.num_tiles = static_cast<int>(per_batch * q.L);
-  // K blocks of the kernel's stage depth: 128 with K-chunk boxes, else 64
-  const int64_t bk = ko ? 128 : kLargeBK;
+  // K blocks of the kernel's stage depth: 128 with K-chunk boxes or the
+  // pair's deep stages, else 64
+  const int64_t bk = deep ? 128 : kLargeBK;
   p.k_blocks = static_cast<int>((K + bk - 1) / bk);
   const int64_t kb64 = (K + kLargeBK - 1) / kLargeBK;
   p.group_m = (pair || wide) ? 8 : 16;
@@ -570,10 +577,10 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   } else if (pair) {
     const int pairs = std::min(p.num_tiles, st.max_pairs);
     const cudaError_t le =
-        ko ? launch_pdl(gemm_tn_large2_kernel<true>, dim3(2 * pairs), dim3(kPairThreads),
-                        PairSmem<true>::kDynamicBytes, stream, tmA, tmB, tmD, p)
-           : launch_pdl(gemm_tn_large2_kernel<false>, dim3(2 * pairs), dim3(kPairThreads),
-                        PairSmem<false>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+        deep ? launch_pdl(gemm_tn_large2_kernel<true>, dim3(2 * pairs), dim3(kPairThreads),
+                          PairSmem<true>::kDynamicBytes, stream, tmA, tmB, tmD, p)
+             : launch_pdl(gemm_tn_large2_kernel<false>, dim3(2 * pairs), dim3(kPairThreads),
+                          PairSmem<false>::kDynamicBytes, stream, tmA, tmB, tmD, p);
     if (le != cudaSuccess) {
       cudaGetLastError();
       return GEMM_TN_ERR_CUDA;
@@ -647,7 +654,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = sk_ws ? 2 : 1;  // the counters' memset counts as a launch
   t_last_kernels = wide ? (sk_ws ? "memset+gemm_tn_wide_kernel" : "gemm_tn_wide_kernel")
-                 : pair ? "gemm_tn_large2_kernel"
+                 : pair ? (deep ? "gemm_tn_large2_kernel<deep>" : "gemm_tn_large2_kernel")
                         : (bn == 256 ? "gemm_tn_large_kernel<256>" : "gemm_tn_large_kernel<128>");
   return GEMM_TN_OK;
 }

@@ -117,16 +117,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int32_t x, int32_t y, int32_t z,
-                                                 int32_t w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
-
 // Same with an L2 eviction-priority hint (createpolicy value).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar, int32_t x, int32_t y,

@@ -139,6 +139,44 @@ def test_ragged_sweep(accum, a_major, b_major, tile_kernel):
         slack_untouched(D_st, C_st, N)
 
 
+@pytest.mark.parametrize("a_major,b_major", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_pair_deep_stages_k_tails(a_major, b_major):
+    """The CTA pair's 128-deep stages (two 64-deep sub-blocks per operand,
+    from K = 1024 on): K ending inside the first sub-block of the last stage
+    (its second sub-block lies wholly past K), inside the second, and on
+    stage and sub-block boundaries; ragged M and N; K-major leading
+    dimensions multiples of 64.  Integer values: bit-exact.  A K-major
+    operand whose rows are not 128-byte aligned keeps 64-deep stages."""
+    rng = np.random.default_rng(700 + 2 * a_major + b_major)
+    M, N = 300, 520
+    for K in (1024, 1030, 1088, 1100, 1152, 1190):
+        ldA = (K + 63) // 64 * 64 if a_major == 0 else (M + 7) // 8 * 8 + 8
+        ldB = (K + 63) // 64 * 64 if b_major == 0 else (N + 7) // 8 * 8 + 8
+        A_st = wl.operand(M, K, ldA, a_major, "int1", int(rng.integers(1 << 30)))
+        B_st = wl.operand(N, K, ldB, b_major, "int1", int(rng.integers(1 << 30)))
+        C_st = wl.operand(M, N, N + 8, 0, "int4", int(rng.integers(1 << 30)))
+        d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), ldA, a_major, np_bits(B_st), ldB,
+                                  b_major, np_bits(C_st), N + 8)
+        D_st, st = run_gpu(M, N, K, A_st, ldA, a_major, B_st, ldB, b_major, C_st, N + 8, 0,
+                           opts={"path": gb.PATH_LARGE, "tile_kernel": 2}, guard_rows=2)
+        assert st == gb.OK, (K, gb.gemm_tn_status_string(st))
+        assert gb.gemm_tn_last_kernels() == "gemm_tn_large2_kernel<deep>"
+        check(result_view(D_st, M, N), d64, d16, K, 0, True, f"deep K={K}")
+        slack_untouched(D_st, C_st, N)
+    # a K-major operand with rows off the 128-byte grid: 64-deep stages
+    K = 1100
+    A_st = wl.operand(M, K, K + 4, 0, "int1", 5)
+    B_st = wl.operand(N, K, K + 12, 0, "int1", 6)
+    C_st = wl.operand(M, N, N, 0, "int4", 7)
+    D_st, st = run_gpu(M, N, K, A_st, K + 4, 0, B_st, K + 12, 0, C_st, N, 0,
+                       opts={"path": gb.PATH_LARGE, "tile_kernel": 2})
+    assert st == gb.OK
+    assert gb.gemm_tn_last_kernels() == "gemm_tn_large2_kernel"
+    d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), K + 4, 0, np_bits(B_st), K + 12, 0,
+                              np_bits(C_st), N)
+    check(result_view(D_st, M, N), d64, d16, K, 0, True, "shallow K=1100")
+
+
 @pytest.mark.parametrize("tile_n,tile_kernel", [(128, 1), (256, 1), (256, 2), (256, 3)])
 def test_large_path_real_values_every_tile_kernel(tile_n, tile_kernel):
     M, N, K = 300, 520, 700
