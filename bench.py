@@ -17,7 +17,9 @@ Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
   clocks        SM clocks and throttle reasons sampled during the timed region
   extra         other paths, each timed on its own: cuBLAS (torch.addmm) on
                 the headline's inputs beside gemm_tn_scaled (context only),
-                the skinny M=16 workload's HBM bandwidth, 4096^3 with K+1 leading dimensions (strided
+                the skinny M=16 workload's HBM bandwidth, the tiny, square
+                (fp16 accumulation) and ragged workloads against both
+                rooflines, 4096^3 with K+1 leading dimensions (strided
                 route), stream-K against the unsplit kernel, the scaled and
                 batched entry point, and the 128-row kernel's K split on
                 few-tile shapes
@@ -463,6 +465,7 @@ def run_ours(args):
             extra["cublas_same_inputs"] = bench_cublas(dev, stream, w, A, Bm,
                                                        steps=max(20, min(400, args.steps)))
         extra["skinny_m16"] = bench_skinny(dev, stream)
+        extra["configs"] = bench_configs(dev, stream)
         extra["strided_4096"] = bench_strided(dev, stream)
         extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
         extra["scaled_batched"] = bench_general(dev, stream)
@@ -602,6 +605,61 @@ def bench_skinny(dev, stream, steps=200):
             "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": kind,
             "launches_per_call": 2, "calls": steps,
             "l2": "B (512 MiB) larger than L2, calls back to back"}
+
+
+def bench_configs(dev, stream, steps=50):
+    """The other workloads of the parity set, each timed through gemm_tn on
+    its own layout: tiny (latency), square 1024^3 with fp16 accumulation and
+    ragged 4000x3000x2500 with an M-major A.  Their inputs fit in L2, so a
+    256 MiB buffer is written between calls and every call is timed on its
+    own with events (the flush is outside the timed spans)."""
+    import torch
+
+    from dense_fp16_tensor_gb300 import binding as gb
+    from dense_fp16_tensor_gb300 import workloads as wl
+    peaks, kind = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sp = stream.cuda_stream
+    out = {}
+    for name in ("tiny", "square1024", "ragged"):
+        w = wl.WORKLOADS[name]
+        A_st, B_st, C_st = wl.make_inputs(w)
+        A, Bm, CD = A_st.to(dev), B_st.to(dev), C_st.to(dev)
+        torch.cuda.synchronize()
+
+        def step():
+            st = gb.gemm_tn(w.M, w.N, w.K, A.data_ptr(), w.ldA, w.a_major, Bm.data_ptr(), w.ldB,
+                            w.b_major, CD.data_ptr(), w.ldC, w.accum, sp)
+            if st != gb.OK:
+                raise gb.GemmTnError(st)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                step()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        tflops = w.flops / (ms * 1e-3) / 1e12
+        gbs = w.min_bytes / (ms * 1e-3) / 1e9
+        out[name] = {"M": w.M, "N": w.N, "K": w.K,
+                     "accumulate": "fp16" if w.accum == gb.ACC_F16 else "fp32",
+                     "a_major": "M" if w.a_major == gb.MAJOR_MN else "K",
+                     "us_per_call_median": ms * 1e3, "TFLOP_per_s": tflops,
+                     "frac_of_tensor_peak": tflops / float(peaks["bf16_tflops"]),
+                     "GB_per_s_algorithmic": gbs,
+                     "frac_of_hbm_peak": gbs / float(peaks["hbm_gbs"]),
+                     "kernels": gb.gemm_tn_last_kernels()}
+        del A, Bm, CD
+    out["l2"] = "256 MiB written between calls; each call timed alone (median of %d)" % steps
+    out["peak_kind"] = kind
+    return out
 
 
 def bench_strided(dev, stream, steps=20):
