@@ -48,6 +48,12 @@ constexpr int kSkinnyMaxM = 256;  // the skinny kernel serves M <= 256
 // enough to stream B faster than the skinny kernel's 4-stage ring at MMA
 // width 256.
 constexpr int64_t kSkinnyWideMaxN = 56 * 256;
+// ... and only from this K on: shorter K loops finish sooner on the tile
+// kernels (one launch, no partial sums; 128 x 128 tiles with their own K
+// split when they leave SMs idle).  Crossovers measured one call at a time
+// with a cold L2: K ~ 2048 for M = 16, ~4096-8192 for M = 64, ~8192 for
+// M = 128 and 256 (tile / skinny at K = 512: 14 / 17-24 us).
+constexpr int64_t skinny_min_k(int64_t M) { return M <= 32 ? 2048 : M <= 64 ? 4096 : 8192; }
 constexpr int kNoallocMaxM = 64;   // the allocation-free entry point's limit
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s per wait
 
@@ -408,13 +414,13 @@ int validate(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA, int a_
   return validate(in_place_problem(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum));
 }
 
-int plan(int64_t M, int64_t N, int a_major, int b_major, int accum, int requested,
+int plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int accum, int requested,
          int64_t L = 1) {
   const bool skinny_ok = M <= kSkinnyMaxM && a_major == GEMM_TN_MAJOR_K &&
                          b_major == GEMM_TN_MAJOR_K && accum == GEMM_TN_ACC_F32 && L <= 1;
   if (requested == GEMM_TN_PATH_SKINNY) return skinny_ok ? GEMM_TN_PATH_SKINNY : -1;
   if (requested == GEMM_TN_PATH_LARGE) return GEMM_TN_PATH_LARGE;
-  const bool auto_ok = M <= 192 || N <= kSkinnyWideMaxN;
+  const bool auto_ok = (M <= 192 || N <= kSkinnyWideMaxN) && K >= skinny_min_k(M);
   return skinny_ok && auto_ok ? GEMM_TN_PATH_SKINNY : GEMM_TN_PATH_LARGE;
 }
 
@@ -784,7 +790,7 @@ int run_problem(const Problem& q, void* stream, const gemm_tn_options* opts) {
   // D = beta * C: nothing to do in place with beta == 1
   if (!q.use_ab() && q.beta == 1.f && q.in_place()) return GEMM_TN_OK;
 
-  const int path = plan(q.M, q.N, q.a_major, q.b_major, q.accum, o.path, q.L);
+  const int path = plan(q.M, q.N, q.K, q.a_major, q.b_major, q.accum, o.path, q.L);
   if (path < 0) return GEMM_TN_ERR_INVALID_ARG;
   DeviceState* st = nullptr;
   s = device_state(st);
@@ -878,7 +884,7 @@ GEMM_TN_API int gemm_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 
 GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major, int b_major) {
   (void)K;
-  return plan(M, N, a_major, b_major, GEMM_TN_ACC_F32, GEMM_TN_PATH_AUTO);
+  return plan(M, N, K, a_major, b_major, GEMM_TN_ACC_F32, GEMM_TN_PATH_AUTO);
 }
 
 GEMM_TN_API int gemm_tn_last_launch_count(void) { return t_last_launches; }
@@ -1123,7 +1129,7 @@ int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if (e == cudaSuccess) {
     gemm_tn_options o;
     std::memset(&o, 0, sizeof o);
-    const int path = plan(M, N, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
+    const int path = plan(M, N, K, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
     const Problem q =
         in_place_problem(M, N, K, Ause, ldA, a_major, Buse, ldB, b_major, Cuse, ldC, accum);
     s = path == GEMM_TN_PATH_SKINNY ? launch_skinny(q, stream, o, st)

@@ -105,7 +105,9 @@ typedef enum {
 typedef enum {
   GEMM_TN_PATH_AUTO = 0,    /* skinny path with K-major A and B and fp32
                                accumulation for M <= 192, and for M <= 256
-                               when N <= 14336; persistent tile path
+                               when N <= 14336, once K is long enough to
+                               stream (K >= 2048 for M <= 32, 4096 for
+                               M <= 64, 8192 above); persistent tile path
                                otherwise */
   GEMM_TN_PATH_LARGE = 1,   /* persistent tile kernels: 256x256 tiles on one
                                CTA or on a CTA pair, or 128xBN tiles */
@@ -232,8 +234,9 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
  *   alignment    A, B, C, D 16-byte aligned, ld* multiples of 8
  *                (GEMM_TN_ERR_ALIGNMENT otherwise; gemm_tn_strided takes
  *                arbitrary strides for the unscaled, single-problem form).
- *   paths        one problem with M <= 128, K-major operands and fp32
- *                accumulation takes the skinny split-K path; everything else
+ *   paths        one problem that GEMM_TN_PATH_AUTO sends to the skinny
+ *                split-K path (small M, long K, K-major operands, fp32
+ *                accumulation) takes it here too; everything else
  *                runs the tile kernels with the batch folded into the tile
  *                list (tile t belongs to problem t / tiles-per-problem).
  *   returns      as gemm_tn; M, N or batch == 0 is a no-op.

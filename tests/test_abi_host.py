@@ -44,16 +44,25 @@ def test_status_strings(lib):
 
 
 def test_plan_path(lib):
-    assert gb.gemm_tn_plan_path(16, 16384, 16384, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(64, 100, 100, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(128, 100, 100, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(192, 65536, 100, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(193, 14336, 100, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(256, 14336, 100, 0, 0) == gb.PATH_SKINNY
-    assert gb.gemm_tn_plan_path(193, 14337, 100, 0, 0) == gb.PATH_LARGE
-    assert gb.gemm_tn_plan_path(257, 100, 100, 0, 0) == gb.PATH_LARGE
-    assert gb.gemm_tn_plan_path(16, 100, 100, 1, 0) == gb.PATH_LARGE
-    assert gb.gemm_tn_plan_path(8192, 8192, 8192, 0, 0) == gb.PATH_LARGE
+    P = gb.gemm_tn_plan_path
+    assert P(16, 16384, 16384, 0, 0) == gb.PATH_SKINNY
+    # long enough K for the skinny path: 2048 up to M = 32, 4096 up to 64, 8192 above
+    assert P(32, 100, 2048, 0, 0) == gb.PATH_SKINNY
+    assert P(32, 100, 2047, 0, 0) == gb.PATH_LARGE
+    assert P(33, 100, 2048, 0, 0) == gb.PATH_LARGE
+    assert P(64, 100, 4096, 0, 0) == gb.PATH_SKINNY
+    assert P(64, 100, 4095, 0, 0) == gb.PATH_LARGE
+    assert P(128, 100, 8192, 0, 0) == gb.PATH_SKINNY
+    assert P(128, 100, 8191, 0, 0) == gb.PATH_LARGE
+    assert P(32, 16, 16, 0, 0) == gb.PATH_LARGE        # the tiny workload
+    # M up to 192 at any N; up to 256 while N <= 14336
+    assert P(192, 65536, 8192, 0, 0) == gb.PATH_SKINNY
+    assert P(193, 14336, 8192, 0, 0) == gb.PATH_SKINNY
+    assert P(256, 14336, 8192, 0, 0) == gb.PATH_SKINNY
+    assert P(193, 14337, 8192, 0, 0) == gb.PATH_LARGE
+    assert P(257, 100, 8192, 0, 0) == gb.PATH_LARGE
+    assert P(16, 100, 8192, 1, 0) == gb.PATH_LARGE     # M-major A
+    assert P(8192, 8192, 8192, 0, 0) == gb.PATH_LARGE
 
 
 P = 0x7F0000000000  # a 16-byte aligned fake device address, never dereferenced

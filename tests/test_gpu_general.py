@@ -160,7 +160,7 @@ def test_batched_small_m_runs_the_tile_kernel():
 def test_skinny_path_scaled_separate_d():
     for M in (16, 40, 64, 160, 256):
         cs = Case(M, 1000, 3000, 1, seed=7 + M)
-        D, k = cs.run(0.5, -2.0, 0)
+        D, k = cs.run(0.5, -2.0, 0, dict(path=gb.PATH_SKINNY))
         assert k == "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel", k
         cs.verify(D, 0.5, -2.0, 0, True, f"skinny M={M}")
 
@@ -180,7 +180,7 @@ def test_beta_zero_does_not_read_c():
     D2, _ = cs.run(3.0, 0.0, 0, pass_c=False)  # C pointer NULL
     assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
     cs1 = Case(40, 500, 2000, 1, seed=10)     # skinny path, C NULL
-    D3, k = cs1.run(1.0, 0.0, 0, pass_c=False)
+    D3, k = cs1.run(1.0, 0.0, 0, dict(path=gb.PATH_SKINNY), pass_c=False)
     assert k.startswith("gemm_tn_skinny_kernel"), k
     cs1.verify(D3, 1.0, 0.0, 0, True, "skinny beta 0")
 
@@ -383,7 +383,7 @@ def test_concurrent_calls_from_host_threads():
     per-thread state is thread-local)."""
     import threading
     dev = torch.device("cuda")
-    shapes = [(512, 512, 8192), (48, 2000, 3000), (600, 700, 2048), (300, 260, 5000)]
+    shapes = [(512, 512, 8192), (48, 2000, 4096), (600, 700, 2048), (300, 260, 5000)]
     cases = [Case(M, N, K, 1, seed=60 + i) for i, (M, N, K) in enumerate(shapes)]
     inputs = [(cs.A.to(dev), cs.B.to(dev), cs.C.to(dev), cs.D0.to(dev)) for cs in cases]
     torch.cuda.synchronize()
