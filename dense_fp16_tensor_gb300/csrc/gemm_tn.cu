@@ -339,6 +339,13 @@ void extent_batched(const void* p, int64_t rows, int64_t cols, int64_t ld, int m
 
 bool overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
+// A batch stride whose last view starts at most 2^61 elements (2^62 bytes)
+// in, so that the byte extents below stay inside 64-bit arithmetic (no
+// allocation comes near that).
+bool stride_in_range(int64_t stride, int64_t L) {
+  return stride >= 0 && (L <= 1 || stride <= (int64_t{1} << 61) / (L - 1));
+}
+
 int validate(const Problem& q) {
   const int64_t kMax = 0x7FFFFFFF;
   if (q.M < 0 || q.N < 0 || q.K < 0 || q.L < 0 || q.M > kMax || q.N > kMax || q.K > kMax ||
@@ -352,11 +359,12 @@ int validate(const Problem& q) {
   const bool batched = q.L > 1;
   // D: written; batches may not overlap one another
   if (q.D == nullptr || q.ldD < q.N || q.ldD > kMax) return GEMM_TN_ERR_INVALID_ARG;
-  if (batched && q.sD < q.M * q.ldD) return GEMM_TN_ERR_INVALID_ARG;
+  if (batched && (q.sD < q.M * q.ldD || !stride_in_range(q.sD, q.L)))
+    return GEMM_TN_ERR_INVALID_ARG;
   uintptr_t d0, d1;
   extent_batched(q.D, q.M, q.N, q.ldD, 0, q.sD, q.L, d0, d1);
   if (q.read_c()) {
-    if (q.C == nullptr || q.ldC < q.N || q.ldC > kMax || (batched && q.sC < 0))
+    if (q.C == nullptr || q.ldC < q.N || q.ldC > kMax || (batched && !stride_in_range(q.sC, q.L)))
       return GEMM_TN_ERR_INVALID_ARG;
     if (!q.in_place()) {
       uintptr_t c0, c1;
@@ -372,7 +380,7 @@ int validate(const Problem& q) {
       return GEMM_TN_ERR_INVALID_ARG;
     // batch strides: 0 (one operand for every problem) or whole views apart
     if (batched && ((q.sA != 0 && q.sA < a_outer * q.ldA) || (q.sB != 0 && q.sB < b_outer * q.ldB) ||
-                    q.sA < 0 || q.sB < 0))
+                    !stride_in_range(q.sA, q.L) || !stride_in_range(q.sB, q.L)))
       return GEMM_TN_ERR_INVALID_ARG;
     uintptr_t a0, a1, b0, b1;
     extent_batched(q.A, q.M, q.K, q.ldA, q.a_major, q.sA, q.L, a0, a1);
@@ -883,7 +891,6 @@ GEMM_TN_API int gemm_tn(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
 }
 
 GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major, int b_major) {
-  (void)K;
   return plan(M, N, K, a_major, b_major, GEMM_TN_ACC_F32, GEMM_TN_PATH_AUTO);
 }
 

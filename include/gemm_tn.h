@@ -226,7 +226,8 @@ GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K,
  *                strideA: 0 (one A for every problem) or at least one view
  *                  (M*ldA K-major, K*ldA M-major); strideB likewise;
  *                strideC: any value >= 0 (0 = one C for every problem);
- *                strideD: at least M*ldD (the problems' D do not overlap).
+ *                strideD: at least M*ldD (the problems' D do not overlap);
+ *                every (batch-1)*stride at most 2^61 (INVALID_ARG above).
  *   aliasing     D may be C itself (same pointer, ldD == ldC, strideD ==
  *                strideC): each C element is read before the D element at
  *                its position is written.  Otherwise D must not overlap C;

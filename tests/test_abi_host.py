@@ -186,6 +186,9 @@ def bcall(M=64, N=64, K=64, L=2, alpha=1.0, A=P, ldA=64, sA=64 * 64, am=0, B=P +
     (dict(sD=64 * 64 + 4), gb.ERR_ALIGNMENT),
     (dict(C=P + 8 * MB + 2, L=1), gb.ERR_ALIGNMENT),
     (dict(ldD=60), gb.ERR_INVALID_ARG),
+    (dict(sC=(1 << 61) + 8), gb.ERR_INVALID_ARG),          # byte extents past 64 bits
+    (dict(L=3, sD=1 << 61), gb.ERR_INVALID_ARG),
+    (dict(L=1 << 30, sA=1 << 40), gb.ERR_INVALID_ARG),
 ])
 def test_batched_argument_checks(lib, kw, status):
     assert bcall(**kw) == status
