@@ -28,7 +28,9 @@
 //     accumulator by arriving on the even CTA's `tmem_empty`.
 //   * Each CTA's epilogue is the staged one of gemm_large.cuh on its 128
 //     rows of the tile, with two accumulators so it overlaps the next
-//     tile's main loop.
+//     tile's main loop; eight warps, two per TMEM lane quadrant, each drain
+//     one 128-column half, so that an accumulator is free again after two
+//     chunk times (with short K loops the drain, not the MMA, set the pace).
 //
 // Every wait is bounded; a CTA that gives up raises its own and its peer's
 // abort flag, both drain what they issued, free the pair's TMEM and return.
@@ -40,7 +42,7 @@ namespace gemm_tn_dev {
 
 constexpr int kPairBM = 256;   // output rows per tile (128 per CTA)
 constexpr int kPairBN = 256;   // output columns per tile (B rows: 128 per CTA)
-constexpr int kPairThreads = 192;
+constexpr int kPairThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kPairTmemCols = 512;  // two 256-column fp32 accumulators
 
 template <bool DEEP = false>
@@ -50,7 +52,7 @@ struct PairSmem {
   static constexpr uint32_t kABytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kBBytes = 128 * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // epilogue staging: 4 warps x 2 buffers x 32 rows x 64 fp16 (1024-aligned)
+  // epilogue staging: 8 warps x 32 rows x 64 fp16 (1024-aligned)
   static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
   static constexpr uint32_t kBarOffset = kStagingOffset + 8 * kStagingBytes;
   static constexpr uint32_t kNumBars = 2 * kStages + 5;
@@ -99,7 +101,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 8);  // the pair's eight epilogue warps
+      mbar_init(tempty0 + 8 * a, 16);  // the pair's sixteen epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -255,11 +257,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // ------------------------------------------------------------ epilogue
     // Staged as in the single-CTA kernels: this CTA's 128 rows of the pair
     // tile, C fetched while the tile's MMAs run, 64-column chunks stored by
-    // TMA; the accumulator goes back to the even CTA's MMA thread.
-    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    // TMA from one staging buffer per warp; the accumulator goes back to the
+    // even CTA's MMA thread.
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes 32*quad ..
+    const int ew = warp - 2;                                // 0..7
+    const int col0 = (ew >> 2) * (kPairBN / 2);             // first tile column of this warp
     const int row0 = static_cast<int>(rank * 128 + quad * 32);  // first tile row of this warp
-    StagingPair staging{smem + L::kStagingOffset + (warp - 2) * 2 * kStagingBytes};
-    constexpr int kChunks = kPairBN / 64;
+    uint8_t* stg = smem + L::kStagingOffset + ew * kStagingBytes;
+    const uint32_t stg_u32 = smem_u32(stg);
+    constexpr int kChunks = kPairBN / 2 / 64;  // per warp
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
@@ -267,9 +273,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
-      const int m_base = tm * kPairBM + row0, n_base = tn * kPairBN;
+      const int m_base = tm * kPairBM + row0, n_base = tn * kPairBN + col0;
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
-      uint8_t* stg = staging.acquire(lane);
+      if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
+      __syncwarp();
       epi_stage_c(stg, lane, cnext);
       epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
@@ -277,11 +284,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         timeout_code(kRoleEpilogue, acc), true, peer_abort))
         break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN;
+      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN + col0;
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         if (c > 0) {
-          stg = staging.acquire(lane);
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
           epi_stage_c(stg, lane, cnext);
           if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
@@ -295,8 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
         }
-        staging.release(
-            epi_store_chunk(p, &tmD, stg, smem_u32(stg), lane, tb, m_base, n_base + 64 * c, r));
+        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
