@@ -20,13 +20,15 @@
 //               issues tcgen05.mma (M=128, N=BN, K=16, four per stage); each
 //               stage is released with tcgen05.commit -> `empty`, each tile
 //               with tcgen05.commit -> `tmem_full`.
-//   warps 2-5   epilogue (staged, shared with the other tile kernels): C of
-//               the next tile arrives in coalesced 32 x 64 chunks into a
-//               128-byte-swizzled staging buffer while its MMAs run; per
-//               chunk tcgen05.ld 64 columns, combine with the staged C
-//               (epi_f32x2 / epi_f16x2), TMA-store the chunk; arrive
-//               `tmem_empty` once all columns are read, so the MMA warp
-//               reuses the accumulator while the epilogue finishes.
+//   warps 2-9   epilogue (staged, shared with the other tile kernels), two
+//               warps per TMEM lane quadrant, each on one half of the
+//               tile's columns: C of the next tile arrives in coalesced
+//               32 x 64 chunks into the warp's 128-byte-swizzled staging
+//               buffer while its MMAs run; per chunk tcgen05.ld 64 columns,
+//               combine with the staged C (epi_f32x2 / epi_f16x2),
+//               TMA-store the chunk; arrive `tmem_empty` once the warp's
+//               columns are read, so the MMA warp reuses the accumulator
+//               while the epilogue finishes.
 //
 // Work units (tiles, or (tile, K range) pairs when ks_splits > 1) are handed
 // out round-robin (u = blockIdx.x, += gridDim.x) in a grouped raster; a
@@ -44,7 +46,7 @@ namespace gemm_tn_dev {
 
 constexpr int kLargeBM = 128;
 constexpr int kLargeBK = 64;   // K per stage (and per p.k_blocks unit) without KO
-constexpr int kLargeThreads = 192;
+constexpr int kLargeThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 
 struct LargeArgs {
   int M, N, K;
@@ -86,7 +88,7 @@ struct LargeSmem {
   static constexpr uint32_t kABytes = kLargeBM * kBK * 2;  // 16 / 32 KiB
   static constexpr uint32_t kBBytes = BN * kBK * 2;        // 16 / 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // epilogue staging: 4 warps x 2 buffers x 32 rows x 64 fp16 (1024-aligned)
+  // epilogue staging: 8 warps x 32 rows x 64 fp16 (1024-aligned)
   static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
   static constexpr uint32_t kBarOffset = kStagingOffset + 8 * 32 * 128;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
@@ -225,31 +227,6 @@ __device__ __forceinline__ bool epi_store_chunk(const LargeArgs& p, const CUtens
   return false;
 }
 
-// Two staging buffers of one epilogue warp: a chunk is staged and combined
-// in one while the TMA store of the previous chunk may still read the other.
-struct StagingPair {
-  uint8_t* base;          // two kStagingBytes buffers
-  uint32_t buf = 0;       // buffer of the next chunk
-  bool last_tma = false;  // lane 0: the previous chunk's store is a pending bulk group
-  // The buffer for the next chunk, once the store that last read it is done:
-  // all bulk groups but the most recent (the other buffer's) when the
-  // previous chunk left by TMA, else all of them.
-  __device__ __forceinline__ uint8_t* acquire(uint32_t lane) {
-    if (lane == 0) {
-      if (last_tma)
-        bulk_wait_group_read1();
-      else
-        bulk_wait_group_read0();
-    }
-    __syncwarp();
-    return base + buf * kStagingBytes;
-  }
-  __device__ __forceinline__ void release(bool tma) {
-    last_tma = tma;
-    buf ^= 1u;
-  }
-};
-
 // KO: stages of 128 of K loaded as K-chunk boxes (see the header); p.k_blocks
 // then counts blocks of 128.
 template <int BN, bool KO = false>
@@ -288,7 +265,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);  // one arrival per epilogue warp
+      mbar_init(tempty0 + 8 * a, 8);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -438,22 +415,29 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     // ------------------------------------------------------------ epilogue
     // Staged: C of the next tile is fetched (coalesced) while its MMAs run;
     // per 64-column chunk the accumulator row is added to the staged C row
-    // and the chunk leaves by TMA store.
+    // and the chunk leaves by TMA store.  Eight warps, two per TMEM lane
+    // quadrant, each drain one half of the tile's columns through one
+    // staging buffer, so that an accumulator is free again after
+    // BN / 128 chunk times.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes 32*quad ..
+    const int ew = warp - 2;                                // 0..7
+    const int half = ew >> 2;                               // column half of the tile
     const int row0 = static_cast<int>(quad * 32);            // first tile row of this warp
-    StagingPair staging{smem + L::kStagingOffset + (warp - 2) * 2 * kStagingBytes};
-    constexpr int kChunks = BN / 64;
+    constexpr int kChunks = BN / 128;                        // 64-column chunks per warp
+    const int col0 = half * (BN / 2);                        // first tile column of this warp
+    uint8_t* stg = smem + L::kStagingOffset + ew * kStagingBytes;
+    const uint32_t stg_u32 = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
     const int units = p.num_tiles * p.ks_splits;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       if (p.ks_splits > 1) {
-        // split-K unit: this warp's 32 rows of the fp32 partial tile -> ks_ws
+        // split-K unit: this warp's 32 x BN/2 of the fp32 partial tile -> ks_ws
         if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                           timeout_code(kRoleEpilogue, acc)))
           break;
         tc_fence_after();
-        const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN;
+        const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN + col0;
         float4* ws4 = reinterpret_cast<float4*>(p.ks_ws);
 #pragma unroll 1
         for (int c = 0; c < kChunks; ++c) {
@@ -466,9 +450,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
           }
+          const int gc = half * kChunks + c;  // chunk of the tile
 #pragma unroll
           for (int g = 0; g < 16; ++g)
-            ws4[ks_partial_index(u, BN, static_cast<int>(quad), c, g, static_cast<int>(lane))] =
+            ws4[ks_partial_index(u, BN, static_cast<int>(quad), gc, g, static_cast<int>(lane))] =
                 make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
                             __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
         }
@@ -480,10 +465,11 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
-      const int m_base = tm * kLargeBM + row0, n_base = tn * BN;
-      // chunk 0 of C staged and chunk 1 in registers
+      const int m_base = tm * kLargeBM + row0, n_base = tn * BN + col0;
+      // chunk 0 of C staged (and chunk 1 in registers)
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
-      uint8_t* stg = staging.acquire(lane);
+      if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
+      __syncwarp();
       epi_stage_c(stg, lane, cnext);
       if (kChunks > 1) epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
@@ -491,11 +477,12 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
                         timeout_code(kRoleEpilogue, acc)))
         break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN;
+      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN + col0;
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         if (c > 0) {
-          stg = staging.acquire(lane);
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
           epi_stage_c(stg, lane, cnext);
           if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
@@ -505,13 +492,12 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
         if (c == kChunks - 1) {
-          // every column of this accumulator is in registers: hand it back
+          // every column of this warp's share is in registers: hand it back
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
         }
-        staging.release(
-            epi_store_chunk(p, &tmD, stg, smem_u32(stg), lane, tb, m_base, n_base + 64 * c, r));
+        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
