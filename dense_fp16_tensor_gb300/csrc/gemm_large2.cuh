@@ -62,6 +62,14 @@ struct PairSmem {
   static_assert(kDynamicBytes <= 232448, "over the 227 KiB of shared memory per CTA");
 };
 
+// Work unit u: split u % ks_splits of tile u / ks_splits, K blocks
+// [kb0, kb1) (the whole K loop when ks_splits == 1).
+__device__ __forceinline__ void pair_unit(const LargeArgs& p, int u, int& t, int& kb0, int& kb1) {
+  t = p.ks_splits > 1 ? u / p.ks_splits : u;
+  kb0 = (u - t * p.ks_splits) * p.ks_kb_per;
+  kb1 = min(kb0 + p.ks_kb_per, p.k_blocks);
+}
+
 template <bool DEEP = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_tn_large2_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -89,6 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const bool leader = rank == 0;
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  const int units = p.num_tiles * p.ks_splits;  // work units, round-robin over the pairs
   // The next kernel in the stream (this call's reduction, or the next
   // call's kernel) may become resident now; it waits for this grid's
   // completion before it touches memory.
@@ -142,19 +151,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
       bool ok = true;
       int local = 0;
-      for (int t = pair; ok && t < p.num_tiles; t += num_pairs, ++local) {
+      for (int u = pair; ok && u < units; u += num_pairs, ++local) {
+        int t, kb0, kb1;
+        pair_unit(p, u, t, kb0, kb1);
         int tb, tm, tn;
         batch_tile(p, t, tb, tm, tn);
         const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
         const int a_row = tm * kPairBM + 128 * static_cast<int>(rank);
         const int b_row = tn * kPairBN + 128 * static_cast<int>(rank);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
                             timeout_code(kRoleProducer, stage), true, peer_abort)) {
             ok = false;
             break;
           }
-          if (!(p.test_stall && local == 0 && kb == 0)) {
+          if (!(p.test_stall && local == 0 && kb == kb0)) {
             const uint32_t fb = full_pair0 + 8 * stage;
             const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t b_dst = a_dst + L::kABytes;
@@ -207,7 +218,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint32_t idesc = make_idesc_f16(kPairBM, kPairBN, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+      for (int u = pair; ok && u < units; u += num_pairs) {
+        int t, kb0, kb1;
+        pair_unit(p, u, t, kb0, kb1);
         if (!wait_bounded<true>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
                                 timeout_code(kRoleMma, 0x200 + acc), true, peer_abort)) {
           ok = false;
@@ -215,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kPairBN;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded<true>(full0 + 8 * stage, phase, abort_flag, p.timeout_ns,
                                   timeout_code(kRoleMma, stage), true, peer_abort)) {
             ok = false;
@@ -234,7 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                                        : make_sw128_desc(as + kk * 32, 16, 1024);
             const uint64_t bd = p.b_mn ? make_sw128_desc(bs + kk * 2048, 8192, 1024)
                                        : make_sw128_desc(bs + kk * 32, 16, 1024);
-            mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            mma_f16_pair(d_tmem, ad, bd, idesc, (kb != kb0) || (k != 0));
           }
           mma_commit_pair_mc(empty0 + 8 * stage, 0x3);  // free the stage in both CTAs
           if (++stage == kPairStages) {
@@ -269,7 +282,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
-    for (int t = pair; t < p.num_tiles; t += num_pairs) {
+    for (int u = pair; u < units; u += num_pairs) {
+      int t, kb0, kb1;
+      pair_unit(p, u, t, kb0, kb1);
+      if (p.ks_splits > 1) {
+        // K-split unit: this warp's 32 x 128 of the fp32 partial, stored as
+        // part of 128-row tile 2t + rank (the reduction's view of the pair
+        // tile), split u - t * ks_splits
+        if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
+                          timeout_code(kRoleEpilogue, acc), true, peer_abort))
+          break;
+        tc_fence_after();
+        const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN + col0;
+        const int64_t ur = (2 * static_cast<int64_t>(t) + rank) * p.ks_splits + (u - t * p.ks_splits);
+        float4* ws4 = reinterpret_cast<float4*>(p.ks_ws);
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
+          tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+          tmem_wait_ld();
+          if (c == kChunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
+          }
+          const int gc = col0 / 64 + c;  // chunk of the tile row
+#pragma unroll
+          for (int g = 0; g < 16; ++g)
+            ws4[ks_partial_index(ur, kPairBN, static_cast<int>(quad), gc, g, static_cast<int>(lane))] =
+                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;

@@ -453,6 +453,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Automatic K split of the CTA-pair kernel for problems with few 256 x 256
+// tiles and long K loops: s splits of at least 4096 of K each, as many as
+// keep the units within the pairs, taken only when the units then fill at
+// least half the pairs (fp32 accumulation, M and N above 128).  Measured
+// with an L2 flush per call, against the automatic choice before it
+// (128-row tiles, with their own K split when few): 1024^2 x 16384 51.2 ->
+// 42.8 us, 512 x 2048 x 16384 52.3 -> 45.1, 1024 x 2048 x 8192 42.6 ->
+// 40.0, 512 x 4096 x 8192 45.1 -> 43.1; with shorter K per split, or fewer
+// units, the 128-row kernel stayed ahead (512^2 x 8192: 20.5 against 22.6
+// at best).  Returns 1 for no split.
+int pair_split_count(int64_t M, int64_t N, int64_t K, int64_t pair_tiles, int accum,
+                     const DeviceState& st) {
+  if (accum != GEMM_TN_ACC_F32 || M <= kLargeBM || N <= 128 || st.max_pairs <= 0 ||
+      pair_tiles <= 0)
+    return 1;
+  const int64_t s = std::min<int64_t>(st.max_pairs / pair_tiles, K / 4096);
+  if (s < 2 || 2 * pair_tiles * s < st.max_pairs) return 1;
+  return static_cast<int>(s);
+}
+
 int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
                  const DeviceState& st) {
   const int64_t M = q.M, N = q.N, K = q.K;
@@ -472,7 +492,10 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     // tiles when a side is too short for 256, and 128 x 128 tiles when even
     // 128 x 256 tiles would leave half the SMs idle.
     const int64_t tiles_128x256 = ((M + 127) / 128) * ((N + 255) / 256) * q.L;
-    if (2 * tiles_128x256 <= st.num_sms) {
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
+    if (pair_split_count(M, N, K, pair_tiles, accum, st) > 1) {
+      kind = 2;  // few pair tiles with long K loops: the pair kernel with a K split
+    } else if (2 * tiles_128x256 <= st.num_sms) {
       kind = 1;
       if (tile_n == 0) tile_n = 128;
     } else if (M > kLargeBM && N > 128) {
@@ -589,12 +612,62 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
       return GEMM_TN_ERR_CUDA;
     }
   } else if (pair) {
-    const int pairs = std::min(p.num_tiles, st.max_pairs);
-    const cudaError_t le =
+    // K split of the pair tiles (fp32 accumulation only): on request
+    // (split_k with tile_kernel 2), or chosen by pair_split_count when the
+    // kernel was chosen automatically.  Each unit stores its CTAs' fp32 partial
+    // rows as two 128-row tiles; gemm_tn_tile_reduce_kernel adds the splits
+    // in order and applies the epilogue.
+    int splits = 1;
+    if (!p.acc_f16 && o.tile_kernel == 2 && o.split_k > 0)
+      splits = o.split_k;
+    else if (o.tile_kernel == 0 && o.split_k == 0)
+      splits = pair_split_count(M, N, K, p.num_tiles, accum, st);
+    splits = std::max(1, std::min(splits, p.k_blocks));
+    void* ks_ws = nullptr;
+    if (splits > 1) {
+      p.ks_kb_per = (p.k_blocks + splits - 1) / splits;
+      p.ks_splits = (p.k_blocks + p.ks_kb_per - 1) / p.ks_kb_per;  // no empty split
+      const size_t bytes =
+          static_cast<size_t>(p.num_tiles) * 2 * p.ks_splits * kLargeBM * kPairBN * 4;
+      if (static_cast<int64_t>(p.num_tiles) * 2 * p.ks_splits > 0x7FFFFFFF ||
+          ws_alloc(&ks_ws, bytes, st, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_TN_ERR_NO_MEMORY;
+      }
+      p.ks_ws = static_cast<float*>(ks_ws);
+    }
+    const int pairs = static_cast<int>(
+        std::min<int64_t>(static_cast<int64_t>(p.num_tiles) * p.ks_splits, st.max_pairs));
+    cudaError_t le =
         deep ? launch_pdl(gemm_tn_large2_kernel<true>, dim3(2 * pairs), dim3(kPairThreads),
                           PairSmem<true>::kDynamicBytes, stream, tmA, tmB, tmD, p)
              : launch_pdl(gemm_tn_large2_kernel<false>, dim3(2 * pairs), dim3(kPairThreads),
                           PairSmem<false>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    if (ks_ws) {
+      if (le == cudaSuccess) {
+        // The reduction sees pair tile t as 128-row tiles 2t and 2t+1: twice
+        // the row tiles and twice the raster group, which keeps that
+        // numbering (tile_coords maps 2t + r to rows 2 tm + r of column tn).
+        LargeArgs pr = p;
+        pr.tiles_m = 2 * p.tiles_m;
+        pr.group_m = 2 * p.group_m;
+        pr.tiles_per_batch = 2 * p.tiles_per_batch;
+        pr.num_tiles = 2 * p.num_tiles;
+        const dim3 rgrid(static_cast<unsigned>(4 * (kPairBN / 64)),
+                         static_cast<unsigned>(pr.num_tiles));
+        le = launch_pdl(gemm_tn_tile_reduce_kernel<kPairBN>, rgrid, dim3(kTileReduceThreads), 0,
+                        stream, pr);
+      }
+      const cudaError_t f = cudaFreeAsync(ks_ws, stream);
+      if (le != cudaSuccess || f != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_TN_ERR_CUDA;
+      }
+      t_last_launches = 2;
+      t_last_kernels = deep ? "gemm_tn_large2_kernel<deep>+gemm_tn_tile_reduce_kernel"
+                            : "gemm_tn_large2_kernel+gemm_tn_tile_reduce_kernel";
+      return GEMM_TN_OK;
+    }
     if (le != cudaSuccess) {
       cudaGetLastError();
       return GEMM_TN_ERR_CUDA;

@@ -129,11 +129,12 @@ typedef struct {
   int split_k;          /* skinny path: at most this many CTAs share the K
                            loops of the output tiles, in ranges of equal
                            length (0 = one per SM).  Large path
-                           with tile_kernel 1: K splits per 128-row tile,
-                           fp32 accumulation only (0 = none; with
+                           with tile_kernel 1: K splits per 128-row tile;
+                           with tile_kernel 2: K splits per 256 x 256 pair
+                           tile; fp32 accumulation only (0 = none; with
                            tile_kernel 0 the library splits by itself when
                            the tiles would leave more than half the SMs
-                           idle and K >= 2048) */
+                           idle and K is long enough) */
   int tile_n;           /* large path, 128-row tiles: output tile width, 128
                            or 256 (0: the library's choice -- 128 when N <=
                            128 or when 128 x 256 tiles would leave half the
@@ -148,7 +149,9 @@ typedef struct {
                            consumer's bounded wait expires and the kernel
                            reports GEMM_TN_ERR_DEVICE_TIMEOUT instead of
                            hanging */
-  int tile_kernel;      /* large path: 0 = choose (1 with 128 x 128 tiles
+  int tile_kernel;      /* large path: 0 = choose (2 with a K split when
+                           few 256 x 256 tiles have K loops of at least
+                           2 x 4096; else 1 with 128 x 128 tiles
                            when 128 x 256 tiles would fill at most half the
                            SMs; else, when M and N exceed 128, 3 if
                            M*N*K*batch >= 2^39, K > 1024 and the 256 x 256

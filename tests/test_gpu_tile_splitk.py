@@ -125,3 +125,54 @@ def test_split_timeout_reports_and_recovers():
     got, d64, d16, k = run(M, N, K, 1, 1.0, 1.0, seed=6)
     assert k == SPLIT
     check(got, d64, d16, K, 0, True, "after timeout")
+
+
+# --- the same K split in the CTA-pair kernel (split_k with tile_kernel 2):
+# each unit stores its two CTAs' rows as two 128-row partial tiles, and the
+# same reduction adds the splits in order.
+
+PAIR_SPLIT = "gemm_tn_large2_kernel{}+gemm_tn_tile_reduce_kernel"
+
+
+@pytest.mark.parametrize("M,N,K,L,am,bm,splits,deep", [
+    (300, 520, 3000, 1, 0, 0, 3, True),     # K-major rows on the 128-byte grid: deep stages
+    (500, 260, 2500, 1, 0, 0, 2, False),    # ld 2512: 64-deep stages
+    (256, 2048, 4088, 1, 0, 0, 2, True),
+    (300, 300, 2000, 1, 1, 1, 3, True),     # both operands M/N-major
+    (130, 700, 1100, 1, 1, 0, 5, False),    # splits of 3-4 K blocks of 64; last split short
+])
+def test_pair_split_integers_bit_exact(M, N, K, L, am, bm, splits, deep):
+    got, d64, d16, k = run(M, N, K, L, 1.0, 1.0, seed=10 + splits, am=am, bm=bm,
+                           opts=dict(path=gb.PATH_LARGE, tile_kernel=2, split_k=splits))
+    assert k == PAIR_SPLIT.format("<deep>" if deep else ""), k
+    check(got, d64, d16, K, 0, True, f"pair split {M}x{N}x{K} s={splits}")
+
+
+def test_pair_split_batched_scalars_and_determinism():
+    o = dict(path=gb.PATH_LARGE, tile_kernel=2, split_k=4)
+    got, d64, d16, k = run(200, 300, 3000, 2, -2.0, 0.5, seed=20, opts=o)
+    assert k == PAIR_SPLIT.format("<deep>"), k
+    check(got, d64, d16, 3000, 0, True, "pair split batched")
+    a = run(520, 260, 3000, 1, 0.75, 0.0, dist="u11", cdist="u11", seed=21, opts=o)
+    b = run(520, 260, 3000, 1, 0.75, 0.0, dist="u11", cdist="u11", seed=21, opts=o)
+    assert np.array_equal(a[0], b[0])  # fixed summation order
+    check(a[0], a[1], a[2], 3000, 0, False, "pair split real")
+
+
+def test_pair_split_timeout_reports_and_recovers():
+    M, N, K = 512, 512, 8192
+    dev = torch.device("cuda")
+    A = wl.draw((M * K,), "int1", 910).to(dev)
+    B = wl.draw((N * K,), "int1", 911).to(dev)
+    C = wl.draw((M * N,), "int4", 912).to(dev)
+    D = torch.empty_like(C)
+    st = gb.gemm_tn_batched_ex(M, N, K, 1, 1.0, A.data_ptr(), K, 0, 0, B.data_ptr(), K, 0, 0, 1.0,
+                               C.data_ptr(), N, 0, D.data_ptr(), N, 0, 0,
+                               torch.cuda.current_stream().cuda_stream,
+                               dict(path=gb.PATH_LARGE, tile_kernel=2, split_k=2, test_stall=1,
+                                    timeout_ns=20_000_000, sync_check=1))
+    assert st == gb.ERR_DEVICE_TIMEOUT
+    got, d64, d16, k = run(M, N, K, 1, 1.0, 1.0, seed=22,
+                           opts=dict(path=gb.PATH_LARGE, tile_kernel=2, split_k=2))
+    assert k == PAIR_SPLIT.format(""), k  # ld 8200: 64-deep stages
+    check(got, d64, d16, K, 0, True, "pair split after timeout")
