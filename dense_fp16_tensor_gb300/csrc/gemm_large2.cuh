@@ -24,13 +24,17 @@
 //     last of its four boxes has landed, with no hop through the odd CTA.
 //     The MMA thread releases a stage in both CTAs with one multicast
 //     tcgen05.commit; accumulators are handed to both CTAs' epilogues the
-//     same way, and the eight epilogue warps of the pair return an
+//     same way, and the sixteen epilogue warps of the pair return an
 //     accumulator by arriving on the even CTA's `tmem_empty`.
 //   * Each CTA's epilogue is the staged one of gemm_large.cuh on its 128
 //     rows of the tile, with two accumulators so it overlaps the next
 //     tile's main loop; eight warps, two per TMEM lane quadrant, each drain
 //     one 128-column half, so that an accumulator is free again after two
 //     chunk times (with short K loops the drain, not the MMA, set the pace).
+//   * Work units are tiles, or with ks_splits > 1 (tile, K range) pairs
+//     (the make_tiled_mma page's K split across workers): a split unit's
+//     CTAs store their fp32 rows as 128-row partial tiles 2t and 2t + 1, and
+//     gemm_tn_tile_reduce_kernel adds the splits in order and C once.
 //
 // Every wait is bounded; a CTA that gives up raises its own and its peer's
 // abort flag, both drain what they issued, free the pair's TMEM and return.
