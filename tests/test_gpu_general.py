@@ -278,17 +278,19 @@ def test_batched_large_sampled_rows():
             check(got, d64, d16, K, 0, False, f"problem {l} rows {m0}..{m0 + rows}")
 
 
-@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "streamk", "tile_split"])
+@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "streamk", "tile_split",
+                                  "pair_split"])
 def test_graph_capture_replays_match_eager(case):
     """A call captured into a CUDA graph (after one eager call has set the
     library up) replays to the same bits as the eager call.  The tile-kernel
     and scale-only paths allocate nothing per call; the skinny path's
     workspace comes from the library's pool in stream order, which capture
     records as graph memory nodes."""
-    M, N, K, L = {"skinny": (16, 1000, 3000, 1),
-                  "tile_split": (300, 200, 4000, 1)}.get(case, (520, 392, 328, 2))
+    M, N, K, L = {"skinny": (16, 1000, 3000, 1), "tile_split": (300, 200, 4000, 1),
+                  "pair_split": (300, 520, 3000, 1)}.get(case, (520, 392, 328, 2))
     tile = {"wide": gb.TILE_WIDE, "single": gb.TILE_SINGLE, "scale": gb.TILE_WIDE,
-            "skinny": 0, "streamk": gb.TILE_WIDE, "tile_split": gb.TILE_SINGLE}[case]
+            "skinny": 0, "streamk": gb.TILE_WIDE, "tile_split": gb.TILE_SINGLE,
+            "pair_split": gb.TILE_PAIR}[case]
     path = gb.PATH_SKINNY if case == "skinny" else gb.PATH_LARGE
     alpha = 0.0 if case == "scale" else -2.0
     cs = Case(M, N, K, L, seed=20)
@@ -302,7 +304,7 @@ def test_graph_capture_replays_match_eager(case):
                                      cs.sC, D.data_ptr(), cs.ldD, cs.sD, 0, stream,
                                      dict(path=path, tile_kernel=tile,
                                           stream_k=1 if case == "streamk" else 0,
-                                          split_k=3 if case == "tile_split" else 0))
+                                          split_k=3 if case in ("tile_split", "pair_split") else 0))
     assert call(D_eager, torch.cuda.current_stream().cuda_stream) == gb.OK
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
