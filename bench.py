@@ -754,23 +754,27 @@ def bench_stream_k(dev, stream, steps=50, rounds=3):
 
 
 def bench_tile_split(dev, stream, steps=100):
-    """K split of the 128-row tile kernel on shapes whose tiles leave most SMs
-    idle: the tile path's automatic choice (split, with its reduction)
-    against the same kernel unsplit; fp32 accumulation.  (M = 256 with this
-    N would otherwise take the skinny path.)"""
+    """K split on shapes whose tiles leave most SMs idle: the tile path's
+    automatic choice (the 128-row kernel's split, or for 1024^2 x 16384 the
+    CTA pair's, with the reduction) against the same kernel unsplit; fp32
+    accumulation.  (M = 256 with this N would otherwise take the skinny
+    path.)"""
     import torch
 
     from dense_fp16_tensor_gb300 import binding as gb
     from dense_fp16_tensor_gb300 import workloads as wl
     out = {}
-    for M, N, K in ((512, 512, 8192), (256, 1024, 16384), (1024, 1024, 8192)):
+    for M, N, K, unsplit in ((512, 512, 8192, {"tile_kernel": 1, "tile_n": 128}),
+                             (256, 1024, 16384, {"tile_kernel": 1, "tile_n": 128}),
+                             (1024, 1024, 8192, {"tile_kernel": 1, "tile_n": 128}),
+                             (1024, 1024, 16384, {"tile_kernel": 2})):
         A = wl.draw((M * K,), "u11", 7301).to(dev)
         Bm = wl.draw((N * K,), "u11", 7302).to(dev)
         CD = torch.zeros(M * N, dtype=torch.float16, device=dev)
         sp = stream.cuda_stream
         row = {}
         for name, opts in (("split", {"path": gb.PATH_LARGE}),
-                           ("unsplit", {"path": gb.PATH_LARGE, "tile_kernel": 1, "tile_n": 128})):
+                           ("unsplit", dict(path=gb.PATH_LARGE, **unsplit))):
             def step():
                 st = gb.gemm_tn_ex(M, N, K, A.data_ptr(), K, 0, Bm.data_ptr(), K, 0, CD.data_ptr(),
                                    N, 0, sp, opts)
