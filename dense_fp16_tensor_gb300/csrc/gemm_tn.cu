@@ -485,10 +485,13 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   if (kind == 0) {
     // The CTA pair (256 x 256 per two SMs, double-buffered accumulators,
     // 128-deep stages) is the fastest kernel on everything but the largest
-    // problems; 256 x 256 tiles on one CTA (undoubled accumulator) do a few
-    // per cent more work per joule, which wins once a stream of such calls
-    // runs at the board's power limit: from M*N*K*L >= 2^39 (one 8192^3
-    // problem) with K > 1024 and enough tiles to fill half the SMs.  128-row
+    // problems with long K; 256 x 256 tiles on one CTA (undoubled
+    // accumulator) do a few per cent more work per joule, which wins once a
+    // stream of such calls runs at the board's power limit: from
+    // M*N*K*L >= 2^39 (one 8192^3 problem) with K >= 8192 and enough tiles to
+    // fill half the SMs.  With shorter K the drain of the undoubled
+    // accumulator costs more than that (16384^2 x 2048: 1317 against 1639
+    // TFLOP/s for the pair, 16384^2 x 4096: 1454 against 1709).  128-row
     // tiles when a side is too short for 256, and 128 x 128 tiles when even
     // 128 x 256 tiles would leave half the SMs idle.
     const int64_t tiles_128x256 = ((M + 127) / 128) * ((N + 255) / 256) * q.L;
@@ -501,7 +504,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     } else if (M > kLargeBM && N > 128) {
       const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
       const double mnkl = static_cast<double>(M) * N * K * q.L;
-      const bool wide_ok = K > 1024 && 2 * tiles256 >= st.num_sms && mnkl >= 549755813888.0;
+      const bool wide_ok = K >= 8192 && 2 * tiles256 >= st.num_sms && mnkl >= 549755813888.0;
       kind = wide_ok ? 3 : (st.max_pairs > 0 ? 2 : 1);
     } else {
       kind = 1;

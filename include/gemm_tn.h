@@ -154,7 +154,7 @@ typedef struct {
                            2 x 4096; else 1 with 128 x 128 tiles
                            when 128 x 256 tiles would fill at most half the
                            SMs; else, when M and N exceed 128, 3 if
-                           M*N*K*batch >= 2^39, K > 1024 and the 256 x 256
+                           M*N*K*batch >= 2^39, K >= 8192 and the 256 x 256
                            tiles of all problems fill at least half the SMs,
                            otherwise 2; else 1),
                            1 = single-CTA 128 x tile_n
