@@ -2,7 +2,8 @@
 oracle, bit for bit: sizes with ragged tails, both majors per operand,
 batches with gaps and shared operands, alpha / beta including 0, fp32 and
 fp16 accumulation, and every path control (automatic, each tile kernel,
-stream-K, explicit K splits, the skinny path).  Operands are integers in
+stream-K, explicit K splits of the 128-row and pair kernels, the skinny
+path).  Operands are integers in
 {-1, 0, 1} and C in {-4..4}, so every result is exact up to the final
 rounding, which both sides take once from the same value (fp16
 accumulation only where its partial sums stay within 2048).  Each case also
@@ -46,13 +47,16 @@ def draw_case(rng):
     alpha = float(rng.choice([1.0, 2.0, -1.0, 0.5, 0.0]))
     beta = float(rng.choice([1.0, 0.0, -0.5, 2.0]))
     opts = {}
-    mode = rng.choice(["auto", "tile1", "tile1_split", "pair", "wide", "wide_sk", "skinny"])
+    mode = rng.choice(["auto", "tile1", "tile1_split", "pair", "pair_split", "wide", "wide_sk",
+                       "skinny"])
     if mode == "tile1":
         opts = dict(path=gb.PATH_LARGE, tile_kernel=1, tile_n=int(rng.choice([128, 256])))
     elif mode == "tile1_split":
         opts = dict(path=gb.PATH_LARGE, tile_kernel=1, split_k=int(rng.integers(2, 5)))
     elif mode == "pair":
         opts = dict(path=gb.PATH_LARGE, tile_kernel=2)
+    elif mode == "pair_split":
+        opts = dict(path=gb.PATH_LARGE, tile_kernel=2, split_k=int(rng.integers(2, 6)))
     elif mode == "wide":
         opts = dict(path=gb.PATH_LARGE, tile_kernel=3)
     elif mode == "wide_sk":
