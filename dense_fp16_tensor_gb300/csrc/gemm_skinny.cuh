@@ -47,10 +47,18 @@ struct SkinnyArgs {
   int test_stall;
 };
 
+// 64-deep K sub-blocks per pipeline stage (and per unit of the K split):
+// two for MMA widths up to 64 -- 256 contiguous bytes of each B row per
+// stage -- and one above, where the A operand's share of a stage grows.
+__host__ __device__ constexpr int skinny_sub(int mp) { return mp <= 64 ? 2 : 1; }
+
 template <int STAGES, int MP>
 struct SkinnySmem {
-  static constexpr uint32_t kBBytes = kSkinnyBN * kSkinnyBK * 2;  // 16 KiB
-  static constexpr uint32_t kABytes = MP * kSkinnyBK * 2;         // MP rows of 128 B
+  static constexpr int kSub = skinny_sub(MP);
+  static constexpr uint32_t kBSub = kSkinnyBN * kSkinnyBK * 2;  // 16 KiB per sub-block
+  static constexpr uint32_t kASub = MP * kSkinnyBK * 2;         // MP rows of 128 B
+  static constexpr uint32_t kBBytes = kSub * kBSub;
+  static constexpr uint32_t kABytes = kSub * kASub;
   static constexpr uint32_t kStageBytes = kBBytes + kABytes;
   static constexpr uint32_t kBarOffset = STAGES * kStageBytes;
   static constexpr uint32_t kNumBars = 2 * STAGES + 5;
@@ -170,8 +178,13 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
             const uint32_t b_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t a_dst = b_dst + L::kBBytes;
             mbar_arrive_expect_tx(fb, L::kStageBytes);
-            tma_load_2d_hint(b_dst, &tmB, fb, kb * kSkinnyBK, tile * kSkinnyBN, stream);
-            tma_load_2d_hint(a_dst, &tmA, fb, kb * kSkinnyBK, 0, keep);
+#pragma unroll
+            for (int sub = 0; sub < L::kSub; ++sub) {
+              // a sub-block past K is zero-filled (and still counted)
+              const int k0 = (kb * L::kSub + sub) * kSkinnyBK;
+              tma_load_2d_hint(b_dst + sub * L::kBSub, &tmB, fb, k0, tile * kSkinnyBN, stream);
+              tma_load_2d_hint(a_dst + sub * L::kASub, &tmA, fb, k0, 0, keep);
+            }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -213,10 +226,12 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
           const uint32_t b_base = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t a_base = b_base + L::kBBytes;
 #pragma unroll
-          for (int k = 0; k < kSkinnyBK / 16; ++k) {
-            // MMA A operand = tile of B (128 x 16), MMA B operand = A (MP x 16)
-            const uint64_t bd = make_sw128_desc(b_base + k * 32, 16, 1024);
-            const uint64_t ad = make_sw128_desc(a_base + k * 32, 16, 1024);
+          for (int k = 0; k < L::kSub * kSkinnyBK / 16; ++k) {
+            // MMA A operand = tile of B (128 x 16), MMA B operand = A (MP x 16);
+            // 16-deep step k is step k % 4 of sub-block k / 4
+            const int sub = k >> 2, kk = k & 3;
+            const uint64_t bd = make_sw128_desc(b_base + sub * L::kBSub + kk * 32, 16, 1024);
+            const uint64_t ad = make_sw128_desc(a_base + sub * L::kASub + kk * 32, 16, 1024);
             mma_f16(d_tmem, bd, ad, idesc, (kb != kb0) || (k != 0));
           }
           mma_commit(empty0 + 8 * stage);

@@ -97,11 +97,12 @@ cudaError_t set_skinny_attr() {
                               SkinnySmem<STAGES, MP>::kDynamicBytes);
 }
 
-// Ring depth of the skinny kernel: 8 stages up to MP = 64 (16 KiB of B plus
-// at most 8 KiB of A each), 6 up to 128 (32 KiB), 5 at 192 (40 KiB) and 4
-// at 256 (48 KiB).
+// Ring depth of the skinny kernel: stages of two 64-deep sub-blocks up to
+// MP = 64 -- 5 of 36-40 KiB up to MP = 32, 4 of 44-48 KiB at 48 and 64 --
+// and of one sub-block above: 6 up to 128 (32 KiB), 5 at 192 (40 KiB) and
+// 4 at 256 (48 KiB).
 constexpr int skinny_stages(int mp) {
-  return mp <= 64 ? 8 : (mp <= 128 ? 6 : (mp <= 192 ? 5 : 4));
+  return mp <= 32 ? 5 : (mp <= 64 ? 4 : (mp <= 128 ? 6 : (mp <= 192 ? 5 : 4)));
 }
 
 // MMA width for M rows of A: M rounded up to 16 up to 64, then 96, 128, 192
@@ -790,7 +791,8 @@ int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& 
   p.K = static_cast<int>(K);
   p.mp = skinny_mp(M);
   p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
-  p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
+  p.k_blocks = static_cast<int>((K + kSkinnyBK * skinny_sub(p.mp) - 1) /
+                                 (kSkinnyBK * skinny_sub(p.mp)));
   p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
   // Ranges of ceil(units / CTAs) units; a range spans at most per / k_blocks
   // + 2 tiles.  Recomputing the grid from per drops CTAs left without work.
@@ -1056,7 +1058,8 @@ extern "C" GEMM_TN_API int gemm_tn_skinny_noalloc(int64_t M, int64_t N, int64_t 
   p.K = static_cast<int>(K);
   p.mp = skinny_mp(M);
   p.tiles = static_cast<int>((N + kSkinnyBN - 1) / kSkinnyBN);
-  p.k_blocks = static_cast<int>((K + kSkinnyBK - 1) / kSkinnyBK);
+  p.k_blocks = static_cast<int>((K + kSkinnyBK * skinny_sub(p.mp) - 1) /
+                                 (kSkinnyBK * skinny_sub(p.mp)));
   p.units = static_cast<int64_t>(p.tiles) * p.k_blocks;
   const int64_t want = std::min<int64_t>(st->num_sms, p.units);
   const int64_t per = (p.units + want - 1) / want;
