@@ -48,9 +48,10 @@ struct SkinnyArgs {
 };
 
 // 64-deep K sub-blocks per pipeline stage (and per unit of the K split):
-// two for MMA widths up to 64 -- 256 contiguous bytes of each B row per
-// stage -- and one above, where the A operand's share of a stage grows.
-__host__ __device__ constexpr int skinny_sub(int mp) { return mp <= 64 ? 2 : 1; }
+// two for MMA widths up to 128 -- 256 contiguous bytes of each B row per
+// stage -- and one above, where A's share of a stage would leave too few
+// stages.
+__host__ __device__ constexpr int skinny_sub(int mp) { return mp <= 128 ? 2 : 1; }
 
 template <int STAGES, int MP>
 struct SkinnySmem {

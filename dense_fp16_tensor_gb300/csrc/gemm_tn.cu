@@ -98,11 +98,11 @@ cudaError_t set_skinny_attr() {
 }
 
 // Ring depth of the skinny kernel: stages of two 64-deep sub-blocks up to
-// MP = 64 -- 5 of 36-40 KiB up to MP = 32, 4 of 44-48 KiB at 48 and 64 --
-// and of one sub-block above: 6 up to 128 (32 KiB), 5 at 192 (40 KiB) and
-// 4 at 256 (48 KiB).
+// MP = 128 -- 5 of 36-40 KiB up to MP = 32, 4 of 44-56 KiB up to 96, 3 of
+// 64 KiB at 128 -- and of one sub-block above: 5 at 192 (40 KiB) and 4 at
+// 256 (48 KiB).
 constexpr int skinny_stages(int mp) {
-  return mp <= 32 ? 5 : (mp <= 64 ? 4 : (mp <= 128 ? 6 : (mp <= 192 ? 5 : 4)));
+  return mp <= 32 ? 5 : (mp <= 64 ? 4 : (mp <= 96 ? 4 : (mp <= 128 ? 3 : (mp <= 192 ? 5 : 4))));
 }
 
 // MMA width for M rows of A: M rounded up to 16 up to 64, then 96, 128, 192
