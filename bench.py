@@ -59,7 +59,11 @@ def parse(argv=None):
     ap.add_argument("--workload", default="large")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the headline workload")
+    ap.add_argument("--all-extras", action="store_true",
+                    help="also time cuBLAS on the headline inputs, the strided route, "
+                         "stream-K, the scaled/batched form and the tile K splits")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stream-k", type=int, default=0,
                     help="256x256 kernel: 0 auto, 1 split any partial last wave, -1 never")
@@ -459,17 +463,21 @@ def run_ours(args):
                     "kernel": kernels_run, "peak_kind": peak_kind,
                     "algorithmic_bytes_per_launch": w.min_bytes}
 
+    # The other workloads of the parity set are timed by default (skinny M=16
+    # against HBM, tiny / square1024 / ragged against both rooflines); the
+    # remaining paths only with --all-extras, so that the line stays short.
     extra = {}
     if not args.no_extra and w.name != "skinny":
-        if w.name == "large":
-            extra["cublas_same_inputs"] = bench_cublas(dev, stream, w, A, Bm,
-                                                       steps=max(20, min(400, args.steps)))
         extra["skinny_m16"] = bench_skinny(dev, stream)
         extra["configs"] = bench_configs(dev, stream)
-        extra["strided_4096"] = bench_strided(dev, stream)
-        extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
-        extra["scaled_batched"] = bench_general(dev, stream)
-        extra["tile_split_k"] = bench_tile_split(dev, stream)
+        if args.all_extras:
+            if w.name == "large":
+                extra["cublas_same_inputs"] = bench_cublas(dev, stream, w, A, Bm,
+                                                           steps=max(20, min(400, args.steps)))
+            extra["strided_4096"] = bench_strided(dev, stream)
+            extra["stream_k_3072x4096x4096"] = bench_stream_k(dev, stream)
+            extra["scaled_batched"] = bench_general(dev, stream)
+            extra["tile_split_k"] = bench_tile_split(dev, stream)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -503,6 +511,10 @@ def run_ours(args):
         "kernel_ms": {"mean": kernel_ms, "min": min(per), "median": statistics.median(per)},
         "extra": extra,
     }
+    # last key on purpose: a short per-workload digest that survives when
+    # only the end of the line is kept
+    out["configs_summary"] = configs_summary(w, kernel_ms, kernels_run, roofline, extra,
+                                             peaks, peak_kind)
     print(json.dumps(out), flush=True)
     if ws > 1:
         dist.barrier()
@@ -608,11 +620,18 @@ def bench_skinny(dev, stream, steps=200):
 
 
 def bench_configs(dev, stream, steps=50):
-    """The other workloads of the parity set, each timed through gemm_tn on
-    its own layout: tiny (latency), square 1024^3 with fp16 accumulation and
-    ragged 4000x3000x2500 with an M-major A.  Their inputs fit in L2, so a
-    256 MiB buffer is written between calls and every call is timed on its
-    own with events (the flush is outside the timed spans)."""
+    """The other workloads of the parity set, each through gemm_tn on its own
+    layout: tiny (latency), square 1024^3 with fp16 accumulation and ragged
+    4000x3000x2500 with an M-major A.  Their inputs fit in L2, so they are
+    timed two ways:
+      isolated  a 256 MiB buffer is written between calls and every call is
+                timed on its own with events (the flush is outside the timed
+                spans): one cold call, launch latency included;
+      stream    calls back to back over enough copies of the inputs that
+                together exceed L2 (each call reads operands no earlier call
+                left in L2), timed as a block: per-call time when a stream
+                of such GEMMs runs (tiny is latency only and has no stream
+                figure)."""
     import torch
 
     from dense_fp16_tensor_gb300 import binding as gb
@@ -624,17 +643,20 @@ def bench_configs(dev, stream, steps=50):
     for name in ("tiny", "square1024", "ragged"):
         w = wl.WORKLOADS[name]
         A_st, B_st, C_st = wl.make_inputs(w)
-        A, Bm, CD = A_st.to(dev), B_st.to(dev), C_st.to(dev)
+        set_bytes = 2 * (A_st.numel() + B_st.numel() + C_st.numel())
+        nsets = 1 if name == "tiny" else max(2, -(-int(160e6) // set_bytes))
+        sets = [(A_st.to(dev), B_st.to(dev), C_st.to(dev)) for _ in range(nsets)]
         torch.cuda.synchronize()
 
-        def step():
+        def step(i=0):
+            A, Bm, CD = sets[i % nsets]
             st = gb.gemm_tn(w.M, w.N, w.K, A.data_ptr(), w.ldA, w.a_major, Bm.data_ptr(), w.ldB,
                             w.b_major, CD.data_ptr(), w.ldC, w.accum, sp)
             if st != gb.OK:
                 raise gb.GemmTnError(st)
         with torch.cuda.stream(stream):
-            for _ in range(5):
-                step()
+            for i in range(max(5, nsets)):
+                step(i)
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
@@ -646,20 +668,77 @@ def bench_configs(dev, stream, steps=50):
                 e1.record(stream)
         torch.cuda.synchronize()
         ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
-        tflops = w.flops / (ms * 1e-3) / 1e12
-        gbs = w.min_bytes / (ms * 1e-3) / 1e9
-        out[name] = {"M": w.M, "N": w.N, "K": w.K,
-                     "accumulate": "fp16" if w.accum == gb.ACC_F16 else "fp32",
-                     "a_major": "M" if w.a_major == gb.MAJOR_MN else "K",
-                     "us_per_call_median": ms * 1e3, "TFLOP_per_s": tflops,
-                     "frac_of_tensor_peak": tflops / float(peaks["bf16_tflops"]),
-                     "GB_per_s_algorithmic": gbs,
-                     "frac_of_hbm_peak": gbs / float(peaks["hbm_gbs"]),
-                     "kernels": gb.gemm_tn_last_kernels()}
-        del A, Bm, CD
-    out["l2"] = "256 MiB written between calls; each call timed alone (median of %d)" % steps
+        row = {"M": w.M, "N": w.N, "K": w.K,
+               "accumulate": "fp16" if w.accum == gb.ACC_F16 else "fp32",
+               "a_major": "M" if w.a_major == gb.MAJOR_MN else "K",
+               "kernels": gb.gemm_tn_last_kernels()}
+        row.update(_rates(w, ms, peaks, ""))
+        if nsets > 1:
+            calls = 10 * nsets
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for i in range(calls):
+                    step(i)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            row.update(_rates(w, e0.elapsed_time(e1) / calls, peaks, "stream_"))
+            row["stream_sets"] = nsets
+        out[name] = row
+        del sets
+    out["l2"] = ("isolated: 256 MiB written between calls, each call timed alone (median of "
+                 f"{steps}); stream: back to back over input copies totalling > 160 MB")
     out["peak_kind"] = kind
     return out
+
+
+def _rates(w, ms, peaks, prefix):
+    """Per-call time of workload w and its rates against both rooflines."""
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    gbs = w.min_bytes / (ms * 1e-3) / 1e9
+    return {prefix + "us_per_call": ms * 1e3, prefix + "TFLOP_per_s": tflops,
+            prefix + "frac_of_tensor_peak": tflops / float(peaks["bf16_tflops"]),
+            prefix + "GB_per_s_algorithmic": gbs,
+            prefix + "frac_of_hbm_peak": gbs / float(peaks["hbm_gbs"])}
+
+
+def _short(kernels: str) -> str:
+    """Kernel list without the common prefix and suffix."""
+    return "+".join(k.replace("gemm_tn_", "").replace("_kernel", "")
+                    for k in kernels.split("+") if k)
+
+
+def configs_summary(w, kernel_ms, kernels_run, roofline, extra, peaks, peak_kind):
+    """One short entry per workload of the parity set: time per call, the
+    rate against the roofline that bounds it, its fraction, the kernels."""
+    r3 = lambda x: None if x is None else round(float(x), 3)  # noqa: E731
+    s = {"peaks": f"{peak_kind}: {float(peaks['bf16_tflops'])} TFLOP/s dense, "
+                  f"{float(peaks['hbm_gbs'])} GB/s copy"}
+    head = {"us": round(kernel_ms * 1e3, 1), roofline["unit"]: round(roofline["achieved"], 1),
+            "frac": r3(roofline["frac"]), "bound": roofline["bound"],
+            "kernel": _short(kernels_run)}
+    sk = extra.get("skinny_m16")
+    if sk:
+        s["skinny"] = {"us": round(sk["ms_per_call"] * 1e3, 1), "GB/s": round(sk["GB_per_s"], 1),
+                       "frac": r3(sk["frac"]), "bound": "hbm", "kernel": "skinny+splitk_reduce"}
+    cf = extra.get("configs", {})
+    for name, bound in (("tiny", "latency"), ("square1024", "tensor"), ("ragged", "tensor")):
+        c = cf.get(name)
+        if not c:
+            continue
+        e = {"us": round(c["us_per_call"], 1)}
+        if bound == "tensor":
+            e["TFLOP/s"] = round(c["TFLOP_per_s"], 1)
+            e["frac"] = r3(c["frac_of_tensor_peak"])
+            if "stream_us_per_call" in c:
+                e["stream_us"] = round(c["stream_us_per_call"], 1)
+                e["stream_frac"] = r3(c["stream_frac_of_tensor_peak"])
+        e["bound"] = bound
+        e["kernel"] = _short(c["kernels"])
+        s[name] = e
+    s[w.name] = head
+    return s
 
 
 def bench_strided(dev, stream, steps=20):

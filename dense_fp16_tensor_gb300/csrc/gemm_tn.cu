@@ -178,26 +178,39 @@ int device_setup(int dev, DeviceState*& st) {
     st->attrs_set = true;
   }
   if (resolve_encoder() != GEMM_TN_OK) return GEMM_TN_ERR_CUDA;
-  if (st->pool == nullptr) {
-    cudaMemPoolProps props;
-    std::memset(&props, 0, sizeof props);
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return GEMM_TN_ERR_CUDA;
-    uint64_t keep = kPoolKeepBytes;
-    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
-      cudaMemPoolDestroy(pool);
-      return GEMM_TN_ERR_CUDA;
-    }
-    st->pool = pool;
-  }
   return GEMM_TN_OK;
 }
 
-// Stream-ordered workspace from the device's library pool.
-cudaError_t ws_alloc(void** p, size_t bytes, const DeviceState& st, cudaStream_t stream) {
+// The device's workspace pool (under g_mu), created on the first call of an
+// entry point that may need a workspace.  The allocation-free entry point
+// never calls this.
+int pool_setup(int dev, DeviceState* st) {
+  if (st->pool != nullptr) return GEMM_TN_OK;
+  cudaMemPoolProps props;
+  std::memset(&props, 0, sizeof props);
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaMemPool_t pool = nullptr;
+  if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  uint64_t keep = kPoolKeepBytes;
+  if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+    cudaMemPoolDestroy(pool);
+    return GEMM_TN_ERR_CUDA;
+  }
+  st->pool = pool;
+  return GEMM_TN_OK;
+}
+
+// Stream-ordered workspace from the device's library pool.  With the
+// test-only `test_fail_alloc` option the request fails as an exhausted pool
+// would, before anything is enqueued.
+cudaError_t ws_alloc(void** p, size_t bytes, const DeviceState& st, cudaStream_t stream,
+                     const gemm_tn_options& o) {
+  if (o.test_fail_alloc) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
   return cudaMallocFromPoolAsync(p, bytes, st.pool, stream);
 }
 
@@ -588,7 +601,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
       const int max_segs = static_cast<int>(per / p.k_blocks + 2);
       const size_t part_bytes = static_cast<size_t>(G) * max_segs * kWideBM * kWideBN * 4;
       const size_t cnt_bytes = static_cast<size_t>(rem) * 8 * sizeof(int);
-      if (ws_alloc(&sk_ws, part_bytes + cnt_bytes, st, stream) == cudaSuccess) {
+      if (ws_alloc(&sk_ws, part_bytes + cnt_bytes, st, stream, o) == cudaSuccess) {
         int* counters = reinterpret_cast<int*>(static_cast<char*>(sk_ws) + part_bytes);
         if (cudaMemsetAsync(counters, 0, cnt_bytes, stream) == cudaSuccess) {
           p.sk_tile0 = full * G;
@@ -621,24 +634,31 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     // kernel was chosen automatically.  Each unit stores its CTAs' fp32 partial
     // rows as two 128-row tiles; gemm_tn_tile_reduce_kernel adds the splits
     // in order and applies the epilogue.
+    // A split the caller asked for fails with GEMM_TN_ERR_NO_MEMORY when its
+    // workspace cannot be had; one the library chose by itself falls back
+    // to the unsplit kernel.
     int splits = 1;
-    if (!p.acc_f16 && o.tile_kernel == 2 && o.split_k > 0)
+    const bool asked = !p.acc_f16 && o.tile_kernel == 2 && o.split_k > 0;
+    if (asked)
       splits = o.split_k;
     else if (o.tile_kernel == 0 && o.split_k == 0)
       splits = pair_split_count(M, N, K, p.num_tiles, accum, st);
     splits = std::max(1, std::min(splits, p.k_blocks));
     void* ks_ws = nullptr;
     if (splits > 1) {
-      p.ks_kb_per = (p.k_blocks + splits - 1) / splits;
-      p.ks_splits = (p.k_blocks + p.ks_kb_per - 1) / p.ks_kb_per;  // no empty split
-      const size_t bytes =
-          static_cast<size_t>(p.num_tiles) * 2 * p.ks_splits * kLargeBM * kPairBN * 4;
-      if (static_cast<int64_t>(p.num_tiles) * 2 * p.ks_splits > 0x7FFFFFFF ||
-          ws_alloc(&ks_ws, bytes, st, stream) != cudaSuccess) {
+      const int kb_per = (p.k_blocks + splits - 1) / splits;
+      const int nsplit = (p.k_blocks + kb_per - 1) / kb_per;  // no empty split
+      const size_t bytes = static_cast<size_t>(p.num_tiles) * 2 * nsplit * kLargeBM * kPairBN * 4;
+      if (static_cast<int64_t>(p.num_tiles) * 2 * nsplit > 0x7FFFFFFF ||
+          ws_alloc(&ks_ws, bytes, st, stream, o) != cudaSuccess) {
         cudaGetLastError();
-        return GEMM_TN_ERR_NO_MEMORY;
+        ks_ws = nullptr;
+        if (asked) return GEMM_TN_ERR_NO_MEMORY;
+      } else {
+        p.ks_kb_per = kb_per;
+        p.ks_splits = nsplit;
+        p.ks_ws = static_cast<float*>(ks_ws);
       }
-      p.ks_ws = static_cast<float*>(ks_ws);
     }
     const int pairs = static_cast<int>(
         std::min<int64_t>(static_cast<int64_t>(p.num_tiles) * p.ks_splits, st.max_pairs));
@@ -683,9 +703,12 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     // chosen automatically, its tiles leave more than half the SMs idle and
     // K is long enough (>= 2048, >= 512 per split) to pay for the partials
     // and the reduction.
+    // As for the pair kernel: a requested split needs its workspace, an
+    // automatic one falls back to the unsplit kernel without it.
     int splits = 1;
+    const bool asked = !p.acc_f16 && o.tile_kernel == 1 && o.split_k > 0;
     if (!p.acc_f16) {
-      if (o.tile_kernel == 1 && o.split_k > 0)
+      if (asked)
         splits = o.split_k;
       else if (o.tile_kernel == 0 && o.split_k == 0 && 2 * p.num_tiles <= st.num_sms &&
                kb64 >= 32)
@@ -694,15 +717,19 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     }
     void* ks_ws = nullptr;
     if (splits > 1) {
-      p.ks_kb_per = (p.k_blocks + splits - 1) / splits;
-      p.ks_splits = (p.k_blocks + p.ks_kb_per - 1) / p.ks_kb_per;  // no empty split
-      const size_t bytes = static_cast<size_t>(p.num_tiles) * p.ks_splits * kLargeBM * bn * 4;
-      if (static_cast<int64_t>(p.num_tiles) * p.ks_splits > 0x7FFFFFFF ||
-          ws_alloc(&ks_ws, bytes, st, stream) != cudaSuccess) {
+      const int kb_per = (p.k_blocks + splits - 1) / splits;
+      const int nsplit = (p.k_blocks + kb_per - 1) / kb_per;  // no empty split
+      const size_t bytes = static_cast<size_t>(p.num_tiles) * nsplit * kLargeBM * bn * 4;
+      if (static_cast<int64_t>(p.num_tiles) * nsplit > 0x7FFFFFFF ||
+          ws_alloc(&ks_ws, bytes, st, stream, o) != cudaSuccess) {
         cudaGetLastError();
-        return GEMM_TN_ERR_NO_MEMORY;
+        ks_ws = nullptr;
+        if (asked) return GEMM_TN_ERR_NO_MEMORY;
+      } else {
+        p.ks_kb_per = kb_per;
+        p.ks_splits = nsplit;
+        p.ks_ws = static_cast<float*>(ks_ws);
       }
-      p.ks_ws = static_cast<float*>(ks_ws);
     }
     const int grid = static_cast<int>(
         std::min<int64_t>(static_cast<int64_t>(p.num_tiles) * p.ks_splits, st.num_sms));
@@ -815,7 +842,7 @@ int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& 
   // Stream-ordered workspace: concurrent calls on different streams never
   // share it, and the pool keeps the memory for the next call.
   void* ws = nullptr;
-  if (ws_alloc(&ws, need, st, stream) != cudaSuccess) {
+  if (ws_alloc(&ws, need, st, stream, o) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_TN_ERR_NO_MEMORY;
   }
@@ -859,7 +886,8 @@ int device_state(DeviceState*& st) {
   if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess)
     return GEMM_TN_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
-  return device_setup(dev, st);
+  const int s = device_setup(dev, st);
+  return s == GEMM_TN_OK ? pool_setup(dev, st) : s;
 }
 
 // Every entry point but the strided and allocation-free ones ends here.
@@ -995,7 +1023,9 @@ GEMM_TN_API const char* gemm_tn_status_string(int status) {
 // gemm_tn_skinny_noalloc: the skinny path with its partial sums in a fixed
 // array compiled into the library, so that callers that cannot have device
 // memory allocated for them (see the header) can still use it.  Nothing here
-// calls cudaMalloc, cudaFree or any other allocating routine.
+// calls cudaMalloc, cudaFree or any other allocating routine, and it does not
+// create the workspace pool (device_setup only probes the device and sets
+// kernel attributes; pool_setup is left to the other entry points).
 
 static __device__ __align__(256) float
     g_noalloc_scratch[GEMM_TN_NOALLOC_SCRATCH_BYTES / sizeof(float)];
@@ -1181,7 +1211,7 @@ int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream
 int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t sAm,
                         int64_t sAk, const void* B, int64_t sBn, int64_t sBk, void* CD,
                         int64_t sCm, int64_t sCn, int accum, const DeviceState& st,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const gemm_tn_options& caller) {
   int a_major = 0, b_major = 0, c_major = 0;
   int64_t ldA = 0, ldB = 0, ldC = 0;
   const bool a_direct = tma_view(A, M, K, sAm, sAk, a_major, ldA);
@@ -1197,7 +1227,7 @@ int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   const size_t c_elems = c_direct ? 0 : static_cast<size_t>(M) * Np;
   const size_t total = (a_elems + b_elems + c_elems) * 2;
   void* ws = nullptr;
-  if (total > 0 && ws_alloc(&ws, total, st, stream) != cudaSuccess) {
+  if (total > 0 && ws_alloc(&ws, total, st, stream, caller) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_TN_ERR_NO_MEMORY;
   }
@@ -1226,6 +1256,8 @@ int strided_repack_path(int64_t M, int64_t N, int64_t K, const void* A, int64_t 
   if (e == cudaSuccess) {
     gemm_tn_options o;
     std::memset(&o, 0, sizeof o);
+    o.timeout_ns = caller.timeout_ns;
+    o.test_fail_alloc = caller.test_fail_alloc;
     const int path = plan(M, N, K, a_major, b_major, accum, GEMM_TN_PATH_AUTO);
     const Problem q =
         in_place_problem(M, N, K, Ause, ldA, a_major, Buse, ldB, b_major, Cuse, ldC, accum);
@@ -1303,6 +1335,7 @@ extern "C" GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K, c
   {
     std::lock_guard<std::mutex> lk(g_mu);
     s = device_setup(dev, st);
+    if (s == GEMM_TN_OK) s = pool_setup(dev, st);
   }
   if (s != GEMM_TN_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -1311,8 +1344,11 @@ extern "C" GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K, c
   // below ~2^24 multiply-adds the copy-producer kernel is as fast.
   const bool big = static_cast<double>(M) * N * K >= 16777216.0;
   if (route == GEMM_TN_PATH_STRIDED_REPACK || (route == GEMM_TN_PATH_AUTO && big)) {
+    gemm_tn_options o;
+    std::memset(&o, 0, sizeof o);
+    if (opts) o = *opts;
     s = strided_repack_path(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype, *st,
-                            cs);
+                            cs, o);
     if (s != GEMM_TN_ERR_NO_MEMORY || route == GEMM_TN_PATH_STRIDED_REPACK) return s;
     // pool exhausted: the copy producer needs no workspace
   }

@@ -39,12 +39,17 @@
  * Ownership: the caller owns A, B, C and D (device memory); the library never
  * frees or retains caller memory.  Workspaces (the skinny path's split-K
  * partial sums, stream-K partial tiles, repacked strided operands) come from
- * a memory pool the library creates for each device on first use: taken with
- * cudaMallocFromPoolAsync on the call's stream and returned with
- * cudaFreeAsync on the same stream, so calls on different streams never
- * share them.  The pool keeps up to 1 GiB cached between calls and lives
- * until process exit (see gemm_tn_skinny_noalloc for a variant that
- * allocates nothing).
+ * a memory pool the library creates for each device on the first call of
+ * an entry point that may need one: taken with cudaMallocFromPoolAsync on
+ * the call's stream and returned with cudaFreeAsync on the same stream, so
+ * calls on different streams never share them.  The pool keeps up to 1 GiB
+ * cached between calls and lives until process exit (see
+ * gemm_tn_skinny_noalloc for a variant that neither allocates nor creates
+ * the pool).  When the pool cannot serve a request, a workspace the caller
+ * asked for (the skinny path, an explicit K split, the forced repack route)
+ * makes the call return GEMM_TN_ERR_NO_MEMORY with nothing enqueued; one
+ * the library chose by itself (an automatic K split, stream-K, the
+ * automatic repack route) is dropped and the call runs without it.
  *
  * Graphs: the first call on a device sets the library up (kernel attributes,
  * the workspace pool); after that, calls can be recorded by stream capture
@@ -172,6 +177,16 @@ typedef struct {
                            saved on every shape measured.  The split needs a
                            workspace from the library's pool; without one
                            the call runs unsplit. */
+  int test_fail_alloc;  /* TEST ONLY: nonzero makes every workspace request
+                           of this call fail as an exhausted pool would, so
+                           that the handling of that case can be checked:
+                           the skinny path and an explicitly requested K
+                           split (split_k with tile_kernel 1 or 2) return
+                           GEMM_TN_ERR_NO_MEMORY with nothing enqueued; a K
+                           split or stream-K the library would choose runs
+                           the unsplit kernel instead; gemm_tn_strided_ex
+                           falls back to the copy producer unless the
+                           repack route was forced. */
 } gemm_tn_options;
 
 /*
@@ -367,9 +382,13 @@ GEMM_TN_API const char* gemm_tn_status_string(int status);
  *     partial-sum scratch than GEMM_TN_NOALLOC_SCRATCH_BYTES (the need is
  *     (SMs) x (tiles one CTA touches) x 128 x round_up(M,16) x 4 bytes; the
  *     M=16, N=K=16384 problem needs about 2.5 MiB);
- *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture on that device;
+ *   - the first call on each device sets the library up there (reads the
+ *     device's attributes, raises the kernels' shared-memory limits, looks
+ *     up the driver's tensor-map encoder) and looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current); none of
+ *     this allocates device memory, and unlike the other entry points this
+ *     one never creates the library's workspace pool.  Make that first call
+ *     before any stream capture on that device;
  *   - every call on a device shares the one array, and the array keeps
  *     whatever the last call left in it.  Nothing in it needs to start at
  *     zero (each partial sum is written before it is read within a call),
