@@ -80,17 +80,31 @@ struct LargeArgs {
   float* ks_ws;
 };
 
+// Epilogue warps of the 128 x BN kernel: two per TMEM lane quadrant, each
+// draining one half of the tile's columns, for BN >= 128; one per quadrant
+// over all 64 columns for BN = 64.
+template <int BN>
+struct LargeEpi {
+  static constexpr int kWarps = BN >= 128 ? 8 : 4;
+  static constexpr int kColsPerWarp = BN >= 128 ? BN / 2 : BN;
+  static constexpr int kChunks = kColsPerWarp / 64;  // 64-column chunks per warp
+  static_assert(BN == 64 || BN == 128 || BN == 256, "tile widths 64, 128 and 256");
+};
+
 template <int BN, bool KO = false>
 struct LargeSmem {
-  static_assert(!KO || BN == 128, "K-chunk boxes only with 128 x 128 tiles");
+  static_assert(!KO || BN <= 128, "K-chunk boxes only with 128 x 128 and 128 x 64 tiles");
   static constexpr int kBK = KO ? 128 : kLargeBK;    // K per stage
-  static constexpr int kStages = KO ? 3 : 4;
+  // 3 stages of 64 KiB (KO, 128 wide), 4 of 48 KiB (KO, 64 wide), 4 of 48 /
+  // 32 KiB (256 / 128 wide), 6 of 24 KiB (64 wide)
+  static constexpr int kStages = KO ? (BN == 64 ? 4 : 3) : (BN == 64 ? 6 : 4);
   static constexpr uint32_t kABytes = kLargeBM * kBK * 2;  // 16 / 32 KiB
-  static constexpr uint32_t kBBytes = BN * kBK * 2;        // 16 / 32 KiB
+  static constexpr uint32_t kBBytes = BN * kBK * 2;        // 8 - 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // epilogue staging: 8 warps x 32 rows x 64 fp16 (1024-aligned)
+  // epilogue staging: one buffer of 32 rows x 64 fp16 per epilogue warp
+  // (1024-aligned)
   static constexpr uint32_t kStagingOffset = kStages * kStageBytes;
-  static constexpr uint32_t kBarOffset = kStagingOffset + 8 * 32 * 128;
+  static constexpr uint32_t kBarOffset = kStagingOffset + LargeEpi<BN>::kWarps * 32 * 128;
   // full[S], empty[S], tmem_full[2], tmem_empty[2], drain
   static constexpr uint32_t kNumBars = 2 * kStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 8);  // one arrival per epilogue warp
+      mbar_init(tempty0 + 8 * a, LargeEpi<BN>::kWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0u;
@@ -423,16 +437,19 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     const int ew = warp - 2;                                // 0..7
     const int half = ew >> 2;                               // column half of the tile
     const int row0 = static_cast<int>(quad * 32);            // first tile row of this warp
-    constexpr int kChunks = BN / 128;                        // 64-column chunks per warp
-    const int col0 = half * (BN / 2);                        // first tile column of this warp
-    uint8_t* stg = smem + L::kStagingOffset + ew * kStagingBytes;
+    using E = LargeEpi<BN>;
+    constexpr int kChunks = E::kChunks;                      // 64-column chunks per warp
+    const int col0 = half * E::kColsPerWarp;                 // first tile column of this warp
+    // with 64-wide tiles the second warp of each quadrant has no columns
+    const bool epi_active = ew < E::kWarps;
+    uint8_t* stg = smem + L::kStagingOffset + (epi_active ? ew : 0) * kStagingBytes;
     const uint32_t stg_u32 = smem_u32(stg);
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
-    const int units = p.num_tiles * p.ks_splits;
+    const int units = epi_active ? p.num_tiles * p.ks_splits : 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       if (p.ks_splits > 1) {
-        // split-K unit: this warp's 32 x BN/2 of the fp32 partial tile -> ks_ws
+        // split-K unit: this warp's 32 rows x kColsPerWarp of the fp32 partial tile -> ks_ws
         if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                           timeout_code(kRoleEpilogue, acc)))
           break;

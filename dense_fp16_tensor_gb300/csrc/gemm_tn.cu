@@ -133,6 +133,14 @@ int device_setup(int dev, DeviceState*& st) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          LargeSmem<256>::kDynamicBytes);
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_large_kernel<64>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               LargeSmem<64>::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_large_kernel<64, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               LargeSmem<64, true>::kDynamicBytes);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_tn_large_kernel<128>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                LargeSmem<128>::kDynamicBytes);
@@ -514,7 +522,12 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
       kind = 2;  // few pair tiles with long K loops: the pair kernel with a K split
     } else if (2 * tiles_128x256 <= st.num_sms) {
       kind = 1;
-      if (tile_n == 0) tile_n = 128;
+      // 128 x 64 tiles when even 128 x 128 tiles would leave more than half
+      // the SMs idle and no K split will spread the work instead (fp16
+      // accumulation is never split; fp32 only from K = 2048 on)
+      const int64_t tiles_128x128 = ((M + 127) / 128) * ((N + 127) / 128) * q.L;
+      const bool no_split = accum == GEMM_TN_ACC_F16 || K < 2048;
+      if (tile_n == 0) tile_n = (2 * tiles_128x128 <= st.num_sms && no_split) ? 64 : 128;
     } else if (M > kLargeBM && N > 128) {
       const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
       const double mnkl = static_cast<double>(M) * N * K * q.L;
@@ -527,7 +540,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   }
   if (kind == 2 && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
   const bool pair = kind == 2, wide = kind == 3;
-  const int bn = (pair || wide) ? 256 : ((tile_n == 128) ? 128 : 256);
+  const int bn = (pair || wide) ? 256 : (tile_n == 64 || tile_n == 128) ? tile_n : 256;
   const int bm = (pair || wide) ? 256 : kLargeBM;
   // K-chunk boxes (stages of 128 of K) for 128 x 128 tiles when both
   // operands are K-major and K is a multiple of 64, from K = 1024 on
@@ -537,7 +550,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   // at K = 1024, and 5-17 % faster than 64-deep stages at 8192^3 with an
   // M-major A), unless a K-major operand's rows are not 128-byte aligned
   // (3-5 % slower there than 64-deep stages).
-  const bool ko = kind == 1 && bn == 128 && a_major == GEMM_TN_MAJOR_K &&
+  const bool ko = kind == 1 && bn <= 128 && a_major == GEMM_TN_MAJOR_K &&
                   b_major == GEMM_TN_MAJOR_K && K % 64 == 0 && K >= 1024;
   const bool deep = ko || (pair && K >= 1024 && (a_major == GEMM_TN_MAJOR_MN || q.ldA % 64 == 0) &&
                            (b_major == GEMM_TN_MAJOR_MN || q.ldB % 64 == 0));
@@ -545,7 +558,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   int s;
   if (ko) {
     s = encode_operand_ko(&tmA, q.A, M, K, q.ldA, q.sA, q.L, 128);
-    if (s == GEMM_TN_OK) s = encode_operand_ko(&tmB, q.B, N, K, q.ldB, q.sB, q.L, 128);
+    if (s == GEMM_TN_OK)
+      s = encode_operand_ko(&tmB, q.B, N, K, q.ldB, q.sB, q.L, static_cast<uint32_t>(bn));
   } else {
     s = encode_operand_batched(&tmA, q.A, M, K, q.ldA, q.sA, q.L, a_major, wide ? 256 : kLargeBM);
     if (s == GEMM_TN_OK)
@@ -737,12 +751,18 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     if (bn == 256)
       le = launch_pdl(gemm_tn_large_kernel<256>, dim3(grid), dim3(kLargeThreads),
                       LargeSmem<256>::kDynamicBytes, stream, tmA, tmB, tmD, p);
-    else if (ko)
+    else if (bn == 128 && ko)
       le = launch_pdl(gemm_tn_large_kernel<128, true>, dim3(grid), dim3(kLargeThreads),
                       LargeSmem<128, true>::kDynamicBytes, stream, tmA, tmB, tmD, p);
-    else
+    else if (bn == 128)
       le = launch_pdl(gemm_tn_large_kernel<128>, dim3(grid), dim3(kLargeThreads),
                       LargeSmem<128>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    else if (ko)
+      le = launch_pdl(gemm_tn_large_kernel<64, true>, dim3(grid), dim3(kLargeThreads),
+                      LargeSmem<64, true>::kDynamicBytes, stream, tmA, tmB, tmD, p);
+    else
+      le = launch_pdl(gemm_tn_large_kernel<64>, dim3(grid), dim3(kLargeThreads),
+                      LargeSmem<64>::kDynamicBytes, stream, tmA, tmB, tmD, p);
     if (le != cudaSuccess && !ks_ws) {
       cudaGetLastError();
       return GEMM_TN_ERR_CUDA;
@@ -753,10 +773,12 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
         // the reduction: resident early, it waits in griddepcontrol.wait for
         // the split kernel's partials
         const dim3 rgrid(static_cast<unsigned>(4 * (bn / 64)), static_cast<unsigned>(p.num_tiles));
-        e = bn == 256 ? launch_pdl(gemm_tn_tile_reduce_kernel<256>, rgrid,
-                                   dim3(kTileReduceThreads), 0, stream, p)
-                      : launch_pdl(gemm_tn_tile_reduce_kernel<128>, rgrid,
-                                   dim3(kTileReduceThreads), 0, stream, p);
+        e = bn == 256   ? launch_pdl(gemm_tn_tile_reduce_kernel<256>, rgrid,
+                                     dim3(kTileReduceThreads), 0, stream, p)
+            : bn == 128 ? launch_pdl(gemm_tn_tile_reduce_kernel<128>, rgrid,
+                                     dim3(kTileReduceThreads), 0, stream, p)
+                        : launch_pdl(gemm_tn_tile_reduce_kernel<64>, rgrid,
+                                     dim3(kTileReduceThreads), 0, stream, p);
       }
       const cudaError_t f = cudaFreeAsync(ks_ws, stream);
       if (e != cudaSuccess || f != cudaSuccess) {
@@ -764,8 +786,9 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
         return GEMM_TN_ERR_CUDA;
       }
       t_last_launches = 2;
-      t_last_kernels = bn == 256 ? "gemm_tn_large_kernel<256>+gemm_tn_tile_reduce_kernel"
-                                 : "gemm_tn_large_kernel<128>+gemm_tn_tile_reduce_kernel";
+      t_last_kernels = bn == 256   ? "gemm_tn_large_kernel<256>+gemm_tn_tile_reduce_kernel"
+                       : bn == 128 ? "gemm_tn_large_kernel<128>+gemm_tn_tile_reduce_kernel"
+                                   : "gemm_tn_large_kernel<64>+gemm_tn_tile_reduce_kernel";
       return GEMM_TN_OK;
     }
   }
@@ -773,7 +796,9 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   t_last_launches = sk_ws ? 2 : 1;  // the counters' memset counts as a launch
   t_last_kernels = wide ? (sk_ws ? "memset+gemm_tn_wide_kernel" : "gemm_tn_wide_kernel")
                  : pair ? (deep ? "gemm_tn_large2_kernel<deep>" : "gemm_tn_large2_kernel")
-                        : (bn == 256 ? "gemm_tn_large_kernel<256>" : "gemm_tn_large_kernel<128>");
+                        : (bn == 256   ? "gemm_tn_large_kernel<256>"
+                           : bn == 128 ? "gemm_tn_large_kernel<128>"
+                                       : "gemm_tn_large_kernel<64>");
   return GEMM_TN_OK;
 }
 
@@ -874,7 +899,8 @@ int launch_scale(const Problem& q, cudaStream_t stream, const DeviceState& st) {
 
 bool options_ok(const gemm_tn_options& o) {
   return !(o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
-           (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) || o.tile_kernel < 0 ||
+           (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) ||
+           o.tile_kernel < 0 ||
            o.tile_kernel > 3);
 }
 

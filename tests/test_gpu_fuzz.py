@@ -50,7 +50,7 @@ def draw_case(rng):
     mode = rng.choice(["auto", "tile1", "tile1_split", "pair", "pair_split", "wide", "wide_sk",
                        "skinny"])
     if mode == "tile1":
-        opts = dict(path=gb.PATH_LARGE, tile_kernel=1, tile_n=int(rng.choice([128, 256])))
+        opts = dict(path=gb.PATH_LARGE, tile_kernel=1, tile_n=int(rng.choice([64, 128, 256])))
     elif mode == "tile1_split":
         opts = dict(path=gb.PATH_LARGE, tile_kernel=1, split_k=int(rng.integers(2, 5)))
     elif mode == "pair":

@@ -105,17 +105,18 @@ def test_large_8192_sampled_and_full():
 SWEEP = [1, 15, 16, 17, 63, 127, 129, 200]
 
 
-KERNEL_NAMES = {1: "gemm_tn_large_kernel<256>", 2: "gemm_tn_large2_kernel",
-                3: "gemm_tn_wide_kernel"}  # (shapes here are too small for stream-K)
+KERNEL_NAMES = {(1, 0): "gemm_tn_large_kernel<256>", (1, 128): "gemm_tn_large_kernel<128>",
+                (1, 64): "gemm_tn_large_kernel<64>", (2, 0): "gemm_tn_large2_kernel",
+                (3, 0): "gemm_tn_wide_kernel"}  # (shapes here are too small for stream-K)
 
 
-@pytest.mark.parametrize("tile_kernel", [1, 2, 3])
+@pytest.mark.parametrize("tile_kernel,tile_n", list(KERNEL_NAMES))
 @pytest.mark.parametrize("accum", [0, 1])
 @pytest.mark.parametrize("a_major,b_major", [(0, 0), (1, 0), (0, 1), (1, 1)])
-def test_ragged_sweep(accum, a_major, b_major, tile_kernel):
+def test_ragged_sweep(accum, a_major, b_major, tile_kernel, tile_n):
     """Tails in M, N and K across both majors and every tile kernel (single
-    CTA 128x256, CTA pair 256x256, single CTA 256x256), integer values:
-    bit-exact."""
+    CTA 128x256, 128x128 and 128x64, CTA pair 256x256, single CTA 256x256),
+    integer values: bit-exact."""
     rng = np.random.default_rng(100 + 10 * accum + 2 * a_major + b_major)
     cases = [(M, N, K) for M in (1, 17, 129, 200) for N in (1, 16, 129, 300)
              for K in (1, 15, 64, 129)]
@@ -129,10 +130,11 @@ def test_ragged_sweep(accum, a_major, b_major, tile_kernel):
         # NaN in C's slack: the kernels must neither read it nor write it
         C_st = wl.operand(M, N, ldC, 0, "int4", int(rng.integers(1 << 30)))
         D_st, st = run_gpu(M, N, K, A_st, ldA, a_major, B_st, ldB, b_major, C_st, ldC, accum,
-                           opts={"path": gb.PATH_LARGE, "tile_kernel": tile_kernel},
+                           opts={"path": gb.PATH_LARGE, "tile_kernel": tile_kernel,
+                                 "tile_n": tile_n},
                            guard_rows=2)
         assert st == gb.OK, (M, N, K, gb.gemm_tn_status_string(st))
-        assert gb.gemm_tn_last_kernels() == KERNEL_NAMES[tile_kernel]
+        assert gb.gemm_tn_last_kernels() == KERNEL_NAMES[(tile_kernel, tile_n)]
         d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), ldA, a_major, np_bits(B_st), ldB,
                                   b_major, np_bits(C_st), ldC)
         check(result_view(D_st, M, N), d64, d16, K, accum, True, f"{M}x{N}x{K}")
@@ -177,7 +179,8 @@ def test_pair_deep_stages_k_tails(a_major, b_major):
     check(result_view(D_st, M, N), d64, d16, K, 0, True, "shallow K=1100")
 
 
-@pytest.mark.parametrize("tile_n,tile_kernel", [(128, 1), (256, 1), (256, 2), (256, 3)])
+@pytest.mark.parametrize("tile_n,tile_kernel", [(64, 1), (128, 1), (256, 1), (256, 2),
+                                                 (256, 3)])
 def test_large_path_real_values_every_tile_kernel(tile_n, tile_kernel):
     M, N, K = 300, 520, 700
     ldA, ldB = K + 12, N + 8
