@@ -78,6 +78,9 @@ struct LargeArgs {
   int ks_splits;       // 1 = no split
   int ks_kb_per;
   float* ks_ws;
+  // CTA-pair kernel: output tile width (a multiple of 32 in [64, 256]; 256
+  // whenever ks_splits > 1).  The other kernels use their compile-time width.
+  int bn;
 };
 
 // Epilogue warps of the 128 x BN kernel: two per TMEM lane quadrant, each
@@ -195,12 +198,12 @@ __device__ __forceinline__ void epi_stage_c(uint8_t* stg, uint32_t lane, const u
   }
 }
 
-// Plain-store copy of this lane's staged row, columns [n0, N), for a right
-// edge that a TMA store would overrun (kept out of line: it runs once per
-// tile row at most and only when N % 8 != 0).
+// Plain-store copy of this lane's staged row, columns [n0, n0 + ncols), for
+// a chunk that a TMA store of 64 columns would overrun: a right edge with
+// N % 8 != 0, or the 32-column last chunk of a tile whose width is not a
+// multiple of 64 (kept out of line: it runs at most once per tile row).
 __device__ __noinline__ void epi_store_ragged(const LargeArgs& p, const uint8_t* my_row,
-                                              uint32_t lane, int tb, int m, int n0) {
-  const int ncols = p.N - n0;
+                                              uint32_t lane, int tb, int m, int n0, int ncols) {
   if (m >= p.M || ncols <= 0) return;
   __half* drow = p.e.D + tb * p.e.sD + static_cast<int64_t>(m) * p.e.ldD + n0;
   for (int s8 = 0; 8 * s8 < ncols; ++s8) {
@@ -216,13 +219,15 @@ __device__ __noinline__ void epi_store_ragged(const LargeArgs& p, const uint8_t*
 }
 
 // Combine this lane's accumulator row r (64 words) with its staged C row,
-// then store the chunk whose first element is D(m_row0, n0) of problem tb.
-// Returns (in lane 0) whether the chunk left by a TMA store, i.e. whether
-// one bulk group now reads the staging buffer.
+// then store the chunk whose first element is D(m_row0, n0) of problem tb;
+// only its first `width` columns (64, or 32 for the last chunk of a tile
+// whose width is an odd multiple of 32) belong to the tile.  Returns (in
+// lane 0) whether the chunk left by a TMA store, i.e. whether one bulk
+// group now reads the staging buffer.
 __device__ __forceinline__ bool epi_store_chunk(const LargeArgs& p, const CUtensorMap* tmD,
                                                 uint8_t* stg, uint32_t stg_u32, uint32_t lane,
                                                 int tb, int m_row0, int n0,
-                                                const uint32_t (&r)[64]) {
+                                                const uint32_t (&r)[64], int width = 64) {
   uint8_t* my_row = stg + lane * 128;
 #pragma unroll
   for (int s8 = 0; s8 < 8; ++s8) {
@@ -231,8 +236,9 @@ __device__ __forceinline__ bool epi_store_chunk(const LargeArgs& p, const CUtens
   }
   fence_proxy_async_smem();
   __syncwarp();
-  if (n0 + 64 > p.N && (p.N & 7)) {
-    epi_store_ragged(p, my_row, lane, tb, m_row0 + static_cast<int>(lane), n0);
+  if (width < 64 || (n0 + 64 > p.N && (p.N & 7))) {
+    epi_store_ragged(p, my_row, lane, tb, m_row0 + static_cast<int>(lane), n0,
+                     min(width, p.N - n0));
   } else if (lane == 0 && m_row0 < p.M && n0 < p.N) {
     tma_store_3d(tmD, stg_u32, n0, m_row0, tb);
     bulk_commit_group();

@@ -31,6 +31,11 @@
 //     tile's main loop; eight warps, two per TMEM lane quadrant, each drain
 //     one 128-column half, so that an accumulator is free again after two
 //     chunk times (with short K loops the drain, not the MMA, set the pace).
+//   * The tile width p.bn is chosen per call (256, 224, 192, 160 or 128):
+//     each CTA holds bn / 2 rows of B, the MMA runs with N = bn, and the
+//     epilogue drains bn columns in 64-column chunks (the last one 32 wide
+//     when bn is an odd multiple of 32), so that the number of tiles can be
+//     matched to the number of pairs.
 //   * Work units are tiles, or with ks_splits > 1 (tile, K range) pairs
 //     (the make_tiled_mma page's K split across workers): a split unit's
 //     CTAs store their fp32 rows as 128-row partial tiles 2t and 2t + 1, and
@@ -45,7 +50,7 @@
 namespace gemm_tn_dev {
 
 constexpr int kPairBM = 256;   // output rows per tile (128 per CTA)
-constexpr int kPairBN = 256;   // output columns per tile (B rows: 128 per CTA)
+constexpr int kPairBN = 256;   // widest tile (B rows: 128 per CTA); p.bn may be narrower
 constexpr int kPairThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr uint32_t kPairTmemCols = 512;  // two 256-column fp32 accumulators
 
@@ -152,6 +157,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       // commit on `empty`), which it does only after the phase completed, so
       // no copy can count against the wrong phase.
       const uint32_t full_pair0 = mapa_shared(full0, 0);
+      // bytes of one pair stage: each CTA's A box(es) and its bn / 2 rows of
+      // B (K-major: one box of bn / 2 rows; M/N-major: 64-wide boxes, the
+      // last possibly reaching past this CTA's rows)
+      const int b_half = p.bn / 2;
+      const int b_boxes_mn = (b_half + 63) / 64;
+      const uint32_t b_sub_bytes = p.b_mn ? b_boxes_mn * 8192u : b_half * 128u;
+      const uint32_t pair_stage_bytes = 2u * (L::kBK / 64) * (16384u + b_sub_bytes);
       uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
       bool ok = true;
       int local = 0;
@@ -162,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         batch_tile(p, t, tb, tm, tn);
         const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
         const int a_row = tm * kPairBM + 128 * static_cast<int>(rank);
-        const int b_row = tn * kPairBN + 128 * static_cast<int>(rank);
+        const int b_row = tn * p.bn + b_half * static_cast<int>(rank);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort_flag, p.timeout_ns,
                             timeout_code(kRoleProducer, stage), true, peer_abort)) {
@@ -173,7 +185,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             const uint32_t fb = full_pair0 + 8 * stage;
             const uint32_t a_dst = smem_u32(smem + stage * L::kStageBytes);
             const uint32_t b_dst = a_dst + L::kABytes;
-            if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * L::kStageBytes);
+            if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, pair_stage_bytes);
             // 64-deep sub-blocks, 16 KiB apart; rows past M / N and K past the
             // end (up to a whole sub-block) are zero-filled
 #pragma unroll
@@ -190,7 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 tma_load_3d_pair(bs, &tmB, fb, k0, b_row, zb);
               } else {
                 tma_load_3d_pair(bs, &tmB, fb, b_row, k0, zb);
-                tma_load_3d_pair(bs + 8192, &tmB, fb, b_row + 64, k0, zb);
+                if (b_boxes_mn > 1) tma_load_3d_pair(bs + 8192, &tmB, fb, b_row + 64, k0, zb);
               }
             }
             issued_mask |= 1u << stage;
@@ -219,7 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer
-      const uint32_t idesc = make_idesc_f16(kPairBM, kPairBN, !p.acc_f16, p.a_mn, p.b_mn);
+      const uint32_t idesc = make_idesc_f16(kPairBM, p.bn, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int u = pair; ok && u < units; u += num_pairs) {
@@ -278,11 +290,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // even CTA's MMA thread.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes 32*quad ..
     const int ew = warp - 2;                                // 0..7
-    const int col0 = (ew >> 2) * (kPairBN / 2);             // first tile column of this warp
+    // The tile's bn columns form ceil(bn / 64) chunks of 64 (the last 32
+    // wide when bn is an odd multiple of 32); the first warp of a quadrant
+    // drains the first half of the chunks, the second the rest.
+    const int tile_chunks = (p.bn + 63) / 64;
+    const int half_chunks = (tile_chunks + 1) / 2;
+    const int chunk0 = (ew >> 2) * half_chunks;
+    const int nchunks = min(half_chunks, tile_chunks - chunk0);  // this warp's chunks
+    const int col0 = chunk0 * 64;                            // first tile column of this warp
     const int row0 = static_cast<int>(rank * 128 + quad * 32);  // first tile row of this warp
     uint8_t* stg = smem + L::kStagingOffset + ew * kStagingBytes;
     const uint32_t stg_u32 = smem_u32(stg);
-    constexpr int kChunks = kPairBN / 2 / 64;  // per warp
     const uint32_t leader_tempty0 = mapa_shared(tempty0, 0);
     uint32_t acc = 0, acc_phase = 0;
     uint4 cnext[8];
@@ -297,16 +315,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                           timeout_code(kRoleEpilogue, acc), true, peer_abort))
           break;
         tc_fence_after();
+        // (split units always have bn = 256: two whole chunks per warp)
         const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN + col0;
         const int64_t ur = (2 * static_cast<int64_t>(t) + rank) * p.ks_splits + (u - t * p.ks_splits);
         float4* ws4 = reinterpret_cast<float4*>(p.ks_ws);
 #pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
+        for (int c = 0; c < nchunks; ++c) {
           uint32_t r[64];
           tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
           tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
           tmem_wait_ld();
-          if (c == kChunks - 1) {
+          if (c == nchunks - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
@@ -325,37 +344,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int tb, tm, tn;
       batch_tile(p, t, tb, tm, tn);
       const __half* cb = p.e.read_c ? p.e.C + tb * p.e.sC : nullptr;
-      const int m_base = tm * kPairBM + row0, n_base = tn * kPairBN + col0;
+      const int m_base = tm * kPairBM + row0, n_base = tn * p.bn + col0;
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
       if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
       __syncwarp();
       epi_stage_c(stg, lane, cnext);
-      epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
+      if (nchunks > 1) epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, acc), true, peer_abort))
         break;
       tc_fence_after();
+      if (nchunks <= 0) {
+        // no columns for this warp (a tile narrower than the host ever
+        // picks): still return the accumulator in this phase
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
+      }
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN + col0;
 #pragma unroll 1
-      for (int c = 0; c < kChunks; ++c) {
+      for (int c = 0; c < nchunks; ++c) {
         if (c > 0) {
           if (lane == 0) bulk_wait_group_read0();
           __syncwarp();
           epi_stage_c(stg, lane, cnext);
-          if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
+          if (c + 1 < nchunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
         }
+        // (the last chunk of a 32-column remainder reads 32 accumulator
+        // columns past the tile; they lie inside the 256-column buffer and
+        // are not stored)
         uint32_t r[64];
         tmem_ld_32x32b_x32(t_row + c * 64, *reinterpret_cast<uint32_t(*)[32]>(r));
         tmem_ld_32x32b_x32(t_row + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        if (c == kChunks - 1) {
+        if (c == nchunks - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8 * acc);
         }
-        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r);
+        epi_store_chunk(p, &tmD, stg, stg_u32, lane, tb, m_base, n_base + 64 * c, r,
+                        min(64, p.bn - (col0 + 64 * c)));
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;

@@ -495,6 +495,34 @@ int pair_split_count(int64_t M, int64_t N, int64_t K, int64_t pair_tiles, int ac
   return static_cast<int>(s);
 }
 
+// Tile width of the CTA-pair kernel (unsplit): the width whose waves of
+// tiles over the pairs take the least time.  A tile's time per 16-deep K
+// step is the MMA's bn / 2 clocks, or, when longer, the time each SM needs
+// to take in its 128 + bn / 2 rows of A and B (32 bytes each) at about 75
+// bytes per clock (the TMA ingress rate measured on GB300).  Narrower tiles
+// are taken only when at least 3 % faster; with an M/N-major B only widths
+// that are whole 64-element boxes per CTA (256, 128).  Ragged 4000 x 3000
+// tiles this way as 16 x 14 tiles of 256 x 224 (2.95 waves over 76 pairs)
+// instead of 16 x 12 of 256 x 256 (2.53 waves, i.e. 3).
+bool p_acc_f16(int accum) { return accum == GEMM_TN_ACC_F16; }
+
+int pair_tile_n(int64_t M, int64_t N, int64_t L, int b_major, int max_pairs) {
+  int best = 256;
+  double best_cost = -1.0;
+  for (int bn = 256; bn >= 128; bn -= 32) {
+    if (b_major == GEMM_TN_MAJOR_MN && bn % 128 != 0) continue;
+    const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn) * L;
+    const int64_t waves = (tiles + max_pairs - 1) / max_pairs;
+    const double step = std::max(bn / 2.0, (4096.0 + 16.0 * bn) / 75.0);
+    const double cost = static_cast<double>(waves) * step;
+    if (best_cost < 0.0 || cost < 0.97 * best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
                  const DeviceState& st) {
   const int64_t M = q.M, N = q.N, K = q.K;
@@ -540,7 +568,26 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   }
   if (kind == 2 && st.max_pairs <= 0) return GEMM_TN_ERR_UNSUPPORTED;
   const bool pair = kind == 2, wide = kind == 3;
-  const int bn = (pair || wide) ? 256 : (tile_n == 64 || tile_n == 128) ? tile_n : 256;
+  // The pair's K split runs 256-wide tiles; an unsplit pair kernel takes the
+  // width that balances its waves (tile_n, when given, is a request: 128 or
+  // 256).
+  const int auto_pair_splits =
+      pair && o.tile_kernel == 0 && o.split_k == 0
+          ? pair_split_count(M, N, K, ((M + 255) / 256) * ((N + 255) / 256) * q.L, accum, st)
+          : 1;
+  const bool pair_split = pair && !p_acc_f16(accum) &&
+                          ((o.tile_kernel == 2 && o.split_k > 0) || auto_pair_splits > 1);
+  const bool pair_width_asked = pair && o.tile_kernel == 2 && o.tile_n != 0;
+  if (pair_width_asked && (pair_split || o.tile_n < 128 ||
+                           (b_major == GEMM_TN_MAJOR_MN && o.tile_n % 128 != 0)))
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (kind == 1 && tile_n != 0 && tile_n != 64 && tile_n != 128 && tile_n != 256)
+    return GEMM_TN_ERR_INVALID_ARG;
+  const int bn = wide ? 256
+               : pair ? (pair_split ? 256
+                         : pair_width_asked ? o.tile_n
+                                            : pair_tile_n(M, N, q.L, b_major, st.max_pairs))
+               : (tile_n == 64 || tile_n == 128) ? tile_n : 256;
   const int bm = (pair || wide) ? 256 : kLargeBM;
   // K-chunk boxes (stages of 128 of K) for 128 x 128 tiles when both
   // operands are K-major and K is a multiple of 64, from K = 1024 on
@@ -552,8 +599,9 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   // (3-5 % slower there than 64-deep stages).
   const bool ko = kind == 1 && bn <= 128 && a_major == GEMM_TN_MAJOR_K &&
                   b_major == GEMM_TN_MAJOR_K && K % 64 == 0 && K >= 1024;
-  const bool deep = ko || (pair && K >= 1024 && (a_major == GEMM_TN_MAJOR_MN || q.ldA % 64 == 0) &&
-                           (b_major == GEMM_TN_MAJOR_MN || q.ldB % 64 == 0));
+  const bool deep_auto = K >= 1024 && (a_major == GEMM_TN_MAJOR_MN || q.ldA % 64 == 0) &&
+                         (b_major == GEMM_TN_MAJOR_MN || q.ldB % 64 == 0);
+  const bool deep = ko || (pair && (o.k_stage ? o.k_stage == 128 : deep_auto));
   CUtensorMap tmA, tmB;
   int s;
   if (ko) {
@@ -564,7 +612,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     s = encode_operand_batched(&tmA, q.A, M, K, q.ldA, q.sA, q.L, a_major, wide ? 256 : kLargeBM);
     if (s == GEMM_TN_OK)
       s = encode_operand_batched(&tmB, q.B, N, K, q.ldB, q.sB, q.L, b_major,
-                                 static_cast<uint32_t>(pair ? 128 : bn));
+                                 static_cast<uint32_t>(pair ? bn / 2 : bn));
   }
   if (s != GEMM_TN_OK) return s;
   LargeArgs p;
@@ -576,6 +624,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.acc_f16 = accum == GEMM_TN_ACC_F16;
   p.a_mn = a_major;
   p.b_mn = b_major;
+  p.bn = bn;
   p.tiles_m = static_cast<int>((M + bm - 1) / bm);
   p.tiles_n = static_cast<int>((N + bn - 1) / bn);
   const int64_t per_batch = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
@@ -655,8 +704,8 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     const bool asked = !p.acc_f16 && o.tile_kernel == 2 && o.split_k > 0;
     if (asked)
       splits = o.split_k;
-    else if (o.tile_kernel == 0 && o.split_k == 0)
-      splits = pair_split_count(M, N, K, p.num_tiles, accum, st);
+    else
+      splits = auto_pair_splits;  // counted on 256-wide tiles (bn is 256 when > 1)
     splits = std::max(1, std::min(splits, p.k_blocks));
     void* ks_ws = nullptr;
     if (splits > 1) {
@@ -897,10 +946,15 @@ int launch_scale(const Problem& q, cudaStream_t stream, const DeviceState& st) {
   return GEMM_TN_OK;
 }
 
+// Tile widths any tile kernel can run (0 = the library's choice).
+bool tile_n_ok(int n) {
+  return n == 0 || n == 64 || n == 128 || n == 160 || n == 192 || n == 224 || n == 256;
+}
+
 bool options_ok(const gemm_tn_options& o) {
   return !(o.path < GEMM_TN_PATH_AUTO || o.path > GEMM_TN_PATH_SKINNY || o.split_k < 0 ||
-           (o.tile_n != 0 && o.tile_n != 64 && o.tile_n != 128 && o.tile_n != 256) ||
-           o.tile_kernel < 0 ||
+           !tile_n_ok(o.tile_n) ||
+           o.tile_kernel < 0 || (o.k_stage != 0 && o.k_stage != 64 && o.k_stage != 128) ||
            o.tile_kernel > 3);
 }
 

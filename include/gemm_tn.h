@@ -140,10 +140,18 @@ typedef struct {
                            tile_kernel 0 the library splits by itself when
                            the tiles would leave more than half the SMs
                            idle and K is long enough) */
-  int tile_n;           /* large path, 128-row tiles: output tile width, 128
-                           or 256 (0: the library's choice -- 128 when N <=
-                           128 or when 128 x 256 tiles would leave half the
-                           SMs idle, else 256) */
+  int tile_n;           /* large path, output tile width (0: the library's
+                           choice).  128-row tiles (tile_kernel 1): 64, 128
+                           or 256; the library takes 128 when N <= 128 or
+                           when 128 x 256 tiles would leave half the SMs
+                           idle, 64 when even 128 x 128 tiles would and K is
+                           not split, else 256.  CTA-pair tiles (only with
+                           tile_kernel 2; not with a K split): 128, 160,
+                           192, 224 or 256 with a K-major B, 128 or 256
+                           with an N-major B; the library takes the width
+                           whose waves of tiles over the SM pairs finish
+                           soonest.  Other values, or a width the chosen
+                           kernel cannot run, are GEMM_TN_ERR_INVALID_ARG */
   int sync_check;       /* nonzero: synchronise `stream` after the launch and
                            return GEMM_TN_ERR_DEVICE_TIMEOUT if a kernel gave
                            up waiting (the sticky device error word is read
@@ -187,6 +195,9 @@ typedef struct {
                            the unsplit kernel instead; gemm_tn_strided_ex
                            falls back to the copy producer unless the
                            repack route was forced. */
+  int k_stage;          /* CTA-pair kernel: K depth of a pipeline stage, 64
+                           or 128 (0 = the library's choice); other values
+                           are GEMM_TN_ERR_INVALID_ARG */
 } gemm_tn_options;
 
 /*

@@ -92,6 +92,8 @@ def call(M=64, N=64, K=64, A=P, ldA=64, am=0, B=P + (1 << 20), ldB=64, bm=0,
     (dict(ldC=68), gb.ERR_ALIGNMENT),
     (dict(opts=gb.make_options(path=7)), gb.ERR_INVALID_ARG),
     (dict(opts=gb.make_options(tile_n=96)), gb.ERR_INVALID_ARG),
+    (dict(opts=gb.make_options(tile_n=300)), gb.ERR_INVALID_ARG),
+    (dict(opts=gb.make_options(k_stage=32)), gb.ERR_INVALID_ARG),
     (dict(M=264, opts=gb.make_options(path=2)), gb.ERR_INVALID_ARG),  # skinny needs M <= 256
 ])
 def test_argument_errors_return_before_any_device_work(lib, kw, status):

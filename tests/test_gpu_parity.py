@@ -179,6 +179,54 @@ def test_pair_deep_stages_k_tails(a_major, b_major):
     check(result_view(D_st, M, N), d64, d16, K, 0, True, "shallow K=1100")
 
 
+@pytest.mark.parametrize("tile_n", [128, 160, 192, 224, 256])
+@pytest.mark.parametrize("a_major,b_major", [(0, 0), (1, 0), (0, 1)])
+def test_pair_tile_widths(tile_n, a_major, b_major):
+    """The CTA-pair kernel at every tile width it runs (B's rows split
+    bn / 2 per CTA, the last epilogue chunk 32 wide for odd multiples of 32):
+    ragged M, N and K over several tiles, both accumulations, 64- and
+    128-deep stages; integer values, bit-exact.  With an N-major B only the
+    widths that are whole 64-element boxes per CTA run; the others are
+    rejected."""
+    M, N = 530, 3 * tile_n + 72
+    for K, k_stage in ((300, 64), (1100, 128)):
+        ldA = ((K if a_major == 0 else M) + 7) // 8 * 8 + 8
+        ldB = (K + 63) // 64 * 64 if b_major == 0 else N + 8
+        A_st = wl.operand(M, K, ldA, a_major, "int1", 900 + tile_n + K)
+        B_st = wl.operand(N, K, ldB, b_major, "int1", 901 + tile_n + K)
+        C_st = wl.operand(M, N, N + 8, 0, "int4", 902 + tile_n + K)
+        d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), ldA, a_major, np_bits(B_st), ldB,
+                                  b_major, np_bits(C_st), N + 8)
+        for accum in (0, 1):
+            opts = {"path": gb.PATH_LARGE, "tile_kernel": 2, "tile_n": tile_n,
+                    "k_stage": k_stage}
+            D_st, st = run_gpu(M, N, K, A_st, ldA, a_major, B_st, ldB, b_major, C_st, N + 8,
+                               accum, opts=opts, guard_rows=2)
+            if b_major == 1 and tile_n % 128 != 0:
+                assert st == gb.ERR_INVALID_ARG
+                continue
+            assert st == gb.OK, gb.gemm_tn_status_string(st)
+            assert gb.gemm_tn_last_kernels() == ("gemm_tn_large2_kernel<deep>" if k_stage == 128
+                                                 else "gemm_tn_large2_kernel")
+            check(result_view(D_st, M, N), d64, d16, K, accum, True,
+                  f"pair bn={tile_n} K={K} acc={accum}")
+            slack_untouched(D_st, C_st, N)
+
+
+def test_pair_tile_width_of_the_ragged_workload_real_values():
+    """The ragged workload on 256 x 224 pair tiles (the width the library
+    picks for it) against the 256-wide ones and the oracle's tolerance."""
+    w = wl.WORKLOADS["ragged"]
+    A_st, B_st, C_st = wl.make_inputs(w)
+    d64, d16 = oracle_full(w, A_st, B_st, C_st)
+    for tile_n in (224, 256):
+        D_st, st = run_gpu(w.M, w.N, w.K, A_st, w.ldA, w.a_major, B_st, w.ldB, w.b_major,
+                           C_st, w.ldC, w.accum,
+                           opts={"path": gb.PATH_LARGE, "tile_kernel": 2, "tile_n": tile_n})
+        assert st == gb.OK
+        check(result_view(D_st, w.M, w.N), d64, d16, w.K, w.accum, False, f"ragged bn={tile_n}")
+
+
 @pytest.mark.parametrize("tile_n,tile_kernel", [(64, 1), (128, 1), (256, 1), (256, 2),
                                                  (256, 3)])
 def test_large_path_real_values_every_tile_kernel(tile_n, tile_kernel):
