@@ -30,7 +30,13 @@ ERR_NO_MEMORY = 6
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
             "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc",
             "gemm_tn_last_kernels", "gemm_tn_strided", "gemm_tn_strided_ex",
-            "gemm_tn_scaled", "gemm_tn_batched", "gemm_tn_batched_ex")
+            "gemm_tn_scaled", "gemm_tn_batched", "gemm_tn_batched_ex", "gemm_tn_trace_read")
+
+# Phase-trace record layout (gemm_tn_trace_read).
+TRACE_SLOTS = 10
+TRACE_CTAS = 512
+TRACE_FIELDS = ("entry", "ready", "first_stage", "last_mma", "first_acc", "last_chunk",
+                "stores_done", "exit", "sm", "units")
 
 # Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -41,7 +47,7 @@ class GemmTnOptions(ctypes.Structure):
                 ("sync_check", ctypes.c_int), ("timeout_ns", ctypes.c_uint64),
                 ("test_stall", ctypes.c_int), ("tile_kernel", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("test_fail_alloc", ctypes.c_int),
-                ("k_stage", ctypes.c_int)]
+                ("k_stage", ctypes.c_int), ("trace", ctypes.c_int)]
 
 
 class GemmTnError(RuntimeError):
@@ -91,6 +97,9 @@ def lib() -> ctypes.CDLL:
                                          i64, i32, vp, ctypes.POINTER(GemmTnOptions)]
         L.gemm_tn_last_kernels.restype = ctypes.c_char_p
         L.gemm_tn_last_kernels.argtypes = []
+        L.gemm_tn_trace_read.restype = i32
+        L.gemm_tn_trace_read.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64), i32,
+                                         ctypes.POINTER(ctypes.c_int)]
         L.gemm_tn_skinny_noalloc.restype = i32
         L.gemm_tn_skinny_noalloc.argtypes = gemm_args
         f32 = ctypes.c_float
@@ -118,9 +127,9 @@ TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_WIDE = 0, 1, 2, 3
 
 
 def make_options(path=0, split_k=0, tile_n=0, sync_check=0, timeout_ns=0, test_stall=0,
-                 tile_kernel=0, stream_k=0, test_fail_alloc=0, k_stage=0):
+                 tile_kernel=0, stream_k=0, test_fail_alloc=0, k_stage=0, trace=0):
     return GemmTnOptions(path, split_k, tile_n, sync_check, timeout_ns, test_stall, tile_kernel,
-                         stream_k, test_fail_alloc, k_stage)
+                         stream_k, test_fail_alloc, k_stage, trace)
 
 
 def gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream,
@@ -166,6 +175,25 @@ def gemm_tn_check_device_error(stream) -> tuple[int, int]:
     d = ctypes.c_uint32(0)
     s = lib().gemm_tn_check_device_error(stream, ctypes.byref(d))
     return s, d.value
+
+
+def gemm_tn_trace_read(stream, max_ctas=TRACE_CTAS):
+    """C ``gemm_tn_trace_read``: returns (status, records) where records is a
+    list of one dict per CTA with an entry stamp (fields TRACE_FIELDS plus
+    "cta")."""
+    n = max(0, min(int(max_ctas), TRACE_CTAS))
+    buf = (ctypes.c_uint64 * (n * TRACE_SLOTS))()
+    rec = ctypes.c_int(0)
+    st = lib().gemm_tn_trace_read(stream, buf, n, ctypes.byref(rec))
+    out = []
+    if st == OK:
+        for c in range(n):
+            row = buf[c * TRACE_SLOTS:(c + 1) * TRACE_SLOTS]
+            if row[0]:
+                d = dict(zip(TRACE_FIELDS, row))
+                d["cta"] = c
+                out.append(d)
+    return st, out
 
 
 def gemm_tn_plan_path(M, N, K, a_major, b_major) -> int:

@@ -100,6 +100,44 @@ __device__ __forceinline__ __half epi_one(const EpiArgs& e, bool acc_f16, uint32
   return __float2half_rn(fmaf(e.alpha, af, e.beta * __half2float(c)));
 }
 
+// Phase trace (gemm_tn_options.trace): when a launch has tracing on, one
+// thread per role stamps %globaltimer into g_trace at fixed points, per CTA,
+// so that a launch's time can be split into set-up, first data, main loop,
+// drain and exit.  Slot layout per CTA (kTraceSlots 64-bit words):
+//   0 entry               kernel start (thread 0)
+//   1 ready               after griddepcontrol.wait (producer)
+//   2 first stage         first pipeline stage complete (MMA issuer)
+//   3 last MMA            last accumulator committed (MMA issuer)
+//   4 first accumulator   first accumulator ready (first epilogue warp)
+//   5 last chunk          last output chunk handed to the copy engine
+//   6 stores done         the CTA's last stores performed (first epilogue warp)
+//   7 exit                before tensor memory is freed (thread 0)
+//   8 SM id, 9 work units of this CTA
+// CTAs past kTraceCtas are not recorded.
+constexpr int kTraceSlots = 10;
+constexpr int kTraceCtas = 512;
+enum : int {
+  kTrEntry = 0, kTrReady, kTrFirstStage, kTrLastMma, kTrFirstAcc, kTrLastChunk,
+  kTrStoresDone, kTrExit, kTrSm, kTrUnits
+};
+
+// (One translation unit: the definition lives here, like g_error_word.)
+__device__ __align__(256) uint64_t g_trace[kTraceCtas * kTraceSlots];
+
+__device__ __forceinline__ void trace_mark(int on, int slot) {
+  if (on && blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceSlots + slot] = globaltimer_ns();
+}
+
+__device__ __forceinline__ void trace_value(int on, int slot, uint64_t v) {
+  if (on && blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceSlots + slot] = v;
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 // Grouped raster over output tiles: runs of `group_m` tile-rows are walked
 // column by column, so CTAs that run at the same time share A row-panels and
 // B column-panels in L2.

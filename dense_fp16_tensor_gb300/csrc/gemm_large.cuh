@@ -81,6 +81,7 @@ struct LargeArgs {
   // CTA-pair kernel: output tile width (a multiple of 32 in [64, 256]; 256
   // whenever ks_splits > 1).  The other kernels use their compile-time width.
   int bn;
+  int trace;           // phase trace on (see trace_mark)
 };
 
 // Epilogue warps of the 128 x BN kernel: two per TMEM lane quadrant, each
@@ -279,6 +280,8 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
+    trace_mark(p.trace, kTrEntry);
+    trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -308,6 +311,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   // (which may write A, B or C, or read a workspace this call reuses) must
   // be complete before any global memory is touched.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrReady);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -378,9 +382,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(kLargeBM, BN, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = true;
+      bool ok = true, first_stage = true;
+      int done = 0;
       const int units = p.num_tiles * p.ks_splits;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++done) {
         const int sp = u % p.ks_splits;
         const int kb0 = sp * p.ks_kb_per, kb1 = min(kb0 + p.ks_kb_per, p.k_blocks);
         if (!wait_bounded(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
@@ -397,6 +402,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
             break;
           }
           tc_fence_after();
+          if (first_stage) {
+            trace_mark(p.trace, kTrFirstStage);
+            first_stage = false;
+          }
           const uint32_t a_base = smem_u32(sA + stage * L::kABytes);
           const uint32_t b_base = smem_u32(sB + stage * L::kBBytes);
 #pragma unroll
@@ -425,6 +434,8 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
+      trace_mark(p.trace, kTrLastMma);
+      trace_value(p.trace, kTrUnits, static_cast<uint64_t>(done));
       if (!ok || *abort_flag) {
         // Wait until every MMA issued so far has finished with TMEM and smem.
         mma_commit(drain);
@@ -500,6 +511,8 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
                         timeout_code(kRoleEpilogue, acc)))
         break;
       tc_fence_after();
+      if (ew == 0 && lane == 0 && u == static_cast<int>(blockIdx.x))
+        trace_mark(p.trace, kTrFirstAcc);
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * BN + col0;
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
@@ -525,13 +538,16 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (ew == 0 && lane == 0) trace_mark(p.trace, kTrLastChunk);
     if (lane == 0) bulk_wait_group0();  // all D stores performed before exit
+    if (ew == 0 && lane == 0) trace_mark(p.trace, kTrStoresDone);
     __syncwarp();
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * BN);

@@ -10,9 +10,7 @@
 //     64-deep sub-blocks per operand, each loaded as in the 64-deep layout;
 //     64 KiB per CTA), and a sub-block past K is zero-filled by the copy;
 //     otherwise 6 stages of one 64-deep K block.  Deep stages halve the
-//     stage hand-offs per byte and win from K = 1024 on, except when a
-//     K-major operand's rows are not 128-byte aligned: then the shallow
-//     ring is faster.
+//     stage hand-offs per byte and win from K = 1024 on.
 //   * One thread of the even CTA issues tcgen05.mma.cta_group::2 with
 //     M = 256, N = 256, K = 16: the instruction reads A from both CTAs'
 //     shared memory (split along M) and B from both (split along N), and
@@ -113,6 +111,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
+    trace_mark(p.trace, kTrEntry);
+    trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < kPairStages; ++s) {
       mbar_init(full0 + 8 * s, 1);  // the even CTA's arming; both CTAs' bytes (odd: unused)
       mbar_init(empty0 + 8 * s, 1);
@@ -144,6 +144,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   // (which may write A, B or C, or read a workspace this call reuses) must
   // be complete before any global memory is touched.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrReady);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -233,8 +234,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idesc = make_idesc_f16(kPairBM, p.bn, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = true;
-      for (int u = pair; ok && u < units; u += num_pairs) {
+      bool ok = true, first_stage = true;
+      int done = 0;
+      for (int u = pair; ok && u < units; u += num_pairs, ++done) {
         int t, kb0, kb1;
         pair_unit(p, u, t, kb0, kb1);
         if (!wait_bounded<true>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
@@ -251,6 +253,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             break;
           }
           tc_fence_after();
+          if (first_stage) {
+            trace_mark(p.trace, kTrFirstStage);
+            first_stage = false;
+          }
           const uint32_t a_base = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t b_base = a_base + L::kABytes;
 #pragma unroll
@@ -276,6 +282,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
+      trace_mark(p.trace, kTrLastMma);
+      trace_value(p.trace, kTrUnits, static_cast<uint64_t>(done));
       if (!ok || *abort_flag) {
         mma_commit_pair(drain);
         wait_bounded(drain, 0, abort_flag, p.timeout_ns, timeout_code(kRoleMma, 0x300), false,
@@ -355,6 +363,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         timeout_code(kRoleEpilogue, acc), true, peer_abort))
         break;
       tc_fence_after();
+      if (ew == 0 && lane == 0 && u == pair) trace_mark(p.trace, kTrFirstAcc);
       if (nchunks <= 0) {
         // no columns for this warp (a tile narrower than the host ever
         // picks): still return the accumulator in this phase
@@ -390,7 +399,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (ew == 0 && lane == 0) trace_mark(p.trace, kTrLastChunk);
     if (lane == 0) bulk_wait_group0();  // all D stores performed before exit
+    if (ew == 0 && lane == 0) trace_mark(p.trace, kTrStoresDone);
     __syncwarp();
   }
 
@@ -398,6 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no CTA leaves while its peer's MMAs or arrivals may touch it
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kPairTmemCols);

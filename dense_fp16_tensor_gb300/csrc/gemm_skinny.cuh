@@ -45,6 +45,7 @@ struct SkinnyArgs {
   float* ws;         // [grid * max_segs][mp/4][128] float4 partials (see skinny_partial)
   uint64_t timeout_ns;
   int test_stall;
+  int trace;         // phase trace on (see trace_mark)
 };
 
 // 64-deep K sub-blocks per pipeline stage (and per unit of the K split):
@@ -130,6 +131,8 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   const int nseg = segs.count();
 
   if (threadIdx.x == 0) {
+    trace_mark(p.trace, kTrEntry);
+    trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -158,6 +161,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   // stream (which may write A, B or C, or read the workspace) must be
   // complete before any global memory is touched.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrReady);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(kSkinnyBN, MP, true, 0, 0);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = true;
+      bool ok = true, first_stage = true;
       for (int j = 0; ok && j < nseg; ++j) {
         int tile, kb0, kb1;
         segs.seg(j, tile, kb0, kb1);
@@ -224,6 +228,10 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
             break;
           }
           tc_fence_after();
+          if (first_stage) {
+            trace_mark(p.trace, kTrFirstStage);
+            first_stage = false;
+          }
           const uint32_t b_base = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t a_base = b_base + L::kBBytes;
 #pragma unroll
@@ -246,6 +254,8 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
+      trace_mark(p.trace, kTrLastMma);
+      trace_value(p.trace, kTrUnits, static_cast<uint64_t>(nseg));
       if (!ok || *abort_flag) {
         mma_commit(drain);
         wait_bounded(drain, 0, abort_flag, p.timeout_ns, timeout_code(kRoleMma, 0x300), false);
@@ -260,6 +270,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
                         timeout_code(kRoleEpilogue, acc)))
         break;
       tc_fence_after();
+      if (warp == 2 && lane == 0 && j == 0) trace_mark(p.trace, kTrFirstAcc);
       const int64_t slot = static_cast<int64_t>(blockIdx.x) * p.max_segs + j;
       float4* dst = reinterpret_cast<float4*>(p.ws) + skinny_partial<MP>(slot, 0, row);
       const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * MP;
@@ -280,11 +291,13 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (warp == 2 && lane == 0) trace_mark(p.trace, kTrLastChunk);
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, L::kTmemCols);

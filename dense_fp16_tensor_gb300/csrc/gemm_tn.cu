@@ -67,6 +67,7 @@ struct DeviceState {
   bool attrs_set = false;
   int max_pairs = 0;  // CTA pairs of gemm_tn_large2_kernel that fit at once
   cudaMemPool_t pool = nullptr;  // library-owned stream-ordered workspace pool
+  uint64_t* trace = nullptr;     // device address of g_trace on this device
 };
 
 // Workspaces come from a pool owned by the library (one per device) that
@@ -111,6 +112,15 @@ int skinny_mp(int64_t M) {
   if (M <= 64) return static_cast<int>((M + 15) / 16 * 16);
   return M <= 96 ? 96 : (M <= 128 ? 128 : (M <= 192 ? 192 : 256));
 }
+
+}  // namespace
+
+// Phase-trace records (g_trace, common.cuh) of the last traced launch on
+// each device (gemm_tn_options.trace).
+static_assert(GEMM_TN_TRACE_CTAS == kTraceCtas && GEMM_TN_TRACE_SLOTS == kTraceSlots,
+              "trace layout of the header and the kernels");
+
+namespace {
 
 // Per-device set-up (under g_mu): capability check, SM count, kernel
 // attributes.  Returns a status.
@@ -186,7 +196,27 @@ int device_setup(int dev, DeviceState*& st) {
     st->attrs_set = true;
   }
   if (resolve_encoder() != GEMM_TN_OK) return GEMM_TN_ERR_CUDA;
+  if (st->trace == nullptr) {
+    void* t = nullptr;
+    if (cudaGetSymbolAddress(&t, gemm_tn_dev::g_trace) != cudaSuccess || t == nullptr) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_CUDA;
+    }
+    st->trace = static_cast<uint64_t*>(t);
+  }
   return GEMM_TN_OK;
+}
+
+// Whether this call's kernel traces (the buffer is cleared on the stream
+// first).
+int trace_for(const gemm_tn_options& o, const DeviceState& st, cudaStream_t stream) {
+  if (!o.trace) return 0;
+  if (cudaMemsetAsync(st.trace, 0, sizeof(uint64_t) * kTraceCtas * kTraceSlots, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return 1;
 }
 
 // The device's workspace pool (under g_mu), created on the first call of an
@@ -599,8 +629,12 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   // (3-5 % slower there than 64-deep stages).
   const bool ko = kind == 1 && bn <= 128 && a_major == GEMM_TN_MAJOR_K &&
                   b_major == GEMM_TN_MAJOR_K && K % 64 == 0 && K >= 1024;
-  const bool deep_auto = K >= 1024 && (a_major == GEMM_TN_MAJOR_MN || q.ldA % 64 == 0) &&
-                         (b_major == GEMM_TN_MAJOR_MN || q.ldB % 64 == 0);
+  // The pair's 128-deep stages from K = 1024 on, also when a K-major
+  // operand's rows are off the 128-byte grid (ragged 4000 x 3000 x 2500 with
+  // B's ld 2504: 43.8 against 48.4 us back to back, 53.3 against 55.2 us
+  // alone after an L2 flush; equal within noise on 8192^3 and 4096 x 3072 x
+  // 2560 with off-grid rows).
+  const bool deep_auto = K >= 1024;
   const bool deep = ko || (pair && (o.k_stage ? o.k_stage == 128 : deep_auto));
   CUtensorMap tmA, tmB;
   int s;
@@ -642,6 +676,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   p.group_m = (pair || wide) ? 8 : 16;
   p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
   p.test_stall = o.test_stall;
+  p.trace = trace_for(o, st, stream);
   p.sk_tile0 = p.num_tiles;  // no split tiles unless stream-K is set up below
   p.ks_splits = 1;           // no K split of the 128-row kernel unless set up below
   p.ks_kb_per = p.k_blocks;
@@ -921,6 +956,7 @@ int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& 
     return GEMM_TN_ERR_NO_MEMORY;
   }
   p.ws = static_cast<float*>(ws);
+  p.trace = trace_for(o, st, stream);
   const cudaError_t e = launch_skinny_kernels(grid, tmA, tmB, p, epi_of(q), stream);
   const cudaError_t f = cudaFreeAsync(ws, stream);
   if (e != cudaSuccess || f != cudaSuccess) {
@@ -1022,6 +1058,25 @@ GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail) {
   }
   if (detail) *detail = word;
   return word ? GEMM_TN_ERR_DEVICE_TIMEOUT : GEMM_TN_OK;
+}
+
+GEMM_TN_API int gemm_tn_trace_read(void* stream, uint64_t* out, int max_ctas, int* recorded) {
+  if (out == nullptr || max_ctas < 0) return GEMM_TN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  const int n = std::min(max_ctas, kTraceCtas);
+  if (n > 0 && (cudaMemcpyFromSymbolAsync(out, gemm_tn_dev::g_trace, sizeof(uint64_t) * kTraceSlots * n, 0,
+                                          cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+                cudaStreamSynchronize(s) != cudaSuccess)) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_CUDA;
+  }
+  if (recorded) {
+    int r = 0;
+    for (int c = 0; c < n; ++c) r += out[c * kTraceSlots + kTrEntry] != 0;
+    *recorded = r;
+  }
+  return GEMM_TN_OK;
 }
 
 GEMM_TN_API int gemm_tn_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t ldA,

@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
+    trace_mark(p.trace, kTrEntry);
+    trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < kWideStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -178,6 +180,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   // (which may write A, B or C, or read a workspace this call reuses) must
   // be complete before any global memory is touched.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrReady);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -236,9 +239,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(128, kWideBN, !p.acc_f16, p.a_mn, p.b_mn);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
-      bool ok = true;
+      bool ok = true, first_stage = true;
+      int done = 0;
       WideItem it;
-      for (int idx = 0; ok && wide_item(p, cta, G, idx, it); ++idx) {
+      for (int idx = 0; ok && wide_item(p, cta, G, idx, it); ++idx, ++done) {
         if (!wait_bounded(tempty, acc_phase ^ 1u, abort_flag, p.timeout_ns,
                           timeout_code(kRoleMma, 0x200))) {
           ok = false;
@@ -252,6 +256,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             break;
           }
           tc_fence_after();
+          if (first_stage) {
+            trace_mark(p.trace, kTrFirstStage);
+            first_stage = false;
+          }
           const uint32_t a_base = smem_u32(smem + stage * L::kStageBytes);
           const uint32_t b_base = a_base + L::kABytes;
 #pragma unroll
@@ -277,6 +285,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         mma_commit(tfull);
         acc_phase ^= 1u;
       }
+      trace_mark(p.trace, kTrLastMma);
+      trace_value(p.trace, kTrUnits, static_cast<uint64_t>(done));
       if (!ok || *abort_flag) {
         mma_commit(drain);
         wait_bounded(drain, 0, abort_flag, p.timeout_ns, timeout_code(kRoleMma, 0x300), false);
@@ -363,6 +373,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       if (!wait_bounded(tfull, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, 0)))
         break;
+      if (ew == 0 && lane == 0 && idx == 0) trace_mark(p.trace, kTrFirstAcc);
       tc_fence_after();
       if (it.slot < 0) {
 #pragma unroll 1
@@ -548,13 +559,16 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       acc_phase ^= 1u;
       prefetch_c(idx + 1);
     }
+    if (ew == 0 && lane == 0) trace_mark(p.trace, kTrLastChunk);
     if (lane == 0) bulk_wait_group0();  // all D stores performed before exit
+    if (ew == 0 && lane == 0) trace_mark(p.trace, kTrStoresDone);
     __syncwarp();
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kWideTmemCols);

@@ -198,6 +198,12 @@ typedef struct {
   int k_stage;          /* CTA-pair kernel: K depth of a pipeline stage, 64
                            or 128 (0 = the library's choice); other values
                            are GEMM_TN_ERR_INVALID_ARG */
+  int trace;            /* nonzero: the call's GEMM kernel (not a K split's
+                           reduction) stamps a phase trace per CTA into the
+                           library's trace buffer, which gemm_tn_trace_read
+                           returns (the buffer is cleared on the stream
+                           first; one buffer per device, so traced calls
+                           that overlap on the GPU mix their records) */
 } gemm_tn_options;
 
 /*
@@ -342,6 +348,25 @@ GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K,
  * 16-23 the role that gave up -- 1 producer, 2 MMA issuer, 3 epilogue -- and
  * bits 0-15 the pipeline stage), or GEMM_TN_ERR_CUDA. */
 GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail);
+
+/* Phase trace of the last launch made with gemm_tn_options.trace on the
+ * current device: GEMM_TN_TRACE_SLOTS 64-bit words per CTA, for the first
+ * GEMM_TN_TRACE_CTAS CTAs of the grid (blockIdx.x order):
+ *   0 kernel entry            1 after the wait for the previous kernel
+ *   2 first stage complete    3 last accumulator committed (MMA issuer)
+ *   4 first accumulator ready 5 last output chunk issued (first epilogue warp)
+ *   6 that warp's stores done 7 exit (before tensor memory is freed)
+ *   8 SM id                   9 work units (tiles or segments) of the CTA
+ * Times are the GPU's global nanosecond timer; 0 marks a point the CTA did
+ * not pass (or a kernel that does not stamp it: the skinny kernel stores
+ * partial sums, so its slot 6 stays 0).  Synchronises `stream`, then copies
+ * max_ctas records (at most GEMM_TN_TRACE_CTAS) to `out` (host memory of
+ * max_ctas * GEMM_TN_TRACE_SLOTS words) and sets *recorded (if non-NULL) to
+ * the number of CTAs with an entry stamp.  Returns GEMM_TN_OK,
+ * GEMM_TN_ERR_INVALID_ARG (out NULL, max_ctas < 0) or GEMM_TN_ERR_CUDA. */
+#define GEMM_TN_TRACE_SLOTS 10
+#define GEMM_TN_TRACE_CTAS 512
+GEMM_TN_API int gemm_tn_trace_read(void* stream, uint64_t* out, int max_ctas, int* recorded);
 
 /* Which path gemm_tn would take for these sizes and majors (gemm_tn_path). */
 GEMM_TN_API int gemm_tn_plan_path(int64_t M, int64_t N, int64_t K, int a_major,

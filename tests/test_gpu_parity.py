@@ -147,8 +147,9 @@ def test_pair_deep_stages_k_tails(a_major, b_major):
     from K = 1024 on): K ending inside the first sub-block of the last stage
     (its second sub-block lies wholly past K), inside the second, and on
     stage and sub-block boundaries; ragged M and N; K-major leading
-    dimensions multiples of 64.  Integer values: bit-exact.  A K-major
-    operand whose rows are not 128-byte aligned keeps 64-deep stages."""
+    dimensions multiples of 64.  Integer values: bit-exact.  Operands whose
+    rows are off the 128-byte grid run both depths (128 by default, 64 on
+    request)."""
     rng = np.random.default_rng(700 + 2 * a_major + b_major)
     M, N = 300, 520
     for K in (1024, 1030, 1088, 1100, 1152, 1190):
@@ -165,18 +166,19 @@ def test_pair_deep_stages_k_tails(a_major, b_major):
         assert gb.gemm_tn_last_kernels() == "gemm_tn_large2_kernel<deep>"
         check(result_view(D_st, M, N), d64, d16, K, 0, True, f"deep K={K}")
         slack_untouched(D_st, C_st, N)
-    # a K-major operand with rows off the 128-byte grid: 64-deep stages
+    # K-major operands with rows off the 128-byte grid
     K = 1100
     A_st = wl.operand(M, K, K + 4, 0, "int1", 5)
     B_st = wl.operand(N, K, K + 12, 0, "int1", 6)
     C_st = wl.operand(M, N, N, 0, "int4", 7)
-    D_st, st = run_gpu(M, N, K, A_st, K + 4, 0, B_st, K + 12, 0, C_st, N, 0,
-                       opts={"path": gb.PATH_LARGE, "tile_kernel": 2})
-    assert st == gb.OK
-    assert gb.gemm_tn_last_kernels() == "gemm_tn_large2_kernel"
     d64, d16 = oracle.gemm_tn(M, N, K, np_bits(A_st), K + 4, 0, np_bits(B_st), K + 12, 0,
                               np_bits(C_st), N)
-    check(result_view(D_st, M, N), d64, d16, K, 0, True, "shallow K=1100")
+    for k_stage, name in ((0, "gemm_tn_large2_kernel<deep>"), (64, "gemm_tn_large2_kernel")):
+        D_st, st = run_gpu(M, N, K, A_st, K + 4, 0, B_st, K + 12, 0, C_st, N, 0,
+                           opts={"path": gb.PATH_LARGE, "tile_kernel": 2, "k_stage": k_stage})
+        assert st == gb.OK
+        assert gb.gemm_tn_last_kernels() == name
+        check(result_view(D_st, M, N), d64, d16, K, 0, True, f"off-grid rows K=1100 {name}")
 
 
 @pytest.mark.parametrize("tile_n", [128, 160, 192, 224, 256])
