@@ -115,6 +115,8 @@ KERNEL_SOURCES = {
     "gemm_tn_large_kernel": ["gemm_large.cuh", "common.cuh", "ptx.cuh"],
     "gemm_tn_large2_kernel": ["gemm_large2.cuh", "gemm_large.cuh", "common.cuh", "ptx.cuh"],
     "gemm_tn_skinny_kernel": ["gemm_skinny.cuh", "common.cuh", "ptx.cuh"],
+    "gemm_tn_skinny_cluster_kernel": ["gemm_skinny_cluster.cuh", "gemm_skinny.cuh", "common.cuh",
+                                      "ptx.cuh"],
     "gemm_tn_wide_kernel": ["gemm_wide.cuh", "gemm_large.cuh", "common.cuh", "ptx.cuh"],
 }
 
@@ -615,7 +617,8 @@ def bench_skinny(dev, stream, steps=200):
             "algorithmic_bytes": w.min_bytes, "GB_per_s": gbs,
             "hbm_peak_GB_per_s": float(peaks["hbm_gbs"]),
             "frac": gbs / float(peaks["hbm_gbs"]), "peak_kind": kind,
-            "launches_per_call": 2, "calls": steps,
+            "kernels": gb.gemm_tn_last_kernels(),
+            "launches_per_call": gb.gemm_tn_last_launch_count(), "calls": steps,
             "l2": "B (512 MiB) larger than L2, calls back to back"}
 
 
@@ -721,7 +724,7 @@ def configs_summary(w, kernel_ms, kernels_run, roofline, extra, peaks, peak_kind
     sk = extra.get("skinny_m16")
     if sk:
         s["skinny"] = {"us": round(sk["ms_per_call"] * 1e3, 1), "GB/s": round(sk["GB_per_s"], 1),
-                       "frac": r3(sk["frac"]), "bound": "hbm", "kernel": "skinny+splitk_reduce"}
+                       "frac": r3(sk["frac"]), "bound": "hbm", "kernel": _short(sk["kernels"])}
     cf = extra.get("configs", {})
     for name, bound in (("tiny", "latency"), ("square1024", "tensor"), ("ragged", "tensor")):
         c = cf.get(name)

@@ -32,6 +32,7 @@
 #include "gemm_large2.cuh"
 #include "gemm_wide.cuh"
 #include "gemm_skinny.cuh"
+#include "gemm_skinny_cluster.cuh"
 #include "gemm_strided.cuh"
 #include "repack.cuh"
 #include "scale.cuh"
@@ -93,9 +94,15 @@ int resolve_encoder() {
 
 template <int STAGES, int MP>
 cudaError_t set_skinny_attr() {
-  return cudaFuncSetAttribute(gemm_tn_skinny_kernel<STAGES, MP>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SkinnySmem<STAGES, MP>::kDynamicBytes);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tn_skinny_kernel<STAGES, MP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SkinnySmem<STAGES, MP>::kDynamicBytes);
+  constexpr int CS = cluster_stages(MP);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tn_skinny_cluster_kernel<CS, MP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ClusterSmem<CS, MP>::kDynamicBytes);
+  return e;
 }
 
 // Ring depth of the skinny kernel: stages of two 64-deep sub-blocks up to
@@ -299,18 +306,19 @@ int encode_operand_batched(CUtensorMap* map, const void* ptr, int64_t rows, int6
 }
 
 // K-major operand as K chunks: dims {64, rows, K/64, L}, the third stepping
-// K by 64 elements (128 bytes), box {64, box_rows, 2, 1}: one box brings 128
-// of K for box_rows rows, as two consecutive 128B-swizzled blocks.  Needs K
+// K by 64 elements (128 bytes), box {64, box_rows, depth, 1}: one box brings
+// 64 * depth of K for box_rows rows, as `depth` consecutive 128B-swizzled
+// blocks.  Needs K
 // a multiple of 64 (the inner dimension is never clipped, so a partial last
 // chunk would read past K); the chunk past the last one is zero-filled.
 int encode_operand_ko(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld,
-                      int64_t bstride, int64_t L, uint32_t box_rows) {
+                      int64_t bstride, int64_t L, uint32_t box_rows, uint32_t depth = 2) {
   const bool batched = L > 1 && bstride != 0;
   cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(K / 64),
                         static_cast<cuuint64_t>(batched ? L : 1)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld) * 2, 128,
                            static_cast<cuuint64_t>(batched ? bstride : rows * ld) * 2};
-  cuuint32_t box[4] = {64, box_rows, 2, 1}, estr[4] = {1, 1, 1, 1};
+  cuuint32_t box[4] = {64, box_rows, depth, 1}, estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -916,8 +924,114 @@ cudaError_t launch_skinny_kernels(int grid, const CUtensorMap& tmA, const CUtens
   }
 }
 
+// The cluster-reduced skinny kernel for MMA width MP: a cluster of p.cs CTAs
+// per 128-row tile of B, a programmatic dependent launch.
+template <int MP>
+cudaError_t launch_skinny_cluster_mp(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                     const SkinnyClusterArgs& p, const EpiArgs& ep,
+                                     cudaStream_t stream) {
+  constexpr int S = cluster_stages(MP);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(p.cs);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles * p.cs));
+  cfg.blockDim = dim3(kSkinnyThreads);
+  cfg.dynamicSmemBytes = ClusterSmem<S, MP>::kDynamicBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_tn_skinny_cluster_kernel<S, MP>, tmA, tmB, p, ep);
+}
+
+cudaError_t launch_skinny_cluster(int mp, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                  const SkinnyClusterArgs& p, const EpiArgs& ep,
+                                  cudaStream_t stream) {
+  switch (mp) {
+    case 16: return launch_skinny_cluster_mp<16>(tmA, tmB, p, ep, stream);
+    case 32: return launch_skinny_cluster_mp<32>(tmA, tmB, p, ep, stream);
+    case 48: return launch_skinny_cluster_mp<48>(tmA, tmB, p, ep, stream);
+    case 64: return launch_skinny_cluster_mp<64>(tmA, tmB, p, ep, stream);
+    case 96: return launch_skinny_cluster_mp<96>(tmA, tmB, p, ep, stream);
+    case 128: return launch_skinny_cluster_mp<128>(tmA, tmB, p, ep, stream);
+    case 192: return launch_skinny_cluster_mp<192>(tmA, tmB, p, ep, stream);
+    default: return launch_skinny_cluster_mp<256>(tmA, tmB, p, ep, stream);
+  }
+}
+
+// Cluster size of the cluster-reduced skinny kernel: the largest power of
+// two up to 8 with tiles * cs within the SMs and at least one K block per
+// split.  It is used for MMA widths up to 64 and at least two CTAs per tile
+// (returns 0 otherwise: the contiguous split over one CTA per SM takes
+// those).  Measured back to back (us, cluster / split): M=16, N=K=8192
+// 24.5 / 26.4; 16 x 4096 x 16384 23.9 / 26.7; 64 x 8192^2 27.5 / 29.3.  One
+// CTA per tile leaves SMs idle, and an SM streams B from HBM at only about
+// 47 GB/s, so the split wins there (16 x 16384^2: 90 / 83; 32 x 16384 x
+// 8192: 46.6 / 45.4); so it does at widths 128 and up, where more of each
+// stage is MMA work (128 x 8192^2: 31.4 / 30.3; 256 x 8192^2 42.5 / 39.1).
+int skinny_cluster_size(int M, int tiles, int k_blocks, const DeviceState& st) {
+  if (skinny_mp(M) > 64 || tiles <= 0 || 2 * tiles > st.num_sms) return 0;
+  int cs = 1;
+  while (cs < kClusterMaxCs && tiles * cs * 2 <= st.num_sms && cs * 2 <= k_blocks) cs *= 2;
+  return cs >= 2 ? cs : 0;
+}
+
+// The skinny path with the K split reduced in a cluster: one kernel, no
+// workspace.
+int launch_skinny_cluster_path(const Problem& q, int cs, cudaStream_t stream,
+                               const gemm_tn_options& o, const DeviceState& st) {
+  const int mp = skinny_mp(q.M);
+  SkinnyClusterArgs p;
+  std::memset(&p, 0, sizeof p);
+  p.M = static_cast<int>(q.M);
+  p.N = static_cast<int>(q.N);
+  p.K = static_cast<int>(q.K);
+  p.tiles = static_cast<int>((q.N + kSkinnyBN - 1) / kSkinnyBN);
+  p.cs = cs;
+  const int sub = cluster_sub(mp);
+  p.k_blocks = static_cast<int>((q.K + kSkinnyBK * sub - 1) / (kSkinnyBK * sub));
+  p.ko = q.K % 64 == 0 ? 1 : 0;
+  p.timeout_ns = o.timeout_ns ? o.timeout_ns : kDefaultTimeoutNs;
+  p.test_stall = o.test_stall;
+  CUtensorMap tmA, tmB;
+  int s;
+  if (p.ko) {
+    s = encode_operand_ko(&tmA, q.A, q.M, q.K, q.ldA, 0, 1, static_cast<uint32_t>(mp),
+                          static_cast<uint32_t>(sub));
+    if (s == GEMM_TN_OK)
+      s = encode_operand_ko(&tmB, q.B, q.N, q.K, q.ldB, 0, 1, kSkinnyBN,
+                            static_cast<uint32_t>(sub));
+  } else {
+    s = encode_operand(&tmA, q.A, q.M, q.K, q.ldA, 0, static_cast<uint32_t>(mp));
+    if (s == GEMM_TN_OK) s = encode_operand(&tmB, q.B, q.N, q.K, q.ldB, 0, kSkinnyBN);
+  }
+  if (s != GEMM_TN_OK) return s;
+  p.trace = trace_for(o, st, stream);
+  if (launch_skinny_cluster(mp, tmA, tmB, p, epi_of(q), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_CUDA;
+  }
+  t_last_launches = 1;
+  t_last_kernels = "gemm_tn_skinny_cluster_kernel";
+  return GEMM_TN_OK;
+}
+
 int launch_skinny(const Problem& q, cudaStream_t stream, const gemm_tn_options& o,
                   const DeviceState& st) {
+  // Without an explicit split count, the cluster-reduced kernel whenever one
+  // wave of clusters covers the tiles.
+  if (o.split_k == 0) {
+    const int mp = skinny_mp(q.M), sub = cluster_sub(mp);
+    const int tiles = static_cast<int>((q.N + kSkinnyBN - 1) / kSkinnyBN);
+    const int k_blocks = static_cast<int>((q.K + kSkinnyBK * sub - 1) / (kSkinnyBK * sub));
+    const int cs = skinny_cluster_size(static_cast<int>(q.M), tiles, k_blocks, st);
+    if (cs > 0) return launch_skinny_cluster_path(q, cs, stream, o, st);
+  }
   const int64_t M = q.M, N = q.N, K = q.K, ldA = q.ldA, ldB = q.ldB;
   const void *A = q.A, *B = q.B;
   SkinnyArgs p;

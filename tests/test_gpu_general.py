@@ -158,11 +158,18 @@ def test_batched_small_m_runs_the_tile_kernel():
 
 
 def test_skinny_path_scaled_separate_d():
+    # both skinny kernels: the cluster-reduced one (the library's choice here
+    # up to M = 64) and the contiguous split with its reduction kernel
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for M in (16, 40, 64, 160, 256):
         cs = Case(M, 1000, 3000, 1, seed=7 + M)
         D, k = cs.run(0.5, -2.0, 0, dict(path=gb.PATH_SKINNY))
+        assert k == ("gemm_tn_skinny_cluster_kernel" if M <= 64 else
+                     "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel"), k
+        cs.verify(D, 0.5, -2.0, 0, True, f"skinny auto M={M}")
+        D, k = cs.run(0.5, -2.0, 0, dict(path=gb.PATH_SKINNY, split_k=sms))
         assert k == "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel", k
-        cs.verify(D, 0.5, -2.0, 0, True, f"skinny M={M}")
+        cs.verify(D, 0.5, -2.0, 0, True, f"skinny split M={M}")
 
 
 def test_stream_k_with_batches_and_scalars():
@@ -180,9 +187,10 @@ def test_beta_zero_does_not_read_c():
     D2, _ = cs.run(3.0, 0.0, 0, pass_c=False)  # C pointer NULL
     assert torch.equal(D.view(torch.int16), D2.view(torch.int16))
     cs1 = Case(40, 500, 2000, 1, seed=10)     # skinny path, C NULL
-    D3, k = cs1.run(1.0, 0.0, 0, dict(path=gb.PATH_SKINNY), pass_c=False)
-    assert k.startswith("gemm_tn_skinny_kernel"), k
-    cs1.verify(D3, 1.0, 0.0, 0, True, "skinny beta 0")
+    for extra in ({}, {"split_k": torch.cuda.get_device_properties(0).multi_processor_count}):
+        D3, k = cs1.run(1.0, 0.0, 0, dict(path=gb.PATH_SKINNY, **extra), pass_c=False)
+        assert k.startswith("gemm_tn_skinny"), k
+        cs1.verify(D3, 1.0, 0.0, 0, True, f"skinny beta 0 {k}")
 
 
 @pytest.mark.parametrize("beta", [0.0, 1.0, -0.5])
@@ -278,20 +286,22 @@ def test_batched_large_sampled_rows():
             check(got, d64, d16, K, 0, False, f"problem {l} rows {m0}..{m0 + rows}")
 
 
-@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "streamk", "tile_split",
-                                  "pair_split"])
+@pytest.mark.parametrize("case", ["wide", "single", "scale", "skinny", "skinny_split", "streamk",
+                                  "tile_split", "pair_split"])
 def test_graph_capture_replays_match_eager(case):
     """A call captured into a CUDA graph (after one eager call has set the
     library up) replays to the same bits as the eager call.  The tile-kernel
-    and scale-only paths allocate nothing per call; the skinny path's
-    workspace comes from the library's pool in stream order, which capture
-    records as graph memory nodes."""
-    M, N, K, L = {"skinny": (16, 1000, 3000, 1), "tile_split": (300, 200, 4000, 1),
+    scale-only and cluster-reduced skinny paths allocate nothing per call;
+    the split skinny path's workspace comes from the library's pool in
+    stream order, which capture records as graph memory nodes."""
+    M, N, K, L = {"skinny": (16, 1000, 3000, 1), "skinny_split": (16, 1000, 3000, 1),
+                  "tile_split": (300, 200, 4000, 1),
                   "pair_split": (300, 520, 3000, 1)}.get(case, (520, 392, 328, 2))
     tile = {"wide": gb.TILE_WIDE, "single": gb.TILE_SINGLE, "scale": gb.TILE_WIDE,
-            "skinny": 0, "streamk": gb.TILE_WIDE, "tile_split": gb.TILE_SINGLE,
-            "pair_split": gb.TILE_PAIR}[case]
-    path = gb.PATH_SKINNY if case == "skinny" else gb.PATH_LARGE
+            "skinny": 0, "skinny_split": 0, "streamk": gb.TILE_WIDE,
+            "tile_split": gb.TILE_SINGLE, "pair_split": gb.TILE_PAIR}[case]
+    path = gb.PATH_SKINNY if case.startswith("skinny") else gb.PATH_LARGE
+    split = {"tile_split": 3, "pair_split": 3, "skinny_split": 64}.get(case, 0)
     alpha = 0.0 if case == "scale" else -2.0
     cs = Case(M, N, K, L, seed=20)
     dev = torch.device("cuda")
@@ -304,7 +314,7 @@ def test_graph_capture_replays_match_eager(case):
                                      cs.sC, D.data_ptr(), cs.ldD, cs.sD, 0, stream,
                                      dict(path=path, tile_kernel=tile,
                                           stream_k=1 if case == "streamk" else 0,
-                                          split_k=3 if case in ("tile_split", "pair_split") else 0))
+                                          split_k=split))
     assert call(D_eager, torch.cuda.current_stream().cuda_stream) == gb.OK
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()

@@ -262,8 +262,12 @@ def test_skinny_path_shapes_and_splits(M):
         D_st, st = run_gpu(M, N, K, A_st, K, 0, B_st, K + 8, 0, C_st, N, 0,
                            opts={"path": gb.PATH_SKINNY, "split_k": split})
         assert st == gb.OK
-        assert gb.gemm_tn_last_launch_count() == 2
-        assert gb.gemm_tn_last_kernels() == "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel"
+        if split or M > 64:  # the contiguous split and its reduction kernel
+            assert gb.gemm_tn_last_launch_count() == 2
+            assert gb.gemm_tn_last_kernels() == "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel"
+        else:  # the library's choice up to M = 64: K split inside a cluster per tile
+            assert gb.gemm_tn_last_launch_count() == 1
+            assert gb.gemm_tn_last_kernels() == "gemm_tn_skinny_cluster_kernel"
         check(result_view(D_st, M, N), d64, d16, K, 0, True, f"skinny M={M} split={split}")
         outs.append(D_st)
     for o in outs[1:]:

@@ -5,10 +5,10 @@ one call fail as an exhausted memory pool would (no device fault is
 involved: the request is refused before anything is enqueued).  The
 library's contract for that case:
 
-  * a workspace the caller asked for -- the skinny split-K path, an explicit
-    K split of the 128-row or CTA-pair kernel, the forced repack route of
-    the strided entry point -- makes the call return GEMM_TN_ERR_NO_MEMORY
-    and leaves D untouched;
+  * a workspace the caller asked for -- the skinny path's contiguous split
+    (an explicit split count), an explicit K split of the 128-row or
+    CTA-pair kernel, the forced repack route of the strided entry point --
+    makes the call return GEMM_TN_ERR_NO_MEMORY and leaves D untouched;
   * a workspace the library chose by itself -- an automatic K split,
     stream-K, the automatic repack route -- is dropped: the call runs the
     kernel that needs none and D matches the oracle bit for bit (integer
@@ -67,7 +67,7 @@ def _oracle(M, N, K, L, ops):
 
 
 @pytest.mark.parametrize("what,M,N,K,opts", [
-    ("skinny path", 16, 2048, 4096, {}),
+    ("skinny split path", 16, 2048, 4096, dict(split_k=64)),
     ("explicit 128-row split", 512, 512, 4096, dict(path=gb.PATH_LARGE, tile_kernel=1,
                                                       tile_n=128, split_k=4)),
     ("explicit pair split", 512, 512, 4096, dict(path=gb.PATH_LARGE, tile_kernel=2,
@@ -105,6 +105,14 @@ def test_chosen_workspace_is_dropped(what, M, N, K, L, opts, split_kernels, plai
     d64, d16 = _oracle(M, N, K, L, ops)
     check(got_plain.reshape(L, M, N), d64, d16, K, 0, True, f"{what}, no workspace")
     assert np.array_equal(got_plain, got_split)
+
+
+def test_skinny_cluster_path_needs_no_workspace():
+    # the library's skinny choice reduces the K split in a cluster: no pool
+    st, k, got, ops = _run(16, 2048, 4096, 1, dict(FAIL), seed=3)
+    assert st == gb.OK and k == "gemm_tn_skinny_cluster_kernel", (st, k)
+    d64, d16 = _oracle(16, 2048, 4096, 1, ops)
+    check(got.reshape(1, 16, 2048), d64, d16, 4096, 0, True, "skinny cluster, no pool")
 
 
 def _strided(opts, M=256, N=320, K=264, seed=2):

@@ -13,8 +13,8 @@ problem before a smaller one), so that a partial sum the second call failed
 to write would show up as the first call's stale value.  Each result is
 checked against the CPU oracle -- bit for bit on integer-valued inputs,
 within the fp32-accumulation tolerance of the parity tests on real values --
-and against gemm_tn's skinny path on the same inputs, which runs the same
-kernels with the same split and so must agree bit for bit.
+and against gemm_tn's skinny path with the same split over one CTA per SM on
+the same inputs, which runs the same kernels and so must agree bit for bit.
 """
 import numpy as np
 import pytest
@@ -64,10 +64,12 @@ def _call_and_check(M, N, K, seed, integer, what):
                               np_bits(C_st), N)
     check(got, d64, d16, K, 0, integer, what)
 
-    # gemm_tn's skinny path: the same kernels and split, a pooled workspace
+    # gemm_tn's skinny path with the contiguous split over one CTA per SM:
+    # the same kernels and split, a pooled workspace
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     ref = C_st.to(dev)
     st = gb.gemm_tn_ex(M, N, K, A.data_ptr(), K, 0, B.data_ptr(), K, 0, ref.data_ptr(), N, 0, s,
-                       dict(path=gb.PATH_SKINNY))
+                       dict(path=gb.PATH_SKINNY, split_k=sms))
     assert st == gb.OK, gb.gemm_tn_status_string(st)
     assert gb.gemm_tn_last_kernels() == "gemm_tn_skinny_kernel+gemm_tn_splitk_reduce_kernel"
     torch.cuda.synchronize()
