@@ -1406,9 +1406,9 @@ namespace {
 cudaError_t repack2d(const void* src, int64_t s_sr, int64_t s_sc, void* dst, int64_t s_dr,
                      int64_t s_dc, int64_t rows, int64_t cols, cudaStream_t stream) {
   if (s_sc == 1 && s_dc == 1 && rows <= 65535) {
-    const int64_t chunks = (cols + 7) / 8;
-    const dim3 grid(static_cast<unsigned>(
-                        std::min<int64_t>((chunks + kRepackThreads - 1) / kRepackThreads, 64)),
+    const int64_t words = (cols + 7) / 8 + 1;  // 16-byte words a row can touch
+    const int64_t span = static_cast<int64_t>(kRepackThreads) * kRowWords;
+    const dim3 grid(static_cast<unsigned>(std::min<int64_t>((words + span - 1) / span, 64)),
                     static_cast<unsigned>(rows), 1);
     repack_rows_kernel<<<grid, kRepackThreads, 0, stream>>>(static_cast<const __half*>(src), s_sr,
                                                             static_cast<__half*>(dst), s_dr,

@@ -47,59 +47,93 @@ __global__ void __launch_bounds__(kRepackThreads)
   }
 }
 
-// 16 bytes at a 2-byte aligned address, read / written with the widest
-// accesses the alignment allows, never outside [p, p + 16).
-__device__ __forceinline__ uint4 ld16_any(const unsigned short* p) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  if ((a & 15u) == 0) return *reinterpret_cast<const uint4*>(p);
-  if ((a & 7u) == 0) {
-    const uint2 lo = reinterpret_cast<const uint2*>(p)[0], hi = reinterpret_cast<const uint2*>(p)[1];
-    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+// Bytes [sh, sh + 16) of the 32-byte concatenation lo:hi (sh even, 0..14):
+// words of the window shifted by whole words (q = sh / 4) and, for sh % 4
+// == 2, by a further half word.
+__device__ __forceinline__ uint4 shift_window(const uint4& lo, const uint4& hi, int sh) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t o[4];
+  const bool half = (sh & 3) != 0;
+  switch (sh >> 2) {
+#define GEMM_TN_SHIFT_CASE(Q)                                                        \
+  case Q:                                                                            \
+    _Pragma("unroll") for (int i = 0; i < 4; ++i) o[i] =                             \
+        half ? __funnelshift_r(w[Q + i], w[Q + i + 1], 16) : w[Q + i];               \
+    break;
+    GEMM_TN_SHIFT_CASE(0)
+    GEMM_TN_SHIFT_CASE(1)
+    GEMM_TN_SHIFT_CASE(2)
+    default:
+      _Pragma("unroll") for (int i = 0; i < 3; ++i) o[i] =
+          half ? __funnelshift_r(w[3 + i], w[4 + i], 16) : w[3 + i];
+      o[3] = half ? __funnelshift_r(w[6], w[7], 16) : w[6];
+      break;
+#undef GEMM_TN_SHIFT_CASE
   }
-  if ((a & 3u) == 0) {
-    const unsigned* w = reinterpret_cast<const unsigned*>(p);
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  const unsigned* w = reinterpret_cast<const unsigned*>(p + 1);
-  const uint32_t h0 = p[0], h7 = p[7], w0 = w[0], w1 = w[1], w2 = w[2];
-  return make_uint4(h0 | (w0 << 16), (w0 >> 16) | (w1 << 16), (w1 >> 16) | (w2 << 16),
-                    (w2 >> 16) | (h7 << 16));
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__device__ __forceinline__ void st16_any(unsigned short* p, uint4 v) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  if ((a & 15u) == 0) {
-    *reinterpret_cast<uint4*>(p) = v;
-  } else if ((a & 7u) == 0) {
-    reinterpret_cast<uint2*>(p)[0] = make_uint2(v.x, v.y);
-    reinterpret_cast<uint2*>(p)[1] = make_uint2(v.z, v.w);
-  } else if ((a & 3u) == 0) {
-    unsigned* w = reinterpret_cast<unsigned*>(p);
-    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
-  } else {
-    unsigned* w = reinterpret_cast<unsigned*>(p + 1);
-    p[0] = static_cast<unsigned short>(v.x);
-    w[0] = (v.x >> 16) | (v.y << 16);
-    w[1] = (v.y >> 16) | (v.z << 16);
-    w[2] = (v.z >> 16) | (v.w << 16);
-    p[7] = static_cast<unsigned short>(v.w >> 16);
-  }
-}
+// dst(r, c) = src(r, c) when both views have unit column stride (any 2-byte
+// alignment of either row): blockIdx.y selects the row, each thread builds
+// whole 16-byte words of the destination row at their aligned addresses
+// from the two aligned 16-byte source words under them (a funnel shift
+// when the two rows are misaligned differently), so every load and every
+// interior store is one aligned vector access.  Source words are read only
+// where they hold bytes of the row (an aligned word never crosses a page);
+// the partial words at the two ends of the destination row are written
+// element by element.  A thread handles kRowWords words, kRepackThreads
+// apart, with all their loads issued before the first store, so that enough
+// bytes are in flight to stream at HBM rate.
+constexpr int kRowWords = 4;
 
-// dst(r, c) = src(r, c) when both views have unit column stride: each thread
-// moves 8 consecutive columns of one row (blockIdx.y selects the row).
 __global__ void __launch_bounds__(kRepackThreads)
     repack_rows_kernel(const __half* __restrict__ src, int64_t s_sr, __half* __restrict__ dst,
                        int64_t s_dr, int rows, int cols) {
+  (void)rows;
   const unsigned short* s =
       reinterpret_cast<const unsigned short*>(src) + static_cast<int64_t>(blockIdx.y) * s_sr;
   unsigned short* d = reinterpret_cast<unsigned short*>(dst) + static_cast<int64_t>(blockIdx.y) * s_dr;
-  for (int c = 8 * (static_cast<int>(blockIdx.x) * kRepackThreads + static_cast<int>(threadIdx.x));
-       c < cols; c += 8 * kRepackThreads * static_cast<int>(gridDim.x)) {
-    if (c + 8 <= cols) {
-      st16_any(d + c, ld16_any(s + c));
-    } else {
-      for (int j = c; j < cols; ++j) d[j] = s[j];
+  const uintptr_t sb = reinterpret_cast<uintptr_t>(s), db = reinterpret_cast<uintptr_t>(d);
+  const uintptr_t s_end = sb + 2 * static_cast<uintptr_t>(cols);  // one past the row's bytes
+  const uintptr_t d_end = db + 2 * static_cast<uintptr_t>(cols);
+  const int a_d = static_cast<int>(db & 15u);
+  // destination word w covers bytes [d0 + 16 w, d0 + 16 w + 16); element j of
+  // the row sits at byte 2 j + a_d of that range, fed from source byte
+  // sb + 2 j, i.e. source bytes [sb - a_d + 16 w, ... + 16)
+  const uintptr_t d0 = db - a_d;
+  const int words = static_cast<int>((d_end - d0 + 15) / 16);
+  const intptr_t src_off = static_cast<intptr_t>(sb) - a_d;  // source byte of dst byte d0
+  const int sh = static_cast<int>(static_cast<uintptr_t>(src_off) & 15u);
+  constexpr int kSpan = kRepackThreads * kRowWords;  // words per block and round
+  for (int w0 = static_cast<int>(blockIdx.x) * kSpan + static_cast<int>(threadIdx.x); w0 < words;
+       w0 += kSpan * static_cast<int>(gridDim.x)) {
+    uint4 lo[kRowWords], hi[kRowWords];
+#pragma unroll
+    for (int i = 0; i < kRowWords; ++i) {
+      const int w = w0 + i * kRepackThreads;
+      const uintptr_t a0 = (src_off + 16 * static_cast<intptr_t>(w)) & ~static_cast<uintptr_t>(15);
+      lo[i] = make_uint4(0u, 0u, 0u, 0u);
+      hi[i] = lo[i];
+      if (w < words && a0 + 16 > sb && a0 < s_end) lo[i] = *reinterpret_cast<const uint4*>(a0);
+      if (w < words && sh != 0 && a0 + 32 > sb && a0 + 16 < s_end)
+        hi[i] = *reinterpret_cast<const uint4*>(a0 + 16);
+    }
+#pragma unroll
+    for (int i = 0; i < kRowWords; ++i) {
+      const int w = w0 + i * kRepackThreads;
+      if (w >= words) break;
+      const uint4 v = sh ? shift_window(lo[i], hi[i], sh) : lo[i];
+      const uintptr_t dw = d0 + 16 * static_cast<uintptr_t>(w);
+      if (dw >= db && dw + 16 <= d_end) {
+        *reinterpret_cast<uint4*>(dw) = v;
+      } else {
+        const unsigned short* vh = reinterpret_cast<const unsigned short*>(&v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uintptr_t a = dw + 2 * e;
+          if (a >= db && a < d_end) *reinterpret_cast<unsigned short*>(a) = vh[e];
+        }
+      }
     }
   }
 }
