@@ -57,6 +57,10 @@ def parse(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large")
+    ap.add_argument("--shape", default="",
+                    help="M,N,K: time that K-major fp32-accumulation problem instead of the "
+                         "named workload (uniform [-1,1] operands, B ~ N(0,1/K) when M <= 256, "
+                         "C = 0), for profiling one kernel on a chosen size")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
@@ -274,9 +278,8 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    from dense_fp16_tensor_gb300 import workloads as wl
     import oracle
-    w = wl.WORKLOADS[args.workload]
+    w = pick_workload(args)
     cores = oracle.default_threads()
     # size each step to about one second of oracle work
     probe = max(1, min(w.M, cores))
@@ -308,6 +311,18 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- our arm
 
+def pick_workload(args):
+    """The named workload, or the K-major problem given by --shape."""
+    from dense_fp16_tensor_gb300 import workloads as wl
+    if not args.shape:
+        return wl.WORKLOADS[args.workload]
+    M, N, K = (int(x) for x in args.shape.split(","))
+    skinny = M <= 256
+    return wl.Workload(f"shape_{M}x{N}x{K}", 9, M, N, K, wl.MAJOR_K, K, wl.MAJOR_K, K, N,
+                       wl.ACC_F32, "normal" if skinny else "u11",
+                       "normal_k" if skinny else "u11", "zero")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -324,7 +339,7 @@ def run_ours(args):
     g.build()
     gb.lib()
 
-    w = wl.WORKLOADS[args.workload]
+    w = pick_workload(args)
     A_st, B_st, C_st = wl.make_inputs(w)
     A, Bm, CD = A_st.to(dev), B_st.to(dev), C_st.to(dev)
     stream = torch.cuda.Stream(dev)
@@ -690,8 +705,22 @@ def bench_configs(dev, stream, steps=50):
             row["stream_sets"] = nsets
         out[name] = row
         del sets
+    # the same isolated timing of a one-element torch kernel: the launch and
+    # event floor under which no isolated call can go
+    one = torch.zeros(1, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            flush.fill_(1)
+            e0.record(stream)
+            one.add_(1.0)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    out["floor_us"] = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
     out["l2"] = ("isolated: 256 MiB written between calls, each call timed alone (median of "
-                 f"{steps}); stream: back to back over input copies totalling > 160 MB")
+                 f"{steps}); stream: back to back over input copies totalling > 160 MB; "
+                 "floor_us: a one-element kernel timed the isolated way")
     out["peak_kind"] = kind
     return out
 
@@ -726,6 +755,8 @@ def configs_summary(w, kernel_ms, kernels_run, roofline, extra, peaks, peak_kind
         s["skinny"] = {"us": round(sk["ms_per_call"] * 1e3, 1), "GB/s": round(sk["GB_per_s"], 1),
                        "frac": r3(sk["frac"]), "bound": "hbm", "kernel": _short(sk["kernels"])}
     cf = extra.get("configs", {})
+    if "floor_us" in cf:
+        s["isolated_floor_us"] = round(cf["floor_us"], 1)
     for name, bound in (("tiny", "latency"), ("square1024", "tensor"), ("ragged", "tensor")):
         c = cf.get(name)
         if not c:
