@@ -78,6 +78,12 @@ struct LargeArgs {
   int ks_splits;       // 1 = no split
   int ks_kb_per;
   float* ks_ws;
+  // CTA-pair kernel: with ks_splits > 1, tiles [0, ks_tile0) run whole and
+  // only tiles [ks_tile0, num_tiles) are split (0: every tile is split).
+  // The reduction kernel's tile t is the partial slot of split tile t, and
+  // ks_tile0 there is the first split tile in its own (128-row) raster.
+  // The 128-row kernel splits every tile (ks_tile0 = 0).
+  int ks_tile0;
   // CTA-pair kernel: output tile width (a multiple of 32 in [64, 256]; 256
   // whenever ks_splits > 1).  The other kernels use their compile-time width.
   int bn;
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kTileReduceThreads)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float sum[32][64 + 4];
-  const int t = static_cast<int>(blockIdx.y);
+  const int t = static_cast<int>(blockIdx.y);  // partial slot (split tile t of the launch)
   const int piece = static_cast<int>(blockIdx.x);
   const int q = piece / (BN / 64), c = piece - q * (BN / 64);
   const float4* ws4 = reinterpret_cast<const float4*>(p.ks_ws);
@@ -594,7 +600,7 @@ __global__ void __launch_bounds__(kTileReduceThreads)
   }
   __syncthreads();
   int tb, tm, tn;
-  batch_tile(p, t, tb, tm, tn);
+  batch_tile(p, p.ks_tile0 + t, tb, tm, tn);
   const int r = static_cast<int>(threadIdx.x) >> 3, seg = static_cast<int>(threadIdx.x) & 7;
   const int m = tm * kLargeBM + 32 * q + r, n = tn * BN + 64 * c + 8 * seg;
   if (m >= p.M || n >= p.N) return;

@@ -69,12 +69,29 @@ struct PairSmem {
   static_assert(kDynamicBytes <= 232448, "over the 227 KiB of shared memory per CTA");
 };
 
-// Work unit u: split u % ks_splits of tile u / ks_splits, K blocks
-// [kb0, kb1) (the whole K loop when ks_splits == 1).
-__device__ __forceinline__ void pair_unit(const LargeArgs& p, int u, int& t, int& kb0, int& kb1) {
-  t = p.ks_splits > 1 ? u / p.ks_splits : u;
-  kb0 = (u - t * p.ks_splits) * p.ks_kb_per;
+// Work units: with ks_splits == 1 unit u is tile u; otherwise units below
+// ks_tile0 are whole tiles and unit ks_tile0 + v is split v % ks_splits of
+// tile ks_tile0 + v / ks_splits.  Sets the tile, its K blocks [kb0, kb1) and
+// the partial slot of a split unit (-1 for a whole tile).
+__device__ __forceinline__ void pair_unit(const LargeArgs& p, int u, int& t, int& kb0, int& kb1,
+                                          int64_t& slot) {
+  if (p.ks_splits <= 1 || u < p.ks_tile0) {
+    t = u;
+    kb0 = 0;
+    kb1 = p.k_blocks;
+    slot = -1;
+    return;
+  }
+  const int v = u - p.ks_tile0;
+  const int j = v / p.ks_splits, sp = v - j * p.ks_splits;
+  t = p.ks_tile0 + j;
+  kb0 = sp * p.ks_kb_per;
   kb1 = min(kb0 + p.ks_kb_per, p.k_blocks);
+  slot = static_cast<int64_t>(j) * p.ks_splits + sp;  // split tile j, split sp
+}
+
+__device__ __forceinline__ int pair_units(const LargeArgs& p) {
+  return p.ks_splits > 1 ? p.ks_tile0 + (p.num_tiles - p.ks_tile0) * p.ks_splits : p.num_tiles;
 }
 
 template <bool DEEP = false>
@@ -104,7 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const bool leader = rank == 0;
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
-  const int units = p.num_tiles * p.ks_splits;  // work units, round-robin over the pairs
+  const int units = pair_units(p);  // work units, round-robin over the pairs
   // The next kernel in the stream (this call's reduction, or the next
   // call's kernel) may become resident now; it waits for this grid's
   // completion before it touches memory.
@@ -170,7 +187,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int local = 0;
       for (int u = pair; ok && u < units; u += num_pairs, ++local) {
         int t, kb0, kb1;
-        pair_unit(p, u, t, kb0, kb1);
+        int64_t slot;
+        pair_unit(p, u, t, kb0, kb1, slot);
         int tb, tm, tn;
         batch_tile(p, t, tb, tm, tn);
         const int za = p.a_batched ? tb : 0, zb = p.b_batched ? tb : 0;
@@ -238,7 +256,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int done = 0;
       for (int u = pair; ok && u < units; u += num_pairs, ++done) {
         int t, kb0, kb1;
-        pair_unit(p, u, t, kb0, kb1);
+        int64_t slot;
+        pair_unit(p, u, t, kb0, kb1, slot);
         if (!wait_bounded<true>(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag, p.timeout_ns,
                                 timeout_code(kRoleMma, 0x200 + acc), true, peer_abort)) {
           ok = false;
@@ -314,18 +333,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     uint4 cnext[8];
     for (int u = pair; u < units; u += num_pairs) {
       int t, kb0, kb1;
-      pair_unit(p, u, t, kb0, kb1);
-      if (p.ks_splits > 1) {
+      int64_t slot;
+      pair_unit(p, u, t, kb0, kb1, slot);
+      if (slot >= 0) {
         // K-split unit: this warp's 32 x 128 of the fp32 partial, stored as
-        // part of 128-row tile 2t + rank (the reduction's view of the pair
-        // tile), split u - t * ks_splits
+        // part of 128-row partial tile 2j + rank of split sp (slot = j *
+        // ks_splits + sp; the reduction's view of the split pair tile)
         if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                           timeout_code(kRoleEpilogue, acc), true, peer_abort))
           break;
         tc_fence_after();
         // (split units always have bn = 256: two whole chunks per warp)
         const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kPairBN + col0;
-        const int64_t ur = (2 * static_cast<int64_t>(t) + rank) * p.ks_splits + (u - t * p.ks_splits);
+        const int64_t jj = slot / p.ks_splits, sp = slot - jj * p.ks_splits;
+        const int64_t ur = (2 * jj + rank) * p.ks_splits + sp;
         float4* ws4 = reinterpret_cast<float4*>(p.ks_ws);
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {

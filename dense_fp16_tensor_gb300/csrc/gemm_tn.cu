@@ -544,7 +544,19 @@ int pair_split_count(int64_t M, int64_t N, int64_t K, int64_t pair_tiles, int ac
 // instead of 16 x 12 of 256 x 256 (2.53 waves, i.e. 3).
 bool p_acc_f16(int accum) { return accum == GEMM_TN_ACC_F16; }
 
-int pair_tile_n(int64_t M, int64_t N, int64_t L, int b_major, int max_pairs) {
+// The last-wave split (see launch_large) counts for 256-wide tiles: the
+// partial last round then takes 1/s of a tile's time, plus ~0.1 of a tile
+// for the partial sums and their reduction.
+int last_wave_splits(int64_t tiles, int max_pairs, int k_blocks) {
+  if (max_pairs <= 0 || tiles < max_pairs) return 0;
+  const int64_t rem = tiles % max_pairs;
+  if (rem == 0) return 0;
+  const int s = static_cast<int>(std::min<int64_t>(std::min<int64_t>(max_pairs / rem, 4), k_blocks / 8));
+  return s >= 2 ? s : 0;
+}
+
+int pair_tile_n(int64_t M, int64_t N, int64_t L, int b_major, int max_pairs, bool split_ok,
+                int k_blocks) {
   int best = 256;
   double best_cost = -1.0;
   for (int bn = 256; bn >= 128; bn -= 32) {
@@ -552,7 +564,9 @@ int pair_tile_n(int64_t M, int64_t N, int64_t L, int b_major, int max_pairs) {
     const int64_t tiles = ((M + 255) / 256) * ((N + bn - 1) / bn) * L;
     const int64_t waves = (tiles + max_pairs - 1) / max_pairs;
     const double step = std::max(bn / 2.0, (4096.0 + 16.0 * bn) / 75.0);
-    const double cost = static_cast<double>(waves) * step;
+    double cost = static_cast<double>(waves) * step;
+    const int s = bn == 256 && split_ok ? last_wave_splits(tiles, max_pairs, k_blocks) : 0;
+    if (s) cost = (static_cast<double>(tiles / max_pairs) + 1.0 / s + 0.1) * step;
     if (best_cost < 0.0 || cost < 0.97 * best_cost) {
       best = bn;
       best_cost = cost;
@@ -571,17 +585,14 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
   int kind = o.tile_kernel;
   int tile_n = o.tile_n;
   if (kind == 0) {
-    // The CTA pair (256 x 256 per two SMs, double-buffered accumulators,
-    // 128-deep stages) is the fastest kernel on everything but the largest
-    // problems with long K; 256 x 256 tiles on one CTA (undoubled
-    // accumulator) do a few per cent more work per joule, which wins once a
-    // stream of such calls runs at the board's power limit: from
-    // M*N*K*L >= 2^39 (one 8192^3 problem) with K >= 8192 and enough tiles to
-    // fill half the SMs.  With shorter K the drain of the undoubled
-    // accumulator costs more than that (16384^2 x 2048: 1317 against 1639
-    // TFLOP/s for the pair, 16384^2 x 4096: 1454 against 1709).  128-row
-    // tiles when a side is too short for 256, and 128 x 128 tiles when even
-    // 128 x 256 tiles would leave half the SMs idle.
+    // The CTA pair (256 x BN per two SMs, double-buffered accumulators,
+    // 128-deep stages) for every problem with both sides above 128: at
+    // 8192^3 it runs 1785-1787 TFLOP/s over 20 calls and 1621-1624 over 400
+    // (power-limited) against 1751-1763 and 1619-1620 for 256 x 256 tiles
+    // on one CTA, whose single accumulator stalls the MMA for each drain
+    // (16384^2 x 2048: 1317 against 1639).  128-row tiles when a side is too
+    // short for 256, and 128 x 128 tiles when even 128 x 256 tiles would
+    // leave half the SMs idle.
     const int64_t tiles_128x256 = ((M + 127) / 128) * ((N + 255) / 256) * q.L;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
     if (pair_split_count(M, N, K, pair_tiles, accum, st) > 1) {
@@ -595,10 +606,7 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
       const bool no_split = accum == GEMM_TN_ACC_F16 || K < 2048;
       if (tile_n == 0) tile_n = (2 * tiles_128x128 <= st.num_sms && no_split) ? 64 : 128;
     } else if (M > kLargeBM && N > 128) {
-      const int64_t tiles256 = ((M + 255) / 256) * ((N + 255) / 256) * q.L;
-      const double mnkl = static_cast<double>(M) * N * K * q.L;
-      const bool wide_ok = K >= 8192 && 2 * tiles256 >= st.num_sms && mnkl >= 549755813888.0;
-      kind = wide_ok ? 3 : (st.max_pairs > 0 ? 2 : 1);
+      kind = st.max_pairs > 0 ? 2 : 3;
     } else {
       kind = 1;
       if (tile_n == 0 && N <= 128) tile_n = 128;  // a 256-wide tile would be half empty
@@ -623,8 +631,13 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
     return GEMM_TN_ERR_INVALID_ARG;
   const int bn = wide ? 256
                : pair ? (pair_split ? 256
-                         : pair_width_asked ? o.tile_n
-                                            : pair_tile_n(M, N, q.L, b_major, st.max_pairs))
+                         : pair_width_asked
+                             ? o.tile_n
+                             : pair_tile_n(M, N, q.L, b_major, st.max_pairs,
+                                           accum == GEMM_TN_ACC_F32 && o.split_k == 0 &&
+                                               o.stream_k != -1,
+                                           static_cast<int>((K + (K >= 1024 ? 127 : 63)) /
+                                                            (K >= 1024 ? 128 : 64))))
                : (tile_n == 64 || tile_n == 128) ? tile_n : 256;
   const int bm = (pair || wide) ? 256 : kLargeBM;
   // K-chunk boxes (stages of 128 of K) for 128 x 128 tiles when both
@@ -765,9 +778,36 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
         p.ks_splits = nsplit;
         p.ks_ws = static_cast<float*>(ks_ws);
       }
+    } else {
+      // The last, partial wave of 256-wide tiles split along K over the
+      // pairs the whole tiles leave idle: after `full` rounds of whole tiles
+      // the rem tiles left run as s splits each in one more round, which
+      // then takes 1/s of a tile's time (s <= 4 and at least 8 K blocks per
+      // split).  fp32 accumulation; off with stream_k = -1; dropped when
+      // the pool cannot serve the partial sums.
+      const int P = st.max_pairs;
+      const int full = P > 0 ? p.num_tiles / P : 0;
+      const int rem = p.num_tiles - full * P;
+      int s = last_wave_splits(p.num_tiles, P, p.k_blocks);
+      if (!p.acc_f16 && bn == 256 && o.split_k == 0 && o.stream_k != -1 && s >= 2) {
+        const int kb_per = (p.k_blocks + s - 1) / s;
+        s = (p.k_blocks + kb_per - 1) / kb_per;
+        const size_t bytes = static_cast<size_t>(rem) * 2 * s * kLargeBM * kPairBN * 4;
+        if (ws_alloc(&ks_ws, bytes, st, stream, o) == cudaSuccess) {
+          p.ks_tile0 = full * P;
+          p.ks_kb_per = kb_per;
+          p.ks_splits = s;
+          p.ks_ws = static_cast<float*>(ks_ws);
+        } else {
+          cudaGetLastError();
+          ks_ws = nullptr;
+        }
+      }
     }
-    const int pairs = static_cast<int>(
-        std::min<int64_t>(static_cast<int64_t>(p.num_tiles) * p.ks_splits, st.max_pairs));
+    const int64_t units = p.ks_splits > 1
+                              ? p.ks_tile0 + static_cast<int64_t>(p.num_tiles - p.ks_tile0) * p.ks_splits
+                              : p.num_tiles;
+    const int pairs = static_cast<int>(std::min<int64_t>(units, st.max_pairs));
     cudaError_t le =
         deep ? launch_pdl(gemm_tn_large2_kernel<true>, dim3(2 * pairs), dim3(kPairThreads),
                           PairSmem<true>::kDynamicBytes, stream, tmA, tmB, tmD, p)
@@ -783,8 +823,9 @@ int launch_large(const Problem& q, cudaStream_t stream, const gemm_tn_options& o
         pr.group_m = 2 * p.group_m;
         pr.tiles_per_batch = 2 * p.tiles_per_batch;
         pr.num_tiles = 2 * p.num_tiles;
+        pr.ks_tile0 = 2 * p.ks_tile0;  // split pair tiles only
         const dim3 rgrid(static_cast<unsigned>(4 * (kPairBN / 64)),
-                         static_cast<unsigned>(pr.num_tiles));
+                         static_cast<unsigned>(2 * (p.num_tiles - p.ks_tile0)));
         le = launch_pdl(gemm_tn_tile_reduce_kernel<kPairBN>, rgrid, dim3(kTileReduceThreads), 0,
                         stream, pr);
       }

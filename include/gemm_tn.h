@@ -164,17 +164,21 @@ typedef struct {
                            hanging */
   int tile_kernel;      /* large path: 0 = choose (2 with a K split when
                            few 256 x 256 tiles have K loops of at least
-                           2 x 4096; else 1 with 128 x 128 tiles
-                           when 128 x 256 tiles would fill at most half the
-                           SMs; else, when M and N exceed 128, 3 if
-                           M*N*K*batch >= 2^39, K >= 8192 and the 256 x 256
-                           tiles of all problems fill at least half the SMs,
-                           otherwise 2; else 1),
+                           2 x 4096; else 1 with 128 x 128 tiles (or
+                           128 x 64) when 128 x 256 tiles would fill at most
+                           half the SMs; else 2 when M and N exceed 128;
+                           else 1),
                            1 = single-CTA 128 x tile_n
                            tiles, 2 = CTA-pair 256 x 256 tiles (two SMs per
                            tile, tcgen05 cta_group::2), 3 = single-CTA
                            256 x 256 tiles (tile_n is ignored by 2 and 3) */
-  int stream_k;         /* single-CTA 256 x 256 kernel, fp32 accumulation:
+  int stream_k;         /* CTA-pair kernel, fp32 accumulation, 256-wide
+                           tiles: unless -1, when the last round of tiles
+                           would leave at least half the pairs idle, its
+                           tiles run as 2-4 K splits each (partial sums
+                           through a workspace, added in a fixed order with
+                           C once by a second kernel); 0 (default) = on.
+                           Single-CTA 256 x 256 kernel, fp32 accumulation:
                            1 = split the last, partial wave of tiles over all
                            SMs (stream-K: K ranges of equal length, partial
                            sums through a workspace, added in a fixed order),

@@ -178,3 +178,32 @@ def test_pair_split_timeout_reports_and_recovers():
                            opts=dict(path=gb.PATH_LARGE, tile_kernel=2, split_k=2))
     assert k == PAIR_SPLIT.format("<deep>"), k
     check(got, d64, d16, K, 0, True, "pair split after timeout")
+
+
+# --- the pair kernel's last-wave split: after the rounds of whole 256 x 256
+# tiles, the tiles of the last, partial round run as K splits over the pairs
+# that would otherwise idle, and the same reduction adds their partials.
+
+@pytest.mark.parametrize("M,N,K,L,am,bm", [
+    (2560, 2048, 4096, 1, 0, 0),    # 80 tiles: one round of 76, then 4 tiles x 4 splits
+    (1280, 2048, 4096, 2, 1, 0),    # two problems of 40 tiles, M-major A
+    (2400, 2100, 3000, 1, 0, 1),    # 90 tiles: 14 x 3 splits; ragged edges, N-major B
+])
+def test_pair_last_wave_split_integers_bit_exact(M, N, K, L, am, bm):
+    o = dict(path=gb.PATH_LARGE, tile_kernel=2, tile_n=256)
+    got, d64, d16, k = run(M, N, K, L, 1.0, 1.0, seed=30, am=am, bm=bm, opts=o)
+    assert k == PAIR_SPLIT.format("<deep>"), k
+    check(got, d64, d16, K, 0, True, f"last-wave split {M}x{N}x{K}xL{L}")
+    # the same call without the split: the same bits
+    got2, _, _, k2 = run(M, N, K, L, 1.0, 1.0, seed=30, am=am, bm=bm,
+                         opts=dict(o, stream_k=-1))
+    assert k2 == "gemm_tn_large2_kernel<deep>", k2
+    assert np.array_equal(got, got2)
+
+
+def test_pair_last_wave_split_scaled_real_values():
+    o = dict(path=gb.PATH_LARGE, tile_kernel=2, tile_n=256)
+    a = run(2560, 2048, 4096, 1, -0.5, 2.0, dist="u11", cdist="u11", seed=31, opts=o)
+    b = run(2560, 2048, 4096, 1, -0.5, 2.0, dist="u11", cdist="u11", seed=31, opts=o)
+    assert np.array_equal(a[0], b[0])  # fixed summation order
+    check(a[0], a[1], a[2], 4096, 0, False, "last-wave split real")
