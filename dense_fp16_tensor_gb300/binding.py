@@ -33,10 +33,10 @@ EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan
             "gemm_tn_scaled", "gemm_tn_batched", "gemm_tn_batched_ex", "gemm_tn_trace_read")
 
 # Phase-trace record layout (gemm_tn_trace_read).
-TRACE_SLOTS = 10
+TRACE_SLOTS = 12
 TRACE_CTAS = 512
 TRACE_FIELDS = ("entry", "ready", "first_stage", "last_mma", "first_acc", "last_chunk",
-                "stores_done", "exit", "sm", "units")
+                "stores_done", "exit", "sm", "units", "cycles_entry", "cycles_exit")
 
 # Size of the fixed scratch array behind gemm_tn_skinny_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024

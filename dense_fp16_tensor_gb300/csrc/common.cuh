@@ -113,12 +113,14 @@ __device__ __forceinline__ __half epi_one(const EpiArgs& e, bool acc_f16, uint32
 //   6 stores done         the CTA's last stores performed (first epilogue warp)
 //   7 exit                before tensor memory is freed (thread 0)
 //   8 SM id, 9 work units of this CTA
+//   10, 11 the SM's cycle counter at entry and at exit (with slots 0 and 7:
+//          the clock the CTA ran at)
 // CTAs past kTraceCtas are not recorded.
-constexpr int kTraceSlots = 10;
+constexpr int kTraceSlots = 12;
 constexpr int kTraceCtas = 512;
 enum : int {
   kTrEntry = 0, kTrReady, kTrFirstStage, kTrLastMma, kTrFirstAcc, kTrLastChunk,
-  kTrStoresDone, kTrExit, kTrSm, kTrUnits
+  kTrStoresDone, kTrExit, kTrSm, kTrUnits, kTrCyclesEntry, kTrCyclesExit
 };
 
 // (One translation unit: the definition lives here, like g_error_word.)
@@ -130,6 +132,21 @@ __device__ __forceinline__ void trace_mark(int on, int slot) {
 
 __device__ __forceinline__ void trace_value(int on, int slot, uint64_t v) {
   if (on && blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceSlots + slot] = v;
+}
+
+// Entry / exit stamps with the SM's cycle counter beside the global time.
+__device__ __forceinline__ void trace_entry(int on) {
+  if (on && blockIdx.x < kTraceCtas) {
+    g_trace[blockIdx.x * kTraceSlots + kTrCyclesEntry] = static_cast<uint64_t>(clock64());
+    g_trace[blockIdx.x * kTraceSlots + kTrEntry] = globaltimer_ns();
+  }
+}
+
+__device__ __forceinline__ void trace_exit(int on) {
+  if (on && blockIdx.x < kTraceCtas) {
+    g_trace[blockIdx.x * kTraceSlots + kTrExit] = globaltimer_ns();
+    g_trace[blockIdx.x * kTraceSlots + kTrCyclesExit] = static_cast<uint64_t>(clock64());
+  }
 }
 
 __device__ __forceinline__ uint32_t sm_id() {

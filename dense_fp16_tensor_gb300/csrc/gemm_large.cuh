@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
-    trace_mark(p.trace, kTrEntry);
+    trace_entry(p.trace);
     trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
+  if (threadIdx.x == 0) trace_exit(p.trace);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * BN);

@@ -128,7 +128,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
-    trace_mark(p.trace, kTrEntry);
+    trace_entry(p.trace);
     trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < kPairStages; ++s) {
       mbar_init(full0 + 8 * s, 1);  // the even CTA's arming; both CTAs' bytes (odd: unused)
@@ -430,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no CTA leaves while its peer's MMAs or arrivals may touch it
-  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
+  if (threadIdx.x == 0) trace_exit(p.trace);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, kPairTmemCols);

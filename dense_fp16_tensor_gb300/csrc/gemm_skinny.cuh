@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   const int nseg = segs.count();
 
   if (threadIdx.x == 0) {
-    trace_mark(p.trace, kTrEntry);
+    trace_entry(p.trace);
     trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
+  if (threadIdx.x == 0) trace_exit(p.trace);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, L::kTmemCols);

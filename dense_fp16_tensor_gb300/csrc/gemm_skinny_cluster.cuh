@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
-    trace_mark(p.trace, kTrEntry);
+    trace_entry(p.trace);
     trace_value(p.trace, kTrSm, sm_id());
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kSkinnyThreads, 1)
   // No CTA leaves (or frees its shared memory) while a peer may still read it.
   __syncthreads();
   cluster_barrier();
-  if (threadIdx.x == 0) trace_mark(p.trace, kTrExit);
+  if (threadIdx.x == 0) trace_exit(p.trace);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);

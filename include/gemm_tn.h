@@ -361,6 +361,7 @@ GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail);
  *   4 first accumulator ready 5 last output chunk issued (first epilogue warp)
  *   6 that warp's stores done 7 exit (before tensor memory is freed)
  *   8 SM id                   9 work units (tiles or segments) of the CTA
+ *  10 SM cycle counter at entry  11 SM cycle counter at exit
  * Times are the GPU's global nanosecond timer; 0 marks a point the CTA did
  * not pass (or a kernel that does not stamp it: the skinny kernel stores
  * partial sums, so its slot 6 stays 0).  Synchronises `stream`, then copies
@@ -368,7 +369,7 @@ GEMM_TN_API int gemm_tn_check_device_error(void* stream, uint32_t* detail);
  * max_ctas * GEMM_TN_TRACE_SLOTS words) and sets *recorded (if non-NULL) to
  * the number of CTAs with an entry stamp.  Returns GEMM_TN_OK,
  * GEMM_TN_ERR_INVALID_ARG (out NULL, max_ctas < 0) or GEMM_TN_ERR_CUDA. */
-#define GEMM_TN_TRACE_SLOTS 10
+#define GEMM_TN_TRACE_SLOTS 12
 #define GEMM_TN_TRACE_CTAS 512
 GEMM_TN_API int gemm_tn_trace_read(void* stream, uint64_t* out, int max_ctas, int* recorded);
 
