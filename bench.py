@@ -954,9 +954,21 @@ def bench_general(dev, stream, steps=20):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
         tf = 2.0 * L * M * N * K / (ms * 1e-3) / 1e12
+        # compulsory bytes: A and B read once, C read when beta != 0, D written
+        nbytes = 2 * L * (M * K + N * K + (M * N if beta != 0.0 else 0) + M * N)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        f_t = tf / float(peaks["bf16_tflops"])
+        f_h = gbs / float(peaks["hbm_gbs"])
+        # FLOP per byte against the ridge point of the two measured peaks
+        intensity = 2.0 * L * M * N * K / nbytes
+        ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
         out[name] = {"M": M, "N": N, "K": K, "batch": L, "alpha": alpha, "beta": beta,
                      "kernels": gb.gemm_tn_last_kernels(), "ms_per_call": ms,
-                     "TFLOP_per_s": tf, "frac_of_peak": tf / float(peaks["bf16_tflops"]),
+                     "TFLOP_per_s": tf, "frac_of_peak": f_t,
+                     "GB_per_s_algorithmic": gbs, "frac_of_hbm_peak": f_h,
+                     "flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+                     "bound": "hbm" if intensity < ridge else "tensor",
+                     "frac_of_bound": f_h if intensity < ridge else f_t,
                      "peak_kind": kind}
         del A, Bm, C, D
     return out

@@ -196,7 +196,10 @@ __device__ __forceinline__ void epi_load_c(const LargeArgs& p, const __half* cb,
   for (int i = 0; i < 8; ++i) v[i] = load_c_piece(p, cb, m_base + 4 * i + prow, n_base + 8 * pseg);
 }
 
-__device__ __forceinline__ void epi_stage_c(uint8_t* stg, uint32_t lane, const uint4 (&v)[8]) {
+// (Nothing to stage when C is not read: the add then skips the buffer.)
+__device__ __forceinline__ void epi_stage_c(const LargeArgs& p, uint8_t* stg, uint32_t lane,
+                                            const uint4 (&v)[8]) {
+  if (!p.e.read_c) return;
   const int prow = static_cast<int>(lane >> 3), pseg = static_cast<int>(lane & 7);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -225,7 +228,8 @@ __device__ __noinline__ void epi_store_ragged(const LargeArgs& p, const uint8_t*
   }
 }
 
-// Combine this lane's accumulator row r (64 words) with its staged C row,
+// Combine this lane's accumulator row r (64 words) with its staged C row
+// (or scale it alone when C is not read: nothing was staged then),
 // then store the chunk whose first element is D(m_row0, n0) of problem tb;
 // only its first `width` columns (64, or 32 for the last chunk of a tile
 // whose width is an odd multiple of 32) belong to the tile.  Returns (in
@@ -236,10 +240,17 @@ __device__ __forceinline__ bool epi_store_chunk(const LargeArgs& p, const CUtens
                                                 int tb, int m_row0, int n0,
                                                 const uint32_t (&r)[64], int width = 64) {
   uint8_t* my_row = stg + lane * 128;
+  if (p.e.read_c) {
 #pragma unroll
-  for (int s8 = 0; s8 < 8; ++s8) {
-    uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
-    *q = add_c8(p, r + 8 * s8, *q);
+    for (int s8 = 0; s8 < 8; ++s8) {
+      uint4* q = reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7)));
+      *q = add_c8(p, r + 8 * s8, *q);
+    }
+  } else {
+#pragma unroll
+    for (int s8 = 0; s8 < 8; ++s8)
+      *reinterpret_cast<uint4*>(my_row + 16 * (s8 ^ static_cast<int>(lane & 7))) =
+          add_c8(p, r + 8 * s8, make_uint4(0u, 0u, 0u, 0u));
   }
   fence_proxy_async_smem();
   __syncwarp();
@@ -510,7 +521,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
       if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
       __syncwarp();
-      epi_stage_c(stg, lane, cnext);
+      epi_stage_c(p, stg, lane, cnext);
       if (kChunks > 1) epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
@@ -525,7 +536,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         if (c > 0) {
           if (lane == 0) bulk_wait_group_read0();
           __syncwarp();
-          epi_stage_c(stg, lane, cnext);
+          epi_stage_c(p, stg, lane, cnext);
           if (c + 1 < kChunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
         }

@@ -377,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       epi_load_c(p, cb, m_base, n_base, lane, cnext);
       if (lane == 0) bulk_wait_group_read0();  // the last store has read the buffer
       __syncwarp();
-      epi_stage_c(stg, lane, cnext);
+      epi_stage_c(p, stg, lane, cnext);
       if (nchunks > 1) epi_load_c(p, cb, m_base, n_base + 64, lane, cnext);
       __syncwarp();
       if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
@@ -398,7 +398,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         if (c > 0) {
           if (lane == 0) bulk_wait_group_read0();
           __syncwarp();
-          epi_stage_c(stg, lane, cnext);
+          epi_stage_c(p, stg, lane, cnext);
           if (c + 1 < nchunks) epi_load_c(p, cb, m_base, n_base + 64 * (c + 1), lane, cnext);
           __syncwarp();
         }

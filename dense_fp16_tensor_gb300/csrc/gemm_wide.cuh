@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     auto load_chunk = [&](int c, uint4 (&v)[8]) {
       epi_load_c(p, cb, tm * kWideBM + row0, tn * kWideBN + 64 * c, lane, v);
     };
-    auto stage_chunk = [&](const uint4 (&v)[8]) { epi_stage_c(stg, lane, v); };
+    auto stage_chunk = [&](const uint4 (&v)[8]) { epi_stage_c(p, stg, lane, v); };
     // C of chunks 0 and 1 (0 staged, 1 in registers), once the previous
     // tile's last store has finished reading the staging buffer.
     auto preload_c = [&]() {
