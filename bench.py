@@ -7,10 +7,11 @@ over that problem (the whole hot path: TMA ring, tcgen05 main loop, C add and
 fp16 epilogue).  The metric is TFLOP/s (2*M*N*K per step).
 
 Prints ONE JSON line (rank 0).  Besides the device-timed value it reports:
-  e2e           the same metric through the C ABI with host buffers: every
-                step copies A, B and C from pinned host memory to the device
-                and D back, inside the timed region (steps pipelined over two
-                buffer sets and three streams; the serial figure beside it)
+  e2e           the same metric through the C ABI with host buffers
+                (gemm_tn_host): every step copies A, B and C from pinned host
+                memory to the device and D back, inside the timed region (row
+                panels overlap copies in, GEMMs and copies out; the serial
+                one-panel figure beside it)
   roofline      the main kernel against the measured dense bf16/fp16 peak
   cpu_baseline  the CPU oracle (fp64 triple loop) timed on a bounded sample
                 of the same workload on this host's cores
@@ -393,62 +394,42 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(ws, w.flops, args.steps, total_ms)
 
-    # ---- end to end through the C ABI with host buffers.  Every step copies
-    # its A, B and C from pinned host memory and its D back.  The steps are
-    # pipelined over two device buffer sets: step i's host-to-device copies
-    # (one copy stream), its GEMM (the compute stream) and its device-to-host
-    # copy (a second copy stream) overlap the neighbouring steps.  The
-    # serial form (one stream, nothing overlapped) is reported beside it.
+    # ---- end to end through the C ABI with host buffers: one gemm_tn_host
+    # call per step, A, B and C read from page-locked host memory and D
+    # written back to it inside the call.  The library copies B in, then
+    # panels of rows of A and C on a copy stream, runs each panel's GEMM as
+    # soon as its rows are in and copies its D rows out on a second copy
+    # stream.  The serial form (one panel: all copies in, the GEMM, the copy
+    # out, nothing overlapped) is reported beside it.
     hA = A_st.pin_memory()
     hB = B_st.pin_memory()
     hC = C_st.pin_memory()
-    hD = [torch.empty_like(C_st).pin_memory() for _ in range(2)]
-    bufs = [(torch.empty_like(A), torch.empty_like(Bm), torch.empty_like(CD)) for _ in range(2)]
+    hD = torch.empty_like(C_st).pin_memory()
     h2d = (hA.numel() + hB.numel() + hC.numel()) * 2
-    d2h = hD[0].numel() * 2
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    d2h = hD.numel() * 2
 
-    def e2e_run(nsteps, pipelined):
+    def e2e_run(nsteps, panel_rows):
+        o = gb.make_options(tile_n=args.tile_n, tile_kernel=args.tile_kernel,
+                            stream_k=args.stream_k, host_panel_rows=panel_rows)
         first = torch.cuda.Event(enable_timing=True)
         last = torch.cuda.Event(enable_timing=True)
-        out_done = []
-        cin = s_in if pipelined else stream
-        cout = s_out if pipelined else stream
-        first.record(cin)
-        for i in range(nsteps):
-            dA, dB, dCD = bufs[i % 2 if pipelined else 0]
-            if pipelined and i >= 2:
-                cin.wait_event(out_done[i - 2])  # buffer set free again
-            with torch.cuda.stream(cin):
-                dA.copy_(hA, non_blocking=True)
-                dB.copy_(hB, non_blocking=True)
-                dCD.copy_(hC, non_blocking=True)
-            if pipelined:
-                ev = torch.cuda.Event()
-                ev.record(cin)
-                stream.wait_event(ev)
-            with torch.cuda.stream(stream):
-                step(dA.data_ptr(), dB.data_ptr(), dCD.data_ptr())
-            if pipelined:
-                ev = torch.cuda.Event()
-                ev.record(stream)
-                cout.wait_event(ev)
-            with torch.cuda.stream(cout):
-                hD[i % 2].copy_(dCD, non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(cout)
-            out_done.append(ev)
-        last.record(cout)
+        first.record(stream)
+        for _ in range(nsteps):
+            st = gb.gemm_tn_host(w.M, w.N, w.K, 1.0, hA.data_ptr(), w.ldA, w.a_major,
+                                 hB.data_ptr(), w.ldB, w.b_major, 1.0, hC.data_ptr(), w.ldC,
+                                 hD.data_ptr(), w.ldC, w.accum, sp, o)
+            if st != gb.OK:
+                raise gb.GemmTnError(st, "gemm_tn_host")
+        last.record(stream)
         torch.cuda.synchronize()
         return first.elapsed_time(last) / nsteps
 
-    e2e_run(2, True)
-    e2e_run(2, False)
+    e2e_run(2, 0)
+    e2e_run(1, w.M)
     barrier()
-    e2e_ms = e2e_run(args.e2e_steps, True)
-    e2e_serial_ms = e2e_run(max(2, args.e2e_steps // 2), False)
+    e2e_ms = e2e_run(args.e2e_steps, 0)
+    e2e_serial_ms = e2e_run(max(2, args.e2e_steps // 2), w.M)
     e2e_ms, e2e_serial_ms = max_over_ranks([e2e_ms, e2e_serial_ms], dev)
-    del bufs
 
     if rank != 0:
         if ws > 1:
@@ -517,7 +498,9 @@ def run_ours(args):
         "e2e": {"value": whole_job_tflops(ws, w.flops, 1, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": args.e2e_steps,
-                "pipelining": "two buffer sets; H2D, GEMM and D2H on three streams",
+                "pipelining": "gemm_tn_host: B in, then row panels of A and C in on a copy "
+                              "stream, each panel's GEMM on the compute stream, its D rows "
+                              "out on a second copy stream",
                 "serial_ms_per_step": e2e_serial_ms,
                 "h2d_gb_per_s": h2d / (e2e_ms * 1e-3) / 1e9,
                 "serial_value": whole_job_tflops(ws, w.flops, 1, e2e_serial_ms)},
@@ -776,8 +759,11 @@ def configs_summary(w, kernel_ms, kernels_run, roofline, extra, peaks, peak_kind
 
 
 def bench_strided(dev, stream, steps=20):
-    """General-stride path (gemm_tn_strided, copy producer) on M=N=K=4096 with
-    leading dimensions K+1 (not TMA-expressible), fp32 accumulation."""
+    """General-stride entry point (gemm_tn_strided) on M=N=K=4096 with
+    leading dimensions K+1 for A and B and N+1 for C/D (rows TMA cannot
+    address), fp32 accumulation: the automatic route (repacking A and B,
+    C/D read and written in place) and the copy-producer kernel (no
+    workspace), calls back to back."""
     import torch
 
     from dense_fp16_tensor_gb300 import binding as gb
@@ -788,30 +774,36 @@ def bench_strided(dev, stream, steps=20):
     Bm = wl.draw((N * ld,), "u11", 7002).to(dev)
     CD = torch.zeros(M * (N + 1), dtype=torch.float16, device=dev)
     sp = stream.cuda_stream
-
-    def step():
-        st = gb.gemm_tn_strided(M, N, K, A.data_ptr(), ld, 1, Bm.data_ptr(), ld, 1,
-                                CD.data_ptr(), N + 1, 1, 0, sp)
-        if st != gb.OK:
-            raise gb.GemmTnError(st)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
     peaks, kind = load_peaks()
-    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-    return {"workload": "M=N=K=4096, ld = K+1 (A, B), ldC = N+1, fp32 accumulate",
-            "kernels": gb.gemm_tn_last_kernels(), "ms_per_call": ms, "TFLOP_per_s": tf,
-            "frac_of_peak": tf / float(peaks["bf16_tflops"]), "peak_kind": kind}
+
+    def timed(route, n):
+        def step():
+            st = gb.gemm_tn_strided_ex(M, N, K, A.data_ptr(), ld, 1, Bm.data_ptr(), ld, 1,
+                                       CD.data_ptr(), N + 1, 1, 0, sp, {"path": route})
+            if st != gb.OK:
+                raise gb.GemmTnError(st)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        return {"kernels": gb.gemm_tn_last_kernels(),
+                "launches": gb.gemm_tn_last_launch_count(), "ms_per_call": ms,
+                "TFLOP_per_s": tf, "frac_of_peak": tf / float(peaks["bf16_tflops"]),
+                "peak_kind": kind}
+    out = {"workload": "M=N=K=4096, ld = K+1 (A, B), ldC = N+1, fp32 accumulate"}
+    out.update(timed(gb.PATH_AUTO, steps))
+    out["copy_route"] = timed(gb.PATH_STRIDED_COPY, max(2, steps // 10))
+    return out
 
 
 def bench_stream_k(dev, stream, steps=50, rounds=3):

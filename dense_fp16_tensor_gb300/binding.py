@@ -30,7 +30,8 @@ ERR_NO_MEMORY = 6
 EXPORTED = ("gemm_tn", "gemm_tn_ex", "gemm_tn_check_device_error", "gemm_tn_plan_path",
             "gemm_tn_last_launch_count", "gemm_tn_status_string", "gemm_tn_skinny_noalloc",
             "gemm_tn_last_kernels", "gemm_tn_strided", "gemm_tn_strided_ex",
-            "gemm_tn_scaled", "gemm_tn_batched", "gemm_tn_batched_ex", "gemm_tn_trace_read")
+            "gemm_tn_scaled", "gemm_tn_batched", "gemm_tn_batched_ex", "gemm_tn_trace_read",
+            "gemm_tn_host")
 
 # Phase-trace record layout (gemm_tn_trace_read).
 TRACE_SLOTS = 12
@@ -47,7 +48,8 @@ class GemmTnOptions(ctypes.Structure):
                 ("sync_check", ctypes.c_int), ("timeout_ns", ctypes.c_uint64),
                 ("test_stall", ctypes.c_int), ("tile_kernel", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("test_fail_alloc", ctypes.c_int),
-                ("k_stage", ctypes.c_int), ("trace", ctypes.c_int)]
+                ("k_stage", ctypes.c_int), ("trace", ctypes.c_int),
+                ("host_panel_rows", ctypes.c_int)]
 
 
 class GemmTnError(RuntimeError):
@@ -112,6 +114,9 @@ def lib() -> ctypes.CDLL:
         L.gemm_tn_scaled.restype = i32
         L.gemm_tn_scaled.argtypes = [i64, i64, i64, f32, vp, i64, i32, vp, i64, i32, f32,
                                      vp, i64, vp, i64, i32, vp]
+        L.gemm_tn_host.restype = i32
+        L.gemm_tn_host.argtypes = [i64, i64, i64, f32, vp, i64, i32, vp, i64, i32, f32,
+                                   vp, i64, vp, i64, i32, vp, ctypes.POINTER(GemmTnOptions)]
         _lib = L
         return L
 
@@ -127,9 +132,10 @@ TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_WIDE = 0, 1, 2, 3
 
 
 def make_options(path=0, split_k=0, tile_n=0, sync_check=0, timeout_ns=0, test_stall=0,
-                 tile_kernel=0, stream_k=0, test_fail_alloc=0, k_stage=0, trace=0):
+                 tile_kernel=0, stream_k=0, test_fail_alloc=0, k_stage=0, trace=0,
+                 host_panel_rows=0):
     return GemmTnOptions(path, split_k, tile_n, sync_check, timeout_ns, test_stall, tile_kernel,
-                         stream_k, test_fail_alloc, k_stage, trace)
+                         stream_k, test_fail_alloc, k_stage, trace, host_panel_rows)
 
 
 def gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream,
@@ -148,6 +154,19 @@ def gemm_tn_scaled(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ld
     beta == 0)."""
     return lib().gemm_tn_scaled(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ldC,
                                 D, ldD, accum_dtype, stream)
+
+
+def gemm_tn_host(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ldC, D, ldD,
+                 accum_dtype, stream, opts=None) -> int:
+    """C ``gemm_tn_host``: the scaled form with A, B, C and D given as HOST
+    addresses (page-locked memory for overlapped copies); ``opts`` as for
+    :func:`gemm_tn_ex`.  The host arrays must stay untouched until the
+    stream has passed the call."""
+    if isinstance(opts, dict):
+        opts = make_options(**opts)
+    p = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_tn_host(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ldC,
+                              D, ldD, accum_dtype, stream, p)
 
 
 def gemm_tn_batched(M, N, K, batch, alpha, A, ldA, strideA, a_major, B, ldB, strideB, b_major,

@@ -1674,3 +1674,225 @@ extern "C" GEMM_TN_API int gemm_tn_strided(int64_t M, int64_t N, int64_t K, cons
   return gemm_tn_strided_ex(M, N, K, A, sAm, sAk, B, sBn, sBk, CD, sCm, sCn, accum_dtype, stream,
                             nullptr);
 }
+
+// ---------------------------------------------------------------------------
+// Host-buffer entry point: B copied once, then panels of M rows of A and C
+// copied in on a copy stream, each panel's GEMM on the caller's stream as
+// soon as its rows have arrived, and its D rows copied out on a second copy
+// stream, so that copies in both directions and the GEMMs overlap.
+
+namespace {
+
+constexpr int kHostMaxPanels = 64;
+constexpr int kHostRing = 3;  // device slots for A and C/D panels
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t in_done[kHostMaxPanels];
+  cudaEvent_t gemm_done[kHostMaxPanels];
+  cudaEvent_t out_done[kHostMaxPanels];
+};
+
+std::mutex g_host_mu;  // held while a gemm_tn_host call enqueues (streams and events are shared)
+HostPipe g_pipe[kMaxDevices];
+
+// The device's copy streams and events, created on first use (under g_host_mu).
+int host_pipe(int dev, HostPipe*& hp) {
+  if (dev < 0 || dev >= kMaxDevices) return GEMM_TN_ERR_UNSUPPORTED;
+  hp = &g_pipe[dev];
+  if (hp->ready) return GEMM_TN_OK;
+  bool ok = cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kHostMaxPanels; ++i)
+    ok = cudaEventCreateWithFlags(&hp->in_done[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp->gemm_done[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp->out_done[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_CUDA;  // (what was created stays for the next attempt to leak; rare)
+  }
+  hp->ready = true;
+  return GEMM_TN_OK;
+}
+
+// Rows of M per panel: the caller's (rounded up to 8), else all of M up to
+// 1024 rows, else ceil(M / 8) rounded up to 256 and at least 512; never more
+// than kHostMaxPanels panels.
+int64_t host_panel_rows(int64_t M, int requested) {
+  int64_t P;
+  if (requested > 0)
+    P = (static_cast<int64_t>(requested) + 7) / 8 * 8;
+  else if (M <= 1024)
+    P = M;
+  else
+    P = std::max<int64_t>(512, ((M + 7) / 8 + 255) / 256 * 256);
+  if ((M + P - 1) / P > kHostMaxPanels) P = ((M + kHostMaxPanels - 1) / kHostMaxPanels + 7) / 8 * 8;
+  return std::max<int64_t>(P, 1);
+}
+
+// height rows of width elements: host (pitch spitch elements) -> device
+// (pitch dpitch elements), or back.
+cudaError_t copy2d(void* dst, int64_t dpitch, const void* src, int64_t spitch, int64_t width,
+                   int64_t height, cudaMemcpyKind kind, cudaStream_t s) {
+  if (width <= 0 || height <= 0) return cudaSuccess;
+  return cudaMemcpy2DAsync(dst, static_cast<size_t>(dpitch) * 2, src, static_cast<size_t>(spitch) * 2,
+                           static_cast<size_t>(width) * 2, static_cast<size_t>(height), kind, s);
+}
+
+// Byte range of a host (rows, cols) view with row pitch ld.
+void host_extent(const void* p, int64_t rows, int64_t cols, int64_t ld, uintptr_t& lo,
+                 uintptr_t& hi) {
+  lo = reinterpret_cast<uintptr_t>(p);
+  hi = lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2);
+}
+
+}  // namespace
+
+extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float alpha,
+                                        const void* A, int64_t ldA, int a_major, const void* B,
+                                        int64_t ldB, int b_major, float beta, const void* C,
+                                        int64_t ldC, void* D, int64_t ldD, int accum_dtype,
+                                        void* stream, const gemm_tn_options* opts) {
+  t_last_launches = 0;
+  t_last_kernels = "";
+  gemm_tn_options o;
+  std::memset(&o, 0, sizeof o);
+  if (opts) o = *opts;
+  if (!options_ok(o) || o.host_panel_rows < 0) return GEMM_TN_ERR_INVALID_ARG;
+  const int64_t kMax = 0x7FFFFFFF;
+  if (M < 0 || N < 0 || K < 0 || M > kMax || N > kMax || K > kMax) return GEMM_TN_ERR_INVALID_ARG;
+  if ((a_major != GEMM_TN_MAJOR_K && a_major != GEMM_TN_MAJOR_MN) ||
+      (b_major != GEMM_TN_MAJOR_K && b_major != GEMM_TN_MAJOR_MN) ||
+      (accum_dtype != GEMM_TN_ACC_F32 && accum_dtype != GEMM_TN_ACC_F16))
+    return GEMM_TN_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_TN_OK;
+  const bool use_ab = alpha != 0.f && K > 0;
+  const bool read_c = beta != 0.f;
+  // A (M,K) and B (N,K) rows of their stride-1 mode, C and D rows of N
+  const int64_t a_rows = a_major == GEMM_TN_MAJOR_K ? M : K, a_cols = a_major == GEMM_TN_MAJOR_K ? K : M;
+  const int64_t b_rows = b_major == GEMM_TN_MAJOR_K ? N : K, b_cols = b_major == GEMM_TN_MAJOR_K ? K : N;
+  if (D == nullptr || ldD < N || (read_c && (C == nullptr || ldC < N))) return GEMM_TN_ERR_INVALID_ARG;
+  if (use_ab && (A == nullptr || B == nullptr || ldA < a_cols || ldB < b_cols))
+    return GEMM_TN_ERR_INVALID_ARG;
+  uintptr_t d0, d1;
+  host_extent(D, M, N, ldD, d0, d1);
+  if (read_c && C != D) {
+    uintptr_t c0, c1;
+    host_extent(C, M, N, ldC, c0, c1);
+    if (overlap(c0, c1, d0, d1)) return GEMM_TN_ERR_INVALID_ARG;
+  }
+  if (read_c && C == D && ldC != ldD) return GEMM_TN_ERR_INVALID_ARG;
+  if (use_ab) {
+    uintptr_t a0, a1, b0, b1;
+    host_extent(A, a_rows, a_cols, ldA, a0, a1);
+    host_extent(B, b_rows, b_cols, ldB, b0, b1);
+    if (overlap(a0, a1, d0, d1) || overlap(b0, b1, d0, d1)) return GEMM_TN_ERR_INVALID_ARG;
+  }
+
+  DeviceState* st = nullptr;
+  int s = device_state(st);
+  if (s != GEMM_TN_OK) return s;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_TN_ERR_CUDA;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  const int64_t P = host_panel_rows(M, o.host_panel_rows);
+  const int panels = static_cast<int>((M + P - 1) / P);
+  const int ring = std::min(kHostRing, panels);
+  const int64_t Kp = round64(std::max<int64_t>(K, 1)), Np = round64(N), Pp = round64(P);
+  // device layouts: B and A panels keep their major (rows on 128-byte
+  // boundaries), C/D panels are row-major with ld Np
+  const size_t b_elems = use_ab ? static_cast<size_t>(b_major == GEMM_TN_MAJOR_K ? N * Kp : K * Np) : 0;
+  const size_t a_slot = use_ab ? static_cast<size_t>(a_major == GEMM_TN_MAJOR_K ? P * Kp : K * Pp) : 0;
+  const size_t c_slot = static_cast<size_t>(P * Np);
+  const size_t bytes = 2 * (b_elems + ring * (a_slot + c_slot));
+
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  HostPipe* hp = nullptr;
+  s = host_pipe(dev, hp);
+  if (s != GEMM_TN_OK) return s;
+  void* ws = nullptr;
+  if (ws_alloc(&ws, bytes, *st, cs, o) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_TN_ERR_NO_MEMORY;
+  }
+  __half* wB = static_cast<__half*>(ws);
+  __half* wA = wB + b_elems;
+  __half* wC = wA + ring * a_slot;
+  const __half* hA = static_cast<const __half*>(A);
+  const __half* hC = static_cast<const __half*>(C);
+  __half* hD = static_cast<__half*>(D);
+
+  gemm_tn_options og = o;
+  og.sync_check = 0;
+  og.host_panel_rows = 0;
+  int launches = 0;
+  const char* kernels = "";
+  int last_in = -1, last_out = -1;  // last recorded events of the copy streams
+  auto done = [&](int status) {
+    // join the copy streams back into `stream` and release the workspace
+    cudaEventRecord(hp->start, hp->in);
+    cudaStreamWaitEvent(cs, hp->start, 0);
+    if (last_out >= 0) cudaStreamWaitEvent(cs, hp->out_done[last_out], 0);
+    if (cudaFreeAsync(ws, cs) != cudaSuccess && status == GEMM_TN_OK) status = GEMM_TN_ERR_CUDA;
+    if (status != GEMM_TN_OK) cudaGetLastError();
+    return status;
+  };
+  if (cudaEventRecord(hp->start, cs) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+    return done(GEMM_TN_ERR_CUDA);
+  if (use_ab && copy2d(wB, b_major == GEMM_TN_MAJOR_K ? Kp : Np, B, ldB, b_cols, b_rows,
+                       cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
+    return done(GEMM_TN_ERR_CUDA);
+  for (int i = 0; i < panels; ++i) {
+    const int64_t m0 = i * P, rows = std::min(P, M - m0);
+    const int slot = i % ring;
+    __half* a_i = wA + slot * a_slot;
+    __half* c_i = wC + slot * c_slot;
+    // the slot's previous panel has been copied out (so its GEMM is done too)
+    if (i >= ring && cudaStreamWaitEvent(hp->in, hp->out_done[i - ring], 0) != cudaSuccess)
+      return done(GEMM_TN_ERR_CUDA);
+    cudaError_t e = cudaSuccess;
+    if (use_ab)
+      e = a_major == GEMM_TN_MAJOR_K
+              ? copy2d(a_i, Kp, hA + m0 * ldA, ldA, K, rows, cudaMemcpyHostToDevice, hp->in)
+              : copy2d(a_i, Pp, hA + m0, ldA, rows, K, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess && read_c)
+      e = copy2d(c_i, Np, hC + m0 * ldC, ldC, N, rows, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in_done[i], hp->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, hp->in_done[i], 0);
+    if (e != cudaSuccess) return done(GEMM_TN_ERR_CUDA);
+    last_in = i;
+    Problem q;
+    std::memset(&q, 0, sizeof q);
+    q.M = rows; q.N = N; q.K = K; q.L = 1;
+    q.alpha = alpha; q.beta = beta;
+    q.A = a_i; q.ldA = a_major == GEMM_TN_MAJOR_K ? Kp : Pp; q.a_major = a_major;
+    q.B = wB; q.ldB = b_major == GEMM_TN_MAJOR_K ? Kp : Np; q.b_major = b_major;
+    q.C = c_i; q.ldC = Np;
+    q.D = c_i; q.ldD = Np;
+    q.accum = accum_dtype;
+    s = run_problem(q, cs, &og);
+    if (s != GEMM_TN_OK) return done(s);
+    launches += t_last_launches;
+    if (i == 0) kernels = t_last_kernels;
+    e = cudaEventRecord(hp->gemm_done[i], cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->gemm_done[i], 0);
+    if (e == cudaSuccess)
+      e = copy2d(hD + m0 * ldD, ldD, c_i, Np, N, rows, cudaMemcpyDeviceToHost, hp->out);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->out_done[i], hp->out);
+    if (e != cudaSuccess) return done(GEMM_TN_ERR_CUDA);
+    last_out = i;
+  }
+  (void)last_in;
+  s = done(GEMM_TN_OK);
+  if (s != GEMM_TN_OK) return s;
+  t_last_launches = launches;
+  t_last_kernels = kernels;
+  if (o.sync_check) return gemm_tn_check_device_error(stream, nullptr);
+  return GEMM_TN_OK;
+}

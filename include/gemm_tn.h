@@ -208,6 +208,11 @@ typedef struct {
                            returns (the buffer is cleared on the stream
                            first; one buffer per device, so traced calls
                            that overlap on the GPU mix their records) */
+  int host_panel_rows;  /* gemm_tn_host: rows of M per panel (rounded up to a
+                           multiple of 8; 0 = the library's choice: all of M
+                           up to 1024 rows, else panels of ceil(M / 8)
+                           rounded up to 256 rows and at least 512; more than
+                           64 panels are merged to 64) */
 } gemm_tn_options;
 
 /*
@@ -345,6 +350,53 @@ GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K,
                                    void* CD, int64_t sCm, int64_t sCn,
                                    int accum_dtype, void* stream,
                                    const gemm_tn_options* opts);
+
+/*
+ * D = alpha * A.B^T + beta * C with A, B, C and D in HOST memory: the
+ * operands, layouts, accumulation modes and rounding are those of
+ * gemm_tn_scaled (A, B, C and D views as in gemm_tn; D may be C itself with
+ * ldD == ldC, but no other overlap of C and D is accepted), and the results
+ * are bit-identical to gemm_tn_scaled on device copies of the same arrays.
+ *
+ * The call copies B to the device, then A, C and D in panels of rows of M
+ * (gemm_tn_options.host_panel_rows), and overlaps the transfers with the
+ * work: panel i's GEMM runs on `stream` as soon as its A and C rows have
+ * arrived, while the next panels' rows are copied in on one of the
+ * library's copy streams and the finished panels' D rows are copied out on
+ * another.  Host-to-device and device-to-host copies share the host link, so
+ * a call of this kind is bound by its copies: per call about
+ * (bytes of A, B and C) / (host-to-device rate) plus the last panel's GEMM
+ * and copy-out.
+ *
+ * Ordering and ownership: the work is ordered after everything enqueued on
+ * `stream` before the call, and everything enqueued on `stream` after the
+ * call is ordered after all of it (the copy streams are joined back).  The
+ * call returns once the work is enqueued: A, B and C must not be written,
+ * and D not read, until `stream` has passed the call
+ * (cudaStreamSynchronize).  The host arrays should be page-locked
+ * (cudaHostAlloc / cudaHostRegister): copies from pageable memory are
+ * staged by the driver and do not overlap.  The device copies live in one
+ * workspace from the library's stream-ordered pool: N x K for B plus up to
+ * three panels of A (panel rows x K) and of C/D (panel rows x N), released
+ * in stream order at the end of the call.  Concurrent calls from several
+ * host threads are serialised while they enqueue (the copy streams are the
+ * library's, one pair per device).
+ *
+ * Only host_panel_rows, sync_check and the large-path controls of
+ * gemm_tn_options (path, tile_kernel, tile_n, split_k, stream_k, k_stage,
+ * timeout_ns) are read; they apply to every panel's GEMM.
+ * Errors: GEMM_TN_ERR_INVALID_ARG for negative or too large sizes, an ld
+ * smaller than its row, NULL with a nonzero extent, or C and D overlapping
+ * other than exactly; GEMM_TN_ERR_NO_MEMORY when the pool cannot serve the
+ * workspace (nothing enqueued); GEMM_TN_ERR_CUDA when a copy or launch
+ * fails.  M == 0 or N == 0 enqueues nothing.
+ */
+GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float alpha,
+                             const void* A, int64_t ldA, int a_major,
+                             const void* B, int64_t ldB, int b_major,
+                             float beta, const void* C, int64_t ldC,
+                             void* D, int64_t ldD, int accum_dtype, void* stream,
+                             const gemm_tn_options* opts);
 
 /* Synchronise `stream`, then read and clear the device error word that a
  * kernel sets when one of its bounded waits expires.  Returns GEMM_TN_OK,

@@ -231,3 +231,28 @@ def test_tensor_front_end_checks_before_the_device():
         tensor_api.gemm_scaled(A, B[:2], beta=1.0)
     with pytest.raises(TypeError, match="CUDA"):
         tensor_api.gemm_scaled(A, B[:2], out=torch.zeros((2, 16, 24), dtype=torch.float16))
+
+
+def _host(M=64, N=48, K=32, alpha=1.0, A=0x10000, ldA=32, a_major=0, B=0x20000, ldB=32,
+          b_major=0, beta=1.0, C=0x30000, ldC=48, D=0x40000, ldD=48, accum=0, opts=None):
+    return gb.gemm_tn_host(M, N, K, alpha, A, ldA, a_major, B, ldB, b_major, beta, C, ldC, D,
+                           ldD, accum, None, opts)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=-1), dict(K=1 << 31), dict(a_major=2), dict(b_major=-1), dict(accum=5),
+    dict(ldA=31), dict(a_major=1, ldA=63), dict(b_major=1, ldB=47), dict(ldC=47), dict(ldD=47),
+    dict(D=0), dict(A=0), dict(C=0),
+    dict(opts=gb.make_options(host_panel_rows=-8)), dict(opts=gb.make_options(tile_n=96)),
+    # C and D overlapping other than exactly, or exactly with another ld
+    dict(C=0x40000 + 2 * 48), dict(C=0x40000, ldC=56, ldD=56 + 8),
+    # D overlapping A or B (D is written while later panels of A are read)
+    dict(D=0x10000 + 64),
+])
+def test_host_entry_point_rejects_bad_arguments_before_device_work(lib, kw):
+    assert _host(**kw) == gb.ERR_INVALID_ARG
+
+
+def test_host_entry_point_noops(lib):
+    assert _host(M=0) == gb.OK
+    assert _host(N=0, D=0) == gb.OK
