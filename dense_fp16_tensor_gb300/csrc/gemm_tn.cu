@@ -1733,6 +1733,32 @@ int64_t host_panel_rows(int64_t M, int requested) {
   return std::max<int64_t>(P, 1);
 }
 
+// Row counts of the panels: P rows each; with the library's choice
+// (tapered) the last P or fewer rows are cut into a half and two quarters
+// (multiples of 8), so that the GEMM and copy-out left after the last
+// copy-in are short.  Returns the number of panels.
+int host_panels(int64_t M, int64_t P, bool tapered, int64_t (&rows)[kHostMaxPanels]) {
+  int n = 0;
+  int64_t left = M;
+  while (left > P && n < kHostMaxPanels - 3) {
+    rows[n++] = P;
+    left -= P;
+  }
+  if (tapered && left >= 64 && left <= P) {
+    const int64_t q = (left / 4 + 7) / 8 * 8;
+    rows[n++] = left - 2 * q;
+    rows[n++] = q;
+    rows[n++] = q;
+  } else {
+    while (left > 0) {  // (only when more than kHostMaxPanels - 3 panels of P were cut)
+      const int64_t r = std::min(left, P);
+      rows[n++] = r;
+      left -= r;
+    }
+  }
+  return n;
+}
+
 // height rows of width elements: host (pitch spitch elements) -> device
 // (pitch dpitch elements), or back.
 cudaError_t copy2d(void* dst, int64_t dpitch, const void* src, int64_t spitch, int64_t width,
@@ -1800,7 +1826,8 @@ extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float a
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
   const int64_t P = host_panel_rows(M, o.host_panel_rows);
-  const int panels = static_cast<int>((M + P - 1) / P);
+  int64_t prow[kHostMaxPanels];
+  const int panels = host_panels(M, P, o.host_panel_rows == 0 && M > 1024, prow);
   const int ring = std::min(kHostRing, panels);
   const int64_t Kp = round64(std::max<int64_t>(K, 1)), Np = round64(N), Pp = round64(P);
   // device layouts: B and A panels keep their major (rows on 128-byte
@@ -1848,8 +1875,9 @@ extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float a
   if (use_ab && copy2d(wB, b_major == GEMM_TN_MAJOR_K ? Kp : Np, B, ldB, b_cols, b_rows,
                        cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
     return done(GEMM_TN_ERR_CUDA);
-  for (int i = 0; i < panels; ++i) {
-    const int64_t m0 = i * P, rows = std::min(P, M - m0);
+  int64_t m0 = 0;
+  for (int i = 0; i < panels; m0 += prow[i], ++i) {
+    const int64_t rows = prow[i];
     const int slot = i % ring;
     __half* a_i = wA + slot * a_slot;
     __half* c_i = wC + slot * c_slot;

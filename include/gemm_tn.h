@@ -211,8 +211,10 @@ typedef struct {
   int host_panel_rows;  /* gemm_tn_host: rows of M per panel (rounded up to a
                            multiple of 8; 0 = the library's choice: all of M
                            up to 1024 rows, else panels of ceil(M / 8)
-                           rounded up to 256 rows and at least 512; more than
-                           64 panels are merged to 64) */
+                           rounded up to 256 rows and at least 512, the
+                           last one cut into a half and two quarters so that
+                           little work is left after the last copy-in; more
+                           than 64 panels are merged to 64) */
 } gemm_tn_options;
 
 /*
