@@ -148,3 +148,69 @@ def test_host_calls_back_to_back_on_one_stream():
         d64, d16 = oracle.gemm_tn_general(M, N, K, 1.0, np_bits(A), K, 0, np_bits(B), K, 0, 1.0,
                                           np_bits(C), N)
         check(np_bits(D).reshape(1, M, N), d64, d16, K, 0, True, "back to back")
+
+
+def test_host_call_captured_in_a_cuda_graph():
+    # the copy streams join the capture through the call's events; the
+    # workspace becomes a graph memory node; replays copy the host arrays as
+    # they are at replay time
+    M, N, K = 520, 264, 384
+    A = wl.operand(M, K, K, 0, "int1", 70).pin_memory()
+    B = wl.operand(N, K, K, 0, "int1", 71).pin_memory()
+    C = wl.operand(M, N, N, 0, "int4", 72).pin_memory()
+    D = torch.empty(M, N, dtype=torch.float16).pin_memory()
+
+    def call(stream):
+        return gb.gemm_tn_host(M, N, K, 1.0, A.data_ptr(), K, 0, B.data_ptr(), K, 0, 1.0,
+                               C.data_ptr(), N, D.data_ptr(), N, 0, stream,
+                               dict(host_panel_rows=128))
+    assert call(torch.cuda.current_stream().cuda_stream) == gb.OK  # eager first call
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        assert call(torch.cuda.current_stream().cuda_stream) == gb.OK
+    for rep in range(2):
+        # new host values between replays
+        A.copy_(wl.operand(M, K, K, 0, "int1", 80 + rep))
+        D.fill_(0.0)
+        g.replay()
+        torch.cuda.synchronize()
+        d64, d16 = oracle.gemm_tn_general(M, N, K, 1.0, np_bits(A), K, 0, np_bits(B), K, 0, 1.0,
+                                          np_bits(C), N)
+        check(np_bits(D).reshape(1, M, N), d64, d16, K, 0, True, f"graph replay {rep}")
+
+
+def test_host_calls_from_two_threads():
+    # each thread on its own stream with its own arrays; the library's copy
+    # streams are shared, so the calls are serialised while they enqueue
+    import threading
+    M, N, K = 384, 200, 256
+    results, errors = {}, []
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            for c in range(3):
+                A = wl.operand(M, K, K, 0, "int1", 900 + 10 * t + c).pin_memory()
+                B = wl.operand(N, K, K, 0, "int1", 950 + 10 * t + c).pin_memory()
+                C = wl.operand(M, N, N, 0, "int4", 990 + 10 * t + c).pin_memory()
+                D = torch.empty(M, N, dtype=torch.float16).pin_memory()
+                st = gb.gemm_tn_host(M, N, K, 1.0, A.data_ptr(), K, 0, B.data_ptr(), K, 0, 1.0,
+                                     C.data_ptr(), N, D.data_ptr(), N, 0, s.cuda_stream,
+                                     dict(host_panel_rows=64))
+                assert st == gb.OK, st
+                results[(t, c)] = (A, B, C, D)
+            s.synchronize()
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+    ths = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for (t, c), (A, B, C, D) in results.items():
+        d64, d16 = oracle.gemm_tn_general(M, N, K, 1.0, np_bits(A), K, 0, np_bits(B), K, 0, 1.0,
+                                          np_bits(C), N)
+        check(np_bits(D).reshape(1, M, N), d64, d16, K, 0, True, f"thread {t} call {c}")
