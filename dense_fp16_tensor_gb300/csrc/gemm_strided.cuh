@@ -6,17 +6,21 @@
 // strides for A (M,K), B (N,K) and C/D (M,N) and keeps everything after the
 // copy the same:
 //
-//   warps 0-3   copy producer: each thread gathers 16-byte K-chunks (8 fp16
-//               along K) of A and B rows through the strides, four chunks in
-//               flight at a time -- for a contiguous chunk the widest loads
-//               its alignment allows, else eight 2-byte loads -- and writes
-//               them to the 128B-swizzled
-//               K-major layout the TMA unit would produce (row r, chunk j at
-//               byte r*128 + 16*(j ^ (r%8))), zero outside the matrix; then
+//   warps 0-7   copy producer: each thread gathers 16-byte K-chunks (8 fp16
+//               along K) of A and B rows through the strides, six chunks in
+//               flight at a time -- a contiguous chunk from the one or two
+//               aligned 16-byte words under it (shift_window), else eight
+//               2-byte loads -- and writes them to the 128B-swizzled K-major
+//               layout the TMA unit would produce (row r, chunk j at byte
+//               r*128 + 16*(j ^ (r%8))), zero outside the matrix; then
 //               fence.proxy.async and one arrival per thread on `full`.
-//   warp 4      TMEM allocation and the single MMA-issuing thread
+//   warp 8      TMEM allocation and the single MMA-issuing thread
 //               (tcgen05.mma M=128, N=256, K=16, always K-major descriptors).
-//   warps 5-8   epilogue: tcgen05.ld, + C, round, element-wise strided D.
+//   warps 9-12  epilogue: tcgen05.ld, + C, round, D.  A row-major C/D view
+//               goes through a per-warp 32 x 32 transpose in shared memory,
+//               so that C is read and D written a row segment per
+//               instruction; any other view element by element with one row
+//               per lane (coalesced when the M mode has stride 1).
 //
 // 128 x 256 tiles, 4 stages of 48 KiB, two TMEM accumulators, persistent
 // grid, bounded waits; no asynchronous copies, so an abort only has to drain
@@ -26,6 +30,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "shift.cuh"
 
 namespace gemm_tn_dev {
 
@@ -33,8 +38,9 @@ constexpr int kStrBM = 128;
 constexpr int kStrBN = 256;
 constexpr int kStrBK = 64;
 constexpr int kStrStages = 4;
-constexpr int kStrProducers = 128;  // four warps
-constexpr int kStrThreads = 288;    // 4 producer warps, MMA warp, 4 epilogue warps
+constexpr int kStrProducers = 256;  // eight warps
+constexpr int kStrThreads = 416;    // 8 producer warps, MMA warp, 4 epilogue warps
+constexpr int kStrMmaWarp = kStrProducers / 32;
 
 struct StridedArgs {
   int M, N, K;
@@ -54,38 +60,15 @@ struct StridedSmem {
   static constexpr uint32_t kABytes = kStrBM * kStrBK * 2;  // 16 KiB
   static constexpr uint32_t kBBytes = kStrBN * kStrBK * 2;  // 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kBarOffset = kStrStages * kStageBytes;
+  // per epilogue warp a 32 x 33 word transpose buffer
+  static constexpr uint32_t kXposeOffset = kStrStages * kStageBytes;
+  static constexpr uint32_t kXposeBytes = 32 * 33 * 4;
+  static constexpr uint32_t kBarOffset = kXposeOffset + 4 * kXposeBytes;
   static constexpr uint32_t kNumBars = 2 * kStrStages + 5;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
 };
-
-// 16 contiguous bytes at a 2-byte aligned address, with the widest loads
-// the alignment allows (never touching bytes outside [src, src + 16)).
-__device__ __forceinline__ uint4 load16_contiguous(const __half* src) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(src);
-  if ((a & 15u) == 0) return __ldg(reinterpret_cast<const uint4*>(src));
-  uint4 v;
-  if ((a & 7u) == 0) {
-    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(src));
-    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(src + 4));
-    v = make_uint4(lo.x, lo.y, hi.x, hi.y);
-  } else if ((a & 3u) == 0) {
-    const unsigned* w = reinterpret_cast<const unsigned*>(src);
-    v = make_uint4(__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3));
-  } else {  // 2 mod 4: one halfword, three words, one halfword
-    const unsigned short* hs = reinterpret_cast<const unsigned short*>(src);
-    const unsigned* w = reinterpret_cast<const unsigned*>(src + 1);
-    const uint32_t h0 = __ldg(hs), h7 = __ldg(hs + 7);
-    const uint32_t w0 = __ldg(w), w1 = __ldg(w + 1), w2 = __ldg(w + 2);
-    v.x = h0 | (w0 << 16);
-    v.y = (w0 >> 16) | (w1 << 16);
-    v.z = (w1 >> 16) | (w2 << 16);
-    v.w = (w2 >> 16) | (h7 << 16);
-  }
-  return v;
-}
 
 // Eight consecutive-k elements X(row, k0..k0+7) of a (rows, K) view with
 // strides (s_row, s_k); zeros outside the matrix.
@@ -94,7 +77,15 @@ __device__ __forceinline__ uint4 gather_chunk(const __half* X, int64_t s_row, in
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
   if (row >= rows || k0 >= K) return v;
   const __half* src = X + static_cast<int64_t>(row) * s_row + static_cast<int64_t>(k0) * s_k;
-  if (s_k == 1 && k0 + 8 <= K) return load16_contiguous(src);
+  if (s_k == 1 && k0 + 8 <= K) {
+    // the one or two aligned 16-byte words holding the chunk's bytes
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t w = a & ~static_cast<uintptr_t>(15);
+    const int sh = static_cast<int>(a & 15u);
+    const uint4 lo = __ldg(reinterpret_cast<const uint4*>(w));
+    if (sh == 0) return lo;
+    return shift_window(lo, __ldg(reinterpret_cast<const uint4*>(w + 16)), sh);
+  }
   unsigned short h[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
@@ -106,34 +97,50 @@ __device__ __forceinline__ uint4 gather_chunk(const __half* X, int64_t s_row, in
   return v;
 }
 
-// Fill `rows` x 64 of one operand's stage in the K-major 128B-swizzled
-// layout.  Chunk q of this thread's share covers row (q / 8) and K-chunk
-// (q % 8) when K is the contiguous mode, else row (q % rows) so that
-// neighbouring threads read neighbouring rows.  Chunks are gathered four at
-// a time so that their loads are in flight together.
-__device__ __forceinline__ void fill_operand(uint8_t* dst, const __half* X, int64_t s_row,
-                                             int64_t s_k, int rows_total, int K, int row0,
-                                             int k0, int rows, int tid) {
-  const bool k_fast = (s_k == 1) || (s_row != 1 && s_k <= s_row);
-  constexpr int kBatch = 4;
-  for (int q0 = tid; q0 < rows * 8; q0 += kBatch * kStrProducers) {
+// Chunk q of one operand's stage (rows x 64 of K): row and 16-byte K-chunk.
+// When K is the contiguous mode consecutive q walk along K (eight chunks per
+// row), else along the rows, so that neighbouring threads read neighbouring
+// elements.
+__device__ __forceinline__ void chunk_coords(bool k_fast, int rows, int q, int& r, int& j) {
+  r = k_fast ? q >> 3 : q % rows;
+  j = k_fast ? q & 7 : q / rows;
+}
+
+// Fill one stage: A's kStrBM x 64 and B's kStrBN x 64 of K in the K-major
+// 128B-swizzled layout.  The stage's chunks (A's first, then B's) are dealt
+// round-robin to the producer threads and gathered kBatch at a time, all
+// their loads issued before the first store, so that enough bytes are in
+// flight per SM.
+__device__ __forceinline__ void fill_stage(uint8_t* dst_a, uint8_t* dst_b, const StridedArgs& p,
+                                           int m0, int n0, int k0, int tid) {
+  const bool a_kfast = (p.sAk == 1) || (p.sAm != 1 && p.sAk <= p.sAm);
+  const bool b_kfast = (p.sBk == 1) || (p.sBn != 1 && p.sBk <= p.sBn);
+  constexpr int kA = kStrBM * 8, kTotal = (kStrBM + kStrBN) * 8;
+  constexpr int kBatch = 6;
+  for (int q0 = tid; q0 < kTotal; q0 += kBatch * kStrProducers) {
     uint4 v[kBatch];
-    int off[kBatch];
+    uint8_t* dst[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int q = q0 + b * kStrProducers;
-      off[b] = -1;
+      dst[b] = nullptr;
       v[b] = make_uint4(0u, 0u, 0u, 0u);
-      if (q < rows * 8) {
-        const int r = k_fast ? q >> 3 : q % rows;
-        const int j = k_fast ? q & 7 : q / rows;
-        v[b] = gather_chunk(X, s_row, s_k, rows_total, K, row0 + r, k0 + 8 * j);
-        off[b] = r * 128 + 16 * (j ^ (r & 7));
+      if (q < kTotal) {
+        int r, j;
+        if (q < kA) {
+          chunk_coords(a_kfast, kStrBM, q, r, j);
+          v[b] = gather_chunk(p.A, p.sAm, p.sAk, p.M, p.K, m0 + r, k0 + 8 * j);
+          dst[b] = dst_a + r * 128 + 16 * (j ^ (r & 7));
+        } else {
+          chunk_coords(b_kfast, kStrBN, q - kA, r, j);
+          v[b] = gather_chunk(p.B, p.sBn, p.sBk, p.N, p.K, n0 + r, k0 + 8 * j);
+          dst[b] = dst_b + r * 128 + 16 * (j ^ (r & 7));
+        }
       }
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b)
-      if (off[b] >= 0) *reinterpret_cast<uint4*>(dst + off[b]) = v[b];
+      if (dst[b]) *reinterpret_cast<uint4*>(dst[b]) = v[b];
   }
 }
 
@@ -170,7 +177,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
     *abort_flag = 0u;
     fence_barrier_init();
   }
-  if (warp == 4) {
+  if (warp == kStrMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 2 * kStrBN);
     tmem_relinquish();
   }
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < 4) {
+  if (warp < kStrMmaWarp) {
     // ------------------------------------------------------------ copy producer
     const int tid = static_cast<int>(threadIdx.x);
     uint32_t stage = 0, phase = 0;
@@ -193,11 +200,8 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
           ok = false;
           break;
         }
-        const int k0 = kb * kStrBK;
-        fill_operand(sA + stage * L::kABytes, p.A, p.sAm, p.sAk, p.M, p.K, tm * kStrBM, k0,
-                     kStrBM, tid);
-        fill_operand(sB + stage * L::kBBytes, p.B, p.sBn, p.sBk, p.N, p.K, tn * kStrBN, k0,
-                     kStrBN, tid);
+        fill_stage(sA + stage * L::kABytes, sB + stage * L::kBBytes, p, tm * kStrBM,
+                   tn * kStrBN, kb * kStrBK, tid);
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         mbar_arrive(full0 + 8 * stage);
         if (++stage == kStrStages) {
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
         }
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == kStrMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(kStrBM, kStrBN, !p.acc_f16, 0, 0);
@@ -251,8 +255,11 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes of this warp
     const int row_in_tile = static_cast<int>(quad * 32 + lane);
+    // 32 x 33 words: row `lane` of a 32 x 32 accumulator block, read back by column
+    uint32_t* xp = reinterpret_cast<uint32_t*>(smem + L::kXposeOffset +
+                                               (warp - kStrMmaWarp - 1) * L::kXposeBytes);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int tm, tn;
@@ -268,7 +275,36 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_wait_ld();
-        if (m < p.M) {
+        if (p.sCn == 1) {
+          // row-major C/D: transpose the block through shared memory, then
+          // row i of the block is read and written by the 32 lanes at once
+#pragma unroll
+          for (int j = 0; j < 32; ++j) xp[lane * 33 + j] = r[j];
+          __syncwarp();
+          const int n = tn * kStrBN + c * 32 + static_cast<int>(lane);
+          const int mrow0 = tm * kStrBM + static_cast<int>(quad * 32);
+#pragma unroll 1
+          for (int i0 = 0; i0 < 32; i0 += 8) {
+            __half cv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int mi = mrow0 + i0 + i;
+              cv[i] = (mi < p.M && n < p.N) ? p.CD[static_cast<int64_t>(mi) * p.sCm + n]
+                                            : __ushort_as_half(0);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int mi = mrow0 + i0 + i;
+              if (mi < p.M && n < p.N) {
+                const uint32_t a = xp[(i0 + i) * 33 + static_cast<int>(lane)];
+                p.CD[static_cast<int64_t>(mi) * p.sCm + n] =
+                    p.acc_f16 ? __hadd(__ushort_as_half(static_cast<unsigned short>(a)), cv[i])
+                              : __float2half_rn(__uint_as_float(a) + __half2float(cv[i]));
+              }
+            }
+          }
+          __syncwarp();  // the block is read before the next one is written
+        } else if (m < p.M) {
           __half* row = p.CD + static_cast<int64_t>(m) * p.sCm;
           const int n0 = tn * kStrBN + c * 32;
 #pragma unroll
@@ -295,7 +331,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kStrMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * kStrBN);
   }

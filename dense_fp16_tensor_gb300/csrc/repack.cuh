@@ -15,6 +15,8 @@
 
 #include <cstdint>
 
+#include "shift.cuh"
+
 namespace gemm_tn_dev {
 
 constexpr int kRepackTile = 64;
@@ -47,36 +49,10 @@ __global__ void __launch_bounds__(kRepackThreads)
   }
 }
 
-// Bytes [sh, sh + 16) of the 32-byte concatenation lo:hi (sh even, 0..14):
-// words of the window shifted by whole words (q = sh / 4) and, for sh % 4
-// == 2, by a further half word.
-__device__ __forceinline__ uint4 shift_window(const uint4& lo, const uint4& hi, int sh) {
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  uint32_t o[4];
-  const bool half = (sh & 3) != 0;
-  switch (sh >> 2) {
-#define GEMM_TN_SHIFT_CASE(Q)                                                        \
-  case Q:                                                                            \
-    _Pragma("unroll") for (int i = 0; i < 4; ++i) o[i] =                             \
-        half ? __funnelshift_r(w[Q + i], w[Q + i + 1], 16) : w[Q + i];               \
-    break;
-    GEMM_TN_SHIFT_CASE(0)
-    GEMM_TN_SHIFT_CASE(1)
-    GEMM_TN_SHIFT_CASE(2)
-    default:
-      _Pragma("unroll") for (int i = 0; i < 3; ++i) o[i] =
-          half ? __funnelshift_r(w[3 + i], w[4 + i], 16) : w[3 + i];
-      o[3] = half ? __funnelshift_r(w[6], w[7], 16) : w[6];
-      break;
-#undef GEMM_TN_SHIFT_CASE
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // dst(r, c) = src(r, c) when both views have unit column stride (any 2-byte
 // alignment of either row): blockIdx.y selects the row, each thread builds
 // whole 16-byte words of the destination row at their aligned addresses
-// from the two aligned 16-byte source words under them (a funnel shift
+// from the two aligned 16-byte source words under them (shift_window
 // when the two rows are misaligned differently), so every load and every
 // interior store is one aligned vector access.  Source words are read only
 // where they hold bytes of the row (an aligned word never crosses a page);
