@@ -4,7 +4,9 @@
 
 A C-ABI library (include/gemm_tn.h, csrc/) with a ctypes binding of the same
 names (``binding``) and a torch-tensor front end (``gemm`` for the in-place
-form, ``gemm_scaled`` for D = alpha A.B^T + beta C, 2-D or batched 3-D).  Build with
+form, ``gemm_scaled`` for D = alpha A.B^T + beta C, 2-D or batched 3-D, and
+``gemm_host`` for the scaled form on CPU tensors, copies overlapped with the
+GEMMs inside the library).  Build with
 ``build()``; there is no CPU or library fallback.
 """
 from ._build import build  # noqa: F401
@@ -12,7 +14,8 @@ from .binding import (ACC_F16, ACC_F32, MAJOR_K, MAJOR_MN, PATH_AUTO, PATH_LARGE
                       PATH_SKINNY, GemmTnError, gemm_tn, gemm_tn_check_device_error,
                       gemm_tn_ex, gemm_tn_last_kernels, gemm_tn_last_launch_count, gemm_tn_plan_path,
                       gemm_tn_status_string, gemm_tn_strided, gemm_tn_strided_ex, library_path,
-                      make_options, gemm_tn_scaled, gemm_tn_batched, gemm_tn_batched_ex)
+                      make_options, gemm_tn_scaled, gemm_tn_batched, gemm_tn_batched_ex,
+                      gemm_tn_host)
 
 
 def gemm(*args, **kwargs):
@@ -23,3 +26,8 @@ def gemm(*args, **kwargs):
 def gemm_scaled(*args, **kwargs):
     from .tensor_api import gemm_scaled as _gemm_scaled
     return _gemm_scaled(*args, **kwargs)
+
+
+def gemm_host(*args, **kwargs):
+    from .tensor_api import gemm_host as _gemm_host
+    return _gemm_host(*args, **kwargs)

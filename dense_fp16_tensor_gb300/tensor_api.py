@@ -134,3 +134,66 @@ def gemm_scaled(A: torch.Tensor, Bm: torch.Tensor, C: torch.Tensor | None = None
     if st != B.OK:
         raise B.GemmTnError(st)
     return out
+
+
+def _host_view(t: torch.Tensor, name: str):
+    """(major, ld) of a 2-D fp16 host operand (rows, K): any leading dimension
+    at least its row, one stride-1 mode."""
+    if t.dim() != 2 or t.dtype != torch.float16:
+        raise TypeError(f"{name} must be a 2-D float16 tensor")
+    rows, k = t.shape
+    s0, s1 = t.stride()
+    if s1 == 1 or k == 1:
+        return B.MAJOR_K, max(s0, k) if rows > 1 else max(k, 1)
+    if s0 == 1 or rows == 1:
+        return B.MAJOR_MN, max(s1, rows) if k > 1 else max(rows, 1)
+    raise ValueError(f"{name}: neither mode is stride-1 (strides {t.stride()})")
+
+
+def gemm_host(A: torch.Tensor, Bm: torch.Tensor, C: torch.Tensor | None = None, *,
+              alpha: float = 1.0, beta: float | None = None, out: torch.Tensor | None = None,
+              accum: str = "f32", stream: torch.cuda.Stream | None = None,
+              synchronize: bool = True, **options) -> torch.Tensor:
+    """out <- alpha * A . Bm^T + beta * C with every tensor in host memory
+    (gemm_tn_host): A (M,K), Bm (N,K), C and out (M,N) fp16 CPU tensors,
+    page-locked (``pin_memory()``) for the copies to overlap the GEMMs.  out
+    is allocated (page-locked) when not given and may be C itself.  The
+    copies and GEMMs are enqueued on ``stream`` (default: the current
+    stream); with ``synchronize`` (default) the call waits for them, else
+    the caller must synchronise the stream before reading out or touching
+    the inputs.  ``options`` are gemm_tn_options fields (host_panel_rows,
+    tile_kernel, ...)."""
+    if A.is_cuda or Bm.is_cuda or (C is not None and C.is_cuda) or \
+            (out is not None and out.is_cuda):
+        raise ValueError("gemm_host takes CPU tensors (use gemm / gemm_scaled on CUDA tensors)")
+    M, K = A.shape
+    N, K2 = Bm.shape
+    if K2 != K:
+        raise ValueError(f"K mismatch: A {tuple(A.shape)}, B {tuple(Bm.shape)}")
+    if beta is None:
+        beta = 1.0 if C is not None else 0.0
+    if beta != 0 and C is None:
+        raise ValueError("beta != 0 needs C")
+    a_major, ldA = _host_view(A, "A")
+    b_major, ldB = _host_view(Bm, "B")
+
+    def check_mn(t, name):
+        if t is not None and (t.dtype != torch.float16 or tuple(t.shape) != (M, N) or
+                              (t.stride(1) != 1 and N > 1)):
+            raise ValueError(f"{name} must be an (M, N) row-major float16 tensor")
+    check_mn(C, "C")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    check_mn(out, "out")
+    ldC = max(C.stride(0), N) if C is not None and M > 1 else N
+    ldD = max(out.stride(0), N) if M > 1 else N
+    s = stream if stream is not None else torch.cuda.current_stream()
+    acc = _ACC[accum] if isinstance(accum, str) else int(accum)
+    st = B.gemm_tn_host(M, N, K, float(alpha), A.data_ptr(), ldA, a_major, Bm.data_ptr(), ldB,
+                        b_major, float(beta), C.data_ptr() if C is not None else 0, ldC,
+                        out.data_ptr(), ldD, acc, s.cuda_stream, options or None)
+    if st != B.OK:
+        raise B.GemmTnError(st, "gemm_tn_host")
+    if synchronize:
+        s.synchronize()
+    return out

@@ -256,3 +256,23 @@ def test_host_entry_point_rejects_bad_arguments_before_device_work(lib, kw):
 def test_host_entry_point_noops(lib):
     assert _host(M=0) == gb.OK
     assert _host(N=0, D=0) == gb.OK
+
+
+def test_host_front_end_argument_checks():
+    import torch
+
+    from dense_fp16_tensor_gb300 import tensor_api
+    A = torch.zeros((32, 16), dtype=torch.float16)
+    B = torch.zeros((24, 16), dtype=torch.float16)
+    with pytest.raises(ValueError):
+        tensor_api.gemm_host(A, torch.zeros((24, 8), dtype=torch.float16))   # K mismatch
+    with pytest.raises(ValueError):
+        tensor_api.gemm_host(A, B, beta=1.0)                                   # beta without C
+    with pytest.raises(ValueError):
+        tensor_api.gemm_host(A, B, torch.zeros((32, 25), dtype=torch.float16))  # C shape
+    with pytest.raises(TypeError):
+        tensor_api.gemm_host(A.float(), B)
+    assert tensor_api._host_view(A, "A") == (gb.MAJOR_K, 16)
+    assert tensor_api._host_view(A.t(), "A") == (gb.MAJOR_MN, 16)
+    assert tensor_api._host_view(torch.zeros((32, 20), dtype=torch.float16)[:, :16], "A") == \
+        (gb.MAJOR_K, 20)

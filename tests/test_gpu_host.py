@@ -214,3 +214,16 @@ def test_host_calls_from_two_threads():
         d64, d16 = oracle.gemm_tn_general(M, N, K, 1.0, np_bits(A), K, 0, np_bits(B), K, 0, 1.0,
                                           np_bits(C), N)
         check(np_bits(D).reshape(1, M, N), d64, d16, K, 0, True, f"thread {t} call {c}")
+
+
+def test_host_tensor_front_end():
+    import dense_fp16_tensor_gb300 as g
+    M, N, K = 300, 200, 256
+    A = wl.operand(M, K, K, 0, "int1", 1200).pin_memory()
+    Bt = wl.operand(N, K, N, 1, "int1", 1201)   # stored (K, N): an N-major view of B
+    Bv = Bt.t()                                  # (N, K) with strides (1, N)
+    C = wl.operand(M, N, N, 0, "int4", 1202).pin_memory()
+    D = g.gemm_host(A, Bv, C, alpha=2.0, beta=-1.0, host_panel_rows=64)
+    d64, d16 = oracle.gemm_tn_general(M, N, K, 2.0, np_bits(A), K, 0, np_bits(Bt), N, 1, -1.0,
+                                      np_bits(C), N)
+    check(np_bits(D).reshape(1, M, N), d64, d16, K, 0, True, "tensor front end")
