@@ -49,7 +49,7 @@ class GemmTnOptions(ctypes.Structure):
                 ("test_stall", ctypes.c_int), ("tile_kernel", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("test_fail_alloc", ctypes.c_int),
                 ("k_stage", ctypes.c_int), ("trace", ctypes.c_int),
-                ("host_panel_rows", ctypes.c_int)]
+                ("host_panel_rows", ctypes.c_int), ("host_inputs_ready", ctypes.c_int)]
 
 
 class GemmTnError(RuntimeError):
@@ -133,9 +133,10 @@ TILE_AUTO, TILE_SINGLE, TILE_PAIR, TILE_WIDE = 0, 1, 2, 3
 
 def make_options(path=0, split_k=0, tile_n=0, sync_check=0, timeout_ns=0, test_stall=0,
                  tile_kernel=0, stream_k=0, test_fail_alloc=0, k_stage=0, trace=0,
-                 host_panel_rows=0):
+                 host_panel_rows=0, host_inputs_ready=0):
     return GemmTnOptions(path, split_k, tile_n, sync_check, timeout_ns, test_stall, tile_kernel,
-                         stream_k, test_fail_alloc, k_stage, trace, host_panel_rows)
+                         stream_k, test_fail_alloc, k_stage, trace, host_panel_rows,
+                         host_inputs_ready)
 
 
 def gemm_tn_ex(M, N, K, A, ldA, a_major, B, ldB, b_major, CD, ldC, accum_dtype, stream,

@@ -1690,6 +1690,15 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr;
+  // Two device workspaces used by alternate calls, each with the event that
+  // marks the end of its last call's use (recorded on that call's stream).
+  // They are the pipeline's own (not the pool's): a pool block freed on one
+  // stream and taken on the copy-in stream would make the copies wait for
+  // the freeing call to finish, and consecutive calls could not overlap.
+  void* ws[2] = {nullptr, nullptr};
+  size_t ws_bytes[2] = {0, 0};
+  cudaEvent_t ws_free[2] = {nullptr, nullptr};
+  unsigned calls = 0;
   cudaEvent_t in_done[kHostMaxPanels];
   cudaEvent_t gemm_done[kHostMaxPanels];
   cudaEvent_t out_done[kHostMaxPanels];
@@ -1705,7 +1714,9 @@ int host_pipe(int dev, HostPipe*& hp) {
   if (hp->ready) return GEMM_TN_OK;
   bool ok = cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) == cudaSuccess;
+            cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp->ws_free[0], cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp->ws_free[1], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; ok && i < kHostMaxPanels; ++i)
     ok = cudaEventCreateWithFlags(&hp->in_done[i], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&hp->gemm_done[i], cudaEventDisableTiming) == cudaSuccess &&
@@ -1764,6 +1775,9 @@ int host_panels(int64_t M, int64_t P, bool tapered, int64_t (&rows)[kHostMaxPane
 cudaError_t copy2d(void* dst, int64_t dpitch, const void* src, int64_t spitch, int64_t width,
                    int64_t height, cudaMemcpyKind kind, cudaStream_t s) {
   if (width <= 0 || height <= 0) return cudaSuccess;
+  if (height == 1 || (dpitch == width && spitch == width))  // one contiguous range
+    return cudaMemcpyAsync(dst, src, static_cast<size_t>(width) * 2 * static_cast<size_t>(height),
+                           kind, s);
   return cudaMemcpy2DAsync(dst, static_cast<size_t>(dpitch) * 2, src, static_cast<size_t>(spitch) * 2,
                            static_cast<size_t>(width) * 2, static_cast<size_t>(height), kind, s);
 }
@@ -1827,7 +1841,11 @@ extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float a
 
   const int64_t P = host_panel_rows(M, o.host_panel_rows);
   int64_t prow[kHostMaxPanels];
-  const int panels = host_panels(M, P, o.host_panel_rows == 0 && M > 1024, prow);
+  // (tapered only for calls that do not overlap their neighbours: with
+  // host_inputs_ready the next call's copies fill the tail instead, and the
+  // extra copies of the small panels cost more than they save)
+  const int panels =
+      host_panels(M, P, o.host_panel_rows == 0 && M > 1024 && o.host_inputs_ready == 0, prow);
   const int ring = std::min(kHostRing, panels);
   const int64_t Kp = round64(std::max<int64_t>(K, 1)), Np = round64(N), Pp = round64(P);
   // device layouts: B and A panels keep their major (rows on 128-byte
@@ -1841,10 +1859,59 @@ extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float a
   HostPipe* hp = nullptr;
   s = host_pipe(dev, hp);
   if (s != GEMM_TN_OK) return s;
-  void* ws = nullptr;
-  if (ws_alloc(&ws, bytes, *st, cs, o) != cudaSuccess) {
+  // With host_inputs_ready the copies in wait only for the copies in of
+  // earlier calls (the copy-in stream is FIFO) and for the end of the call
+  // before last, which used the same workspace, so that a call's copies in
+  // overlap the previous call's last GEMMs and copies out.
+  // Under stream capture the workspace comes from the pool in `stream`'s
+  // order instead (a graph memory node), and the copies in follow `stream`.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) {
     cudaGetLastError();
-    return GEMM_TN_ERR_NO_MEMORY;
+    return GEMM_TN_ERR_CUDA;
+  }
+  const bool captured = cap != cudaStreamCaptureStatusNone;
+  const bool eager = o.host_inputs_ready != 0 && !captured;
+  const int wsi = static_cast<int>(hp->calls & 1u);
+  void* ws = nullptr;
+  if (captured) {
+    if (ws_alloc(&ws, bytes, *st, cs, o) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_NO_MEMORY;
+    }
+  } else {
+    if (o.test_fail_alloc) return GEMM_TN_ERR_NO_MEMORY;
+    if (hp->ws_bytes[0] < bytes) {
+      // grow both workspaces once their last calls are done with them (a
+      // host wait; only when a call needs more than any earlier one)
+      for (int j = 0; j < 2; ++j) {
+        if (hp->ws[j] != nullptr &&
+            (cudaEventSynchronize(hp->ws_free[j]) != cudaSuccess || cudaFree(hp->ws[j]) != cudaSuccess)) {
+          cudaGetLastError();
+          return GEMM_TN_ERR_CUDA;
+        }
+        hp->ws[j] = nullptr;
+        hp->ws_bytes[j] = 0;
+      }
+      for (int j = 0; j < 2; ++j) {
+        if (cudaMalloc(&hp->ws[j], bytes) != cudaSuccess) {
+          cudaGetLastError();
+          for (int i = 0; i < 2; ++i) {
+            if (hp->ws[i]) cudaFree(hp->ws[i]);
+            hp->ws[i] = nullptr;
+            hp->ws_bytes[i] = 0;
+          }
+          return GEMM_TN_ERR_NO_MEMORY;
+        }
+        hp->ws_bytes[j] = bytes;
+      }
+    }
+    ++hp->calls;
+    ws = hp->ws[wsi];
+    if (cudaStreamWaitEvent(hp->in, hp->ws_free[wsi], 0) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_TN_ERR_CUDA;
+    }
   }
   __half* wB = static_cast<__half*>(ws);
   __half* wA = wB + b_elems;
@@ -1856,6 +1923,7 @@ extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float a
   gemm_tn_options og = o;
   og.sync_check = 0;
   og.host_panel_rows = 0;
+  og.host_inputs_ready = 0;
   int launches = 0;
   const char* kernels = "";
   int last_in = -1, last_out = -1;  // last recorded events of the copy streams
@@ -1864,12 +1932,17 @@ extern "C" GEMM_TN_API int gemm_tn_host(int64_t M, int64_t N, int64_t K, float a
     cudaEventRecord(hp->start, hp->in);
     cudaStreamWaitEvent(cs, hp->start, 0);
     if (last_out >= 0) cudaStreamWaitEvent(cs, hp->out_done[last_out], 0);
-    if (cudaFreeAsync(ws, cs) != cudaSuccess && status == GEMM_TN_OK) status = GEMM_TN_ERR_CUDA;
+    // the workspace is free again once `stream` has passed this point
+    const cudaError_t e = captured ? cudaFreeAsync(ws, cs) : cudaEventRecord(hp->ws_free[wsi], cs);
+    if (e != cudaSuccess && status == GEMM_TN_OK) status = GEMM_TN_ERR_CUDA;
     if (status != GEMM_TN_OK) cudaGetLastError();
     return status;
   };
+  // D is written only after everything enqueued on `stream` before the call
+  // (which may still read it); A, B and C are read after it too unless the
+  // caller declared them ready
   if (cudaEventRecord(hp->start, cs) != cudaSuccess ||
-      cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      (!eager && cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess) ||
       cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
     return done(GEMM_TN_ERR_CUDA);
   if (use_ab && copy2d(wB, b_major == GEMM_TN_MAJOR_K ? Kp : Np, B, ldB, b_cols, b_rows,

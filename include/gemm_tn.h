@@ -211,10 +211,19 @@ typedef struct {
   int host_panel_rows;  /* gemm_tn_host: rows of M per panel (rounded up to a
                            multiple of 8; 0 = the library's choice: all of M
                            up to 1024 rows, else panels of ceil(M / 8)
-                           rounded up to 256 rows and at least 512, the
-                           last one cut into a half and two quarters so that
-                           little work is left after the last copy-in; more
-                           than 64 panels are merged to 64) */
+                           rounded up to 256 rows and at least 512 -- without
+                           host_inputs_ready the last one cut into a half
+                           and two quarters so that little work is left
+                           after the last copy-in; more than 64 panels are
+                           merged to 64) */
+  int host_inputs_ready; /* gemm_tn_host: nonzero declares that A, B and C
+                           already hold their values when the call is made
+                           (nothing enqueued earlier on `stream` writes
+                           them), so their copies to the device need not
+                           wait for that work: they start once the copies
+                           in of earlier gemm_tn_host calls are done, and
+                           back-to-back calls overlap.  D is still written
+                           only after the earlier work on `stream`. */
 } gemm_tn_options;
 
 /*
@@ -377,14 +386,23 @@ GEMM_TN_API int gemm_tn_strided_ex(int64_t M, int64_t N, int64_t K,
  * and D not read, until `stream` has passed the call
  * (cudaStreamSynchronize).  The host arrays should be page-locked
  * (cudaHostAlloc / cudaHostRegister): copies from pageable memory are
- * staged by the driver and do not overlap.  The device copies live in one
- * workspace from the library's stream-ordered pool: N x K for B plus up to
- * three panels of A (panel rows x K) and of C/D (panel rows x N), released
- * in stream order at the end of the call.  Concurrent calls from several
- * host threads are serialised while they enqueue (the copy streams are the
- * library's, one pair per device).
+ * staged by the driver and do not overlap.  The device copies live in a
+ * workspace of N x K for B plus three panels of A (panel rows x K) and of
+ * C/D (panel rows x N).  The library keeps two such workspaces per device
+ * for this entry point, used by alternate calls, each reused once the call
+ * before last is done with it, grown (with a host wait for the calls still
+ * using them) when a call needs more than any earlier one, and kept until
+ * the process exits; under stream capture the workspace is taken from the
+ * library's pool in `stream`'s order instead (a graph memory node).
+ * Concurrent calls from several host threads are serialised while they
+ * enqueue (the copy streams are the library's, one pair per device).
  *
- * Only host_panel_rows, sync_check and the large-path controls of
+ * With gemm_tn_options.host_inputs_ready the copies in are ordered only
+ * after the copies in of earlier gemm_tn_host calls on the device (see the
+ * option), so that a stream of independent calls keeps the host link busy
+ * across call boundaries.
+ *
+ * Only host_panel_rows, host_inputs_ready, sync_check and the large-path controls of
  * gemm_tn_options (path, tile_kernel, tile_n, split_k, stream_k, k_stage,
  * timeout_ns) are read; they apply to every panel's GEMM.
  * Errors: GEMM_TN_ERR_INVALID_ARG for negative or too large sizes, an ld

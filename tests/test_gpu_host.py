@@ -33,7 +33,7 @@ def _lib():
 
 
 def _case(M, N, K, a_major=0, b_major=0, accum=0, alpha=1.0, beta=1.0, in_place=False,
-          panel_rows=0, integer=True, pinned=True, seed=0):
+          panel_rows=0, integer=True, pinned=True, seed=0, ready=0):
     dist, cdist = ("int1", "int4") if integer else ("normal_k", "u11")
     ldA = (K if a_major == 0 else M) + 5
     ldB = (K if b_major == 0 else N) + 3
@@ -49,7 +49,7 @@ def _case(M, N, K, a_major=0, b_major=0, accum=0, alpha=1.0, beta=1.0, in_place=
     s = torch.cuda.current_stream().cuda_stream
     st = gb.gemm_tn_host(M, N, K, alpha, A.data_ptr(), ldA, a_major, B.data_ptr(), ldB, b_major,
                          beta, C.data_ptr(), ldC, Dout.data_ptr(), ldC if in_place else ldD,
-                         accum, s, dict(host_panel_rows=panel_rows))
+                         accum, s, dict(host_panel_rows=panel_rows, host_inputs_ready=ready))
     assert st == gb.OK, gb.gemm_tn_status_string(st)
     kernels = gb.gemm_tn_last_kernels()
     torch.cuda.synchronize()
@@ -109,6 +109,15 @@ def test_host_degenerate_terms():
     _case(200, 100, 0, panel_rows=64, seed=10)                  # K = 0: D = C
 
 
+def test_host_inputs_ready_sizes_and_growth():
+    # calls of growing size (the workspaces grow between them) and shrinking
+    # size with the inputs declared ready, in place and not
+    for i, (M, N, K) in enumerate([(100, 80, 64), (1500, 300, 700), (2100, 260, 520),
+                                   (300, 100, 100)]):
+        _case(M, N, K, in_place=bool(i % 2), panel_rows=0 if i != 1 else 128, seed=40 + i,
+              ready=1)
+
+
 def test_host_pageable_memory():
     _case(300, 200, 256, panel_rows=64, pinned=False, seed=11)
 
@@ -128,9 +137,12 @@ def test_host_workspace_exhaustion_enqueues_nothing():
     assert bool((D == 7.0).all())
 
 
-def test_host_calls_back_to_back_on_one_stream():
+@pytest.mark.parametrize("ready", [0, 1])
+def test_host_calls_back_to_back_on_one_stream(ready):
     # several calls queued before one synchronisation: each call's device
-    # slots and the shared copy streams must not mix up the calls
+    # slots, the two alternating workspaces and the shared copy streams must
+    # not mix up the calls (with host_inputs_ready the copies in of a call
+    # start before the previous call has finished)
     M, N, K = 384, 256, 512
     s = torch.cuda.current_stream().cuda_stream
     outs = []
@@ -140,7 +152,8 @@ def test_host_calls_back_to_back_on_one_stream():
         C = wl.operand(M, N, N, 0, "int4", 60 + c).pin_memory()
         D = torch.empty(M, N, dtype=torch.float16).pin_memory()
         st = gb.gemm_tn_host(M, N, K, 1.0, A.data_ptr(), K, 0, B.data_ptr(), K, 0, 1.0,
-                             C.data_ptr(), N, D.data_ptr(), N, 0, s, dict(host_panel_rows=64))
+                             C.data_ptr(), N, D.data_ptr(), N, 0, s,
+                             dict(host_panel_rows=64, host_inputs_ready=ready))
         assert st == gb.OK
         outs.append((A, B, C, D))
     torch.cuda.synchronize()
