@@ -25,6 +25,17 @@
 // 128 x 256 tiles, 4 stages of 48 KiB, two TMEM accumulators, persistent
 // grid, bounded waits; no asynchronous copies, so an abort only has to drain
 // the MMAs.
+//
+// Row-class variant (kTma, both operands with a stride-1 K mode): the rows
+// of a view with any leading dimension ld fall into eight classes r % 8,
+// and the rows of one class are 16 * ld bytes apart -- a stride TMA
+// accepts.  One tensor map per class and operand, on the class's first row
+// rounded down to 16 bytes (the row then starts delta = 0..7 elements into
+// the map's rows), brings a K block in as boxes 72 elements wide (the block
+// plus the offset) into a raw ring; warps 0-7 then cut each 8-element chunk
+// out of the two raw 16-byte words under it (shift_window) into the
+// swizzled stage the MMA reads.  Rows past M / N and K past the end arrive
+// as zeros from the tensor maps' bounds.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -44,6 +55,7 @@ constexpr int kStrMmaWarp = kStrProducers / 32;
 
 struct StridedArgs {
   int M, N, K;
+  int a_shift[8], b_shift[8];  // row-class variant: byte offset of a row in its map row
   const __half* A;
   int64_t sAm, sAk;
   const __half* B;
@@ -56,15 +68,33 @@ struct StridedArgs {
   uint64_t timeout_ns;
 };
 
+// Tensor maps of the row-class variant: class c of A (rows c, c + 8, ...)
+// and of B.
+struct StridedMaps {
+  CUtensorMap a[8];
+  CUtensorMap b[8];
+};
+
+constexpr int kStrRawK = kStrBK + 8;        // elements per raw row (the block plus the offset)
+constexpr int kStrRawRowBytes = kStrRawK * 2;  // 144
+
+template <bool kTma>
 struct StridedSmem {
+  static constexpr int kStages = kTma ? 2 : kStrStages;  // swizzled stages the MMA reads
+  static constexpr int kRawStages = kTma ? 2 : 0;
   static constexpr uint32_t kABytes = kStrBM * kStrBK * 2;  // 16 KiB
   static constexpr uint32_t kBBytes = kStrBN * kStrBK * 2;  // 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  // raw ring: per class 16 rows of A and 32 rows of B, 144 bytes each
+  static constexpr uint32_t kRawABytes = kStrBM * kStrRawRowBytes;  // 18 KiB
+  static constexpr uint32_t kRawBBytes = kStrBN * kStrRawRowBytes;  // 36 KiB
+  static constexpr uint32_t kRawStageBytes = kRawABytes + kRawBBytes;
+  static constexpr uint32_t kRawOffset = kStages * kStageBytes;
   // per epilogue warp a 32 x 33 word transpose buffer
-  static constexpr uint32_t kXposeOffset = kStrStages * kStageBytes;
+  static constexpr uint32_t kXposeOffset = kRawOffset + kRawStages * kRawStageBytes;
   static constexpr uint32_t kXposeBytes = 32 * 33 * 4;
   static constexpr uint32_t kBarOffset = kXposeOffset + 4 * kXposeBytes;
-  static constexpr uint32_t kNumBars = 2 * kStrStages + 5;
+  static constexpr uint32_t kNumBars = 2 * kStages + 5 + 2 * kRawStages;
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
@@ -144,28 +174,56 @@ __device__ __forceinline__ void fill_stage(uint8_t* dst_a, uint8_t* dst_b, const
   }
 }
 
-__global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const StridedArgs p) {
-  using L = StridedSmem;
+// Row-class variant: cut stage `ss` of the swizzled ring out of raw stage
+// `slot` (this thread's chunks: A's 1024 first, then B's 2048).
+template <typename L>
+__device__ __forceinline__ void rows_to_stage(const uint8_t* raw, uint8_t* dst_a, uint8_t* dst_b,
+                                              const StridedArgs& p, int tid) {
+  constexpr int kA = kStrBM * 8, kTotal = (kStrBM + kStrBN) * 8;
+#pragma unroll 4
+  for (int q = tid; q < kTotal; q += kStrProducers) {
+    const bool is_a = q < kA;
+    const int qq = is_a ? q : q - kA;
+    const int r = qq >> 3, k8 = qq & 7, c = r & 7, j = r >> 3;
+    // raw row of (class c, row j of the class) and the chunk's first byte in it
+    const uint8_t* row = is_a ? raw + (c * (kStrBM / 8) + j) * kStrRawRowBytes
+                              : raw + L::kRawABytes + (c * (kStrBN / 8) + j) * kStrRawRowBytes;
+    const int sh = is_a ? p.a_shift[c] : p.b_shift[c];
+    const uint4* w = reinterpret_cast<const uint4*>(row + 16 * k8);
+    const uint4 v = sh ? shift_window(w[0], w[1], sh) : w[0];
+    uint8_t* dst = (is_a ? dst_a : dst_b) + r * 128 + 16 * (k8 ^ (r & 7));
+    *reinterpret_cast<uint4*>(dst) = v;
+  }
+}
+
+template <bool kTma>
+__global__ void __launch_bounds__(kStrThreads, 1)
+    gemm_tn_strided_kernel(const __grid_constant__ StridedMaps maps, const StridedArgs p) {
+  using L = StridedSmem<kTma>;
+  constexpr int kStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                                // stage s at s * kABytes
-  uint8_t* sB = smem + kStrStages * L::kABytes;      // stage s at s * kBBytes
+  uint8_t* sA = smem;                             // stage s at s * kABytes
+  uint8_t* sB = smem + kStages * L::kABytes;      // stage s at s * kBBytes
+  uint8_t* raw0 = smem + L::kRawOffset;           // raw stage s at s * kRawStageBytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOffset + 4);
 
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + kStrStages);
-  const uint32_t tfull0 = smem_u32(bars + 2 * kStrStages);
-  const uint32_t tempty0 = smem_u32(bars + 2 * kStrStages + 2);
-  const uint32_t drain = smem_u32(bars + 2 * kStrStages + 4);
+  const uint32_t empty0 = smem_u32(bars + kStages);
+  const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
+  const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
+  const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+  const uint32_t raw_full0 = smem_u32(bars + 2 * kStages + 5);
+  const uint32_t raw_empty0 = raw_full0 + 8 * L::kRawStages;
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStrStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, kStrProducers);
       mbar_init(empty0 + 8 * s, 1);
     }
@@ -174,8 +232,18 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
       mbar_init(tempty0 + 8 * a, 4);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < L::kRawStages; ++s) {
+      mbar_init(raw_full0 + 8 * s, 1);
+      mbar_init(raw_empty0 + 8 * s, kStrProducers);
+    }
     *abort_flag = 0u;
     fence_barrier_init();
+  }
+  if (kTma && threadIdx.x == 32) {
+    for (int c = 0; c < 8; ++c) {
+      tma_prefetch_desc(&maps.a[c]);
+      tma_prefetch_desc(&maps.b[c]);
+    }
   }
   if (warp == kStrMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 2 * kStrBN);
@@ -186,7 +254,69 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < kStrMmaWarp) {
+  if (warp < kStrMmaWarp && kTma) {
+    // ------------------------------------------------ row-class TMA producer
+    const int tid = static_cast<int>(threadIdx.x);
+    const int my_tiles = p.num_tiles > static_cast<int>(blockIdx.x)
+                             ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+    const int units = my_tiles * p.k_blocks;  // (tile, K block) pairs of this CTA, in order
+    uint32_t issued_mask = 0, issued_parity = 0;  // thread 0: raw stages with copies in flight
+    // thread 0 loads unit u into raw stage u % 2 once the stage's previous
+    // unit has been cut out by every producer thread
+    auto issue = [&](int u) -> bool {
+      const int slot = u % L::kRawStages;
+      const uint32_t use = static_cast<uint32_t>(u / L::kRawStages);
+      if (!wait_bounded(raw_empty0 + 8 * slot, (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
+                        timeout_code(kRoleProducer, 0x400 + slot)))
+        return false;
+      const int t = static_cast<int>(blockIdx.x) + (u / p.k_blocks) * static_cast<int>(gridDim.x);
+      const int kb = u % p.k_blocks;
+      int tm, tn;
+      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      const uint32_t fb = raw_full0 + 8 * slot;
+      const uint32_t dst = smem_u32(raw0 + slot * L::kRawStageBytes);
+      mbar_arrive_expect_tx(fb, L::kRawStageBytes);
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        tma_load_2d(dst + c * (kStrBM / 8) * kStrRawRowBytes, &maps.a[c], fb, kb * kStrBK,
+                    tm * (kStrBM / 8));
+        tma_load_2d(dst + L::kRawABytes + c * (kStrBN / 8) * kStrRawRowBytes, &maps.b[c], fb,
+                    kb * kStrBK, tn * (kStrBN / 8));
+      }
+      issued_mask |= 1u << slot;
+      issued_parity = (issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
+      return true;
+    };
+    bool ok = true;
+    if (tid == 0) {
+      for (int u = 0; ok && u < min(units, L::kRawStages); ++u) ok = issue(u);
+    }
+    for (int u = 0; ok && u < units; ++u) {
+      const int slot = u % L::kRawStages;
+      const int ss = u % kStages;
+      if (!wait_bounded(raw_full0 + 8 * slot, static_cast<uint32_t>(u / L::kRawStages) & 1u,
+                        abort_flag, p.timeout_ns, timeout_code(kRoleProducer, 0x500 + slot)) ||
+          !wait_bounded(empty0 + 8 * ss, (static_cast<uint32_t>(u / kStages) & 1u) ^ 1u,
+                        abort_flag, p.timeout_ns, timeout_code(kRoleProducer, ss))) {
+        ok = false;
+        break;
+      }
+      rows_to_stage<L>(raw0 + slot * L::kRawStageBytes, sA + ss * L::kABytes,
+                       sB + ss * L::kBBytes, p, tid);
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+      mbar_arrive(full0 + 8 * ss);
+      mbar_arrive(raw_empty0 + 8 * slot);
+      if (tid == 0 && u + L::kRawStages < units) ok = issue(u + L::kRawStages);
+    }
+    if (tid == 0 && (!ok || *abort_flag)) {
+      // every copy this thread issued lands before the CTA can leave
+      for (int s = 0; s < L::kRawStages; ++s)
+        if (issued_mask >> s & 1u)
+          wait_bounded(raw_full0 + 8 * s, issued_parity >> s & 1u, abort_flag, p.timeout_ns,
+                       timeout_code(kRoleProducer, 0x600 + s), false);
+    }
+  } else if (warp < kStrMmaWarp) {
     // ------------------------------------------------------------ copy producer
     const int tid = static_cast<int>(threadIdx.x);
     uint32_t stage = 0, phase = 0;
@@ -204,7 +334,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
                    tn * kStrBN, kb * kStrBK, tid);
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         mbar_arrive(full0 + 8 * stage);
-        if (++stage == kStrStages) {
+        if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
@@ -238,7 +368,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) gemm_tn_strided_kernel(const S
             mma_f16(d_tmem, make_sw128_desc(a_base + k * 32, 16, 1024),
                     make_sw128_desc(b_base + k * 32, 16, 1024), idesc, (kb | k) != 0);
           mma_commit(empty0 + 8 * stage);
-          if (++stage == kStrStages) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }

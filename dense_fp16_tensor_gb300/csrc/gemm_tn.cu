@@ -177,8 +177,13 @@ int device_setup(int dev, DeviceState*& st) {
       e = cudaFuncSetAttribute(gemm_tn_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                WideSmem::kDynamicBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_tn_strided_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               StridedSmem::kDynamicBytes);
+      e = cudaFuncSetAttribute(gemm_tn_strided_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               StridedSmem<false>::kDynamicBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tn_strided_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               StridedSmem<true>::kDynamicBytes);
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg;
       std::memset(&cfg, 0, sizeof cfg);
@@ -1485,13 +1490,54 @@ bool tma_view(const void* p, int64_t rows, int64_t K, int64_t s_r, int64_t s_k, 
   return false;
 }
 
+// Tensor map of row class c (rows c, c + 8, ...) of a (rows, K) operand with
+// a stride-1 K mode and row stride ld elements: base rounded down to 16
+// bytes, the class's rows 16 * ld bytes apart, dims {K + delta, class rows},
+// box {K block + 8, tile rows / 8}, no swizzle.  Returns the byte offset of
+// the rows in the map's rows (2 * delta) or -1.
+int encode_row_class(CUtensorMap* map, const void* X, int64_t rows, int64_t K, int64_t ld, int c,
+                     uint32_t box_rows) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(X) + 2 * static_cast<uintptr_t>(c) *
+                                                          static_cast<uintptr_t>(ld);
+  const uintptr_t base = a & ~static_cast<uintptr_t>(15);
+  const int shift = static_cast<int>(a - base);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K + shift / 2),
+                        static_cast<cuuint64_t>((rows - c + 7) / 8)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 16};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kStrRawK), box_rows}, estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, reinterpret_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? shift : -1;
+}
+
 int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream_t stream) {
   StridedArgs p = base;
   const int grid = std::min(p.num_tiles, st.num_sms);
-  gemm_tn_strided_kernel<<<grid, kStrThreads, StridedSmem::kDynamicBytes, stream>>>(p);
+  // The row-class TMA variant when both operands have a stride-1 K mode,
+  // rows that do not overlap (ld >= K) and at least one row of every class
+  // (M, N >= 8); otherwise every chunk is gathered by the producer threads.
+  StridedMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  const int64_t kMaxLd = int64_t{1} << 35;  // class strides of 16 * ld bytes stay below 2^40
+  bool tma = p.sAk == 1 && p.sBk == 1 && p.M >= 8 && p.N >= 8 && p.K >= 1 && p.sAm >= p.K &&
+             p.sBn >= p.K && p.sAm < kMaxLd && p.sBn < kMaxLd;
+  for (int c = 0; tma && c < 8; ++c) {
+    p.a_shift[c] = encode_row_class(&maps.a[c], p.A, p.M, p.K, p.sAm, c, kStrBM / 8);
+    p.b_shift[c] = encode_row_class(&maps.b[c], p.B, p.N, p.K, p.sBn, c, kStrBN / 8);
+    tma = p.a_shift[c] >= 0 && p.b_shift[c] >= 0;
+  }
+  if (tma) {
+    gemm_tn_strided_kernel<true><<<grid, kStrThreads, StridedSmem<true>::kDynamicBytes, stream>>>(
+        maps, p);
+  } else {
+    gemm_tn_strided_kernel<false><<<grid, kStrThreads, StridedSmem<false>::kDynamicBytes,
+                                    stream>>>(maps, p);
+  }
   if (cudaGetLastError() != cudaSuccess) return GEMM_TN_ERR_CUDA;
   t_last_launches = 1;
-  t_last_kernels = "gemm_tn_strided_kernel";
+  t_last_kernels = tma ? "gemm_tn_strided_kernel<rows>" : "gemm_tn_strided_kernel";
   return GEMM_TN_OK;
 }
 

@@ -57,7 +57,7 @@ def run_case(M, N, K, view, accum, dist_ab, dist_c, seed, route=gb.PATH_STRIDED_
     assert st == gb.OK, gb.gemm_tn_status_string(st)
     kernels = gb.gemm_tn_last_kernels()
     if route == gb.PATH_STRIDED_COPY:
-        assert kernels == "gemm_tn_strided_kernel"
+        assert kernels.startswith("gemm_tn_strided_kernel"), kernels
     elif route == gb.PATH_STRIDED_REPACK:
         assert "gemm_tn_strided_kernel" not in kernels and kernels
     torch.cuda.synchronize()
@@ -98,3 +98,14 @@ def test_strided_auto_route_picks_repack_for_large_problems():
     got, d64, d16 = run_case(M, N, K, "odd_ld_k_major", 0, "int1", "int4", 950, gb.PATH_AUTO)
     assert gb.gemm_tn_last_kernels().startswith("repack2d_kernel+")
     check(got, d64, d16, K, 0, True, "auto route")
+
+
+@pytest.mark.parametrize("view,variant", [("odd_ld_k_major", "<rows>"), ("offset_by_one", "<rows>"),
+                                          ("odd_ld_mn_major", ""), ("no_unit_stride", "")])
+def test_copy_route_variant(view, variant):
+    # stride-1 K modes for both operands (any ld, any 2-byte offset) take the
+    # row-class TMA variant; other views gather through the strides
+    M, N, K = 300, 280, 700
+    got, d64, d16 = run_case(M, N, K, view, 0, "int1", "int4", 1950)
+    assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel" + variant
+    check(got, d64, d16, K, 0, True, f"copy route {view}")

@@ -143,7 +143,7 @@ def test_strided_routes_without_workspace():
     # automatic route on a problem large enough for repacking: falls back to
     # the copy producer, which needs no workspace
     st, k, _, view, d64, d16, _ = _strided(FAIL)
-    assert st == gb.OK and k == "gemm_tn_strided_kernel", k
+    assert st == gb.OK and k.startswith("gemm_tn_strided_kernel"), k
     check(view, d64, d16, 264, 0, True, "strided fallback")
     st, k, _, view2, _, _, _ = _strided({})
     assert st == gb.OK and k.startswith("repack2d_kernel+"), k
