@@ -6,7 +6,7 @@
 // strides for A (M,K), B (N,K) and C/D (M,N) and keeps everything after the
 // copy the same:
 //
-//   warps 0-7   copy producer: each thread gathers 16-byte K-chunks (8 fp16
+//   warps 0-15  copy producer: each thread gathers 16-byte K-chunks (8 fp16
 //               along K) of A and B rows through the strides, six chunks in
 //               flight at a time -- a contiguous chunk from the one or two
 //               aligned 16-byte words under it (shift_window), else eight
@@ -14,9 +14,9 @@
 //               layout the TMA unit would produce (row r, chunk j at byte
 //               r*128 + 16*(j ^ (r%8))), zero outside the matrix; then
 //               fence.proxy.async and one arrival per thread on `full`.
-//   warp 8      TMEM allocation and the single MMA-issuing thread
+//   warp 16     TMEM allocation and the single MMA-issuing thread
 //               (tcgen05.mma M=128, N=256, K=16, always K-major descriptors).
-//   warps 9-12  epilogue: tcgen05.ld, + C, round, D.  A row-major C/D view
+//   warps 17-20 epilogue: tcgen05.ld, + C, round, D.  A row-major C/D view
 //               goes through a per-warp 32 x 32 transpose in shared memory,
 //               so that C is read and D written a row segment per
 //               instruction; any other view element by element with one row
@@ -32,7 +32,7 @@
 // accepts.  One tensor map per class and operand, on the class's first row
 // rounded down to 16 bytes (the row then starts delta = 0..7 elements into
 // the map's rows), brings a K block in as boxes 72 elements wide (the block
-// plus the offset) into a raw ring; warps 0-7 then cut each 8-element chunk
+// plus the offset) into a raw ring; warps 0-15 then cut each 8-element chunk
 // out of the two raw 16-byte words under it (shift_window) into the
 // swizzled stage the MMA reads.  Rows past M / N and K past the end arrive
 // as zeros from the tensor maps' bounds.
@@ -49,13 +49,16 @@ constexpr int kStrBM = 128;
 constexpr int kStrBN = 256;
 constexpr int kStrBK = 64;
 constexpr int kStrStages = 4;
-constexpr int kStrProducers = 256;  // eight warps
-constexpr int kStrThreads = 416;    // 8 producer warps, MMA warp, 4 epilogue warps
+constexpr int kStrProducers = 512;  // sixteen warps
+constexpr int kStrThreads = 672;    // 16 producer warps, MMA warp, 4 epilogue warps
 constexpr int kStrMmaWarp = kStrProducers / 32;
 
 struct StridedArgs {
   int M, N, K;
-  int a_shift[8], b_shift[8];  // row-class variant: byte offset of a row in its map row
+  // row-class variant: byte offset of a row of class c in its map row, in
+  // bits 4c..4c+3 (a register-held word: indexing an array of the kernel's
+  // parameters by the class would read it through memory on every chunk)
+  uint32_t a_shifts, b_shifts;
   const __half* A;
   int64_t sAm, sAk;
   const __half* B;
@@ -174,21 +177,47 @@ __device__ __forceinline__ void fill_stage(uint8_t* dst_a, uint8_t* dst_b, const
   }
 }
 
+// wait_bounded for a wait that normally lasts a whole tile's main loop: the
+// waiting warp sleeps between probes instead of spinning, so that it does not
+// take issue slots from the producer warps that share its SM sub-partitions.
+__device__ __forceinline__ bool wait_bounded_sleeping(uint32_t bar, uint32_t parity,
+                                                      volatile uint32_t* abort_flag,
+                                                      uint64_t limit_ns, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(500);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicCAS(&g_error_word, 0u, code);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
 // Row-class variant: cut stage `ss` of the swizzled ring out of raw stage
-// `slot` (this thread's chunks: A's 1024 first, then B's 2048).
+// `slot` (this thread's chunks: A's 1024 first, then B's 2048).  Chunks are
+// numbered class by class (row j of class c is tile row c + 8j), so the 32
+// chunks of one warp instruction share a class and its shift: the shift's
+// branch is uniform across the warp.
 template <typename L>
 __device__ __forceinline__ void rows_to_stage(const uint8_t* raw, uint8_t* dst_a, uint8_t* dst_b,
-                                              const StridedArgs& p, int tid) {
+                                              uint32_t a_shifts, uint32_t b_shifts, int tid) {
   constexpr int kA = kStrBM * 8, kTotal = (kStrBM + kStrBN) * 8;
 #pragma unroll 4
   for (int q = tid; q < kTotal; q += kStrProducers) {
     const bool is_a = q < kA;
     const int qq = is_a ? q : q - kA;
-    const int r = qq >> 3, k8 = qq & 7, c = r & 7, j = r >> 3;
+    // chunks of one class: rows / 8 * 8 = 128 (A) or 256 (B)
+    static_assert(kStrBM == 128 && kStrBN == 256, "class sizes below");
+    const int c = is_a ? qq >> 7 : qq >> 8, within = is_a ? qq & 127 : qq & 255;
+    const int j = within >> 3, k8 = within & 7, r = c + 8 * j;
     // raw row of (class c, row j of the class) and the chunk's first byte in it
     const uint8_t* row = is_a ? raw + (c * (kStrBM / 8) + j) * kStrRawRowBytes
                               : raw + L::kRawABytes + (c * (kStrBN / 8) + j) * kStrRawRowBytes;
-    const int sh = is_a ? p.a_shift[c] : p.b_shift[c];
+    const int sh = static_cast<int>(((is_a ? a_shifts : b_shifts) >> (4 * c)) & 15u);
     const uint4* w = reinterpret_cast<const uint4*>(row + 16 * k8);
     const uint4 v = sh ? shift_window(w[0], w[1], sh) : w[0];
     uint8_t* dst = (is_a ? dst_a : dst_b) + r * 128 + 16 * (k8 ^ (r & 7));
@@ -289,6 +318,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
       return true;
     };
     bool ok = true;
+    const uint32_t a_shifts = p.a_shifts, b_shifts = p.b_shifts;
     if (tid == 0) {
       for (int u = 0; ok && u < min(units, L::kRawStages); ++u) ok = issue(u);
     }
@@ -303,7 +333,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
         break;
       }
       rows_to_stage<L>(raw0 + slot * L::kRawStageBytes, sA + ss * L::kABytes,
-                       sB + ss * L::kBBytes, p, tid);
+                       sB + ss * L::kBBytes, a_shifts, b_shifts, tid);
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
       mbar_arrive(full0 + 8 * ss);
       mbar_arrive(raw_empty0 + 8 * slot);
@@ -394,7 +424,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int tm, tn;
       tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-      if (!wait_bounded(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
+      if (!wait_bounded_sleeping(tfull0 + 8 * acc, acc_phase, abort_flag, p.timeout_ns,
                         timeout_code(kRoleEpilogue, acc)))
         break;
       tc_fence_after();

@@ -1524,9 +1524,13 @@ int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream
   bool tma = p.sAk == 1 && p.sBk == 1 && p.M >= 8 && p.N >= 8 && p.K >= 1 && p.sAm >= p.K &&
              p.sBn >= p.K && p.sAm < kMaxLd && p.sBn < kMaxLd;
   for (int c = 0; tma && c < 8; ++c) {
-    p.a_shift[c] = encode_row_class(&maps.a[c], p.A, p.M, p.K, p.sAm, c, kStrBM / 8);
-    p.b_shift[c] = encode_row_class(&maps.b[c], p.B, p.N, p.K, p.sBn, c, kStrBN / 8);
-    tma = p.a_shift[c] >= 0 && p.b_shift[c] >= 0;
+    const int sa = encode_row_class(&maps.a[c], p.A, p.M, p.K, p.sAm, c, kStrBM / 8);
+    const int sb = encode_row_class(&maps.b[c], p.B, p.N, p.K, p.sBn, c, kStrBN / 8);
+    tma = sa >= 0 && sb >= 0;
+    if (tma) {
+      p.a_shifts |= static_cast<uint32_t>(sa) << (4 * c);
+      p.b_shifts |= static_cast<uint32_t>(sb) << (4 * c);
+    }
   }
   if (tma) {
     gemm_tn_strided_kernel<true><<<grid, kStrThreads, StridedSmem<true>::kDynamicBytes, stream>>>(
