@@ -197,32 +197,62 @@ __device__ __forceinline__ bool wait_bounded_sleeping(uint32_t bar, uint32_t par
   }
 }
 
-// Row-class variant: cut stage `ss` of the swizzled ring out of raw stage
-// `slot` (this thread's chunks: A's 1024 first, then B's 2048).  Chunks are
-// numbered class by class (row j of class c is tile row c + 8j), so the 32
-// chunks of one warp instruction share a class and its shift: the shift's
-// branch is uniform across the warp.
+// Row-class variant: this thread's chunks of a stage, kStrChunks of them (A's
+// 1024 chunks first, then B's 2048, dealt round-robin to the producer
+// threads).  Chunks are numbered class by class (row j of class c is tile
+// row c + 8j), so the 32 chunks of one warp instruction share a class and
+// its shift: the shift's branch is uniform across the warp.  The offsets do
+// not depend on the K block, so they are worked out once.
+constexpr int kStrChunks = (kStrBM + kStrBN) * 8 / kStrProducers;
+static_assert(kStrChunks * kStrProducers == (kStrBM + kStrBN) * 8, "whole chunks per thread");
+static_assert(kStrBM * 8 % kStrProducers == 0, "A's chunks end on a round");
+
+struct RowChunks {
+  // per chunk: bits 0-15 its first aligned word in the raw stage (< 64 KiB),
+  // bits 16-31 its 16 bytes in the A or B part of the swizzled stage
+  uint32_t off[kStrChunks];
+  uint32_t shifts;  // bits 4i..4i+3: byte offset of chunk i in its first word
+};
+
 template <typename L>
-__device__ __forceinline__ void rows_to_stage(const uint8_t* raw, uint8_t* dst_a, uint8_t* dst_b,
-                                              uint32_t a_shifts, uint32_t b_shifts, int tid) {
-  constexpr int kA = kStrBM * 8, kTotal = (kStrBM + kStrBN) * 8;
-#pragma unroll 4
-  for (int q = tid; q < kTotal; q += kStrProducers) {
-    const bool is_a = q < kA;
+__device__ __forceinline__ RowChunks row_chunks(uint32_t a_shifts, uint32_t b_shifts, int tid) {
+  static_assert(kStrBM == 128 && kStrBN == 256, "class sizes below");
+  constexpr int kA = kStrBM * 8;
+  static_assert(L::kRawStageBytes <= 65536 && kStrBN * 128 <= 65536, "16-bit offsets");
+  RowChunks rc;
+  uint32_t shifts = 0;
+#pragma unroll
+  for (int i = 0; i < kStrChunks; ++i) {
+    const int q = tid + i * kStrProducers;
+    const bool is_a = q < kA;  // (the same for every thread at a given i)
     const int qq = is_a ? q : q - kA;
-    // chunks of one class: rows / 8 * 8 = 128 (A) or 256 (B)
-    static_assert(kStrBM == 128 && kStrBN == 256, "class sizes below");
     const int c = is_a ? qq >> 7 : qq >> 8, within = is_a ? qq & 127 : qq & 255;
     const int j = within >> 3, k8 = within & 7, r = c + 8 * j;
-    // raw row of (class c, row j of the class) and the chunk's first byte in it
-    const uint8_t* row = is_a ? raw + (c * (kStrBM / 8) + j) * kStrRawRowBytes
-                              : raw + L::kRawABytes + (c * (kStrBN / 8) + j) * kStrRawRowBytes;
-    const int sh = static_cast<int>(((is_a ? a_shifts : b_shifts) >> (4 * c)) & 15u);
-    const uint4* w = reinterpret_cast<const uint4*>(row + 16 * k8);
-    const uint4 v = sh ? shift_window(w[0], w[1], sh) : w[0];
-    uint8_t* dst = (is_a ? dst_a : dst_b) + r * 128 + 16 * (k8 ^ (r & 7));
-    *reinterpret_cast<uint4*>(dst) = v;
+    const uint32_t raw_off = (is_a ? (c * (kStrBM / 8) + j) * kStrRawRowBytes
+                                    : L::kRawABytes + (c * (kStrBN / 8) + j) * kStrRawRowBytes) +
+                             16 * k8;
+    const uint32_t dst_off = r * 128 + 16 * (k8 ^ (r & 7));
+    rc.off[i] = raw_off | (dst_off << 16);
+    shifts |= (((is_a ? a_shifts : b_shifts) >> (4 * c)) & 15u) << (4 * i);
   }
+  rc.shifts = shifts;
+  return rc;
+}
+
+// Cut one stage of the swizzled ring out of a raw stage.
+__device__ __forceinline__ void rows_to_stage(const uint8_t* raw, uint8_t* dst_a, uint8_t* dst_b,
+                                              const RowChunks& rc) {
+  constexpr int kAChunks = kStrBM * 8 / kStrProducers;
+  uint4 v[kStrChunks];
+#pragma unroll
+  for (int i = 0; i < kStrChunks; ++i) {
+    const uint4* w = reinterpret_cast<const uint4*>(raw + (rc.off[i] & 0xFFFFu));
+    const int sh = static_cast<int>((rc.shifts >> (4 * i)) & 15u);
+    v[i] = sh ? shift_window(w[0], w[1], sh) : w[0];
+  }
+#pragma unroll
+  for (int i = 0; i < kStrChunks; ++i)
+    *reinterpret_cast<uint4*>((i < kAChunks ? dst_a : dst_b) + (rc.off[i] >> 16)) = v[i];
 }
 
 template <bool kTma>
@@ -318,7 +348,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
       return true;
     };
     bool ok = true;
-    const uint32_t a_shifts = p.a_shifts, b_shifts = p.b_shifts;
+    const RowChunks rc = row_chunks<L>(p.a_shifts, p.b_shifts, tid);
     if (tid == 0) {
       for (int u = 0; ok && u < min(units, L::kRawStages); ++u) ok = issue(u);
     }
@@ -332,8 +362,8 @@ __global__ void __launch_bounds__(kStrThreads, 1)
         ok = false;
         break;
       }
-      rows_to_stage<L>(raw0 + slot * L::kRawStageBytes, sA + ss * L::kABytes,
-                       sB + ss * L::kBBytes, a_shifts, b_shifts, tid);
+      rows_to_stage(raw0 + slot * L::kRawStageBytes, sA + ss * L::kABytes,
+                    sB + ss * L::kBBytes, rc);
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
       mbar_arrive(full0 + 8 * ss);
       mbar_arrive(raw_empty0 + 8 * slot);
