@@ -6,7 +6,7 @@
 // strides for A (M,K), B (N,K) and C/D (M,N) and keeps everything after the
 // copy the same:
 //
-//   warps 0-15  copy producer: each thread gathers 16-byte K-chunks (8 fp16
+//   warps 0-11  copy producer: each thread gathers 16-byte K-chunks (8 fp16
 //               along K) of A and B rows through the strides, six chunks in
 //               flight at a time -- a contiguous chunk from the one or two
 //               aligned 16-byte words under it (shift_window), else eight
@@ -14,9 +14,9 @@
 //               layout the TMA unit would produce (row r, chunk j at byte
 //               r*128 + 16*(j ^ (r%8))), zero outside the matrix; then
 //               fence.proxy.async and one arrival per thread on `full`.
-//   warp 16     TMEM allocation and the single MMA-issuing thread
+//   warp 12     TMEM allocation and the single MMA-issuing thread
 //               (tcgen05.mma M=128, N=256, K=16, always K-major descriptors).
-//   warps 17-20 epilogue: tcgen05.ld, + C, round, D.  A row-major C/D view
+//   warps 13-16 epilogue: tcgen05.ld, + C, round, D.  A row-major C/D view
 //               goes through a per-warp 32 x 32 transpose in shared memory,
 //               so that C is read and D written a row segment per
 //               instruction; any other view element by element with one row
@@ -32,7 +32,7 @@
 // accepts.  One tensor map per class and operand, on the class's first row
 // rounded down to 16 bytes (the row then starts delta = 0..7 elements into
 // the map's rows), brings a K block in as boxes 72 elements wide (the block
-// plus the offset) into a raw ring; warps 0-15 then cut each 8-element chunk
+// plus the offset) into a raw ring; warps 0-11 then cut each 8-element chunk
 // out of the two raw 16-byte words under it (shift_window) into the
 // swizzled stage the MMA reads.  Rows past M / N and K past the end arrive
 // as zeros from the tensor maps' bounds.
@@ -49,8 +49,11 @@ constexpr int kStrBM = 128;
 constexpr int kStrBN = 256;
 constexpr int kStrBK = 64;
 constexpr int kStrStages = 4;
-constexpr int kStrProducers = 512;  // sixteen warps
-constexpr int kStrThreads = 672;    // 16 producer warps, MMA warp, 4 epilogue warps
+// Twelve producer warps: with the MMA and four epilogue warps, 17 warps put
+// at most five on an SM sub-partition, which leaves 96 registers a thread
+// (sixteen producer warps would cap it at 80 and spill in the shift pass).
+constexpr int kStrProducers = 384;
+constexpr int kStrThreads = 544;    // 12 producer warps, MMA warp, 4 epilogue warps
 constexpr int kStrMmaWarp = kStrProducers / 32;
 
 struct StridedArgs {
@@ -205,11 +208,12 @@ __device__ __forceinline__ bool wait_bounded_sleeping(uint32_t bar, uint32_t par
 // not depend on the K block, so they are worked out once.
 constexpr int kStrChunks = (kStrBM + kStrBN) * 8 / kStrProducers;
 static_assert(kStrChunks * kStrProducers == (kStrBM + kStrBN) * 8, "whole chunks per thread");
-static_assert(kStrBM * 8 % kStrProducers == 0, "A's chunks end on a round");
+static_assert(kStrBM * 8 % 32 == 0, "A's chunks end on a warp boundary");
 
 struct RowChunks {
   // per chunk: bits 0-15 its first aligned word in the raw stage (< 64 KiB),
-  // bits 16-31 its 16 bytes in the A or B part of the swizzled stage
+  // bits 16-30 its 16 bytes in the A or B part of the swizzled stage, bit 31
+  // set for B (the same in a whole warp: A's chunks end on a warp boundary)
   uint32_t off[kStrChunks];
   uint32_t shifts;  // bits 4i..4i+3: byte offset of chunk i in its first word
 };
@@ -218,13 +222,13 @@ template <typename L>
 __device__ __forceinline__ RowChunks row_chunks(uint32_t a_shifts, uint32_t b_shifts, int tid) {
   static_assert(kStrBM == 128 && kStrBN == 256, "class sizes below");
   constexpr int kA = kStrBM * 8;
-  static_assert(L::kRawStageBytes <= 65536 && kStrBN * 128 <= 65536, "16-bit offsets");
+  static_assert(L::kRawStageBytes <= 65536 && kStrBN * 128 <= 32768, "packed offsets");
   RowChunks rc;
   uint32_t shifts = 0;
 #pragma unroll
   for (int i = 0; i < kStrChunks; ++i) {
     const int q = tid + i * kStrProducers;
-    const bool is_a = q < kA;  // (the same for every thread at a given i)
+    const bool is_a = q < kA;
     const int qq = is_a ? q : q - kA;
     const int c = is_a ? qq >> 7 : qq >> 8, within = is_a ? qq & 127 : qq & 255;
     const int j = within >> 3, k8 = within & 7, r = c + 8 * j;
@@ -232,7 +236,7 @@ __device__ __forceinline__ RowChunks row_chunks(uint32_t a_shifts, uint32_t b_sh
                                     : L::kRawABytes + (c * (kStrBN / 8) + j) * kStrRawRowBytes) +
                              16 * k8;
     const uint32_t dst_off = r * 128 + 16 * (k8 ^ (r & 7));
-    rc.off[i] = raw_off | (dst_off << 16);
+    rc.off[i] = raw_off | (dst_off << 16) | (is_a ? 0u : 0x80000000u);
     shifts |= (((is_a ? a_shifts : b_shifts) >> (4 * c)) & 15u) << (4 * i);
   }
   rc.shifts = shifts;
@@ -242,17 +246,26 @@ __device__ __forceinline__ RowChunks row_chunks(uint32_t a_shifts, uint32_t b_sh
 // Cut one stage of the swizzled ring out of a raw stage.
 __device__ __forceinline__ void rows_to_stage(const uint8_t* raw, uint8_t* dst_a, uint8_t* dst_b,
                                               const RowChunks& rc) {
-  constexpr int kAChunks = kStrBM * 8 / kStrProducers;
-  uint4 v[kStrChunks];
+  // four chunks at a time: their loads in flight together, within the
+  // registers the block's size leaves a thread
+  constexpr int kBatch = 4;
+  static_assert(kStrChunks % kBatch == 0, "whole batches");
 #pragma unroll
-  for (int i = 0; i < kStrChunks; ++i) {
-    const uint4* w = reinterpret_cast<const uint4*>(raw + (rc.off[i] & 0xFFFFu));
-    const int sh = static_cast<int>((rc.shifts >> (4 * i)) & 15u);
-    v[i] = sh ? shift_window(w[0], w[1], sh) : w[0];
+  for (int b = 0; b < kStrChunks; b += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const uint32_t off = rc.off[b + i];
+      const uint4* w = reinterpret_cast<const uint4*>(raw + (off & 0xFFFFu));
+      const int sh = static_cast<int>((rc.shifts >> (4 * (b + i))) & 15u);
+      v[i] = sh ? shift_window(w[0], w[1], sh) : w[0];
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const uint32_t off = rc.off[b + i];
+      *reinterpret_cast<uint4*>(((off >> 31) ? dst_b : dst_a) + ((off >> 16) & 0x7FFFu)) = v[i];
+    }
   }
-#pragma unroll
-  for (int i = 0; i < kStrChunks; ++i)
-    *reinterpret_cast<uint4*>((i < kAChunks ? dst_a : dst_b) + (rc.off[i] >> 16)) = v[i];
 }
 
 template <bool kTma>
