@@ -69,6 +69,10 @@ def parse(argv=None):
     ap.add_argument("--all-extras", action="store_true",
                     help="also time cuBLAS on the headline inputs, the strided route, "
                          "stream-K, the scaled/batched form and the tile K splits")
+    ap.add_argument("--only-strided", action="store_true",
+                    help="time only the general-stride entry point (4096^3, leading "
+                         "dimensions K+1 and N+1; both routes) and print its figures, "
+                         "for profiling its kernels")
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stream-k", type=int, default=0,
                     help="256x256 kernel: 0 auto, 1 split any partial last wave, -1 never")
@@ -339,6 +343,9 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     g.build()
     gb.lib()
+    if args.only_strided:
+        print(json.dumps({"strided_4096": bench_strided(dev, torch.cuda.Stream(dev))}), flush=True)
+        return 0
 
     w = pick_workload(args)
     A_st, B_st, C_st = wl.make_inputs(w)

@@ -31,11 +31,17 @@
 // and the rows of one class are 16 * ld bytes apart -- a stride TMA
 // accepts.  One tensor map per class and operand, on the class's first row
 // rounded down to 16 bytes (the row then starts delta = 0..7 elements into
-// the map's rows), brings a K block in as boxes 72 elements wide (the block
-// plus the offset) into a raw ring; warps 0-11 then cut each 8-element chunk
-// out of the two raw 16-byte words under it (shift_window) into the
-// swizzled stage the MMA reads.  Rows past M / N and K past the end arrive
-// as zeros from the tensor maps' bounds.
+// the map's rows), brings a K block in as one 128B-swizzled box per class
+// (16 rows of A, 32 of B) straight into the stage the MMA reads; each of
+// warps 0-11's threads owns one stage row and shifts it left in place by
+// its delta, the last delta elements taken from the same row of the next K
+// block's box (or, after a tile's last K block, read from the row itself).
+// The stage then holds the tile's rows in class order (row s of the A part
+// is tile row s / 16 + 8 (s % 16)); the MMA does not mind, and the epilogue
+// reads the accumulator back in tile order.  Rows past M / N and K past the
+// end arrive as zeros from the tensor maps' bounds.  The route's speed is
+// set by its sixteen boxes per K block (each box costs the TMA unit a
+// roughly fixed time), not by the shift.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -81,26 +87,21 @@ struct StridedMaps {
   CUtensorMap b[8];
 };
 
-constexpr int kStrRawK = kStrBK + 8;        // elements per raw row (the block plus the offset)
-constexpr int kStrRawRowBytes = kStrRawK * 2;  // 144
-
 template <bool kTma>
 struct StridedSmem {
-  static constexpr int kStages = kTma ? 2 : kStrStages;  // swizzled stages the MMA reads
-  static constexpr int kRawStages = kTma ? 2 : 0;
+  // swizzled stages the MMA reads (the row-class variant's boxes land in
+  // them and are shifted in place)
+  static constexpr int kStages = kStrStages;
   static constexpr uint32_t kABytes = kStrBM * kStrBK * 2;  // 16 KiB
   static constexpr uint32_t kBBytes = kStrBN * kStrBK * 2;  // 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  // raw ring: per class 16 rows of A and 32 rows of B, 144 bytes each
-  static constexpr uint32_t kRawABytes = kStrBM * kStrRawRowBytes;  // 18 KiB
-  static constexpr uint32_t kRawBBytes = kStrBN * kStrRawRowBytes;  // 36 KiB
-  static constexpr uint32_t kRawStageBytes = kRawABytes + kRawBBytes;
-  static constexpr uint32_t kRawOffset = kStages * kStageBytes;
   // per epilogue warp a 32 x 33 word transpose buffer
-  static constexpr uint32_t kXposeOffset = kRawOffset + kRawStages * kRawStageBytes;
+  static constexpr uint32_t kXposeOffset = kStages * kStageBytes;
   static constexpr uint32_t kXposeBytes = 32 * 33 * 4;
   static constexpr uint32_t kBarOffset = kXposeOffset + 4 * kXposeBytes;
-  static constexpr uint32_t kNumBars = 2 * kStages + 5 + 2 * kRawStages;
+  // full and empty per stage, two tfull, two tempty, drain; row-class
+  // variant: `landed` per stage (the stage's boxes are in)
+  static constexpr uint32_t kNumBars = 2 * kStages + 5 + (kTma ? kStages : 0);
   static constexpr uint32_t kCtlOffset = kBarOffset + kNumBars * 8;
   static constexpr uint32_t kBytes = kCtlOffset + 16;
   static constexpr uint32_t kDynamicBytes = kBytes + 1024;
@@ -200,72 +201,53 @@ __device__ __forceinline__ bool wait_bounded_sleeping(uint32_t bar, uint32_t par
   }
 }
 
-// Row-class variant: this thread's chunks of a stage, kStrChunks of them (A's
-// 1024 chunks first, then B's 2048, dealt round-robin to the producer
-// threads).  Chunks are numbered class by class (row j of class c is tile
-// row c + 8j), so the 32 chunks of one warp instruction share a class and
-// its shift: the shift's branch is uniform across the warp.  The offsets do
-// not depend on the K block, so they are worked out once.
-constexpr int kStrChunks = (kStrBM + kStrBN) * 8 / kStrProducers;
-static_assert(kStrChunks * kStrProducers == (kStrBM + kStrBN) * 8, "whole chunks per thread");
-static_assert(kStrBM * 8 % 32 == 0, "A's chunks end on a warp boundary");
+// Row-class variant.  A class box (16 rows of A, 32 of B, 64 elements of K)
+// lands as consecutive rows of a stage, so stage row s of the A part holds
+// tile row (s / 16) + 8 (s % 16), and stage row s of the B part tile column
+// (s / 32) + 8 (s % 32).  The MMA multiplies the rows in that order; the
+// epilogue reads accumulator lane s and column t back as those tile rows
+// and columns.
+__device__ __forceinline__ int class_row_a(int s) { return (s >> 4) + 8 * (s & 15); }
+__device__ __forceinline__ int class_row_b(int s) { return (s >> 5) + 8 * (s & 31); }
 
-struct RowChunks {
-  // per chunk: bits 0-15 its first aligned word in the raw stage (< 64 KiB),
-  // bits 16-30 its 16 bytes in the A or B part of the swizzled stage, bit 31
-  // set for B (the same in a whole warp: A's chunks end on a warp boundary)
-  uint32_t off[kStrChunks];
-  uint32_t shifts;  // bits 4i..4i+3: byte offset of chunk i in its first word
-};
-
-template <typename L>
-__device__ __forceinline__ RowChunks row_chunks(uint32_t a_shifts, uint32_t b_shifts, int tid) {
-  static_assert(kStrBM == 128 && kStrBN == 256, "class sizes below");
-  constexpr int kA = kStrBM * 8;
-  static_assert(L::kRawStageBytes <= 65536 && kStrBN * 128 <= 32768, "packed offsets");
-  RowChunks rc;
-  uint32_t shifts = 0;
+// A box row starts `sh` bytes (even, 0..14) before the row's K block: the
+// row, 128B-swizzled at stage row s (16-byte chunk j at 16 (j ^ (s % 8))),
+// is shifted left in place by sh bytes, its last sh bytes taken from `next`
+// (the first 16 bytes of the same row of the following K block).
+__device__ __forceinline__ void shift_row_in_place(uint8_t* row, uint32_t sw, int sh,
+                                                   const uint4& next) {
+  uint4 w[8];
 #pragma unroll
-  for (int i = 0; i < kStrChunks; ++i) {
-    const int q = tid + i * kStrProducers;
-    const bool is_a = q < kA;
-    const int qq = is_a ? q : q - kA;
-    const int c = is_a ? qq >> 7 : qq >> 8, within = is_a ? qq & 127 : qq & 255;
-    const int j = within >> 3, k8 = within & 7, r = c + 8 * j;
-    const uint32_t raw_off = (is_a ? (c * (kStrBM / 8) + j) * kStrRawRowBytes
-                                    : L::kRawABytes + (c * (kStrBN / 8) + j) * kStrRawRowBytes) +
-                             16 * k8;
-    const uint32_t dst_off = r * 128 + 16 * (k8 ^ (r & 7));
-    rc.off[i] = raw_off | (dst_off << 16) | (is_a ? 0u : 0x80000000u);
-    shifts |= (((is_a ? a_shifts : b_shifts) >> (4 * c)) & 15u) << (4 * i);
-  }
-  rc.shifts = shifts;
-  return rc;
+  for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(row + 16 * (j ^ sw));
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(row + 16 * (j ^ sw)) = shift_window(w[j], j < 7 ? w[j + 1] : next, sh);
 }
 
-// Cut one stage of the swizzled ring out of a raw stage.
-__device__ __forceinline__ void rows_to_stage(const uint8_t* raw, uint8_t* dst_a, uint8_t* dst_b,
-                                              const RowChunks& rc) {
-  // four chunks at a time: their loads in flight together, within the
-  // registers the block's size leaves a thread
-  constexpr int kBatch = 4;
-  static_assert(kStrChunks % kBatch == 0, "whole batches");
+// The 16 bytes after the last K block of a row that starts sh bytes into its
+// box: elements k0 - sh/2 .. k0 - 1 of the row (k0 = the blocks' end), those
+// below K, in bytes [0, sh); zeros elsewhere.  Plain 2-byte loads inside
+// the row (the next box would start past the blocks' end).
+__device__ __forceinline__ uint4 row_tail(const __half* row, int K, int k0, int sh) {
+  uint32_t v[4] = {0u, 0u, 0u, 0u};
+  const int d = sh >> 1;
 #pragma unroll
-  for (int b = 0; b < kStrChunks; b += kBatch) {
-    uint4 v[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const uint32_t off = rc.off[b + i];
-      const uint4* w = reinterpret_cast<const uint4*>(raw + (off & 0xFFFFu));
-      const int sh = static_cast<int>((rc.shifts >> (4 * (b + i))) & 15u);
-      v[i] = sh ? shift_window(w[0], w[1], sh) : w[0];
-    }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const uint32_t off = rc.off[b + i];
-      *reinterpret_cast<uint4*>(((off >> 31) ? dst_b : dst_a) + ((off >> 16) & 0x7FFFu)) = v[i];
+  for (int e = 0; e < 7; ++e) {
+    const int k = k0 - d + e;
+    if (e < d && k < K) {
+      const uint32_t h = __ldg(reinterpret_cast<const unsigned short*>(row + k));
+      v[e >> 1] |= h << (16 * (e & 1));
     }
   }
+  return make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+// tcgen05.ld of 4 consecutive accumulator columns for the warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
 }
 
 template <bool kTma>
@@ -278,7 +260,6 @@ __global__ void __launch_bounds__(kStrThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;                             // stage s at s * kABytes
   uint8_t* sB = smem + kStages * L::kABytes;      // stage s at s * kBBytes
-  uint8_t* raw0 = smem + L::kRawOffset;           // raw stage s at s * kRawStageBytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kCtlOffset);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOffset + 4);
@@ -288,8 +269,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
   const uint32_t tfull0 = smem_u32(bars + 2 * kStages);
   const uint32_t tempty0 = smem_u32(bars + 2 * kStages + 2);
   const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
-  const uint32_t raw_full0 = smem_u32(bars + 2 * kStages + 5);
-  const uint32_t raw_empty0 = raw_full0 + 8 * L::kRawStages;
+  const uint32_t land0 = smem_u32(bars + 2 * kStages + 5);  // row-class variant only
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -304,10 +284,8 @@ __global__ void __launch_bounds__(kStrThreads, 1)
       mbar_init(tempty0 + 8 * a, 4);
     }
     mbar_init(drain, 1);
-    for (int s = 0; s < L::kRawStages; ++s) {
-      mbar_init(raw_full0 + 8 * s, 1);
-      mbar_init(raw_empty0 + 8 * s, kStrProducers);
-    }
+    if (kTma)
+      for (int s = 0; s < kStages; ++s) mbar_init(land0 + 8 * s, 1);
     *abort_flag = 0u;
     fence_barrier_init();
   }
@@ -328,66 +306,100 @@ __global__ void __launch_bounds__(kStrThreads, 1)
 
   if (warp < kStrMmaWarp && kTma) {
     // ------------------------------------------------ row-class TMA producer
+    // Thread tid owns stage row s of the A part (tid < 128) or of the B part
+    // in every stage: it shifts that row in place once the row's box and the
+    // following K block's box have landed.  No other thread touches the row,
+    // so the next block's first 16 bytes are read before this thread shifts
+    // that block.
     const int tid = static_cast<int>(threadIdx.x);
+    const bool is_b = tid >= kStrBM;
+    const int s = is_b ? tid - kStrBM : tid;
+    const int cls = is_b ? s >> 5 : s >> 4;
+    const int sh = static_cast<int>(((is_b ? p.b_shifts : p.a_shifts) >> (4 * cls)) & 15u);
+    const uint32_t sw = static_cast<uint32_t>(s & 7);
+    uint8_t* const part0 = (is_b ? sB : sA) + s * 128;  // this row in stage 0
+    const uint32_t part_bytes = is_b ? L::kBBytes : L::kABytes;
+    const __half* const X = is_b ? p.B : p.A;
+    const int64_t ldx = is_b ? p.sBn : p.sAm;
+    const int rows = is_b ? p.N : p.M;
+    const int my_row = is_b ? class_row_b(s) : class_row_a(s);  // in its tile
     const int my_tiles = p.num_tiles > static_cast<int>(blockIdx.x)
                              ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                              : 0;
     const int units = my_tiles * p.k_blocks;  // (tile, K block) pairs of this CTA, in order
-    uint32_t issued_mask = 0, issued_parity = 0;  // thread 0: raw stages with copies in flight
-    // thread 0 loads unit u into raw stage u % 2 once the stage's previous
-    // unit has been cut out by every producer thread
+    // threads 0-15 (lanes of warp 0): stages with copies in flight
+    uint32_t issued_mask = 0, issued_parity = 0;
+    // Unit u goes into stage u % 4 once the MMA has released the stage.  Its
+    // sixteen boxes (A classes 0-7, B classes 0-7) are issued by sixteen
+    // threads, one each, after thread 0 has armed `landed` with the stage's
+    // bytes (a copy that lands before the arming drives the barrier's byte
+    // count below zero; the phase still needs the arrival).  One thread
+    // issuing all sixteen boxes was measurably slower.
     auto issue = [&](int u) -> bool {
-      const int slot = u % L::kRawStages;
-      const uint32_t use = static_cast<uint32_t>(u / L::kRawStages);
-      if (!wait_bounded(raw_empty0 + 8 * slot, (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
+      const int slot = u % kStages;
+      const uint32_t use = static_cast<uint32_t>(u / kStages);
+      if (!wait_bounded(empty0 + 8 * slot, (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
                         timeout_code(kRoleProducer, 0x400 + slot)))
         return false;
       const int t = static_cast<int>(blockIdx.x) + (u / p.k_blocks) * static_cast<int>(gridDim.x);
       const int kb = u % p.k_blocks;
       int tm, tn;
       tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-      const uint32_t fb = raw_full0 + 8 * slot;
-      const uint32_t dst = smem_u32(raw0 + slot * L::kRawStageBytes);
-      mbar_arrive_expect_tx(fb, L::kRawStageBytes);
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        tma_load_2d(dst + c * (kStrBM / 8) * kStrRawRowBytes, &maps.a[c], fb, kb * kStrBK,
-                    tm * (kStrBM / 8));
-        tma_load_2d(dst + L::kRawABytes + c * (kStrBN / 8) * kStrRawRowBytes, &maps.b[c], fb,
+      const uint32_t lb = land0 + 8 * slot;
+      if (tid == 0) mbar_arrive_expect_tx(lb, L::kStageBytes);
+      const int c = tid & 7;
+      if (tid < 8)
+        tma_load_2d(smem_u32(sA + slot * L::kABytes + c * (kStrBM / 8) * 128), &maps.a[c], lb,
+                    kb * kStrBK, tm * (kStrBM / 8));
+      else
+        tma_load_2d(smem_u32(sB + slot * L::kBBytes + c * (kStrBN / 8) * 128), &maps.b[c], lb,
                     kb * kStrBK, tn * (kStrBN / 8));
-      }
       issued_mask |= 1u << slot;
       issued_parity = (issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
       return true;
     };
     bool ok = true;
-    const RowChunks rc = row_chunks<L>(p.a_shifts, p.b_shifts, tid);
-    if (tid == 0) {
-      for (int u = 0; ok && u < min(units, L::kRawStages); ++u) ok = issue(u);
+    if (tid < 16) {
+      for (int u = 0; ok && u < min(units, kStages - 1); ++u) ok = issue(u);
     }
     for (int u = 0; ok && u < units; ++u) {
-      const int slot = u % L::kRawStages;
-      const int ss = u % kStages;
-      if (!wait_bounded(raw_full0 + 8 * slot, static_cast<uint32_t>(u / L::kRawStages) & 1u,
-                        abort_flag, p.timeout_ns, timeout_code(kRoleProducer, 0x500 + slot)) ||
-          !wait_bounded(empty0 + 8 * ss, (static_cast<uint32_t>(u / kStages) & 1u) ^ 1u,
-                        abort_flag, p.timeout_ns, timeout_code(kRoleProducer, ss))) {
+      const int slot = u % kStages;
+      const int kb = u % p.k_blocks;
+      const bool last = kb == p.k_blocks - 1;
+      const int nslot = (u + 1) % kStages;
+      if (!wait_bounded(land0 + 8 * slot, static_cast<uint32_t>(u / kStages) & 1u, abort_flag,
+                        p.timeout_ns, timeout_code(kRoleProducer, 0x500 + slot)) ||
+          (!last && !wait_bounded(land0 + 8 * nslot, static_cast<uint32_t>((u + 1) / kStages) & 1u,
+                                  abort_flag, p.timeout_ns,
+                                  timeout_code(kRoleProducer, 0x500 + nslot)))) {
         ok = false;
         break;
       }
-      rows_to_stage(raw0 + slot * L::kRawStageBytes, sA + ss * L::kABytes,
-                    sB + ss * L::kBBytes, rc);
+      if (sh != 0) {
+        uint4 next;
+        if (!last) {
+          next = *reinterpret_cast<const uint4*>(part0 + nslot * part_bytes + 16 * sw);
+        } else {
+          const int t = static_cast<int>(blockIdx.x) + (u / p.k_blocks) * static_cast<int>(gridDim.x);
+          int tm, tn;
+          tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+          const int grow = (is_b ? tn * kStrBN : tm * kStrBM) + my_row;
+          next = grow < rows ? row_tail(X + static_cast<int64_t>(grow) * ldx, p.K,
+                                        p.k_blocks * kStrBK, sh)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+        shift_row_in_place(part0 + slot * part_bytes, sw, sh, next);
+      }
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-      mbar_arrive(full0 + 8 * ss);
-      mbar_arrive(raw_empty0 + 8 * slot);
-      if (tid == 0 && u + L::kRawStages < units) ok = issue(u + L::kRawStages);
+      mbar_arrive(full0 + 8 * slot);
+      if (tid < 16 && u + kStages - 1 < units) ok = issue(u + kStages - 1);
     }
-    if (tid == 0 && (!ok || *abort_flag)) {
+    if (tid < 16 && (!ok || *abort_flag)) {
       // every copy this thread issued lands before the CTA can leave
-      for (int s = 0; s < L::kRawStages; ++s)
-        if (issued_mask >> s & 1u)
-          wait_bounded(raw_full0 + 8 * s, issued_parity >> s & 1u, abort_flag, p.timeout_ns,
-                       timeout_code(kRoleProducer, 0x600 + s), false);
+      for (int q = 0; q < kStages; ++q)
+        if (issued_mask >> q & 1u)
+          wait_bounded(land0 + 8 * q, issued_parity >> q & 1u, abort_flag, p.timeout_ns,
+                       timeout_code(kRoleProducer, 0x600 + q), false);
     }
   } else if (warp < kStrMmaWarp) {
     // ------------------------------------------------------------ copy producer
@@ -459,7 +471,10 @@ __global__ void __launch_bounds__(kStrThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes of this warp
-    const int row_in_tile = static_cast<int>(quad * 32 + lane);
+    // tile row of this lane's accumulator lane (rows come in class order in
+    // the row-class variant)
+    const int row_in_tile = kTma ? class_row_a(static_cast<int>(quad * 32 + lane))
+                                 : static_cast<int>(quad * 32 + lane);
     // 32 x 33 words: row `lane` of a 32 x 32 accumulator block, read back by column
     uint32_t* xp = reinterpret_cast<uint32_t*>(smem + L::kXposeOffset +
                                                (warp - kStrMmaWarp - 1) * L::kXposeBytes);
@@ -476,7 +491,19 @@ __global__ void __launch_bounds__(kStrThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < kStrBN / 32; ++c) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        if (kTma) {
+          // tile columns 32c .. 32c + 31: column 32c + q + 8i (class q, i < 4)
+          // is accumulator column 32q + 4c + i
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint32_t r4[4];
+            tmem_ld_32x32b_x4(t_row + 32 * q + 4 * c, r4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r[q + 8 * i] = r4[i];
+          }
+        } else {
+          tmem_ld_32x32b_x32(t_row + c * 32, r);
+        }
         tmem_wait_ld();
         if (p.sCn == 1) {
           // row-major C/D: transpose the block through shared memory, then
@@ -485,19 +512,21 @@ __global__ void __launch_bounds__(kStrThreads, 1)
           for (int j = 0; j < 32; ++j) xp[lane * 33 + j] = r[j];
           __syncwarp();
           const int n = tn * kStrBN + c * 32 + static_cast<int>(lane);
-          const int mrow0 = tm * kStrBM + static_cast<int>(quad * 32);
+          const int mrow0 = static_cast<int>(quad * 32);  // first accumulator lane of the block
 #pragma unroll 1
           for (int i0 = 0; i0 < 32; i0 += 8) {
             __half cv[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int mi = mrow0 + i0 + i;
+              const int li = mrow0 + i0 + i;
+              const int mi = tm * kStrBM + (kTma ? class_row_a(li) : li);
               cv[i] = (mi < p.M && n < p.N) ? p.CD[static_cast<int64_t>(mi) * p.sCm + n]
                                             : __ushort_as_half(0);
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int mi = mrow0 + i0 + i;
+              const int li = mrow0 + i0 + i;
+              const int mi = tm * kStrBM + (kTma ? class_row_a(li) : li);
               if (mi < p.M && n < p.N) {
                 const uint32_t a = xp[(i0 + i) * 33 + static_cast<int>(lane)];
                 p.CD[static_cast<int64_t>(mi) * p.sCm + n] =

@@ -1493,7 +1493,7 @@ bool tma_view(const void* p, int64_t rows, int64_t K, int64_t s_r, int64_t s_k, 
 // Tensor map of row class c (rows c, c + 8, ...) of a (rows, K) operand with
 // a stride-1 K mode and row stride ld elements: base rounded down to 16
 // bytes, the class's rows 16 * ld bytes apart, dims {K + delta, class rows},
-// box {K block + 8, tile rows / 8}, no swizzle.  Returns the byte offset of
+// box {K block, tile rows / 8}, 128B swizzle.  Returns the byte offset of
 // the rows in the map's rows (2 * delta) or -1.
 int encode_row_class(CUtensorMap* map, const void* X, int64_t rows, int64_t K, int64_t ld, int c,
                      uint32_t box_rows) {
@@ -1504,10 +1504,12 @@ int encode_row_class(CUtensorMap* map, const void* X, int64_t rows, int64_t K, i
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K + shift / 2),
                         static_cast<cuuint64_t>((rows - c + 7) / 8)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 16};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kStrRawK), box_rows}, estr[2] = {1, 1};
+  // one K block per box, 128B-swizzled as the MMA reads it (the producer
+  // then shifts each row in place by the row's start within the box)
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kStrBK), box_rows}, estr[2] = {1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, reinterpret_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? shift : -1;
 }
