@@ -87,13 +87,20 @@ struct StridedMaps {
   CUtensorMap b[8];
 };
 
+// Tile rows: the row-class variant takes 256 x 256 tiles (two M = 128 MMAs
+// per step into the two halves of the tensor memory), so that each of its
+// sixteen boxes per K block feeds twice the MMA work.
+template <bool kTma>
+__host__ __device__ constexpr int str_bm() { return kTma ? 2 * kStrBM : kStrBM; }
+
 template <bool kTma>
 struct StridedSmem {
   // swizzled stages the MMA reads (the row-class variant's boxes land in
   // them and are shifted in place)
-  static constexpr int kStages = kStrStages;
-  static constexpr uint32_t kABytes = kStrBM * kStrBK * 2;  // 16 KiB
-  static constexpr uint32_t kBBytes = kStrBN * kStrBK * 2;  // 32 KiB
+  static constexpr int kStages = kTma ? 3 : kStrStages;
+  static constexpr int kAccs = kTma ? 1 : 2;  // accumulator sets (512 TMEM columns in all)
+  static constexpr uint32_t kABytes = str_bm<kTma>() * kStrBK * 2;  // 32 / 16 KiB
+  static constexpr uint32_t kBBytes = kStrBN * kStrBK * 2;          // 32 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   // per epilogue warp a 32 x 33 word transpose buffer
   static constexpr uint32_t kXposeOffset = kStages * kStageBytes;
@@ -201,14 +208,13 @@ __device__ __forceinline__ bool wait_bounded_sleeping(uint32_t bar, uint32_t par
   }
 }
 
-// Row-class variant.  A class box (16 rows of A, 32 of B, 64 elements of K)
+// Row-class variant.  A class box (32 rows of A or B, 64 elements of K)
 // lands as consecutive rows of a stage, so stage row s of the A part holds
-// tile row (s / 16) + 8 (s % 16), and stage row s of the B part tile column
+// tile row (s / 32) + 8 (s % 32), and stage row s of the B part tile column
 // (s / 32) + 8 (s % 32).  The MMA multiplies the rows in that order; the
-// epilogue reads accumulator lane s and column t back as those tile rows
-// and columns.
-__device__ __forceinline__ int class_row_a(int s) { return (s >> 4) + 8 * (s & 15); }
-__device__ __forceinline__ int class_row_b(int s) { return (s >> 5) + 8 * (s & 31); }
+// epilogue reads accumulator lanes and columns back as those tile rows and
+// columns.
+__device__ __forceinline__ int class_row(int s) { return (s >> 5) + 8 * (s & 31); }
 
 // A box row starts `sh` bytes (even, 0..14) before the row's K block: the
 // row, 128B-swizzled at stage row s (16-byte chunk j at 16 (j ^ (s % 8))),
@@ -306,35 +312,26 @@ __global__ void __launch_bounds__(kStrThreads, 1)
 
   if (warp < kStrMmaWarp && kTma) {
     // ------------------------------------------------ row-class TMA producer
-    // Thread tid owns stage row s of the A part (tid < 128) or of the B part
-    // in every stage: it shifts that row in place once the row's box and the
-    // following K block's box have landed.  No other thread touches the row,
-    // so the next block's first 16 bytes are read before this thread shifts
-    // that block.
+    // A stage has 2 * 256 rows (A's, then B's); thread tid owns rows tid and
+    // tid + 384 (the latter for tid < 128) in every stage and shifts them in
+    // place once the rows' box and the following K block's box have landed.
+    // No other thread touches those rows, so the next block's first 16 bytes
+    // are read before this thread shifts that block.
+    constexpr int kBM = str_bm<kTma>();
     const int tid = static_cast<int>(threadIdx.x);
-    const bool is_b = tid >= kStrBM;
-    const int s = is_b ? tid - kStrBM : tid;
-    const int cls = is_b ? s >> 5 : s >> 4;
-    const int sh = static_cast<int>(((is_b ? p.b_shifts : p.a_shifts) >> (4 * cls)) & 15u);
-    const uint32_t sw = static_cast<uint32_t>(s & 7);
-    uint8_t* const part0 = (is_b ? sB : sA) + s * 128;  // this row in stage 0
-    const uint32_t part_bytes = is_b ? L::kBBytes : L::kABytes;
-    const __half* const X = is_b ? p.B : p.A;
-    const int64_t ldx = is_b ? p.sBn : p.sAm;
-    const int rows = is_b ? p.N : p.M;
-    const int my_row = is_b ? class_row_b(s) : class_row_a(s);  // in its tile
+    const int n_own = tid + kStrProducers < kBM + kStrBN ? 2 : 1;
     const int my_tiles = p.num_tiles > static_cast<int>(blockIdx.x)
                              ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                              : 0;
     const int units = my_tiles * p.k_blocks;  // (tile, K block) pairs of this CTA, in order
     // threads 0-15 (lanes of warp 0): stages with copies in flight
     uint32_t issued_mask = 0, issued_parity = 0;
-    // Unit u goes into stage u % 4 once the MMA has released the stage.  Its
-    // sixteen boxes (A classes 0-7, B classes 0-7) are issued by sixteen
-    // threads, one each, after thread 0 has armed `landed` with the stage's
-    // bytes (a copy that lands before the arming drives the barrier's byte
-    // count below zero; the phase still needs the arrival).  One thread
-    // issuing all sixteen boxes was measurably slower.
+    // Unit u goes into stage u % kStages once the MMA has released the
+    // stage.  Its sixteen boxes (A classes 0-7, B classes 0-7, 32 rows each)
+    // are issued by sixteen threads, one each, after thread 0 has armed
+    // `landed` with the stage's bytes (a copy that lands before the arming
+    // drives the barrier's byte count below zero; the phase still needs the
+    // arrival).  One thread issuing all sixteen boxes was measurably slower.
     auto issue = [&](int u) -> bool {
       const int slot = u % kStages;
       const uint32_t use = static_cast<uint32_t>(u / kStages);
@@ -349,8 +346,8 @@ __global__ void __launch_bounds__(kStrThreads, 1)
       if (tid == 0) mbar_arrive_expect_tx(lb, L::kStageBytes);
       const int c = tid & 7;
       if (tid < 8)
-        tma_load_2d(smem_u32(sA + slot * L::kABytes + c * (kStrBM / 8) * 128), &maps.a[c], lb,
-                    kb * kStrBK, tm * (kStrBM / 8));
+        tma_load_2d(smem_u32(sA + slot * L::kABytes + c * (kBM / 8) * 128), &maps.a[c], lb,
+                    kb * kStrBK, tm * (kBM / 8));
       else
         tma_load_2d(smem_u32(sB + slot * L::kBBytes + c * (kStrBN / 8) * 128), &maps.b[c], lb,
                     kb * kStrBK, tn * (kStrBN / 8));
@@ -375,20 +372,31 @@ __global__ void __launch_bounds__(kStrThreads, 1)
         ok = false;
         break;
       }
-      if (sh != 0) {
+#pragma unroll
+      for (int o = 0; o < 2; ++o) {
+        if (o >= n_own) continue;
+        const int row = tid + o * kStrProducers;  // of the stage's A rows, then B rows
+        const bool is_b = row >= kBM;
+        const int s = is_b ? row - kBM : row;
+        const int sh = static_cast<int>(((is_b ? p.b_shifts : p.a_shifts) >> (4 * (s >> 5))) & 15u);
+        if (sh == 0) continue;
+        uint8_t* const at = (is_b ? sB : sA) + s * 128;  // the row in stage 0
+        const uint32_t step = is_b ? L::kBBytes : L::kABytes;
+        const uint32_t sw = static_cast<uint32_t>(s & 7);
         uint4 next;
         if (!last) {
-          next = *reinterpret_cast<const uint4*>(part0 + nslot * part_bytes + 16 * sw);
+          next = *reinterpret_cast<const uint4*>(at + nslot * step + 16 * sw);
         } else {
           const int t = static_cast<int>(blockIdx.x) + (u / p.k_blocks) * static_cast<int>(gridDim.x);
           int tm, tn;
           tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-          const int grow = (is_b ? tn * kStrBN : tm * kStrBM) + my_row;
-          next = grow < rows ? row_tail(X + static_cast<int64_t>(grow) * ldx, p.K,
-                                        p.k_blocks * kStrBK, sh)
-                             : make_uint4(0u, 0u, 0u, 0u);
+          const int grow = (is_b ? tn * kStrBN : tm * kBM) + class_row(s);
+          next = grow < (is_b ? p.N : p.M)
+                     ? row_tail((is_b ? p.B : p.A) + static_cast<int64_t>(grow) * (is_b ? p.sBn : p.sAm),
+                                p.K, p.k_blocks * kStrBK, sh)
+                     : make_uint4(0u, 0u, 0u, 0u);
         }
-        shift_row_in_place(part0 + slot * part_bytes, sw, sh, next);
+        shift_row_in_place(at + slot * step, sw, sh, next);
       }
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
       mbar_arrive(full0 + 8 * slot);
@@ -449,9 +457,14 @@ __global__ void __launch_bounds__(kStrThreads, 1)
           const uint32_t a_base = smem_u32(sA + stage * L::kABytes);
           const uint32_t b_base = smem_u32(sB + stage * L::kBBytes);
 #pragma unroll
-          for (int k = 0; k < kStrBK / 16; ++k)
-            mma_f16(d_tmem, make_sw128_desc(a_base + k * 32, 16, 1024),
-                    make_sw128_desc(b_base + k * 32, 16, 1024), idesc, (kb | k) != 0);
+          for (int k = 0; k < kStrBK / 16; ++k) {
+            const uint64_t bd = make_sw128_desc(b_base + k * 32, 16, 1024);
+            mma_f16(d_tmem, make_sw128_desc(a_base + k * 32, 16, 1024), bd, idesc, (kb | k) != 0);
+            // row-class tiles: stage rows 128..255 into accumulator columns 256..511
+            if (kTma)
+              mma_f16(d_tmem + kStrBN, make_sw128_desc(a_base + kStrBM * 128 + k * 32, 16, 1024),
+                      bd, idesc, (kb | k) != 0);
+          }
           mma_commit(empty0 + 8 * stage);
           if (++stage == kStages) {
             stage = 0;
@@ -460,8 +473,10 @@ __global__ void __launch_bounds__(kStrThreads, 1)
         }
         if (!ok) break;
         mma_commit(tfull0 + 8 * acc);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == L::kAccs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       if (!ok || *abort_flag) {
         mma_commit(drain);
@@ -470,11 +485,9 @@ __global__ void __launch_bounds__(kStrThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    constexpr int kBM = str_bm<kTma>();
+    constexpr int kHalves = kBM / 128;  // accumulator halves (stage rows 128h ..)
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes of this warp
-    // tile row of this lane's accumulator lane (rows come in class order in
-    // the row-class variant)
-    const int row_in_tile = kTma ? class_row_a(static_cast<int>(quad * 32 + lane))
-                                 : static_cast<int>(quad * 32 + lane);
     // 32 x 33 words: row `lane` of a 32 x 32 accumulator block, read back by column
     uint32_t* xp = reinterpret_cast<uint32_t*>(smem + L::kXposeOffset +
                                                (warp - kStrMmaWarp - 1) * L::kXposeBytes);
@@ -486,8 +499,14 @@ __global__ void __launch_bounds__(kStrThreads, 1)
                         timeout_code(kRoleEpilogue, acc)))
         break;
       tc_fence_after();
-      const int m = tm * kStrBM + row_in_tile;
-      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kStrBN;
+#pragma unroll 1
+      for (int h = 0; h < kHalves; ++h) {
+      // accumulator lane quad * 32 + lane of half h is stage row 128 h + that
+      // lane: its tile row (rows come in class order in the row-class variant)
+      const int first_lane = 128 * h + static_cast<int>(quad * 32);
+      const int m = tm * kBM + (kTma ? class_row(first_lane + static_cast<int>(lane))
+                                     : first_lane + static_cast<int>(lane));
+      const uint32_t t_row = tmem_base + ((quad * 32) << 16) + acc * kStrBN + h * kStrBN;
 #pragma unroll 1
       for (int c = 0; c < kStrBN / 32; ++c) {
         uint32_t r[32];
@@ -512,21 +531,20 @@ __global__ void __launch_bounds__(kStrThreads, 1)
           for (int j = 0; j < 32; ++j) xp[lane * 33 + j] = r[j];
           __syncwarp();
           const int n = tn * kStrBN + c * 32 + static_cast<int>(lane);
-          const int mrow0 = static_cast<int>(quad * 32);  // first accumulator lane of the block
 #pragma unroll 1
           for (int i0 = 0; i0 < 32; i0 += 8) {
             __half cv[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int li = mrow0 + i0 + i;
-              const int mi = tm * kStrBM + (kTma ? class_row_a(li) : li);
+              const int li = first_lane + i0 + i;
+              const int mi = tm * kBM + (kTma ? class_row(li) : li);
               cv[i] = (mi < p.M && n < p.N) ? p.CD[static_cast<int64_t>(mi) * p.sCm + n]
                                             : __ushort_as_half(0);
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const int li = mrow0 + i0 + i;
-              const int mi = tm * kStrBM + (kTma ? class_row_a(li) : li);
+              const int li = first_lane + i0 + i;
+              const int mi = tm * kBM + (kTma ? class_row(li) : li);
               if (mi < p.M && n < p.N) {
                 const uint32_t a = xp[(i0 + i) * 33 + static_cast<int>(lane)];
                 p.CD[static_cast<int64_t>(mi) * p.sCm + n] =
@@ -552,11 +570,14 @@ __global__ void __launch_bounds__(kStrThreads, 1)
           }
         }
       }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == L::kAccs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
   }
 

@@ -1516,7 +1516,6 @@ int encode_row_class(CUtensorMap* map, const void* X, int64_t rows, int64_t K, i
 
 int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream_t stream) {
   StridedArgs p = base;
-  const int grid = std::min(p.num_tiles, st.num_sms);
   // The row-class TMA variant when both operands have a stride-1 K mode,
   // rows that do not overlap (ld >= K) and at least one row of every class
   // (M, N >= 8); otherwise every chunk is gathered by the producer threads.
@@ -1526,7 +1525,7 @@ int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream
   bool tma = p.sAk == 1 && p.sBk == 1 && p.M >= 8 && p.N >= 8 && p.K >= 1 && p.sAm >= p.K &&
              p.sBn >= p.K && p.sAm < kMaxLd && p.sBn < kMaxLd;
   for (int c = 0; tma && c < 8; ++c) {
-    const int sa = encode_row_class(&maps.a[c], p.A, p.M, p.K, p.sAm, c, kStrBM / 8);
+    const int sa = encode_row_class(&maps.a[c], p.A, p.M, p.K, p.sAm, c, str_bm<true>() / 8);
     const int sb = encode_row_class(&maps.b[c], p.B, p.N, p.K, p.sBn, c, kStrBN / 8);
     tma = sa >= 0 && sb >= 0;
     if (tma) {
@@ -1535,9 +1534,14 @@ int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream
     }
   }
   if (tma) {
+    // 256 x 256 tiles in this variant
+    p.tiles_m = (p.M + str_bm<true>() - 1) / str_bm<true>();
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    const int grid = std::min(p.num_tiles, st.num_sms);
     gemm_tn_strided_kernel<true><<<grid, kStrThreads, StridedSmem<true>::kDynamicBytes, stream>>>(
         maps, p);
   } else {
+    const int grid = std::min(p.num_tiles, st.num_sms);
     gemm_tn_strided_kernel<false><<<grid, kStrThreads, StridedSmem<false>::kDynamicBytes,
                                     stream>>>(maps, p);
   }
