@@ -61,6 +61,11 @@ constexpr int kStrStages = 4;
 constexpr int kStrProducers = 384;
 constexpr int kStrThreads = 544;    // 12 producer warps, MMA warp, 4 epilogue warps
 constexpr int kStrMmaWarp = kStrProducers / 32;
+// The row-class variant adds a warp that issues the boxes (18 warps still
+// leave at most five on an SM sub-partition).
+constexpr int kStrIssueWarp = kStrMmaWarp + 5;
+template <bool kTma>
+__host__ __device__ constexpr int str_threads() { return kTma ? kStrThreads + 32 : kStrThreads; }
 
 struct StridedArgs {
   int M, N, K;
@@ -257,7 +262,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[
 }
 
 template <bool kTma>
-__global__ void __launch_bounds__(kStrThreads, 1)
+__global__ void __launch_bounds__(str_threads<kTma>(), 1)
     gemm_tn_strided_kernel(const __grid_constant__ StridedMaps maps, const StridedArgs p) {
   using L = StridedSmem<kTma>;
   constexpr int kStages = L::kStages;
@@ -324,41 +329,7 @@ __global__ void __launch_bounds__(kStrThreads, 1)
                              ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                              : 0;
     const int units = my_tiles * p.k_blocks;  // (tile, K block) pairs of this CTA, in order
-    // threads 0-15 (lanes of warp 0): stages with copies in flight
-    uint32_t issued_mask = 0, issued_parity = 0;
-    // Unit u goes into stage u % kStages once the MMA has released the
-    // stage.  Its sixteen boxes (A classes 0-7, B classes 0-7, 32 rows each)
-    // are issued by sixteen threads, one each, after thread 0 has armed
-    // `landed` with the stage's bytes (a copy that lands before the arming
-    // drives the barrier's byte count below zero; the phase still needs the
-    // arrival).  One thread issuing all sixteen boxes was measurably slower.
-    auto issue = [&](int u) -> bool {
-      const int slot = u % kStages;
-      const uint32_t use = static_cast<uint32_t>(u / kStages);
-      if (!wait_bounded(empty0 + 8 * slot, (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
-                        timeout_code(kRoleProducer, 0x400 + slot)))
-        return false;
-      const int t = static_cast<int>(blockIdx.x) + (u / p.k_blocks) * static_cast<int>(gridDim.x);
-      const int kb = u % p.k_blocks;
-      int tm, tn;
-      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-      const uint32_t lb = land0 + 8 * slot;
-      if (tid == 0) mbar_arrive_expect_tx(lb, L::kStageBytes);
-      const int c = tid & 7;
-      if (tid < 8)
-        tma_load_2d(smem_u32(sA + slot * L::kABytes + c * (kBM / 8) * 128), &maps.a[c], lb,
-                    kb * kStrBK, tm * (kBM / 8));
-      else
-        tma_load_2d(smem_u32(sB + slot * L::kBBytes + c * (kStrBN / 8) * 128), &maps.b[c], lb,
-                    kb * kStrBK, tn * (kStrBN / 8));
-      issued_mask |= 1u << slot;
-      issued_parity = (issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
-      return true;
-    };
     bool ok = true;
-    if (tid < 16) {
-      for (int u = 0; ok && u < min(units, kStages - 1); ++u) ok = issue(u);
-    }
     for (int u = 0; ok && u < units; ++u) {
       const int slot = u % kStages;
       const int kb = u % p.k_blocks;
@@ -400,14 +371,58 @@ __global__ void __launch_bounds__(kStrThreads, 1)
       }
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
       mbar_arrive(full0 + 8 * slot);
-      if (tid < 16 && u + kStages - 1 < units) ok = issue(u + kStages - 1);
     }
-    if (tid < 16 && (!ok || *abort_flag)) {
-      // every copy this thread issued lands before the CTA can leave
-      for (int q = 0; q < kStages; ++q)
-        if (issued_mask >> q & 1u)
-          wait_bounded(land0 + 8 * q, issued_parity >> q & 1u, abort_flag, p.timeout_ns,
-                       timeout_code(kRoleProducer, 0x600 + q), false);
+    (void)ok;
+  } else if (kTma && warp == kStrIssueWarp) {
+    // ------------------------------------------------ row-class box issue
+    // Lanes 0-15 load unit v into stage v % kStages as soon as the MMA has
+    // released the stage: lane i issues box i (A classes 0-7, then B
+    // classes 0-7, 32 rows each) after lane 0 has armed `landed` with the
+    // stage's bytes (a copy that lands before the arming drives the byte
+    // count below zero; the phase still needs the arrival).  With a warp of
+    // their own the loads run two stages ahead of the shift; issued by the
+    // shifting threads after their own rows, every shift waited a whole
+    // round trip for the next block's boxes.
+    if (lane < 16) {
+      constexpr int kBM = str_bm<kTma>();
+      const int i = static_cast<int>(lane);
+      const int my_tiles = p.num_tiles > static_cast<int>(blockIdx.x)
+                               ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                               : 0;
+      const int units = my_tiles * p.k_blocks;
+      uint32_t issued_mask = 0, issued_parity = 0;  // stages with copies in flight
+      bool ok = true;
+      for (int v = 0; ok && v < units; ++v) {
+        const int slot = v % kStages;
+        const uint32_t use = static_cast<uint32_t>(v / kStages);
+        if (!wait_bounded(empty0 + 8 * slot, (use & 1u) ^ 1u, abort_flag, p.timeout_ns,
+                          timeout_code(kRoleProducer, 0x400 + slot))) {
+          ok = false;
+          break;
+        }
+        const int t = static_cast<int>(blockIdx.x) + (v / p.k_blocks) * static_cast<int>(gridDim.x);
+        const int kb = v % p.k_blocks;
+        int tm, tn;
+        tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        const uint32_t lb = land0 + 8 * slot;
+        if (i == 0) mbar_arrive_expect_tx(lb, L::kStageBytes);
+        const int c = i & 7;
+        if (i < 8)
+          tma_load_2d(smem_u32(sA + slot * L::kABytes + c * (kBM / 8) * 128), &maps.a[c], lb,
+                      kb * kStrBK, tm * (kBM / 8));
+        else
+          tma_load_2d(smem_u32(sB + slot * L::kBBytes + c * (kStrBN / 8) * 128), &maps.b[c], lb,
+                      kb * kStrBK, tn * (kStrBN / 8));
+        issued_mask |= 1u << slot;
+        issued_parity = (issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
+      }
+      if (!ok || *abort_flag) {
+        // every copy this lane issued lands before the CTA can leave
+        for (int q = 0; q < kStages; ++q)
+          if (issued_mask >> q & 1u)
+            wait_bounded(land0 + 8 * q, issued_parity >> q & 1u, abort_flag, p.timeout_ns,
+                         timeout_code(kRoleProducer, 0x600 + q), false);
+      }
     }
   } else if (warp < kStrMmaWarp) {
     // ------------------------------------------------------------ copy producer

@@ -1538,8 +1538,8 @@ int strided_copy_path(const StridedArgs& base, const DeviceState& st, cudaStream
     p.tiles_m = (p.M + str_bm<true>() - 1) / str_bm<true>();
     p.num_tiles = p.tiles_m * p.tiles_n;
     const int grid = std::min(p.num_tiles, st.num_sms);
-    gemm_tn_strided_kernel<true><<<grid, kStrThreads, StridedSmem<true>::kDynamicBytes, stream>>>(
-        maps, p);
+    gemm_tn_strided_kernel<true><<<grid, str_threads<true>(), StridedSmem<true>::kDynamicBytes,
+                                   stream>>>(maps, p);
   } else {
     const int grid = std::min(p.num_tiles, st.num_sms);
     gemm_tn_strided_kernel<false><<<grid, kStrThreads, StridedSmem<false>::kDynamicBytes,
