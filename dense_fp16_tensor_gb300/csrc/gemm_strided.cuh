@@ -60,12 +60,16 @@ constexpr int kStrStages = 4;
 // (sixteen producer warps would cap it at 80 and spill in the shift pass).
 constexpr int kStrProducers = 384;
 constexpr int kStrThreads = 544;    // 12 producer warps, MMA warp, 4 epilogue warps
-constexpr int kStrMmaWarp = kStrProducers / 32;
-// The row-class variant adds a warp that issues the boxes (18 warps still
-// leave at most five on an SM sub-partition).
-constexpr int kStrIssueWarp = kStrMmaWarp + 5;
+// The row-class variant has sixteen producer warps (one stage row each)
+// and a warp that issues the boxes: 22 warps, six on some SM
+// sub-partitions, so at most 80 registers a thread (its launch bounds are
+// declared for 768 threads to make the compiler keep to that).
 template <bool kTma>
-__host__ __device__ constexpr int str_threads() { return kTma ? kStrThreads + 32 : kStrThreads; }
+__host__ __device__ constexpr int str_producers() { return kTma ? 512 : kStrProducers; }
+template <bool kTma>
+__host__ __device__ constexpr int str_threads() { return str_producers<kTma>() + (kTma ? 6 : 5) * 32; }
+template <bool kTma>
+__host__ __device__ constexpr int str_bound_threads() { return kTma ? 768 : kStrThreads; }
 
 struct StridedArgs {
   int M, N, K;
@@ -262,10 +266,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[
 }
 
 template <bool kTma>
-__global__ void __launch_bounds__(str_threads<kTma>(), 1)
+__global__ void __launch_bounds__(str_bound_threads<kTma>(), 1)
     gemm_tn_strided_kernel(const __grid_constant__ StridedMaps maps, const StridedArgs p) {
   using L = StridedSmem<kTma>;
   constexpr int kStages = L::kStages;
+  constexpr int kProducers = str_producers<kTma>();  // producer threads
+  constexpr int kMmaWarp = kProducers / 32;          // then 4 epilogue warps
+  constexpr int kIssueWarp = kMmaWarp + 5;           // row-class variant only
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -287,7 +294,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, kStrProducers);
+      mbar_init(full0 + 8 * s, kProducers);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
       tma_prefetch_desc(&maps.b[c]);
     }
   }
-  if (warp == kStrMmaWarp) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 2 * kStrBN);
     tmem_relinquish();
   }
@@ -315,16 +322,17 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < kStrMmaWarp && kTma) {
+  if (warp < kMmaWarp && kTma) {
     // ------------------------------------------------ row-class TMA producer
-    // A stage has 2 * 256 rows (A's, then B's); thread tid owns rows tid and
-    // tid + 384 (the latter for tid < 128) in every stage and shifts them in
-    // place once the rows' box and the following K block's box have landed.
+    // A stage has 2 * 256 rows (A's, then B's); thread tid owns row tid (and
+    // tid + kProducers, were there fewer threads than rows) in every stage
+    // and shifts it in place once the row's box and the following K block's
+    // box have landed.
     // No other thread touches those rows, so the next block's first 16 bytes
     // are read before this thread shifts that block.
     constexpr int kBM = str_bm<kTma>();
     const int tid = static_cast<int>(threadIdx.x);
-    const int n_own = tid + kStrProducers < kBM + kStrBN ? 2 : 1;
+    const int n_own = tid + kProducers < kBM + kStrBN ? 2 : 1;
     const int my_tiles = p.num_tiles > static_cast<int>(blockIdx.x)
                              ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                              : 0;
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
 #pragma unroll
       for (int o = 0; o < 2; ++o) {
         if (o >= n_own) continue;
-        const int row = tid + o * kStrProducers;  // of the stage's A rows, then B rows
+        const int row = tid + o * kProducers;  // of the stage's A rows, then B rows
         const bool is_b = row >= kBM;
         const int s = is_b ? row - kBM : row;
         const int sh = static_cast<int>(((is_b ? p.b_shifts : p.a_shifts) >> (4 * (s >> 5))) & 15u);
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
       mbar_arrive(full0 + 8 * slot);
     }
     (void)ok;
-  } else if (kTma && warp == kStrIssueWarp) {
+  } else if (kTma && warp == kIssueWarp) {
     // ------------------------------------------------ row-class box issue
     // Lanes 0-15 load unit v into stage v % kStages as soon as the MMA has
     // released the stage: lane i issues box i (A classes 0-7, then B
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
                          timeout_code(kRoleProducer, 0x600 + q), false);
       }
     }
-  } else if (warp < kStrMmaWarp) {
+  } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ copy producer
     const int tid = static_cast<int>(threadIdx.x);
     uint32_t stage = 0, phase = 0;
@@ -448,7 +456,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
         }
       }
     }
-  } else if (warp == kStrMmaWarp) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = make_idesc_f16(kStrBM, kStrBN, !p.acc_f16, 0, 0);
@@ -505,7 +513,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
     const uint32_t quad = static_cast<uint32_t>(warp & 3);  // TMEM lanes of this warp
     // 32 x 33 words: row `lane` of a 32 x 32 accumulator block, read back by column
     uint32_t* xp = reinterpret_cast<uint32_t*>(smem + L::kXposeOffset +
-                                               (warp - kStrMmaWarp - 1) * L::kXposeBytes);
+                                               (warp - kMmaWarp - 1) * L::kXposeBytes);
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int tm, tn;
@@ -599,7 +607,7 @@ __global__ void __launch_bounds__(str_threads<kTma>(), 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kStrMmaWarp) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * kStrBN);
   }
