@@ -62,3 +62,11 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     monkeypatch.setenv("LOCAL_RANK", "1")
     args = bench.parse(["--impl", "reference", "--gpus", "2"])
     assert bench.run_reference(args) == 0                # returns at once, prints nothing
+
+
+def test_profiling_switches_default_off():
+    # the driver's plain `bench.py` run times the headline workload; the
+    # profiling switches only narrow what a single run times
+    args = bench.parse([])
+    assert not args.only_strided and args.shape == "" and not args.all_extras
+    assert bench.parse(["--only-strided"]).only_strided
