@@ -109,3 +109,16 @@ def test_copy_route_variant(view, variant):
     got, d64, d16 = run_case(M, N, K, view, 0, "int1", "int4", 1950)
     assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel" + variant
     check(got, d64, d16, K, 0, True, f"copy route {view}")
+
+
+@pytest.mark.parametrize("view", ["odd_ld_k_major", "offset_by_one"])
+@pytest.mark.parametrize("accum", [0, 1])
+def test_copy_route_rows_k_multiple_of_64(view, accum):
+    # the row-class variant shifts each row by its offset in the boxes; with K
+    # a multiple of 64 the last K block's final elements come from the row
+    # itself (no box past the end), so such K need their own cases, over
+    # several 256 x 256 tiles and ragged M / N
+    for i, (M, N, K) in enumerate([(520, 300, 256), (264, 520, 64), (300, 280, 1024)]):
+        got, d64, d16 = run_case(M, N, K, view, accum, "int2", "int4", 2100 + 10 * i)
+        assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel<rows>"
+        check(got, d64, d16, K, accum, True, f"rows {view} {M}x{N}x{K}")
