@@ -122,3 +122,23 @@ def test_copy_route_rows_k_multiple_of_64(view, accum):
         got, d64, d16 = run_case(M, N, K, view, accum, "int2", "int4", 2100 + 10 * i)
         assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel<rows>"
         check(got, d64, d16, K, accum, True, f"rows {view} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("accum", [0, 1])
+def test_copy_route_rows_real_values(accum):
+    # real values through the row-class variant (the class order of the
+    # stage rows must not change what is summed)
+    M, N, K = 384, 520, 1000
+    for view in ("odd_ld_k_major", "offset_by_one"):
+        got, d64, d16 = run_case(M, N, K, view, accum, "u11", "u11", 2300)
+        assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel<rows>"
+        check(got, d64, d16, K, accum, False, f"rows real {view}")
+
+
+def test_copy_route_rows_smallest_views():
+    # the row-class variant takes M, N >= 8: exactly one row per class, one K
+    # element, and a single partial K block
+    for i, (M, N, K) in enumerate([(8, 8, 1), (8, 300, 7), (300, 8, 64), (9, 17, 129)]):
+        got, d64, d16 = run_case(M, N, K, "odd_ld_k_major", 0, "int2", "int4", 2400 + 10 * i)
+        assert gb.gemm_tn_last_kernels() == "gemm_tn_strided_kernel<rows>"
+        check(got, d64, d16, K, 0, True, f"rows small {M}x{N}x{K}")
