@@ -1456,18 +1456,15 @@ cudaError_t repack2d(const void* src, int64_t s_sr, int64_t s_sc, void* dst, int
     const int64_t span = static_cast<int64_t>(kRepackThreads) * kRowWords;
     const dim3 grid(static_cast<unsigned>(std::min<int64_t>((words + span - 1) / span, 64)),
                     static_cast<unsigned>(rows), 1);
-    repack_rows_kernel<<<grid, kRepackThreads, 0, stream>>>(static_cast<const __half*>(src), s_sr,
-                                                            static_cast<__half*>(dst), s_dr,
-                                                            static_cast<int>(rows),
-                                                            static_cast<int>(cols));
-    return cudaGetLastError();
+    return launch_pdl(repack_rows_kernel, grid, dim3(kRepackThreads), 0, stream,
+                      static_cast<const __half*>(src), s_sr, static_cast<__half*>(dst), s_dr,
+                      static_cast<int>(rows), static_cast<int>(cols));
   }
   const dim3 grid(static_cast<unsigned>((cols + kRepackTile - 1) / kRepackTile),
                   static_cast<unsigned>((rows + kRepackTile - 1) / kRepackTile), 1);
-  repack2d_kernel<<<grid, kRepackThreads, 0, stream>>>(
-      static_cast<const __half*>(src), s_sr, s_sc, static_cast<__half*>(dst), s_dr, s_dc,
-      static_cast<int>(rows), static_cast<int>(cols));
-  return cudaGetLastError();
+  return launch_pdl(repack2d_kernel, grid, dim3(kRepackThreads), 0, stream,
+                    static_cast<const __half*>(src), s_sr, s_sc, static_cast<__half*>(dst), s_dr,
+                    s_dc, static_cast<int>(rows), static_cast<int>(cols));
 }
 
 int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }

@@ -26,6 +26,10 @@ __global__ void __launch_bounds__(kRepackThreads)
     repack2d_kernel(const __half* __restrict__ src, int64_t s_sr, int64_t s_sc,
                     __half* __restrict__ dst, int64_t s_dr, int64_t s_dc, int rows, int cols) {
   __shared__ unsigned short tile[kRepackTile][kRepackTile + 2];
+  // launched as a programmatic dependent: resident while the kernel before
+  // it drains, touching memory only once that kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int r0 = static_cast<int>(blockIdx.y) * kRepackTile;
   const int c0 = static_cast<int>(blockIdx.x) * kRepackTile;
   const unsigned short* s = reinterpret_cast<const unsigned short*>(src);
@@ -66,6 +70,9 @@ __global__ void __launch_bounds__(kRepackThreads)
     repack_rows_kernel(const __half* __restrict__ src, int64_t s_sr, __half* __restrict__ dst,
                        int64_t s_dr, int rows, int cols) {
   (void)rows;
+  // a programmatic dependent launch, as repack2d_kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const unsigned short* s =
       reinterpret_cast<const unsigned short*>(src) + static_cast<int64_t>(blockIdx.y) * s_sr;
   unsigned short* d = reinterpret_cast<unsigned short*>(dst) + static_cast<int64_t>(blockIdx.y) * s_dr;
